@@ -1,0 +1,456 @@
+/*
+ * moe_oracle.c -- plain, slow, obviously-correct CPU oracle of the single-GPU
+ * MoE layer path: group-limited top-k router, dispatch permutation, SwiGLU
+ * expert FFN, weighted combine.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline of the benchmark may load this library.  It shares no code,
+ * header, table or constant with the CUDA path, and it never calls into it.
+ *
+ * Sources (web pages on the MoE dispatch/combine path):
+ *   [ch15]   "第十五章：多节点大模型推理", section 4.1 (gating picks top-k
+ *            logical experts), section 4.3 (assignment counts n_e, R_imbalance,
+ *            capacity), section 3.4 (dispatch/combine volume T*k*H*b).
+ *   [par02]  "推理INFRA方法论-02-parallelism", MoE-TP/EP comparison (gate_up
+ *            fused expert GEMM, masked layout, M_e = B_local*P*k/E).
+ *   [trace]  token trace through TP/CP/SP/EP/DP/PP, hop 4 "dispatch to two
+ *            experts": y = p5*E5(x) + p27*E27(x).
+ *   [ep]     "ep-deploy" handbook page, section "EPLB 与路由约束": 256 experts in
+ *            8 groups, group score = sum of the group's two best scores, keep
+ *            4 groups, pick 8 experts inside them.
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes):
+ *   R1  router logits are fp32 sums of exact bf16*bf16 products in a fixed
+ *       order: "lane" l in [0,32) owns every i with (i/8) mod 32 == l and sums
+ *       its products in increasing i from +0; the 32 lane sums are combined by
+ *       the xor butterfly (offsets 16,8,4,2,1).
+ *   R2  exp is a Cody-Waite reduction (ln2 split in a 16-bit head and a tail)
+ *       followed by a degree-7 Taylor polynomial with coefficients 1/j!
+ *       rounded to fp32, evaluated by fused multiply-add Horner steps, then an
+ *       exact scaling by 2^n.  sigma(l) = 1 / (1 + exp(-l)), IEEE division.
+ *   R3  selection score s' = sigma(l) + fl(bias_scale * b)   (sigmoid router)
+ *       or s' = l                                          (softmax router;
+ *       softmax is monotone so top-k over logits equals top-k over softmax).
+ *   R4  group score = sum of the two largest s' of the group (fp32 sum in the
+ *       fp32 router; fp64 for the fp64 routing simulation of [ep]).
+ *   R5  keep the topk_group best groups, ties to the lower group index.
+ *   R6  top-k experts among kept groups, ties to the lower expert index,
+ *       output in descending score order.
+ *   R7  sigmoid weights: sigma of the chosen experts (no bias) divided by
+ *       their sequential fp32 sum; softmax weights: exp(l_j - l_0) divided by
+ *       the sequential fp32 sum (the renormalised top-k of softmax).
+ *   R8  dispatch is a stable counting sort of the flat assignments a = t*k+j.
+ *   R9  expert FFN: h = silu(x.Wg) * (x.Wu), y = h.Wd, accumulated in fp64.
+ *   R10 combine: y[t] = sum_j w[t,j] * y_perm[dest[t*k+j]], j ascending.
+ *
+ * Compile with -O2 -ffp-contract=off, no fast-math, so that every floating
+ * point operation is exactly the one written.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* bf16 helpers                                                              */
+/* ------------------------------------------------------------------------ */
+
+static float bf16_value(uint16_t h) {
+  uint32_t u = ((uint32_t)h) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* round-to-nearest-even fp32 -> bf16 (finite inputs) */
+static uint16_t bf16_round(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7FFFu + lsb;
+  return (uint16_t)(u >> 16);
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* R1: router logits, canonical fp32 order                                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * logits[t*E+e] = sum_i x[t,i] * w_r[i,e]  ([trace] hop 4: the router scores
+ * every expert from the token's hidden state; [ch15] 4.1 gating).
+ * x: [T,d] bf16, w_r: [d,E] bf16.  Order per reading R1.
+ */
+void oracle_router_logits(const uint16_t *x, const uint16_t *w_r, int T, int d,
+                          int E, float *logits) {
+  /* w_r widened to fp32 once (exact) */
+  float *wf = (float *)malloc(sizeof(float) * (size_t)d * E);
+  for (size_t q = 0; q < (size_t)d * E; ++q) wf[q] = bf16_value(w_r[q]);
+#pragma omp parallel
+  {
+    /* lane[l*E + e]: partial sum of lane l for expert e */
+    float *lane = (float *)malloc(sizeof(float) * 32 * (size_t)E);
+#pragma omp for schedule(dynamic, 4)
+    for (int t = 0; t < T; ++t) {
+      for (int q = 0; q < 32 * E; ++q) lane[q] = 0.0f;
+      for (int i = 0; i < d; ++i) {
+        int l = (i / 8) % 32;
+        float xi = bf16_value(x[(size_t)t * d + i]);
+        const float *wrow = wf + (size_t)i * E;
+        float *acc = lane + (size_t)l * E;
+        for (int e = 0; e < E; ++e) {
+          float prod = xi * wrow[e]; /* exact: 8-bit x 8-bit significands */
+          acc[e] = acc[e] + prod;
+        }
+      }
+      for (int e = 0; e < E; ++e) {
+        float a[32], b[32];
+        for (int l = 0; l < 32; ++l) a[l] = lane[(size_t)l * E + e];
+        for (int off = 16; off >= 1; off /= 2) {
+          for (int l = 0; l < 32; ++l) b[l] = a[l] + a[l ^ off];
+          for (int l = 0; l < 32; ++l) a[l] = b[l];
+        }
+        logits[(size_t)t * E + e] = a[0];
+      }
+    }
+    free(lane);
+  }
+  free(wf);
+}
+
+/* ------------------------------------------------------------------------ */
+/* R2: exp and sigmoid                                                       */
+/* ------------------------------------------------------------------------ */
+
+/* ln 2 = LN2_HEAD + LN2_TAIL; the head keeps 16 significant bits of fl(ln 2)
+ * (low 8 stored bits cleared) so that n * LN2_HEAD is exact for |n| < 256. */
+static const float LN2_HEAD = 0x1.62e4p-1f;          /* 0.693145751953125 */
+static const float LN2_TAIL = 0x1.7f7d1cp-20f;       /* fl(ln2 - head)    */
+static const float LOG2_E = 0x1.715476p+0f;          /* fl(1/ln 2)        */
+/* 1/j! rounded to fp32, j = 0..7 */
+static const float INV_FACT[8] = {0x1p+0f,      0x1p+0f,      0x1p-1f,
+                                  0x1.555556p-3f, 0x1.555556p-5f, 0x1.111112p-7f,
+                                  0x1.6c16c2p-10f, 0x1.a01a02p-13f};
+
+float oracle_exp(float y) {
+  if (y > 80.0f) y = 80.0f;
+  if (y < -80.0f) y = -80.0f;
+  float n = rintf(y * LOG2_E);
+  float r = fmaf(-n, LN2_HEAD, y);
+  r = fmaf(-n, LN2_TAIL, r);
+  float p = INV_FACT[7];
+  for (int j = 6; j >= 0; --j) p = fmaf(p, r, INV_FACT[j]);
+  return ldexpf(p, (int)n);
+}
+
+float oracle_sigmoid(float l) {
+  float den = 1.0f + oracle_exp(-l);
+  return 1.0f / den;
+}
+
+void oracle_exp_array(const float *in, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_exp(in[i]);
+}
+
+void oracle_sigmoid_array(const float *in, float *out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_sigmoid(in[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* R4-R6: group-limited top-k selection                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Group-limited routing of [ep] "EPLB 与路由约束": experts are split in G equal
+ * groups; a group's score is the sum of its two best expert scores; the
+ * topk_group best groups are kept; the k best experts inside the kept groups
+ * are chosen.  Scores are given as doubles; when group_sum_f32 is set every
+ * score is an fp32 value and the group sum is rounded to fp32 (the binary64
+ * sum of two binary32 values rounded to binary32 is the correctly rounded
+ * binary32 sum).  With G == 1 the group step is skipped (plain top-k).
+ * ids: [T,k], descending score, ties to the lower index.
+ */
+void oracle_select(const double *s, int T, int E, int G, int topk_group, int k,
+                   int group_sum_f32, int32_t *ids) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const double *st = s + (size_t)t * E;
+    int gs = E / G;
+    unsigned char *eligible = (unsigned char *)calloc((size_t)E, 1);
+    unsigned char *chosen = (unsigned char *)calloc((size_t)E, 1);
+    if (G > 1) {
+      double *gscore = (double *)malloc(sizeof(double) * G);
+      unsigned char *kept = (unsigned char *)calloc((size_t)G, 1);
+      for (int g = 0; g < G; ++g) {
+        double m1 = -INFINITY, m2 = -INFINITY;
+        for (int e = g * gs; e < (g + 1) * gs; ++e) {
+          if (st[e] > m1) {
+            m2 = m1;
+            m1 = st[e];
+          } else if (st[e] > m2) {
+            m2 = st[e];
+          }
+        }
+        double sum = (gs >= 2) ? m1 + m2 : m1;
+        if (group_sum_f32) sum = (double)(float)sum;
+        gscore[g] = sum;
+      }
+      for (int r = 0; r < topk_group; ++r) {
+        int best = -1;
+        for (int g = 0; g < G; ++g)
+          if (!kept[g] && (best < 0 || gscore[g] > gscore[best])) best = g;
+        kept[best] = 1;
+      }
+      for (int e = 0; e < E; ++e) eligible[e] = kept[e / gs];
+      free(kept);
+      free(gscore);
+    } else {
+      for (int e = 0; e < E; ++e) eligible[e] = 1;
+    }
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e)
+        if (eligible[e] && !chosen[e] && (best < 0 || st[e] > st[best])) best = e;
+      chosen[best] = 1;
+      ids[(size_t)t * k + j] = best;
+    }
+    free(chosen);
+    free(eligible);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Full router: logits -> scores -> selection -> weights                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * score_kind 0: sigmoid router with bias (R3, R7); 1: softmax router (R7').
+ * bias: [E] fp32 (ignored for softmax).  Outputs ids [T,k], weights [T,k],
+ * and optionally the selection scores s' [T,E] (sel may be NULL).
+ */
+void oracle_route_from_logits(const float *logits, const float *bias, int T, int E,
+                              int G, int topk_group, int k, int score_kind,
+                              float bias_scale, int32_t *ids, float *weights,
+                              float *sel) {
+  double *s = (double *)malloc(sizeof(double) * (size_t)T * E);
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      float l = logits[(size_t)t * E + e];
+      float v;
+      if (score_kind == 0) {
+        float b = bias_scale * bias[e];
+        v = oracle_sigmoid(l) + b;
+      } else {
+        v = l;
+      }
+      s[(size_t)t * E + e] = (double)v;
+      if (sel) sel[(size_t)t * E + e] = v;
+    }
+  }
+  oracle_select(s, T, E, G, topk_group, k, 1, ids);
+  free(s);
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const int32_t *id = ids + (size_t)t * k;
+    float *w = weights + (size_t)t * k;
+    const float *lt = logits + (size_t)t * E;
+    float num[64];
+    float *nump = (k <= 64) ? num : (float *)malloc(sizeof(float) * k);
+    float sum = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      float v;
+      if (score_kind == 0)
+        v = oracle_sigmoid(lt[id[j]]);
+      else
+        v = oracle_exp(lt[id[j]] - lt[id[0]]);
+      nump[j] = v;
+      sum = (j == 0) ? v : sum + v;
+    }
+    for (int j = 0; j < k; ++j) w[j] = nump[j] / sum;
+    if (nump != num) free(nump);
+  }
+}
+
+void oracle_route(const uint16_t *x, const uint16_t *w_r, const float *bias, int T,
+                  int d, int E, int G, int topk_group, int k, int score_kind,
+                  float bias_scale, int32_t *ids, float *weights, float *logits_out) {
+  float *logits = logits_out ? logits_out
+                             : (float *)malloc(sizeof(float) * (size_t)T * E);
+  oracle_router_logits(x, w_r, T, d, E, logits);
+  oracle_route_from_logits(logits, bias, T, E, G, topk_group, k, score_kind,
+                           bias_scale, ids, weights, NULL);
+  if (!logits_out) free(logits);
+}
+
+/* ------------------------------------------------------------------------ */
+/* R8: dispatch permutation                                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * counts[e] = number of assignments to e ([ch15] 4.3 n_e; sum = T*k),
+ * offsets = exclusive prefix sum (E+1 entries), dest[a] = row of assignment a
+ * in the expert-contiguous buffer, src_token[dest[a]] = a / k.
+ * Returns 0, or -1 if an id is out of range.
+ */
+int oracle_dispatch(const int32_t *ids, int T, int k, int E, int32_t *counts,
+                    int32_t *offsets, int32_t *dest, int32_t *src_token) {
+  int64_t n = (int64_t)T * k;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int64_t a = 0; a < n; ++a) {
+    if (ids[a] < 0 || ids[a] >= E) return -1;
+    counts[ids[a]] += 1;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+  for (int e = 0; e < E; ++e) cursor[e] = offsets[e];
+  for (int64_t a = 0; a < n; ++a) {
+    int32_t p = cursor[ids[a]]++;
+    dest[a] = p;
+    src_token[p] = (int32_t)(a / k);
+  }
+  free(cursor);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* R9: SwiGLU expert FFN, row by row                                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For each of n rows r: expert e = row_expert[r], x = x_rows[r, :d] (bf16),
+ *   g_j = sum_i x_i Wgu[e, j, i],  u_j = sum_i x_i Wgu[e, inter + j, i]
+ *   h_j = silu(g_j) * u_j,          silu(g) = g / (1 + exp(-g))
+ *   y_c = sum_j h_j Wd[e, c, j]
+ * w_gu: [E, 2*inter, d] (rows 0..inter-1 gate, inter..2*inter-1 up),
+ * w_down: [E, d, inter]; both bf16, out x in ([par02]: gate_up fused weight).
+ * All sums in fp64.  round_h_bf16 != 0 rounds h to bf16 before the down
+ * projection (diagnostic variant only).  h_out ([n, inter]) may be NULL.
+ */
+void oracle_expert_ffn_rows(const uint16_t *x_rows, const int32_t *row_expert,
+                            int n, int d, int inter, const uint16_t *w_gu,
+                            const uint16_t *w_down, int round_h_bf16,
+                            float *h_out, float *y_out) {
+#pragma omp parallel
+  {
+    double *xv = (double *)malloc(sizeof(double) * (size_t)d);
+    double *h = (double *)malloc(sizeof(double) * (size_t)inter);
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < n; ++r) {
+      int e = row_expert[r];
+      const uint16_t *xr = x_rows + (size_t)r * d;
+      for (int i = 0; i < d; ++i) xv[i] = (double)bf16_value(xr[i]);
+      const uint16_t *wg = w_gu + (size_t)e * 2 * inter * d;
+      for (int j = 0; j < inter; ++j) {
+        const uint16_t *gr = wg + (size_t)j * d;
+        const uint16_t *ur = wg + (size_t)(inter + j) * d;
+        double g = 0.0, u = 0.0;
+        for (int i = 0; i < d; ++i) {
+          g += xv[i] * (double)bf16_value(gr[i]);
+          u += xv[i] * (double)bf16_value(ur[i]);
+        }
+        double hv = g / (1.0 + exp(-g)) * u;
+        if (round_h_bf16) hv = (double)bf16_value(bf16_round((float)hv));
+        h[j] = hv;
+        if (h_out) h_out[(size_t)r * inter + j] = (float)hv;
+      }
+      const uint16_t *wd = w_down + (size_t)e * d * inter;
+      for (int c = 0; c < d; ++c) {
+        const uint16_t *dr = wd + (size_t)c * inter;
+        double y = 0.0;
+        for (int j = 0; j < inter; ++j) y += h[j] * (double)bf16_value(dr[j]);
+        y_out[(size_t)r * d + c] = (float)y;
+      }
+    }
+    free(h);
+    free(xv);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* R10: combine                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * y[t, c] = sum_{j<k} w[t,j] * y_perm[dest[t*k+j], c]  ([trace] hop 4:
+ * y = p5 E5(x) + p27 E27(x)), fp64 sum in ascending j.
+ */
+void oracle_combine(const float *y_perm, const int32_t *dest, const float *w, int T,
+                    int k, int d, double *y) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    for (int c = 0; c < d; ++c) {
+      double acc = 0.0;
+      for (int j = 0; j < k; ++j) {
+        int32_t p = dest[(size_t)t * k + j];
+        acc += (double)w[(size_t)t * k + j] * (double)y_perm[(size_t)p * d + c];
+      }
+      y[(size_t)t * d + c] = acc;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Whole layer for a subset of tokens                                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For each listed token t: route it (R1-R7), run its k experts (R9) on its own
+ * row and combine (R10).  Tokens are independent, so any subset can be
+ * checked one by one.  y: [n_tok, d] fp64.  ids/weights: [n_tok, k].
+ */
+void oracle_layer_tokens(const uint16_t *x, const uint16_t *w_r, const float *bias,
+                         const uint16_t *w_gu, const uint16_t *w_down, int T, int d,
+                         int E, int G, int topk_group, int k, int inter,
+                         int score_kind, float bias_scale, const int32_t *tokens,
+                         int n_tok, int32_t *ids, float *weights, double *y) {
+  if (n_tok <= 0) return;
+  uint16_t *xs = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n_tok * d);
+  for (int q = 0; q < n_tok; ++q)
+    memcpy(xs + (size_t)q * d, x + (size_t)tokens[q] * d, sizeof(uint16_t) * d);
+  (void)T;
+  oracle_route(xs, w_r, bias, n_tok, d, E, G, topk_group, k, score_kind, bias_scale,
+               ids, weights, NULL);
+  int nrows = n_tok * k;
+  uint16_t *xr = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)nrows * d);
+  int32_t *re = (int32_t *)malloc(sizeof(int32_t) * (size_t)nrows);
+  float *yr = (float *)malloc(sizeof(float) * (size_t)nrows * d);
+  for (int q = 0; q < n_tok; ++q)
+    for (int j = 0; j < k; ++j) {
+      memcpy(xr + (size_t)(q * k + j) * d, xs + (size_t)q * d, sizeof(uint16_t) * d);
+      re[q * k + j] = ids[q * k + j];
+    }
+  oracle_expert_ffn_rows(xr, re, nrows, d, inter, w_gu, w_down, 0, NULL, yr);
+  for (int q = 0; q < n_tok; ++q)
+    for (int c = 0; c < d; ++c) {
+      double acc = 0.0;
+      for (int j = 0; j < k; ++j)
+        acc += (double)weights[q * k + j] * (double)yr[(size_t)(q * k + j) * d + c];
+      y[(size_t)q * d + c] = acc;
+    }
+  free(yr);
+  free(re);
+  free(xr);
+  free(xs);
+}
