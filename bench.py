@@ -1,0 +1,482 @@
+"""Benchmark of the single-GPU MoE layer (router -> dispatch -> SwiGLU experts
+-> combine) on GB300.
+
+One step = one moe_layer call over one batch of T synthetic tokens, with
+inputs resident in HBM.  Prints ONE JSON line (rank 0):
+  metric  "MoE-layer tokens/s (1 GB300); % of HBM / bf16 tensor roofline per stage"
+  value   whole-job tokens/s over the K timed steps (max time over ranks)
+  e2e     the same metric through the C-ABI call with host buffers: every step
+          copies x from pinned host memory and reads y back
+  roofline  for the dominant kernel, achieved vs the measured peak
+  stages  per-stage time and roofline fraction (CUDA events inside moe_layer)
+  cpu_baseline  the CPU oracle on a bounded token sample (host cores)
+
+Multi-GPU (torchrun, N ranks): each rank runs its own replica of the layer on
+its own batch (data-parallel replicas, no collective on the data path); the
+only collectives are the timing barrier and the max-over-ranks reduction.
+
+``--impl reference`` times the CPU oracle instead (rank 0 only), on a bounded
+token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from moe_inputs import CONFIGS, SCORE_SIGMOID_BIAS  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (1 GB300); % of HBM / bf16 tensor roofline per stage"
+UNIT = "tokens/s"
+DEFAULT_CONFIG = "few_large"
+L2_BYTES = 126 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------
+# algorithmic work (the arithmetic below is pinned by tests/test_arith_pins.py)
+# --------------------------------------------------------------------------
+
+def expert_weight_bytes(c) -> int:
+    """gate, up and down weights of one expert, bf16."""
+    return 3 * c.d * c.inter * 2
+
+
+def ffn_flops_per_row(c) -> int:
+    """gate_up (2*d*2*inter) + down (2*inter*d) per routed row."""
+    return 6 * c.d * c.inter
+
+
+def stage_bytes(c) -> dict:
+    """Algorithmic bytes of the bandwidth stages for one layer call.
+
+    router:   read x and W_r, write ids + weights
+    dispatch: read ids and x, write x_perm (bf16) and dest + src_token
+    combine:  read y_perm (fp32) and dest + weights, write y (bf16)
+    """
+    T, d, E, k = c.T, c.d, c.E, c.k
+    return {
+        "router": T * d * 2 + d * E * 2 + T * k * 8,
+        "dispatch": T * k * 4 + T * d * 2 + T * k * d * 2 + T * k * 8,
+        "combine": T * k * d * 4 + T * k * 8 + T * d * 2,
+    }
+
+
+def ffn_work(c, n_touched: int) -> dict:
+    rows = c.T * c.k
+    return {
+        "gate_up": {"flops": 4 * c.d * c.inter * rows,
+                    "bytes": n_touched * 2 * c.inter * c.d * 2},
+        "down": {"flops": 2 * c.d * c.inter * rows, "bytes": n_touched * c.d * c.inter * 2},
+    }
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(c) -> str:
+    score = "sigmoid+0.15*bias" if c.score == SCORE_SIGMOID_BIAS else "softmax"
+    g = f"E={c.E} in G={c.G} groups, topk_group={c.topk_group}" if c.G > 1 else f"E={c.E}, G=1"
+    return (f"{c.name}: T={c.T}, d={c.d}, {g}, k={c.k}, {score} router, "
+            f"SwiGLU inter={c.inter}, bf16")
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which: str):
+        setattr(self, which, time.time())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0 = getattr(self, "t_start", 0.0)
+        t1 = getattr(self, "t_end", float("inf"))
+        inside = [ln for ts, ln in self.lines if t0 <= ts <= t1 + 0.25]
+        if not inside:  # region shorter than the sampling period
+            inside = [ln for _, ln in self.lines[-3:]]
+        for ln in inside:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() in ("active", "1", "0x1"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples taken while the timed region ran
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+# distributed helpers (replicas; only timing collectives)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def job_value(tokens_per_rank: int, world: int, seconds: float, steps: int) -> float:
+    """Whole-job throughput: tokens processed by all ranks / wall time."""
+    return tokens_per_rank * world * steps / seconds
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (reported baseline and the reference arm)
+# --------------------------------------------------------------------------
+
+def time_oracle(c, host: dict, n_tokens: int, seed: int = 0) -> dict:
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(c.T, size=min(n_tokens, c.T), replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.layer_tokens(host["x"], host["w_r"], host["bias"], host["w_gate_up"],
+                        host["w_down"], c.shape(), toks)
+    dt = time.perf_counter() - t0
+    return {"value": len(toks) / dt, "seconds": dt, "tokens": int(len(toks)),
+            "cores": oracle.num_threads()}
+
+
+def oracle_sample_size(c, seconds: float, threads: int) -> int:
+    """Tokens of oracle work that take about `seconds` on `threads` cores."""
+    flops_per_token = ffn_flops_per_row(c) * c.k + 2 * c.d * c.E
+    rate = 0.6e9 * max(threads, 1)  # plain fp64 loops, order of magnitude
+    return max(1, int(seconds * rate / flops_per_token))
+
+
+def host_inputs(t: dict) -> dict:
+    from moe_inputs import bf16_bits
+    return {"x": bf16_bits(t["x"]), "w_r": bf16_bits(t["w_r"]),
+            "bias": t["bias"].detach().cpu().numpy(), "w_gate_up": bf16_bits(t["w_gate_up"]),
+            "w_down": bf16_bits(t["w_down"])}
+
+
+def run_reference(args, c):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    from moe_inputs import make_layer_tensors
+    t = make_layer_tensors(c, device="cpu", seed=0)
+    host = host_inputs(t)
+    n = oracle_sample_size(c, args.ref_step_s, oracle.num_threads())
+    for w in range(args.warmup):  # untimed warm-up steps (one token each)
+        time_oracle(c, host, 1, seed=1000 + w)
+    total_s, total_tok = 0.0, 0
+    for s in range(args.steps):
+        r = time_oracle(c, host, n, seed=s)
+        total_s += r["seconds"]
+        total_tok += r["tokens"]
+    value = total_tok / total_s
+    sample = (f"{n} of {c.T} tokens per step (seeded), full layer per token: canonical "
+              f"router, k={c.k} SwiGLU experts in fp64, combine")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(c), "T": c.T, "d": c.d, "E": c.E, "k": c.k,
+                   "inter": c.inter},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    del torch
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def run_gpu(args, c):
+    import torch
+    import dispatch_combine_gb300 as moe
+    from moe_inputs import make_layer_tensors
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the MoE path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    moe.lib()  # raises if libmoe.so is missing
+
+    t = make_layer_tensors(c, device=device, seed=0)
+    bias = t["bias"] if c.score == SCORE_SIGMOID_BIAS else None
+    shape = c.shape()
+    ws = moe.Workspace(moe.moe_workspace_size(shape), device=device)
+    y = torch.empty(c.T, c.d, dtype=torch.bfloat16, device=device)
+    counts = torch.empty(c.E, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(events=None):
+        moe.moe_layer(shape, t["x"], t["w_r"], bias, t["w_gate_up"], t["w_down"], ws, y=y,
+                      counts=counts, stage_events=events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status error during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row in evs:  # create the events before the timed region
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler.mark("t_start")
+    start.record(stream)
+    for s in range(K):
+        step(evs[s])
+    end.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("t_end")
+    barrier(world)
+    clocks = sampler.stop()
+    ms_total = start.elapsed_time(end)
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status error in the timed region")
+    ms_total_max = max_over_ranks(ms_total, world, device)
+    value = job_value(c.T, world, ms_total_max / 1000.0, K)
+
+    # per-stage durations (events recorded on the launching stream)
+    names = ["router", "dispatch", "gate_up", "down", "combine"]
+    stage_ms = {n: 0.0 for n in names}
+    for row in evs:
+        for i, n in enumerate(names):
+            stage_ms[n] += row[i].elapsed_time(row[i + 1])
+    stage_ms = {n: v / K for n, v in stage_ms.items()}
+
+    cnt = counts.cpu()
+    n_touched = int((cnt > 0).sum())
+    mean = float(cnt.float().mean())
+    r_imb = float(cnt.max()) / mean if mean > 0 else 0.0
+
+    peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"] * 1e9
+    tensor = peaks["bf16_tflops_sustained"] * 1e12
+    sb = stage_bytes(c)
+    fw = ffn_work(c, n_touched)
+    stages = {}
+    for n in ("router", "dispatch", "combine"):
+        sec = stage_ms[n] / 1000.0
+        stages[n] = {"us": stage_ms[n] * 1000.0, "bound": "hbm", "bytes": sb[n],
+                     "achieved_gbs": sb[n] / sec / 1e9, "frac": sb[n] / hbm / sec}
+    for n in ("gate_up", "down"):
+        sec = stage_ms[n] / 1000.0
+        t_hbm, t_tc = fw[n]["bytes"] / hbm, fw[n]["flops"] / tensor
+        stages[n] = {"us": stage_ms[n] * 1000.0,
+                     "bound": "tensor" if t_tc >= t_hbm else "hbm",
+                     "flops": fw[n]["flops"], "weight_bytes": fw[n]["bytes"],
+                     "achieved_tflops": fw[n]["flops"] / sec / 1e12,
+                     "achieved_gbs": fw[n]["bytes"] / sec / 1e9,
+                     "frac": max(t_hbm, t_tc) / sec}
+    ffn_sec = (stage_ms["gate_up"] + stage_ms["down"]) / 1000.0
+    ffn_bound = max((fw["gate_up"]["bytes"] + fw["down"]["bytes"]) / hbm,
+                    (fw["gate_up"]["flops"] + fw["down"]["flops"]) / tensor)
+    dominant = max(names, key=lambda n: stage_ms[n])
+    dom = stages[dominant]
+    if dom["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": dom["achieved_tflops"],
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": dom["achieved_tflops"] / peaks["bf16_tflops_sustained"],
+                "traffic": None}
+    else:
+        ach = dom.get("weight_bytes", dom.get("bytes")) / (stage_ms[dominant] / 1000.0) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": None}
+    roof["kernel"] = dominant
+    roof["peak_source"] = (f"{peak_src} ({'bf16 sustained' if roof['bound'] == 'tensor' else 'HBM copy'})")
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        x_host = t["x"].cpu().pin_memory()
+        y_host = torch.empty(c.T, c.d, dtype=torch.bfloat16).pin_memory()
+        x_dev = torch.empty_like(t["x"])
+
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.moe_layer(shape, x_dev, t["w_r"], bias, t["w_gate_up"], t["w_down"], ws, y=y)
+            y_host.copy_(y, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+        e2e = {"value": job_value(c.T, world, ms / 1000.0, args.e2e_steps), "unit": UNIT,
+               "h2d_bytes_per_step": c.T * c.d * 2, "d2h_bytes_per_step": c.T * c.d * 2,
+               "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_sample_s > 0:
+        import oracle
+        host = host_inputs(t)
+        n = oracle_sample_size(c, args.cpu_sample_s, oracle.num_threads())
+        r = time_oracle(c, host, n)
+        cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+               "sample": f"{r['tokens']} of {c.T} tokens (seeded), full layer per token, "
+                         f"{r['seconds']:.1f} s"}
+
+    l2_note = ("inputs larger than L2 (expert weights "
+               f"{c.E * expert_weight_bytes(c) / 1e9:.2f} GB)"
+               if c.E * expert_weight_bytes(c) > L2_BYTES else
+               "all inputs fit in L2 (hot-L2 timing)")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_total_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(c), "T": c.T, "d": c.d, "E": c.E, "G": c.G,
+                   "topk_group": c.topk_group, "k": c.k, "inter": c.inter,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": l2_note},
+        "roofline": roof,
+        "stages": stages,
+        "ffn": {"us": ffn_sec * 1e6, "frac": ffn_bound / ffn_sec,
+                "n_touched_experts": n_touched, "r_imbalance": r_imb},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": moe.moe_layer_launch_count(shape) * K,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default=DEFAULT_CONFIG)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-sample-s", type=float, default=15.0,
+                    help="seconds of CPU oracle work for cpu_baseline (0 = skip)")
+    ap.add_argument("--ref-step-s", type=float, default=4.0,
+                    help="seconds of oracle work per step of --impl reference")
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    c = CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, c)
+    return run_gpu(args, c)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,421 @@
+// api.cu -- the C ABI of libmoe: argument validation, workspace layout and
+// the launch sequence of each entry point.  Nothing here allocates device
+// memory; every buffer is the caller's.
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using moe::GemmProblem;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Workspace regions, in this order (each 256-byte aligned):
+//   status word | mtile_base [E+1] | dispatch chunk counts [chunks*E] |
+//   logits [T*E] f32 | h [h_rows*inter] bf16 |
+//   (layer only) ids [T*k] | w [T*k] | counts [E] | offsets [E+1] |
+//   dest [T*k] | src [T*k] | x_perm [T*k*d] bf16 | y_perm [T*k*d] f32
+struct Layout {
+  size_t status, mtile, chunk, logits, h, ids, w, counts, offsets, dest, src, x_perm, y_perm;
+  size_t end_route, end_dispatch, end_ffn, end_layer;
+};
+
+Layout make_layout(const moe_shape_t &s, int64_t h_rows) {
+  Layout L;
+  const int64_t n = static_cast<int64_t>(s.T) * s.k;
+  size_t off = 0;
+  L.status = off;
+  off = align_up(off + 4);
+  L.mtile = off;
+  off = align_up(off + 4 * static_cast<size_t>(s.E + 1));
+  L.chunk = off;
+  off = align_up(off + 4 * static_cast<size_t>(moe::dispatch_num_chunks(n)) * s.E);
+  L.end_dispatch = off;
+  L.logits = off;
+  off = align_up(off + 4 * static_cast<size_t>(s.T) * s.E);
+  L.end_route = off;
+  L.h = off;
+  off = align_up(off + 2 * static_cast<size_t>(h_rows) * s.inter);
+  L.end_ffn = off;
+  L.ids = off;
+  off = align_up(off + 4 * static_cast<size_t>(n));
+  L.w = off;
+  off = align_up(off + 4 * static_cast<size_t>(n));
+  L.counts = off;
+  off = align_up(off + 4 * static_cast<size_t>(s.E));
+  L.offsets = off;
+  off = align_up(off + 4 * static_cast<size_t>(s.E + 1));
+  L.dest = off;
+  off = align_up(off + 4 * static_cast<size_t>(n));
+  L.src = off;
+  off = align_up(off + 4 * static_cast<size_t>(n));
+  L.x_perm = off;
+  off = align_up(off + 2 * static_cast<size_t>(n) * s.d);
+  L.y_perm = off;
+  off = align_up(off + 4 * static_cast<size_t>(n) * s.d);
+  L.end_layer = off;
+  return L;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+moe_status_t check_shape(const moe_shape_t *s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->T < 0 || s->d <= 0 || s->E <= 0 || s->G <= 0 || s->k <= 0 || s->inter <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (s->E > 1024 || s->G > 32) return MOE_ERR_INVALID_ARG;
+  if (s->E % s->G != 0) return MOE_ERR_INVALID_ARG;
+  if (s->topk_group < 1 || s->topk_group > s->G) return MOE_ERR_INVALID_ARG;
+  if (s->k > 32 || s->k > s->topk_group * (s->E / s->G)) return MOE_ERR_INVALID_ARG;
+  if (s->d % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (s->score != MOE_SCORE_SIGMOID_BIAS && s->score != MOE_SCORE_SOFTMAX)
+    return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(s->T) * s->k >= (int64_t{1} << 31)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t check_ffn_shape(const moe_shape_t *s) {
+  if (s->d % 64 != 0 || s->inter % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(void *ws, size_t ws_bytes, size_t need) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                    \
+  do {                                   \
+    moe_status_t _st = (expr);           \
+    if (_st != MOE_OK) return _st;       \
+  } while (0)
+
+moe_status_t ffn_rows(const moe_shape_t *s, int32_t layout, int32_t M_max, int64_t *rows) {
+  if (layout == MOE_LAYOUT_CONTIGUOUS) {
+    *rows = static_cast<int64_t>(s->T) * s->k;
+    return MOE_OK;
+  }
+  if (layout == MOE_LAYOUT_MASKED) {
+    if (M_max < 0) return MOE_ERR_INVALID_ARG;
+    const int64_t r = static_cast<int64_t>(s->E) * M_max;
+    if (r >= (int64_t{1} << 31)) return MOE_ERR_INVALID_ARG;
+    *rows = r;
+    return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+// gate_up + SwiGLU (and optionally down) over `rows` rows with mtile_base
+// already computed in the workspace.
+moe_status_t run_gate_up(const moe_shape_t *s, int32_t layout, const void *x_in,
+                         const int32_t *seg, int32_t M_max, int64_t rows, const int32_t *mtile,
+                         const void *w_gate_up, void *h, uint32_t *status, cudaStream_t st) {
+  GemmProblem p;
+  std::memset(&p, 0, sizeof p);
+  p.E = s->E;
+  p.K = s->d;
+  p.n_out = s->inter;
+  p.layout = layout;
+  p.seg = seg;
+  p.M_max = M_max;
+  p.rows_total = rows;
+  p.mtile_base = mtile;
+  p.a = x_in;
+  p.b = w_gate_up;
+  p.b_rows = 2 * s->inter;
+  p.out = h;
+  p.status = status;
+  return cuda_status(moe::launch_gemm_gate_up_swiglu(p, st));
+}
+
+moe_status_t run_down(const moe_shape_t *s, int32_t layout, const void *h, const int32_t *seg,
+                      int32_t M_max, int64_t rows, const int32_t *mtile, const void *w_down,
+                      float *y, uint32_t *status, cudaStream_t st) {
+  GemmProblem p;
+  std::memset(&p, 0, sizeof p);
+  p.E = s->E;
+  p.K = s->inter;
+  p.n_out = s->d;
+  p.layout = layout;
+  p.seg = seg;
+  p.M_max = M_max;
+  p.rows_total = rows;
+  p.mtile_base = mtile;
+  p.a = h;
+  p.b = w_down;
+  p.b_rows = s->d;
+  p.out = y;
+  p.status = status;
+  return cuda_status(moe::launch_gemm_down(p, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_OVERFLOW: return "MOE_ERR_OVERFLOW";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_workspace_size(const moe_shape_t *shape, size_t *bytes) {
+  MOE_TRY(check_shape(shape));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*shape, static_cast<int64_t>(shape->T) * shape->k).end_layer;
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_ffn_workspace_size(const moe_shape_t *shape, int32_t layout,
+                                           int32_t M_max, size_t *bytes) {
+  MOE_TRY(check_shape(shape));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  int64_t rows = 0;
+  MOE_TRY(ffn_rows(shape, layout, M_max, &rows));
+  *bytes = make_layout(*shape, rows).end_ffn;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_ws(ws, ws_bytes, 4));
+  return cuda_status(cudaMemsetAsync(ws, 0, 4, stream));
+}
+
+moe_status_t moe_get_device_status(void *ws, size_t ws_bytes, moe_stream_t stream,
+                                   moe_status_t *status) {
+  MOE_TRY(check_ws(ws, ws_bytes, 4));
+  if (!status) return MOE_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_status_t out = MOE_OK;
+  for (int b = 31; b >= 1; --b)
+    if (word & (1u << b)) {
+      out = static_cast<moe_status_t>(b);
+      break;
+    }
+  *status = out;
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *w_r,
+                       const float *bias, int32_t *topk_ids, float *topk_w, float *logits,
+                       void *ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  if (shape->T == 0) return MOE_OK;
+  const moe_shape_t &s = *shape;
+  if (!x || !w_r || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (s.score == MOE_SCORE_SIGMOID_BIAS && !bias) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(s, 0);
+  MOE_TRY(check_ws(ws, ws_bytes, L.end_route));
+  float *lg = logits ? logits : at<float>(ws, L.logits);
+  MOE_TRY(cuda_status(moe::launch_router_logits(x, w_r, s.T, s.d, s.E, lg, stream)));
+  return cuda_status(moe::launch_router_select(lg, bias, s.T, s.E, s.G, s.topk_group, s.k,
+                                               s.score, s.bias_scale, 0, topk_ids, topk_w,
+                                               stream));
+}
+
+moe_status_t moe_route_from_logits(const moe_shape_t *shape, const float *logits,
+                                   const float *bias, int32_t *topk_ids, float *topk_w,
+                                   moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  if (shape->T == 0) return MOE_OK;
+  const moe_shape_t &s = *shape;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (s.score == MOE_SCORE_SIGMOID_BIAS && !bias) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_router_select(logits, bias, s.T, s.E, s.G, s.topk_group, s.k,
+                                               s.score, s.bias_scale, 0, topk_ids, topk_w,
+                                               stream));
+}
+
+moe_status_t moe_group_topk(const moe_shape_t *shape, const float *scores, int32_t *topk_ids,
+                            moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  if (shape->T == 0) return MOE_OK;
+  const moe_shape_t &s = *shape;
+  if (!scores || !topk_ids) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_router_select(scores, nullptr, s.T, s.E, s.G, s.topk_group,
+                                               s.k, s.score, s.bias_scale, 1, topk_ids,
+                                               nullptr, stream));
+}
+
+moe_status_t moe_dispatch(const moe_shape_t *shape, const int32_t *topk_ids, const void *x,
+                          int32_t *counts, int32_t *offsets, int32_t *src_token, int32_t *dest,
+                          void *x_perm, void *ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  if (shape->T == 0) return MOE_OK;
+  const moe_shape_t &s = *shape;
+  if (!topk_ids || !counts || !offsets || !src_token || !dest) return MOE_ERR_INVALID_ARG;
+  if (x && !x_perm) return MOE_ERR_INVALID_ARG;
+  if (x && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(s, 0);
+  MOE_TRY(check_ws(ws, ws_bytes, L.end_dispatch));
+  return cuda_status(moe::launch_dispatch(topk_ids, s.T, s.k, s.E, x, s.d, counts, offsets,
+                                          src_token, dest, x_perm, at<int32_t>(ws, L.chunk),
+                                          nullptr, at<uint32_t>(ws, L.status), stream));
+}
+
+static moe_status_t ffn_common(const moe_shape_t *shape, int32_t layout, const void *x_in,
+                               const int32_t *seg, int32_t M_max, void *ws, size_t ws_bytes,
+                               int64_t *rows, Layout *L) {
+  MOE_TRY(check_shape(shape));
+  MOE_TRY(check_ffn_shape(shape));
+  MOE_TRY(ffn_rows(shape, layout, M_max, rows));
+  if (!x_in || !seg) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_in)) return MOE_ERR_INVALID_ARG;
+  *L = make_layout(*shape, *rows);
+  return check_ws(ws, ws_bytes, L->end_ffn);
+}
+
+moe_status_t moe_expert_ffn(const moe_shape_t *shape, int32_t layout, const void *x_in,
+                            const int32_t *seg, int32_t M_max, const void *w_gate_up,
+                            const void *w_down, float *y_out, void *ws, size_t ws_bytes,
+                            moe_stream_t stream) {
+  if (shape && shape->T == 0 && layout == MOE_LAYOUT_CONTIGUOUS) return check_shape(shape);
+  int64_t rows = 0;
+  Layout L;
+  MOE_TRY(ffn_common(shape, layout, x_in, seg, M_max, ws, ws_bytes, &rows, &L));
+  if (!w_gate_up || !w_down || !y_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y_out))
+    return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  uint32_t *status = at<uint32_t>(ws, L.status);
+  int32_t *mtile = at<int32_t>(ws, L.mtile);
+  void *h = at<void>(ws, L.h);
+  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max, mtile, status, stream)));
+  MOE_TRY(run_gate_up(shape, layout, x_in, seg, M_max, rows, mtile, w_gate_up, h, status,
+                      stream));
+  return run_down(shape, layout, h, seg, M_max, rows, mtile, w_down, y_out, status, stream);
+}
+
+moe_status_t moe_expert_gate_up(const moe_shape_t *shape, int32_t layout, const void *x_in,
+                                const int32_t *seg, int32_t M_max, const void *w_gate_up,
+                                void *h_out, void *ws, size_t ws_bytes, moe_stream_t stream) {
+  if (shape && shape->T == 0 && layout == MOE_LAYOUT_CONTIGUOUS) return check_shape(shape);
+  int64_t rows = 0;
+  Layout L;
+  MOE_TRY(ffn_common(shape, layout, x_in, seg, M_max, ws, ws_bytes, &rows, &L));
+  if (!w_gate_up || !h_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_gate_up) || !aligned16(h_out)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  uint32_t *status = at<uint32_t>(ws, L.status);
+  int32_t *mtile = at<int32_t>(ws, L.mtile);
+  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max, mtile, status, stream)));
+  return run_gate_up(shape, layout, x_in, seg, M_max, rows, mtile, w_gate_up, h_out, status,
+                     stream);
+}
+
+moe_status_t moe_expert_down(const moe_shape_t *shape, int32_t layout, const void *h_in,
+                             const int32_t *seg, int32_t M_max, const void *w_down,
+                             float *y_out, void *ws, size_t ws_bytes, moe_stream_t stream) {
+  if (shape && shape->T == 0 && layout == MOE_LAYOUT_CONTIGUOUS) return check_shape(shape);
+  int64_t rows = 0;
+  Layout L;
+  MOE_TRY(ffn_common(shape, layout, h_in, seg, M_max, ws, ws_bytes, &rows, &L));
+  if (!w_down || !y_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_down) || !aligned16(y_out)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  uint32_t *status = at<uint32_t>(ws, L.status);
+  int32_t *mtile = at<int32_t>(ws, L.mtile);
+  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max, mtile, status, stream)));
+  return run_down(shape, layout, h_in, seg, M_max, rows, mtile, w_down, y_out, status, stream);
+}
+
+moe_status_t moe_combine(const moe_shape_t *shape, const float *y_perm, const int32_t *dest,
+                         const float *topk_w, void *y, moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  if (shape->T == 0) return MOE_OK;
+  if (!y_perm || !dest || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      moe::launch_combine(y_perm, dest, topk_w, shape->T, shape->k, shape->d, y, stream));
+}
+
+moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
+                       const float *bias, const void *w_gate_up, const void *w_down, void *y,
+                       int32_t *topk_ids, float *topk_w, int32_t *counts, void *ws,
+                       size_t ws_bytes, void *const *stage_events, moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  if (shape->T == 0) return MOE_OK;
+  MOE_TRY(check_ffn_shape(shape));
+  const moe_shape_t &s = *shape;
+  if (!x || !w_r || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (s.score == MOE_SCORE_SIGMOID_BIAS && !bias) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_r) || !aligned16(w_gate_up) || !aligned16(w_down) ||
+      !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t n = static_cast<int64_t>(s.T) * s.k;
+  const Layout L = make_layout(s, n);
+  MOE_TRY(check_ws(ws, ws_bytes, L.end_layer));
+  uint32_t *status = at<uint32_t>(ws, L.status);
+  int32_t *ids = topk_ids ? topk_ids : at<int32_t>(ws, L.ids);
+  float *w = topk_w ? topk_w : at<float>(ws, L.w);
+  int32_t *cnt = counts ? counts : at<int32_t>(ws, L.counts);
+  int32_t *offsets = at<int32_t>(ws, L.offsets);
+  int32_t *mtile = at<int32_t>(ws, L.mtile);
+  int32_t *dest = at<int32_t>(ws, L.dest);
+  int32_t *src = at<int32_t>(ws, L.src);
+  void *x_perm = at<void>(ws, L.x_perm);
+  float *y_perm = at<float>(ws, L.y_perm);
+  void *h = at<void>(ws, L.h);
+  float *logits = at<float>(ws, L.logits);
+
+  auto mark = [&](int i) -> moe_status_t {
+    if (!stage_events) return MOE_OK;
+    return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), stream));
+  };
+  MOE_TRY(mark(0));
+  MOE_TRY(cuda_status(moe::launch_router_logits(x, w_r, s.T, s.d, s.E, logits, stream)));
+  MOE_TRY(cuda_status(moe::launch_router_select(logits, bias, s.T, s.E, s.G, s.topk_group, s.k,
+                                                s.score, s.bias_scale, 0, ids, w, stream)));
+  MOE_TRY(mark(1));
+  MOE_TRY(cuda_status(moe::launch_dispatch(ids, s.T, s.k, s.E, x, s.d, cnt, offsets, src, dest,
+                                           x_perm, at<int32_t>(ws, L.chunk), mtile, status,
+                                           stream)));
+  MOE_TRY(mark(2));
+  MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_perm, offsets, 0, n, mtile, w_gate_up, h,
+                      status, stream));
+  MOE_TRY(mark(3));
+  MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, offsets, 0, n, mtile, w_down, y_perm, status,
+                   stream));
+  MOE_TRY(mark(4));
+  MOE_TRY(cuda_status(moe::launch_combine(y_perm, dest, w, s.T, s.k, s.d, y, stream)));
+  return mark(5);
+}
+
+int32_t moe_layer_launch_count(const moe_shape_t *shape) {
+  if (check_shape(shape) != MOE_OK || shape->T == 0) return 0;
+  // router logits, select, count, scan, scatter, gather, gate_up, down, combine
+  return 9;
+}
+
+moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, uint64_t limit_ns,
+                                       moe_stream_t stream) {
+  MOE_TRY(check_ws(ws, ws_bytes, 4));
+  return cuda_status(moe::launch_wait_selftest(at<uint32_t>(ws, 0), limit_ns, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,246 @@
+// dispatch.cu -- dispatch as a permutation into expert-contiguous rows.
+//
+// "第十五章：多节点大模型推理" section 3.4: dispatch sends each token's
+// activation to the k experts it was routed to, combine brings the results
+// back; section 4.3 counts n_e, the assignments of expert e.  On one GPU the
+// all-to-all becomes a stable counting sort of the T*k assignments
+// a = t*k + j by expert:
+//   1. per-chunk histograms (shared-memory counters, any order is fine),
+//   2. one scan over chunks and experts -> counts, offsets and every chunk's
+//      first row per expert,
+//   3. one warp per chunk walks its assignments in order; lanes with the same
+//      expert are ranked with __match_any_sync, so each assignment's row is
+//      offsets[e] + (assignments to e before it) -- stable and independent
+//      of scheduling,
+//   4. a row gather x_perm[p] = x[src_token[p]] with 16-byte vectors.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kCountThreads = 256;
+
+__global__ void __launch_bounds__(kCountThreads)
+    dispatch_count_kernel(const int32_t *__restrict__ ids, int64_t n, int E,
+                          int32_t *__restrict__ chunk_counts, uint32_t *status) {
+  extern __shared__ int hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t a0 = (int64_t)blockIdx.x * kDispatchChunk;
+  for (int q = threadIdx.x; q < kDispatchChunk; q += blockDim.x) {
+    const int64_t a = a0 + q;
+    if (a < n) {
+      const int id = ids[a];
+      if (id >= 0 && id < E)
+        atomicAdd(&hist[id], 1);
+      else
+        set_status(status, kStatusBadId);
+    }
+  }
+  __syncthreads();
+  int32_t *dst = chunk_counts + (size_t)blockIdx.x * E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) dst[e] = hist[e];
+}
+
+// exclusive scan of one int per thread over a 1024-thread block;
+// *total receives the sum of all 1024 values.
+__device__ int block_exclusive_scan(int v, int *total) {
+  __shared__ int warp_excl[32];
+  __shared__ int grand;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_excl[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = warp_excl[lane];
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += o;
+    }
+    warp_excl[lane] = wi - w;
+    if (lane == 31) grand = wi;
+  }
+  __syncthreads();
+  const int res = warp_excl[warp] + incl - v;
+  *total = grand;
+  __syncthreads();  // the shared words may be reused by the next call
+  return res;
+}
+
+// one CTA of 1024 threads, thread e owns expert e (E <= 1024)
+__global__ void __launch_bounds__(1024)
+    dispatch_scan_kernel(int32_t *__restrict__ chunk_counts, int nchunks, int E,
+                         int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                         int32_t *__restrict__ mtile_base) {
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = chunk_counts[(size_t)c * E + e];
+      chunk_counts[(size_t)c * E + e] = run;
+      run += v;
+    }
+  }
+  int total = 0;
+  const int excl = block_exclusive_scan(e < E ? run : 0, &total);
+  if (e < E) {
+    counts[e] = run;
+    offsets[e] = excl;
+  }
+  if (e == 0) offsets[E] = total;
+  if (mtile_base) {
+    int mt_total = 0;
+    const int mt = (e < E) ? (run + 127) / 128 : 0;
+    const int mt_excl = block_exclusive_scan(mt, &mt_total);
+    if (e < E) mtile_base[e] = mt_excl;
+    if (e == 0) mtile_base[E] = mt_total;
+  }
+}
+
+constexpr int kScatterWarps = 4;
+
+__global__ void __launch_bounds__(kScatterWarps * 32)
+    dispatch_scatter_kernel(const int32_t *__restrict__ ids, int64_t n, int k, int E,
+                            int64_t nchunks, const int32_t *__restrict__ chunk_base,
+                            const int32_t *__restrict__ offsets, int32_t *__restrict__ dest,
+                            int32_t *__restrict__ src_token) {
+  extern __shared__ int cursor_all[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t chunk = (int64_t)blockIdx.x * kScatterWarps + warp;
+  if (chunk >= nchunks) return;
+  int *cursor = cursor_all + warp * E;
+  for (int e = lane; e < E; e += 32) cursor[e] = chunk_base[chunk * E + e] + offsets[e];
+  __syncwarp();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int s = 0; s < kDispatchChunk / 32; ++s) {
+    const int64_t a = chunk * kDispatchChunk + s * 32 + lane;
+    int id = (a < n) ? ids[a] : -1;
+    const bool valid = id >= 0 && id < E;
+    if (!valid) id = -1;
+    const unsigned grp = __match_any_sync(0xffffffffu, id);
+    const int leader = __ffs(grp) - 1;
+    const int rank = __popc(grp & lt_mask);
+    int base = 0;
+    if (valid && lane == leader) {
+      base = cursor[id];
+      cursor[id] = base + __popc(grp);
+    }
+    base = __shfl_sync(0xffffffffu, base, leader);
+    __syncwarp();
+    if (valid) {
+      const int p = base + rank;
+      dest[a] = p;
+      src_token[p] = static_cast<int32_t>(a / k);
+    }
+  }
+}
+
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(kGatherWarps * 32)
+    dispatch_gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ src_token,
+                           const int32_t *__restrict__ offsets_end, int64_t n, int T,
+                           int vec_per_row, uint4 *__restrict__ x_perm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // rows past offsets[E] exist only if some ids were invalid; they have no
+  // source token and are left untouched
+  const int64_t rows = min(n, static_cast<int64_t>(*offsets_end));
+  for (int64_t row = (int64_t)blockIdx.x * kGatherWarps + warp; row < rows;
+       row += (int64_t)gridDim.x * kGatherWarps) {
+    const int t = src_token[row];
+    if (t < 0 || t >= T) continue;
+    const uint4 *src = x + (size_t)t * vec_per_row;
+    uint4 *dst = x_perm + (size_t)row * vec_per_row;
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
+                  d = __ldg(src + v + 96);
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = d;
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+// mtile_base from offsets (layout 0) or masked_m clamped to M_max (layout 1)
+__global__ void __launch_bounds__(1024)
+    ffn_tiles_kernel(const int32_t *__restrict__ seg, int layout, int E, int M_max,
+                     int32_t *__restrict__ mtile_base, uint32_t *status) {
+  const int e = threadIdx.x;
+  int rows = 0;
+  if (e < E) {
+    if (layout == MOE_LAYOUT_CONTIGUOUS) {
+      rows = seg[e + 1] - seg[e];
+      if (rows < 0) {
+        set_status(status, kStatusBadId);
+        rows = 0;
+      }
+    } else {
+      rows = seg[e];
+      if (rows > M_max) {
+        set_status(status, kStatusOverflow);
+        rows = M_max;
+      }
+      if (rows < 0) {
+        set_status(status, kStatusBadId);
+        rows = 0;
+      }
+    }
+  }
+  int total = 0;
+  const int excl = block_exclusive_scan((rows + 127) / 128, &total);
+  if (e < E) mtile_base[e] = excl;
+  if (e == 0) mtile_base[E] = total;
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void *x, int d,
+                            int32_t *counts, int32_t *offsets, int32_t *src_token,
+                            int32_t *dest, void *x_perm, int32_t *chunk_scratch,
+                            int32_t *mtile_base, uint32_t *status, cudaStream_t s) {
+  const int64_t n = (int64_t)T * k;
+  const int64_t nchunks = dispatch_num_chunks(n);
+  if (n == 0) return cudaSuccess;
+  dispatch_count_kernel<<<(unsigned)nchunks, kCountThreads, E * sizeof(int), s>>>(
+      ids, n, E, chunk_scratch, status);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_scratch, (int)nchunks, E, counts, offsets,
+                                          mtile_base);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const unsigned sblocks = (unsigned)((nchunks + kScatterWarps - 1) / kScatterWarps);
+  dispatch_scatter_kernel<<<sblocks, kScatterWarps * 32, kScatterWarps * E * sizeof(int), s>>>(
+      ids, n, k, E, nchunks, chunk_scratch, offsets, dest, src_token);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (x != nullptr && x_perm != nullptr) {
+    const int64_t want = (n + kGatherWarps - 1) / kGatherWarps;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    const unsigned gblocks = (unsigned)(want < cap ? want : cap);
+    dispatch_gather_kernel<<<gblocks, kGatherWarps * 32, 0, s>>>(
+        static_cast<const uint4 *>(x), src_token, offsets + E, n, T, d / 8,
+        static_cast<uint4 *>(x_perm));
+    err = cudaGetLastError();
+  }
+  return err;
+}
+
+cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max,
+                             int32_t *mtile_base, uint32_t *status, cudaStream_t s) {
+  ffn_tiles_kernel<<<1, 1024, 0, s>>>(seg, layout, E, M_max, mtile_base, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

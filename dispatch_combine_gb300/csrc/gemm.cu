@@ -1,0 +1,455 @@
+// gemm.cu -- grouped expert GEMMs on the 5th-generation tensor cores.
+//
+// The expert FFN of the MoE-TP/EP comparison on "推理INFRA方法论-02-parallelism"
+// is a grouped GEMM over experts with gate and up fused into one weight
+// ("DeepGEMM masked, gate_up fused"); experts that received no token are
+// skipped ("fused_moe" skips unhit experts), and the masked variant gives each
+// expert a padded slab with a valid-row count.  This file rebuilds that for
+// sm_103a:
+//
+//   * persistent kernel, one CTA per SM, static round-robin over tiles
+//     (expert, n-tile, m-tile) with m fastest, so the CTAs working at the same
+//     time share the expert's weight tile through L2;
+//   * warp 0 (one lane): TMA producer, 128x64 A tile + two 64-column halves of
+//     the B tile per stage, 128-byte swizzle, multi-stage mbarrier ring;
+//   * warp 1 (one lane): issues tcgen05.mma (M=128, N=BN, K=16, bf16 in, fp32
+//     accumulator in TMEM), two TMEM accumulators so the epilogue of one tile
+//     overlaps the main loop of the next;
+//   * warps 2-5: epilogue, tcgen05.ld of their 32-lane quadrant; gate_up
+//     tiles hold gate columns [0,BN/2) and the matching up columns
+//     [BN/2,BN) of the same intermediate indices, so SwiGLU
+//     h = silu(g) * u is applied in registers and only h (bf16) is written;
+//     down tiles are written as fp32.
+//
+// Every wait is bounded (MOE_ERR_TIMEOUT in the status word, then the CTA
+// drains its in-flight copies and MMAs, frees TMEM and returns).
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;  // 64 bf16 = one 128-byte swizzle row
+constexpr int kGemmThreads = 192;
+constexpr int kStageBudget = 196608;
+constexpr int kMaxE = 1024;
+
+template <int BN, bool SWIGLU>
+struct Cfg {
+  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = kStageBudget / STAGE_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BN_OUT = SWIGLU ? BN / 2 : BN;
+  static constexpr int HALF = BN / 2;  // rows of B per TMA load
+  // [A stages][B stages][barriers: full, empty, tmem_full x2, tmem_empty x2,
+  // drain][tmem slot][abort][mtile_base copy]
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int MT_OFF = MISC_OFF + 16;
+  static constexpr int SMEM_BYTES = MT_OFF + (kMaxE + 1) * 4 + 1024;  // + alignment slack
+  static_assert(STAGES >= 2, "need at least two stages");
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "bad BN");
+  static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
+};
+
+struct Tile {
+  int e, m, n;
+  int row0;        // first row of the tile in A / out
+  int rows_valid;  // valid rows in the tile (<= 128)
+};
+
+struct KArgs {
+  int E, K, n_tiles, layout, M_max, b_rows, up_off;
+  int64_t rows_total;
+  const int32_t *seg;
+  const int32_t *mtile_base;
+  void *out;
+  int64_t ldo;
+  uint32_t *status;
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ Tile decode_tile(const KArgs &a, const int32_t *mt, int u) {
+  Tile t;
+  const int q = u / a.n_tiles;
+  int lo = 0, hi = a.E - 1;  // largest e with mt[e] <= q
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (mt[mid] <= q)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  t.e = lo;
+  const int mt_e = mt[lo + 1] - mt[lo];
+  const int local = u - mt[lo] * a.n_tiles;
+  t.n = local / mt_e;
+  t.m = local - t.n * mt_e;
+  int rows, start;
+  if (a.layout == MOE_LAYOUT_CONTIGUOUS) {
+    start = a.seg[t.e];
+    rows = a.seg[t.e + 1] - start;
+  } else {
+    start = t.e * a.M_max;
+    rows = min(max(a.seg[t.e], 0), a.M_max);
+  }
+  t.row0 = start + t.m * kBM;
+  t.rows_valid = min(kBM, rows - t.m * kBM);
+  return t;
+}
+
+// Wait bounded by time only (used to drain after an abort).
+__device__ __forceinline__ bool wait_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+template <int BN, bool SWIGLU>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const KArgs args) {
+  using C = Cfg<BN, SWIGLU>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *smA = smem;
+  uint8_t *smB = smem + C::STAGES * C::A_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + C::STAGES;
+  uint64_t *tmem_full = bars + 2 * C::STAGES;
+  uint64_t *tmem_empty = tmem_full + 2;
+  uint64_t *drain = tmem_full + 4;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+  int32_t *mt = reinterpret_cast<int32_t *>(smem + C::MT_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) mt[i] = args.mtile_base[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int total = mt[args.E] * args.n_tiles;
+  if (static_cast<int>(blockIdx.x) >= total) return;  // uniform across the CTA
+
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int kblocks = args.K / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[C::STAGES];
+      bool issued[C::STAGES];
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) issued[s] = false;
+      for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x) {
+        const Tile t = decode_tile(args, mt, u);
+        int b0, b1;
+        if (SWIGLU) {
+          b0 = t.e * args.b_rows + t.n * C::HALF;
+          b1 = t.e * args.b_rows + args.up_off + t.n * C::HALF;
+        } else {
+          b0 = t.e * args.b_rows + t.n * BN;
+          b1 = b0 + C::HALF;
+        }
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
+                                 args.wait_limit_ns))
+            break;
+          uint8_t *a_dst = smA + stage * C::A_BYTES;
+          uint8_t *b_dst = smB + stage * C::B_BYTES;
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_2d(a_dst, &tmA, &full[stage], kb * kBK, t.row0);
+          tma_load_2d(b_dst, &tmB, &full[stage], kb * kBK, b0);
+          tma_load_2d(b_dst + C::HALF * 128, &tmB, &full[stage], kb * kBK, b1);
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // drain: every issued copy must have landed before the CTA exits
+      for (int s = 0; s < C::STAGES; ++s)
+        if (issued[s]) wait_drain(&full[s], issued_phase[s], args.wait_limit_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t kIdesc = mma_idesc_bf16_f32(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool any_mma = false;
+      for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x) {
+        if (!mbar_wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, args.status,
+                               args.wait_limit_ns))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.status,
+                                 args.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(smA + stage * C::A_BYTES));
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // +32 bytes along K inside the 128-byte swizzle row
+            mma_bf16_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          any_mma = true;
+          mma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tmem_full[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (any_mma) {
+        mma_commit(drain);
+        wait_drain(drain, 0, args.wait_limit_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quad = warp & 3;  // TMEM lanes quad*32 .. +31
+    const int row = quad * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const Tile t = decode_tile(args, mt, u);
+      const bool waited = mbar_wait_bounded(&tmem_full[acc], acc_phase, abort_flag,
+                                            args.status, args.wait_limit_ns);
+      // the tcgen05.ld below is warp-collective: leave together if any lane gave up
+      if (!__all_sync(0xffffffffu, waited)) break;
+      tc_fence_after();
+      const uint32_t tb =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const int64_t grow = static_cast<int64_t>(t.row0) + row;
+      // rows_total guards against caller offsets that overrun the buffers
+      const bool ok = row < t.rows_valid && grow >= 0 && grow < args.rows_total;
+      if (SWIGLU) {
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(args.out) + grow * args.ldo +
+                             static_cast<int64_t>(t.n) * C::BN_OUT;
+#pragma unroll 1
+        for (int c = 0; c < C::BN_OUT / 32; ++c) {
+          uint32_t g[32], v[32];
+          tmem_ld_32x32b_x32(tb + c * 32, g);
+          tmem_ld_32x32b_x32(tb + C::HALF + c * 32, v);
+          tmem_ld_wait();
+          tmem_regs_fence(g);
+          tmem_regs_fence(v);
+          if (ok) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+              const float u0 = __uint_as_float(v[2 * i]), u1 = __uint_as_float(v[2 * i + 1]);
+              const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+              const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+              packed[i] = pack_bf16x2(h0, h1);
+            }
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                 packed[4 * i + 3]);
+          }
+        }
+      } else {
+        float *dst = static_cast<float *>(args.out) + grow * args.ldo +
+                     static_cast<int64_t>(t.n) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + c * 32, v);
+          tmem_ld_wait();
+          tmem_regs_fence(v);
+          if (ok) {
+            float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// bounded-wait self test: one thread waits on a barrier nobody arrives on
+// ---------------------------------------------------------------------------
+__global__ void wait_selftest_kernel(uint32_t *status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, &abort_flag, status, limit_ns);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D bf16 tensor [rows, inner] row-major; box = box_rows x 64 elements,
+// 128-byte swizzle, out-of-bounds rows read as zero.
+bool make_tmap(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+               uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool SWIGLU>
+cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
+  using C = Cfg<BN, SWIGLU>;
+  CUtensorMap tmA, tmB;
+  if (!make_tmap(&tmA, p.a, static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.rows_total),
+                 kBM))
+    return cudaErrorInvalidValue;
+  if (!make_tmap(&tmB, p.b, static_cast<uint64_t>(p.K),
+                 static_cast<uint64_t>(p.E) * static_cast<uint64_t>(p.b_rows), C::HALF))
+    return cudaErrorInvalidValue;
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BN, SWIGLU>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  KArgs a;
+  a.E = p.E;
+  a.K = p.K;
+  a.n_tiles = p.n_out / C::BN_OUT;
+  a.layout = p.layout;
+  a.M_max = p.M_max;
+  a.b_rows = p.b_rows;
+  a.up_off = up_off;
+  a.seg = p.seg;
+  a.mtile_base = p.mtile_base;
+  a.out = p.out;
+  a.ldo = p.n_out;
+  a.rows_total = p.rows_total;
+  a.status = p.status;
+  a.wait_limit_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitLimitNs;
+  grouped_gemm_kernel<BN, SWIGLU><<<num_sms(), kGemmThreads, C::SMEM_BYTES, s>>>(tmA, tmB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  static int cache[64] = {0};
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 1;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s) {
+  // p.n_out = inter, p.b_rows = 2*inter, K = d
+  if (p.n_out % 128 == 0) return run_gemm<256, true>(p, p.n_out, s);
+  if (p.n_out % 64 == 0) return run_gemm<128, true>(p, p.n_out, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s) {
+  // p.n_out = d, p.b_rows = d, K = inter
+  if (p.n_out % 256 == 0) return run_gemm<256, false>(p, 0, s);
+  if (p.n_out % 128 == 0) return run_gemm<128, false>(p, 0, s);
+  if (p.n_out % 64 == 0) return run_gemm<64, false>(p, 0, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_wait_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,61 @@
+// kernels.h -- host-side launchers of the MoE kernels (internal to libmoe).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// router.cu
+cudaError_t launch_router_logits(const void *x, const void *w_r, int T, int d, int E,
+                                 float *logits, cudaStream_t s);
+// mode 0: scores from logits (score kind); mode 1: the input already holds
+// selection scores (group top-k only; weights not written).
+cudaError_t launch_router_select(const float *logits, const float *bias, int T, int E, int G,
+                                 int topk_group, int k, int score, float bias_scale, int mode,
+                                 int32_t *ids, float *weights, cudaStream_t s);
+
+// dispatch.cu
+constexpr int kDispatchChunk = 512;
+inline int64_t dispatch_num_chunks(int64_t n) {
+  return (n + kDispatchChunk - 1) / kDispatchChunk;
+}
+cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void *x, int d,
+                            int32_t *counts, int32_t *offsets, int32_t *src_token,
+                            int32_t *dest, void *x_perm, int32_t *chunk_scratch,
+                            int32_t *mtile_base, uint32_t *status, cudaStream_t s);
+// mtile_base[e] = sum_{e'<e} ceil(M_e'/128) for the contiguous (seg = offsets)
+// or masked (seg = masked_m, clamped to M_max) layout.
+cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max,
+                             int32_t *mtile_base, uint32_t *status, cudaStream_t s);
+
+// combine.cu
+cudaError_t launch_combine(const float *y_perm, const int32_t *dest, const float *w, int T,
+                           int k, int d, void *y, cudaStream_t s);
+
+// gemm.cu
+struct GemmProblem {
+  int E;
+  int K;                     // reduction length (d for gate_up, inter for down)
+  int n_out;                 // output columns (inter for gate_up, d for down)
+  int layout;                // 0 contiguous, 1 masked
+  const int32_t *seg;        // offsets [E+1] or masked_m [E]
+  int M_max;                 // masked slab rows
+  int64_t rows_total;        // rows of A / out (T*k or E*M_max)
+  const int32_t *mtile_base; // [E+1]
+  const void *a;             // [rows_total, K] bf16
+  const void *b;             // [E, b_rows, K] bf16
+  int b_rows;                // 2*inter (gate_up) or d (down)
+  void *out;                 // bf16 h [rows, inter] or fp32 y [rows, d]
+  uint32_t *status;
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s);
+cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s);
+// one CTA waits on an mbarrier nobody completes, bounded by limit_ns
+cudaError_t launch_wait_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,239 @@
+/*
+ * moe.h -- C ABI of the single-GPU MoE layer path for GB300 (sm_103a).
+ *
+ * The path ("gating -> dispatch -> experts -> combine") is the runtime MoE
+ * execution path described in "第十五章：多节点大模型推理" section 4.1/4.3 and
+ * in the token trace page, hop 4 ("dispatch to two experts"), with the
+ * group-limited routing of the "ep-deploy" handbook page (section "EPLB 与路由
+ * 约束") and the gate_up-fused, masked expert GEMM of the MoE-TP/EP comparison
+ * on "推理INFRA方法论-02-parallelism".  On one GPU the all-to-all of those pages
+ * becomes a permutation into expert-contiguous rows and back.
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *    the shape struct and the `bytes`/`status` out-parameters, which are host
+ *    pointers.  The library never allocates or frees device memory.
+ *  - Tensors are dense and row-major.  bf16 means IEEE bfloat16 (uint16 bit
+ *    pattern).  Pointers to bf16/fp32 tensors must be 16-byte aligned; the
+ *    workspace must be 256-byte aligned.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream) and runs asynchronously.  Host-side validation returns a status
+ *    synchronously before anything is enqueued; MOE_ERR_CUDA means a launch
+ *    failed (cudaGetLastError()).
+ *  - Errors detected on the device (an expert id out of range, masked_m >
+ *    M_max, a bounded wait that timed out) are OR-ed into a status word at
+ *    the start of the workspace and read with moe_get_device_status().
+ *    Kernels never trap; a timed-out wait returns and leaves the context
+ *    usable.
+ *  - T == 0 is a valid no-op returning MOE_OK.
+ *  - Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
+
+/* Router score function. */
+typedef enum {
+  /* s'_e = sigmoid(l_e) + bias_scale * bias_e selects; weights are the
+   * selected sigmoid(l) renormalised to sum 1 (bias only selects). */
+  MOE_SCORE_SIGMOID_BIAS = 0,
+  /* softmax over the logits; the top-k of softmax equals the top-k of the
+   * logits; weights are the selected softmax values renormalised. */
+  MOE_SCORE_SOFTMAX = 1
+} moe_score_t;
+
+/* Problem statement: T tokens of hidden size d, E experts in G equal groups,
+ * keep topk_group groups, route each token to k experts; each expert is a
+ * SwiGLU FFN of width inter. */
+typedef struct {
+  int32_t T;
+  int32_t d;
+  int32_t E;
+  int32_t G;
+  int32_t topk_group;
+  int32_t k;
+  int32_t inter;
+  int32_t score;    /* moe_score_t */
+  float bias_scale; /* 0.15 in the routing simulation of the ep-deploy page */
+} moe_shape_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misalignment */
+  MOE_ERR_UNSUPPORTED = 2, /* valid shape the kernels do not handle */
+  MOE_ERR_WORKSPACE = 3,   /* workspace too small or misaligned */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+  MOE_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out */
+  MOE_ERR_OVERFLOW = 6     /* masked_m[e] > M_max (rows beyond are ignored) */
+} moe_status_t;
+
+typedef enum { MOE_LAYOUT_CONTIGUOUS = 0, MOE_LAYOUT_MASKED = 1 } moe_layout_t;
+
+/* Shape limits (MOE_ERR_INVALID_ARG beyond them unless noted):
+ *   E % G == 0, 1 <= topk_group <= G <= 32, 1 <= k <= min(32, topk_group*E/G),
+ *   E <= 1024, d % 8 == 0, T*k < 2^31.
+ * Expert FFN additionally needs d % 64 == 0 and inter % 64 == 0
+ * (MOE_ERR_UNSUPPORTED otherwise). */
+
+/* Human-readable name of a status. Never NULL. */
+const char *moe_status_string(moe_status_t status);
+
+/* Bytes of workspace that moe_route, moe_dispatch, moe_expert_ffn
+ * (contiguous layout) and moe_layer need for `shape`. */
+moe_status_t moe_workspace_size(const moe_shape_t *shape, size_t *bytes);
+
+/* Bytes of workspace for moe_expert_ffn / moe_expert_gate_up /
+ * moe_expert_down with the given layout (M_max is ignored for the contiguous
+ * layout, where the rows are T*k). */
+moe_status_t moe_expert_ffn_workspace_size(const moe_shape_t *shape, int32_t layout,
+                                           int32_t M_max, size_t *bytes);
+
+/* Clears the device status word at the start of a fresh workspace (async). */
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronises `stream`, returns the OR of device-side errors recorded in the
+ * workspace since the last call (as the highest-numbered status found), and
+ * clears the word.  The only entry point that blocks the host. */
+moe_status_t moe_get_device_status(void *ws, size_t ws_bytes, moe_stream_t stream,
+                                   moe_status_t *status);
+
+/*
+ * Gating ("第十五章" 4.1: the model's gating picks the top-k logical experts
+ * from the hidden state; "ep-deploy" page: group-limited top-k).
+ *   x      [T,d]  bf16     token hidden states
+ *   w_r    [d,E]  bf16     router weight
+ *   bias   [E]    fp32     per-expert selection bias (NULL for softmax)
+ *   topk_ids [T,k] int32   out: experts, descending selection score, ties to
+ *                          the lower index
+ *   topk_w   [T,k] fp32    out: combine weights (sum to 1 per token)
+ *   logits   [T,E] fp32    out, optional (NULL): router logits
+ * Logits are fp32 sums of exact bf16 products in a fixed order (lane l of 32
+ * owns the 8-element chunks c with c mod 32 == l and sums them in order; the
+ * 32 lane sums are combined by an xor butterfly), and sigmoid/exp use a
+ * fixed Cody-Waite + Taylor evaluation, so ids are reproducible bit-exactly.
+ */
+moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *w_r,
+                       const float *bias, int32_t *topk_ids, float *topk_w,
+                       float *logits, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * The scoring + group-limited selection half of moe_route on given logits
+ * [T,E] fp32 (same outputs).  Needs no workspace.
+ */
+moe_status_t moe_route_from_logits(const moe_shape_t *shape, const float *logits,
+                                   const float *bias, int32_t *topk_ids, float *topk_w,
+                                   moe_stream_t stream);
+
+/*
+ * Group-limited top-k alone ("ep-deploy" page, section "EPLB 与路由约束": a
+ * group's score is the sum of its two best expert scores, the topk_group best
+ * groups are kept, the k best experts inside them are chosen) on given fp32
+ * scores [T,E].  Group sums are fp32.  Ties go to the lower index.
+ */
+moe_status_t moe_group_topk(const moe_shape_t *shape, const float *scores,
+                            int32_t *topk_ids, moe_stream_t stream);
+
+/*
+ * Dispatch as a permutation ("第十五章" 3.4: dispatch sends each token's
+ * activation to its k experts; single GPU: expert-contiguous rows).
+ *   topk_ids [T,k] int32  expert of each assignment a = t*k + j
+ *   x        [T,d] bf16   (may be NULL to compute indices only)
+ *   counts   [E]   int32  out: assignments per expert (sum T*k)
+ *   offsets  [E+1] int32  out: exclusive prefix sum of counts
+ *   src_token [T*k] int32 out: token of each permuted row
+ *   dest     [T*k] int32  out: permuted row of each assignment
+ *   x_perm   [T*k,d] bf16 out (ignored if x is NULL): x_perm[dest[a]] = x[a/k]
+ * Order inside an expert is stable in a (a counting sort); no atomics-order
+ * dependence.  Ids outside [0,E) set MOE_ERR_INVALID_ARG on the device.
+ */
+moe_status_t moe_dispatch(const moe_shape_t *shape, const int32_t *topk_ids,
+                          const void *x, int32_t *counts, int32_t *offsets,
+                          int32_t *src_token, int32_t *dest, void *x_perm, void *ws,
+                          size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Expert SwiGLU FFN as grouped GEMMs on the tensor cores (the "DeepGEMM
+ * masked, gate_up fused" kernel of the MoE-TP/EP comparison page, rebuilt for
+ * tcgen05): per expert e, h = silu(X_e Wg_e^T) * (X_e Wu_e^T) (bf16), then
+ * y = h Wd_e^T (fp32).
+ *   layout MOE_LAYOUT_CONTIGUOUS: x_in [T*k, d] bf16, rows of expert e are
+ *       [offsets[e], offsets[e+1]) (seg = offsets, [E+1]); y_out [T*k, d].
+ *   layout MOE_LAYOUT_MASKED: x_in [E, M_max, d] bf16, rows [0, masked_m[e])
+ *       of slab e are valid (seg = masked_m, [E]); y_out [E, M_max, d]; rows
+ *       past masked_m are not written.
+ *   w_gate_up [E, 2*inter, d] bf16 (rows 0..inter-1 gate, inter.. up)
+ *   w_down    [E, d, inter] bf16
+ *   y_out     fp32
+ * Experts with no rows cost nothing (their weights are not read).
+ */
+moe_status_t moe_expert_ffn(const moe_shape_t *shape, int32_t layout, const void *x_in,
+                            const int32_t *seg, int32_t M_max, const void *w_gate_up,
+                            const void *w_down, float *y_out, void *ws, size_t ws_bytes,
+                            moe_stream_t stream);
+
+/* First half of moe_expert_ffn: h_out = silu(X Wg^T) * (X Wu^T), bf16,
+ * [rows, inter] in the same layout as x_in. */
+moe_status_t moe_expert_gate_up(const moe_shape_t *shape, int32_t layout,
+                                const void *x_in, const int32_t *seg, int32_t M_max,
+                                const void *w_gate_up, void *h_out, void *ws,
+                                size_t ws_bytes, moe_stream_t stream);
+
+/* Second half: y_out = h Wd^T, fp32, [rows, d] in the same layout as h_in. */
+moe_status_t moe_expert_down(const moe_shape_t *shape, int32_t layout, const void *h_in,
+                             const int32_t *seg, int32_t M_max, const void *w_down,
+                             float *y_out, void *ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
+/*
+ * Combine (token trace page, hop 4: y = p5 E5(x) + p27 E27(x)):
+ *   y[t] = sum_{j<k} topk_w[t,j] * y_perm[dest[t*k+j]]   (fp32, j ascending)
+ *   y_perm [T*k, d] fp32, dest [T*k] int32, topk_w [T,k] fp32, y [T,d] bf16.
+ */
+moe_status_t moe_combine(const moe_shape_t *shape, const float *y_perm,
+                         const int32_t *dest, const float *topk_w, void *y,
+                         moe_stream_t stream);
+
+/*
+ * The whole layer: route -> dispatch -> gate_up+SwiGLU -> down -> combine,
+ * all on `stream`, no host synchronisation, intermediates in the workspace.
+ *   x [T,d] bf16, w_r [d,E] bf16, bias [E] fp32 (NULL for softmax),
+ *   w_gate_up [E,2*inter,d] bf16, w_down [E,d,inter] bf16, y [T,d] bf16 out,
+ *   topk_ids [T,k] int32 / topk_w [T,k] fp32 / counts [E] int32: optional
+ *   copies of the routing and the per-expert counts (NULL to skip).
+ *   stage_events: NULL, or 6 cudaEvent_t handles (host array) recorded on
+ *   `stream` before the router, after the router, after dispatch, after the
+ *   gate_up GEMM, after the down GEMM and after combine (per-stage timing).
+ */
+moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
+                       const float *bias, const void *w_gate_up, const void *w_down,
+                       void *y, int32_t *topk_ids, float *topk_w, int32_t *counts,
+                       void *ws, size_t ws_bytes, void *const *stage_events,
+                       moe_stream_t stream);
+
+/*
+ * Number of kernels moe_layer launches per call for this shape (for launch
+ * accounting).
+ */
+int32_t moe_layer_launch_count(const moe_shape_t *shape);
+
+/*
+ * Self-test of the bounded wait used by every device-side spin: launches one
+ * CTA that waits on a barrier nobody completes, gives up after `limit_ns`
+ * nanoseconds and records MOE_ERR_TIMEOUT in the workspace status word.
+ */
+moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, uint64_t limit_ns,
+                                       moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,144 @@
+"""GPU expert FFN (tcgen05 grouped GEMMs, SwiGLU fused) against the oracle's
+fp64 FFN: contiguous and masked layouts, ragged expert sizes spanning
+several 128-row tiles, every N-tile variant, empty experts."""
+import numpy as np
+import pytest
+import torch
+
+import dispatch_combine_gb300 as moe
+import oracle
+from tests.gpu_common import bits, check_close, ensure_lib
+
+pytestmark = pytest.mark.gpu
+
+
+def _weights(E, d, inter, seed):
+    # scaled so that g, u, h and y are O(1) and the absolute bound bites
+    g = torch.Generator().manual_seed(seed)
+    w_gu = (torch.randn(E, 2 * inter, d, generator=g) * (1.5 / d ** 0.5)).to(torch.bfloat16)
+    w_down = (torch.randn(E, d, inter, generator=g) * (2.0 / inter ** 0.5)).to(torch.bfloat16)
+    return w_gu, w_down
+
+
+def _shape(E, d, inter, T=1, k=1):
+    return dict(T=T, d=d, E=E, G=1, topk_group=1, k=k, inter=inter, score=1, bias_scale=0.15)
+
+
+def _contiguous_case(counts, d, inter, seed):
+    E = len(counts)
+    rows = int(sum(counts))
+    g = torch.Generator().manual_seed(seed + 1)
+    x = torch.randn(rows, d, generator=g).to(torch.bfloat16)
+    offsets = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32)
+    row_e = np.repeat(np.arange(E), counts).astype(np.int32)
+    return x, offsets, row_e
+
+
+@pytest.mark.parametrize("counts,d,inter", [
+    ([0, 1, 127, 128, 129, 300], 256, 128),   # gate_up BN=256, down BN=256
+    ([5, 0, 0, 260], 512, 64),                # gate_up BN=128 (inter 64)
+    ([130, 7], 192, 128),                     # down BN=64
+    ([40, 300, 1], 384, 192),                 # down BN=128, gate_up BN=128
+    ([3, 200], 4096, 1024),                   # long K in both GEMMs
+])
+def test_ffn_contiguous(counts, d, inter):
+    ensure_lib()
+    E = len(counts)
+    w_gu, w_down = _weights(E, d, inter, seed=d + inter)
+    x, offsets, row_e = _contiguous_case(counts, d, inter, seed=d)
+    rows = x.shape[0]
+    shape = _shape(E, d, inter, T=rows, k=1)
+    ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    y = moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_CONTIGUOUS, x.cuda(), offsets.cuda(), 0,
+                           w_gu.cuda(), w_down.cuda(), ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    ref = oracle.expert_ffn_rows(bits(x), row_e, bits(w_gu), bits(w_down))
+    check_close(y.cpu().numpy(), ref, bf16_output=False, what="y")
+    # with h rounded to bf16 (as the GPU stores it) the match is much tighter
+    ref_h = oracle.expert_ffn_rows(bits(x), row_e, bits(w_gu), bits(w_down), round_h_bf16=True)
+    err = np.abs(y.cpu().numpy() - ref_h).max() / max(np.abs(ref_h).max(), 1e-30)
+    assert err < 2e-2, err
+
+
+def test_gate_up_alone_matches_oracle_h():
+    ensure_lib()
+    counts = [17, 129, 0, 256]
+    E, d, inter = 4, 512, 256
+    w_gu, w_down = _weights(E, d, inter, seed=3)
+    x, offsets, row_e = _contiguous_case(counts, d, inter, seed=4)
+    shape = _shape(E, d, inter, T=x.shape[0], k=1)
+    ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    h = moe.moe_expert_gate_up(shape, moe.MOE_LAYOUT_CONTIGUOUS, x.cuda(), offsets.cuda(), 0,
+                               w_gu.cuda(), ws)
+    _, ref_h = oracle.expert_ffn_rows(bits(x), row_e, bits(w_gu), bits(w_down), return_h=True)
+    check_close(h.float().cpu().numpy(), ref_h, bf16_output=True, what="h")
+    # down alone on the GPU's own h equals the oracle's down projection of it
+    y = moe.moe_expert_down(shape, moe.MOE_LAYOUT_CONTIGUOUS, h, offsets.cuda(), 0,
+                            w_down.cuda(), ws)
+    hd = h.float().cpu().numpy().astype(np.float64)
+    wd = w_down.float().numpy().astype(np.float64)
+    ref_y = np.stack([wd[row_e[r]] @ hd[r] for r in range(hd.shape[0])])
+    check_close(y.cpu().numpy(), ref_y, bf16_output=False, what="y(down)")
+    assert np.abs(y.cpu().numpy() - ref_y).max() < 1e-3
+
+
+@pytest.mark.parametrize("masked_m,M_max,d,inter", [
+    ([0, 5, 256, 130], 256, 256, 128),
+    ([64, 1, 128], 128, 512, 64),
+])
+def test_ffn_masked(masked_m, M_max, d, inter):
+    ensure_lib()
+    E = len(masked_m)
+    w_gu, w_down = _weights(E, d, inter, seed=9)
+    g = torch.Generator().manual_seed(10)
+    x = torch.randn(E, M_max, d, generator=g).to(torch.bfloat16)
+    shape = _shape(E, d, inter)
+    ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_MASKED, M_max))
+    y = torch.full((E, M_max, d), float("nan"), dtype=torch.float32, device="cuda")
+    mm = torch.tensor(masked_m, dtype=torch.int32)
+    moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_MASKED, x.cuda(), mm.cuda(), M_max, w_gu.cuda(),
+                       w_down.cuda(), ws, y_out=y)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    yh = y.cpu().numpy()
+    xb = bits(x)
+    for e in range(E):
+        m = masked_m[e]
+        assert np.all(np.isnan(yh[e, m:])), "rows past masked_m were written"
+        if m == 0:
+            continue
+        ref = oracle.expert_ffn_rows(xb[e, :m], np.full(m, e, np.int32), bits(w_gu),
+                                     bits(w_down))
+        check_close(yh[e, :m], ref, bf16_output=False, what=f"expert {e}")
+
+
+def test_ffn_masked_overflow_is_flagged_and_clamped():
+    ensure_lib()
+    E, M_max, d, inter = 2, 128, 256, 128
+    w_gu, w_down = _weights(E, d, inter, seed=11)
+    x = torch.randn(E, M_max, d, generator=torch.Generator().manual_seed(12)).to(torch.bfloat16)
+    shape = _shape(E, d, inter)
+    ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_MASKED, M_max))
+    mm = torch.tensor([M_max + 50, 3], dtype=torch.int32)
+    y = moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_MASKED, x.cuda(), mm.cuda(), M_max,
+                           w_gu.cuda(), w_down.cuda(), ws)
+    assert moe.moe_get_device_status(ws) == 6  # MOE_ERR_OVERFLOW
+    ref = oracle.expert_ffn_rows(bits(x)[0], np.zeros(M_max, np.int32), bits(w_gu),
+                                 bits(w_down))
+    check_close(y[0].cpu().numpy(), ref, bf16_output=False, what="clamped expert")
+
+
+def test_ffn_all_experts_empty_writes_nothing():
+    ensure_lib()
+    E, d, inter = 3, 256, 128
+    w_gu, w_down = _weights(E, d, inter, seed=13)
+    shape = _shape(E, d, inter, T=4, k=1)
+    x = torch.randn(4, d).to(torch.bfloat16).cuda()
+    offsets = torch.zeros(E + 1, dtype=torch.int32).cuda()
+    ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    y = torch.full((4, d), 7.0, dtype=torch.float32, device="cuda")
+    moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_CONTIGUOUS, x, offsets, 0, w_gu.cuda(),
+                       w_down.cuda(), ws, y_out=y)
+    assert moe.moe_get_device_status(ws) == 0
+    assert torch.all(y == 7.0)

@@ -1,0 +1,100 @@
+"""GPU router (moe_route / moe_route_from_logits / moe_group_topk) against the
+oracle: logits and ids bit-exact, weights within 1e-6 relative."""
+import numpy as np
+import pytest
+import torch
+
+import dispatch_combine_gb300 as moe
+import oracle
+from moe_inputs import CONFIGS, SCORE_SIGMOID_BIAS, SCORE_SOFTMAX
+from tests.gpu_common import ensure_lib, host_bits, layer_inputs
+from tests.test_oracle_router import page_sim_scores, placement_stats, _golden_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _route_gpu(cfg, x, w_r, bias):
+    ws = moe.Workspace(moe.moe_workspace_size(cfg.shape()))
+    ids, w, logits = moe.moe_route(cfg.shape(), x, w_r,
+                                   bias if cfg.score == SCORE_SIGMOID_BIAS else None, ws,
+                                   want_logits=True)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    return ids.cpu().numpy(), w.cpu().numpy(), logits.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "few_large", "decode", "prefill"])
+def test_route_bit_exact_full_size(name):
+    ensure_lib()
+    cfg = CONFIGS[name]
+    t = layer_inputs(name)
+    ids, w, logits = _route_gpu(cfg, t["x"], t["w_r"], t["bias"])
+    x_h, wr_h = host_bits(name, "x"), host_bits(name, "w_r")
+    ref_logits = oracle.router_logits(x_h, wr_h)
+    assert np.array_equal(logits.view(np.uint32), ref_logits.view(np.uint32))
+    ref_ids, ref_w, _ = oracle.route_from_logits(ref_logits, t["bias"].cpu().numpy(), cfg.G,
+                                                 cfg.topk_group, cfg.k, cfg.score,
+                                                 cfg.bias_scale)
+    assert np.array_equal(ids, ref_ids)
+    assert np.all(np.abs(w - ref_w) <= 1e-6 * np.abs(ref_w))
+    # invariants: k distinct experts from at most topk_group groups, sum 1
+    gs = cfg.E // cfg.G
+    for r in range(0, cfg.T, max(1, cfg.T // 512)):
+        assert len(set(ids[r].tolist())) == cfg.k
+        assert len(set((ids[r] // gs).tolist())) <= cfg.topk_group
+    assert np.all(np.abs(w.astype(np.float64).sum(1) - 1.0) <= cfg.k * 2.0 ** -23)
+
+
+def _rand_logits(T, E, seed, kind):
+    g = np.random.default_rng(seed)
+    if kind == "normal":
+        return g.normal(0, 3, (T, E)).astype(np.float32)
+    if kind == "ties":
+        return (np.round(g.normal(0, 2, (T, E)) * 2) / 2).astype(np.float32)
+    if kind == "const":
+        return np.full((T, E), 0.25, dtype=np.float32)
+    if kind == "saturated":
+        return g.normal(0, 40, (T, E)).astype(np.float32)
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("T,E,G,tg,k,score,kind", [
+    (1, 256, 8, 4, 8, SCORE_SIGMOID_BIAS, "normal"),
+    (1000, 256, 8, 4, 8, SCORE_SIGMOID_BIAS, "ties"),
+    (333, 256, 8, 4, 8, SCORE_SIGMOID_BIAS, "const"),
+    (500, 256, 8, 4, 8, SCORE_SIGMOID_BIAS, "saturated"),
+    (257, 16, 4, 2, 2, SCORE_SIGMOID_BIAS, "ties"),
+    (100, 48, 3, 2, 5, SCORE_SIGMOID_BIAS, "normal"),
+    (129, 1024, 32, 7, 32, SCORE_SIGMOID_BIAS, "normal"),
+    (64, 64, 8, 2, 16, SCORE_SIGMOID_BIAS, "ties"),       # k = all eligible experts
+    (300, 8, 1, 1, 2, SCORE_SOFTMAX, "normal"),
+    (300, 8, 1, 1, 2, SCORE_SOFTMAX, "ties"),
+    (77, 96, 1, 1, 6, SCORE_SOFTMAX, "saturated"),
+])
+def test_route_from_logits_edge_cases(T, E, G, tg, k, score, kind):
+    ensure_lib()
+    logits = _rand_logits(T, E, T + E, kind)
+    bias = np.random.default_rng(E).normal(0, 1, E).astype(np.float32)
+    if kind == "ties":
+        bias = np.round(bias * 4) / 4
+    shape = dict(T=T, d=8, E=E, G=G, topk_group=tg, k=k, score=score, inter=64,
+                 bias_scale=0.15)
+    ids, w = moe.moe_route_from_logits(shape, torch.from_numpy(logits).cuda(),
+                                       torch.from_numpy(bias).cuda())
+    ref_ids, ref_w, _ = oracle.route_from_logits(logits, bias, G, tg, k, score, 0.15)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    got_w = w.cpu().numpy()
+    assert np.all(np.abs(got_w - ref_w) <= 1e-6 * np.abs(ref_w))
+
+
+def test_group_topk_reproduces_ep_deploy_simulation():
+    ensure_lib()
+    s32 = page_sim_scores().astype(np.float32)
+    shape = dict(T=s32.shape[0], d=8, E=256, G=8, topk_group=4, k=8, inter=64,
+                 score=SCORE_SIGMOID_BIAS, bias_scale=0.15)
+    ids = moe.moe_group_topk(shape, torch.from_numpy(s32).cuda()).cpu().numpy()
+    ref = oracle.select(s32.astype(np.float64), 8, 4, 8, True)
+    assert np.array_equal(ids, ref)
+    for nodes, gpus, place, ratio, ntok in _golden_rows():
+        if place == "by_number":
+            assert placement_stats(ids, 256, nodes, gpus) == (ratio, ntok)
