@@ -13,11 +13,23 @@ pytestmark = pytest.mark.gpu
 
 
 def _weights(E, d, inter, seed):
-    # scaled so that g, u, h and y are O(1) and the absolute bound bites
+    # g, u ~ N(0, 1) and y of order 1, so that the absolute bound is meaningful
     g = torch.Generator().manual_seed(seed)
-    w_gu = (torch.randn(E, 2 * inter, d, generator=g) * (1.5 / d ** 0.5)).to(torch.bfloat16)
-    w_down = (torch.randn(E, d, inter, generator=g) * (2.0 / inter ** 0.5)).to(torch.bfloat16)
+    w_gu = (torch.randn(E, 2 * inter, d, generator=g) / d ** 0.5).to(torch.bfloat16)
+    w_down = (torch.randn(E, d, inter, generator=g) / inter ** 0.5).to(torch.bfloat16)
     return w_gu, w_down
+
+
+def check_ffn(got, x_bits, row_e, w_gu_bits, w_down_bits, what):
+    """Stated tolerance against the fp64 oracle, plus a much tighter relative
+    Frobenius bound against the oracle variant that rounds h to bf16 (the
+    GPU's storage format for h): what remains there is only fp32
+    accumulation order and the rare bf16 rounding flips of h."""
+    ref = oracle.expert_ffn_rows(x_bits, row_e, w_gu_bits, w_down_bits)
+    check_close(got, ref, bf16_output=False, what=what)
+    ref_hb = oracle.expert_ffn_rows(x_bits, row_e, w_gu_bits, w_down_bits, round_h_bf16=True)
+    rel = np.linalg.norm(got - ref_hb) / max(np.linalg.norm(ref_hb), 1e-30)
+    assert rel <= 1e-3, f"{what}: rel Frobenius vs h-in-bf16 oracle {rel:.3e}"
 
 
 def _shape(E, d, inter, T=1, k=1):
@@ -53,12 +65,7 @@ def test_ffn_contiguous(counts, d, inter):
                            w_gu.cuda(), w_down.cuda(), ws)
     torch.cuda.synchronize()
     assert moe.moe_get_device_status(ws) == 0
-    ref = oracle.expert_ffn_rows(bits(x), row_e, bits(w_gu), bits(w_down))
-    check_close(y.cpu().numpy(), ref, bf16_output=False, what="y")
-    # with h rounded to bf16 (as the GPU stores it) the match is much tighter
-    ref_h = oracle.expert_ffn_rows(bits(x), row_e, bits(w_gu), bits(w_down), round_h_bf16=True)
-    err = np.abs(y.cpu().numpy() - ref_h).max() / max(np.abs(ref_h).max(), 1e-30)
-    assert err < 2e-2, err
+    check_ffn(y.cpu().numpy(), bits(x), row_e, bits(w_gu), bits(w_down), "y")
 
 
 def test_gate_up_alone_matches_oracle_h():
@@ -108,9 +115,8 @@ def test_ffn_masked(masked_m, M_max, d, inter):
         assert np.all(np.isnan(yh[e, m:])), "rows past masked_m were written"
         if m == 0:
             continue
-        ref = oracle.expert_ffn_rows(xb[e, :m], np.full(m, e, np.int32), bits(w_gu),
-                                     bits(w_down))
-        check_close(yh[e, :m], ref, bf16_output=False, what=f"expert {e}")
+        check_ffn(yh[e, :m], xb[e, :m], np.full(m, e, np.int32), bits(w_gu), bits(w_down),
+                  f"expert {e}")
 
 
 def test_ffn_masked_overflow_is_flagged_and_clamped():
@@ -124,9 +130,8 @@ def test_ffn_masked_overflow_is_flagged_and_clamped():
     y = moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_MASKED, x.cuda(), mm.cuda(), M_max,
                            w_gu.cuda(), w_down.cuda(), ws)
     assert moe.moe_get_device_status(ws) == 6  # MOE_ERR_OVERFLOW
-    ref = oracle.expert_ffn_rows(bits(x)[0], np.zeros(M_max, np.int32), bits(w_gu),
-                                 bits(w_down))
-    check_close(y[0].cpu().numpy(), ref, bf16_output=False, what="clamped expert")
+    check_ffn(y[0].cpu().numpy(), bits(x)[0], np.zeros(M_max, np.int32), bits(w_gu),
+              bits(w_down), "clamped expert")
 
 
 def test_ffn_all_experts_empty_writes_nothing():
