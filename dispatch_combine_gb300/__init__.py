@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     lib,
     moe_combine,
     moe_dispatch,
+    moe_dispatch_noalloc,
     moe_expert_down,
     moe_expert_ffn,
     moe_expert_ffn_workspace_size,

@@ -59,6 +59,7 @@ SIGNATURES = {
     "moe_route_from_logits": (_I32, [_PS, _P, _P, _P, _P, _P]),
     "moe_group_topk": (_I32, [_PS, _P, _P, _P]),
     "moe_dispatch": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_dispatch_noalloc": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (_I32, [_PS, _I32, _P, _P, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_gate_up": (_I32, [_PS, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
     "moe_expert_down": (_I32, [_PS, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
@@ -263,6 +264,33 @@ def moe_dispatch(shape, topk_ids, x, ws: Workspace, stream=None):
                                               _ptr(counts), _ptr(offsets), _ptr(src),
                                               _ptr(dest), _ptr(x_perm), ws.c_ptr, ws.nbytes,
                                               _stream(stream)))
+    return counts, offsets, src, dest, x_perm
+
+
+def moe_dispatch_noalloc(shape, topk_ids, x, stream=None):
+    """moe_dispatch without a workspace, for callers that cannot allocate
+    device memory (the library keeps a fixed 1 MiB scratch array per GPU).
+
+    The output tensors are allocated here by PyTorch for convenience; a
+    caller that owns its buffers passes them to the C entry point directly.
+    Returns (counts [E], offsets [E+1], src_token [T*k], dest [T*k], x_perm).
+    """
+    s = as_shape(shape)
+    dev = topk_ids.device
+    n = s.T * s.k
+    _expect(topk_ids, torch.int32, (s.T, s.k), "topk_ids")
+    counts = torch.empty(s.E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(s.E + 1, dtype=torch.int32, device=dev)
+    src = torch.empty(n, dtype=torch.int32, device=dev)
+    dest = torch.empty(n, dtype=torch.int32, device=dev)
+    x_perm = None
+    if x is not None:
+        _expect(x, torch.bfloat16, (s.T, s.d), "x")
+        x_perm = torch.empty((n, s.d), dtype=torch.bfloat16, device=dev)
+    _check("moe_dispatch_noalloc",
+           lib().moe_dispatch_noalloc(ctypes.byref(s), _ptr(topk_ids), _ptr(x), _ptr(counts),
+                                      _ptr(offsets), _ptr(src), _ptr(dest), _ptr(x_perm),
+                                      _stream(stream)))
     return counts, offsets, src, dest, x_perm
 
 

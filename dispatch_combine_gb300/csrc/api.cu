@@ -164,6 +164,8 @@ moe_status_t run_down(const moe_shape_t *s, int32_t layout, const void *h, const
 
 }  // namespace
 
+moe_status_t moe::check_shape_for_abi(const moe_shape_t *shape) { return check_shape(shape); }
+
 extern "C" {
 
 const char *moe_status_string(moe_status_t st) {

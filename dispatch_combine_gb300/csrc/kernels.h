@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
+
 namespace moe {
 
 // router.cu
@@ -57,5 +59,8 @@ cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t s);
 
 int num_sms();
+
+// api.cu: the shape validation every entry point applies (MOE_OK or an error)
+moe_status_t check_shape_for_abi(const moe_shape_t *shape);
 
 }  // namespace moe

@@ -1,0 +1,73 @@
+// noalloc.cu -- a dispatch entry point that needs no workspace.
+//
+// Some callers cannot hand this library a workspace: a serving runtime that
+// reserves all of HBM for weights and KV cache when it starts and gives out
+// no further buffers, plain C code that links only this library and has no
+// device allocator of its own, or code running where a cudaMalloc would be
+// unsafe or forbidden (inside a memory pool that must not grow, or on a path
+// that must not synchronise the device, which cudaMalloc/cudaFree can do).
+// moe_dispatch_noalloc serves them: the per-chunk expert histograms that
+// moe_dispatch keeps in the caller's workspace live here in one file-scope
+// device array instead, of a fixed size.
+//
+// Every GPU that loads this library holds the array until the process
+// exits.  All calls on a device share it, so two calls that overlap on the
+// GPU (different streams, no ordering between them) race on it; calls on
+// one stream, or otherwise ordered, are safe.  Each call overwrites every
+// entry it reads, so nothing needs clearing between calls.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+// chunks * E int32 histograms; 1 MiB.
+constexpr int64_t kNoAllocScratchInts = 262144;
+static __device__ __align__(256) int32_t g_dispatch_scratch[kNoAllocScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+int32_t *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up
+// once per device, with that device current, and cached.
+moe_status_t scratch_address(int32_t **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    g_scratch_addr[dev] = static_cast<int32_t *>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_dispatch_noalloc(const moe_shape_t *shape, const int32_t *topk_ids,
+                                              const void *x, int32_t *counts, int32_t *offsets,
+                                              int32_t *src_token, int32_t *dest, void *x_perm,
+                                              moe_stream_t stream) {
+  const moe_status_t st = moe::check_shape_for_abi(shape);
+  if (st != MOE_OK) return st;
+  if (shape->T == 0) return MOE_OK;
+  if (!topk_ids || !counts || !offsets || !src_token || !dest) return MOE_ERR_INVALID_ARG;
+  if (x && !x_perm) return MOE_ERR_INVALID_ARG;
+  if (x && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(x_perm)) & 15u))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t n = static_cast<int64_t>(shape->T) * shape->k;
+  if (moe::dispatch_num_chunks(n) * shape->E > kNoAllocScratchInts) return MOE_ERR_UNSUPPORTED;
+  int32_t *scratch = nullptr;
+  const moe_status_t ast = scratch_address(&scratch);
+  if (ast != MOE_OK) return ast;
+  const cudaError_t err = moe::launch_dispatch(topk_ids, shape->T, shape->k, shape->E, x,
+                                               shape->d, counts, offsets, src_token, dest, x_perm,
+                                               scratch, nullptr, nullptr, stream);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -219,6 +219,30 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
                        moe_stream_t stream);
 
 /*
+ * moe_dispatch without a workspace, for callers that cannot allocate device
+ * memory: a serving runtime that reserves all of HBM up front and hands out
+ * no further buffers, plain C code with no device allocator of its own, or
+ * code on a path where cudaMalloc/cudaFree (which may synchronise the
+ * device) are not allowed.  The pages have no counterpart; it is a
+ * convenience of this library.
+ *   Arguments and outputs are those of moe_dispatch minus the workspace.
+ *   The per-chunk expert histograms live in a 1 MiB device array inside the
+ *   library (every GPU that loads the library holds it until exit), which
+ *   limits ceil(T*k / 512) * E to 262144 entries (T*k <= 524288 at E = 256);
+ *   larger shapes return MOE_ERR_UNSUPPORTED.  Nothing is allocated.
+ *   The first call on a device looks up the array's device address (no
+ *   allocation); make that first call before any stream capture.
+ *   All calls share the array: calls that overlap on the GPU race; calls
+ *   ordered on one stream are safe, and nothing needs clearing between them.
+ *   Out-of-range ids are skipped (their counts are missing from `counts`)
+ *   but, with no workspace, not reported in a status word.
+ */
+moe_status_t moe_dispatch_noalloc(const moe_shape_t *shape, const int32_t *topk_ids,
+                                  const void *x, int32_t *counts, int32_t *offsets,
+                                  int32_t *src_token, int32_t *dest, void *x_perm,
+                                  moe_stream_t stream);
+
+/*
  * Number of kernels moe_layer launches per call for this shape (for launch
  * accounting).
  */
