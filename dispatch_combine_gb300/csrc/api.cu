@@ -18,11 +18,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Workspace regions, in this order (each 256-byte aligned):
 //   status word | mtile_base [E+1] | dispatch chunk counts [chunks*E] |
-//   logits [T*E] f32 | h [h_rows*inter] bf16 |
+//   logits [T*E] f32 | padded router weight | h [h_rows*inter] bf16 |
 //   (layer only) ids [T*k] | w [T*k] | counts [E] | offsets [E+1] |
 //   dest [T*k] | src [T*k] | x_perm [T*k*d] bf16 | y_perm [T*k*d] f32
 struct Layout {
-  size_t status, mtile, chunk, logits, h, ids, w, counts, offsets, dest, src, x_perm, y_perm;
+  size_t status, mtile, chunk, logits, wr32, h, ids, w, counts, offsets, dest, src, x_perm,
+      y_perm;
   size_t end_route, end_dispatch, end_ffn, end_layer;
 };
 
@@ -39,6 +40,8 @@ Layout make_layout(const moe_shape_t &s, int64_t h_rows) {
   L.end_dispatch = off;
   L.logits = off;
   off = align_up(off + 4 * static_cast<size_t>(s.T) * s.E);
+  L.wr32 = off;
+  off = align_up(off + moe::router_scratch_bytes(s.d, s.E));
   L.end_route = off;
   L.h = off;
   off = align_up(off + 2 * static_cast<size_t>(h_rows) * s.inter);
@@ -234,7 +237,8 @@ moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *w_r,
   const Layout L = make_layout(s, 0);
   MOE_TRY(check_ws(ws, ws_bytes, L.end_route));
   float *lg = logits ? logits : at<float>(ws, L.logits);
-  MOE_TRY(cuda_status(moe::launch_router_logits(x, w_r, s.T, s.d, s.E, lg, stream)));
+  MOE_TRY(cuda_status(
+      moe::launch_router_logits(x, w_r, s.T, s.d, s.E, lg, at<void>(ws, L.wr32), stream)));
   return cuda_status(moe::launch_router_select(lg, bias, s.T, s.E, s.G, s.topk_group, s.k,
                                                s.score, s.bias_scale, 0, topk_ids, topk_w,
                                                stream));
@@ -390,7 +394,8 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
     return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), stream));
   };
   MOE_TRY(mark(0));
-  MOE_TRY(cuda_status(moe::launch_router_logits(x, w_r, s.T, s.d, s.E, logits, stream)));
+  MOE_TRY(cuda_status(
+      moe::launch_router_logits(x, w_r, s.T, s.d, s.E, logits, at<void>(ws, L.wr32), stream)));
   MOE_TRY(cuda_status(moe::launch_router_select(logits, bias, s.T, s.E, s.G, s.topk_group, s.k,
                                                 s.score, s.bias_scale, 0, ids, w, stream)));
   MOE_TRY(mark(1));
@@ -410,8 +415,9 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
 
 int32_t moe_layer_launch_count(const moe_shape_t *shape) {
   if (check_shape(shape) != MOE_OK || shape->T == 0) return 0;
-  // router logits, select, count, scan, scatter, gather, gate_up, down, combine
-  return 9;
+  // router widen, logits, select, count, scan, scatter, gather, gate_up, down,
+  // combine
+  return 10;
 }
 
 moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, uint64_t limit_ns,

@@ -66,6 +66,7 @@ struct Tile {
 
 struct KArgs {
   int E, K, n_tiles, layout, M_max, b_rows, up_off;
+  int m_block;  // m-tiles per rasterization block (A rows of a block stay in L2)
   int64_t rows_total;
   const int32_t *seg;
   const int32_t *mtile_base;
@@ -87,10 +88,18 @@ __device__ __forceinline__ Tile decode_tile(const KArgs &a, const int32_t *mt, i
       hi = mid - 1;
   }
   t.e = lo;
+  // Inside an expert, tiles go in blocks of m_block m-tiles; inside a block
+  // the m-tile index runs fastest, then n.  CTAs working at the same time
+  // then share the block's A rows and each B tile through L2, and A is read
+  // from HBM once however many n-tiles there are.
   const int mt_e = mt[lo + 1] - mt[lo];
   const int local = u - mt[lo] * a.n_tiles;
-  t.n = local / mt_e;
-  t.m = local - t.n * mt_e;
+  const int full = mt_e / a.m_block;
+  const int blk = local / (a.m_block * a.n_tiles);
+  const int mb = (blk < full) ? a.m_block : mt_e - full * a.m_block;
+  const int within = local - blk * a.m_block * a.n_tiles;
+  t.n = within / mb;
+  t.m = blk * a.m_block + (within - t.n * mb);
   int rows, start;
   if (a.layout == MOE_LAYOUT_CONTIGUOUS) {
     start = a.seg[t.e];
@@ -413,6 +422,9 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.out = p.out;
   a.ldo = p.n_out;
   a.rows_total = p.rows_total;
+  // A rows of one block: about 24 MB (a 128-row tile holds 256*K bytes)
+  a.m_block = static_cast<int>((24ll << 20) / (256ll * p.K));
+  if (a.m_block < 1) a.m_block = 1;
   a.status = p.status;
   a.wait_limit_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitLimitNs;
   grouped_gemm_kernel<BN, SWIGLU><<<num_sms(), kGemmThreads, C::SMEM_BYTES, s>>>(tmA, tmB, a);

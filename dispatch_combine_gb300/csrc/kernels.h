@@ -10,8 +10,11 @@
 namespace moe {
 
 // router.cu
+// w_scratch: router_scratch_bytes(d, E) bytes of workspace (a zero-padded
+// copy of w_r made by the first of the two kernels launched here)
+size_t router_scratch_bytes(int d, int E);
 cudaError_t launch_router_logits(const void *x, const void *w_r, int T, int d, int E,
-                                 float *logits, cudaStream_t s);
+                                 float *logits, void *w_scratch, cudaStream_t s);
 // mode 0: scores from logits (score kind); mode 1: the input already holds
 // selection scores (group top-k only; weights not written).
 cudaError_t launch_router_select(const float *logits, const float *bias, int T, int E, int G,

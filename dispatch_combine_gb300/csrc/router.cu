@@ -24,123 +24,270 @@ namespace {
 
 // ---------------------------------------------------------------------------
 // logits: a CUDA-core GEMM [T,d] x [d,E] whose K dimension is split in 32
-// interleaved slices (one per lane), each slice summed in order.
-// CTA tile: 16 tokens x 64 experts, 8 warps; warp w owns tokens
-// (w & 1) * 8 .. +8 and experts (w >> 1) * 16 .. +16; lane = slice.
+// interleaved slices, each slice summed in order, then combined by a fixed
+// pairwise tree.
+//
+// A "round" covers 256 consecutive inputs i: chunk c of the round (8 inputs
+// i = 256r + 8c + j, j = 0..7) belongs to slice c.  The CTA tile is CT tokens
+// x CE experts.  Warp w owns slices SW*w .. SW*w+SW-1 (SW = 32 / warps) for
+// the whole tile: all lanes of a warp read the same slice's row at the same
+// time (shared-memory broadcast), each lane owning LT tokens x LE experts.
+// x sits in shared memory as fp32, W_r as bf16 (widened to fp32 pairs in
+// registers: exact), so each round brings as few bytes as possible into the
+// SM.  W_r tiles come from a zero-padded copy by cp.async, STAGES rounds
+// deep; the next round's x tile is loaded into registers while the current
+// round is computed; one barrier per round.  The multiply-adds are paired
+// over adjacent experts with fma.rn.f32x2 (two IEEE fp32 fused multiply-adds
+// per instruction, each rounded exactly as a scalar fma.rn); on this part the
+// packed form holds half of the FMA pipe for two cycles, and the kernel runs
+// near that ceiling (scalar-FMA layouts measured were issue-bound and not
+// faster).  At the end the
+// 32 slice sums of every output go through shared memory and are combined as
+// s_l <- s_l + s_{l+off}, off = 16, 8, 4, 2, 1 -- the pairs of the xor
+// butterfly, so the value equals lane 0's butterfly result.
 // ---------------------------------------------------------------------------
-constexpr int kRtTok = 16;
-constexpr int kRtExp = 64;
-constexpr int kRtThreads = 256;
-constexpr int kXsStride = 8 * kRtTok + 4;  // floats per slice in xs (padded)
-constexpr int kWsStride = 8 * kRtExp + 4;  // floats per slice in ws (padded)
-constexpr int kRtSmemBytes = 32 * (kXsStride + kWsStride) * 4;
+constexpr int kRtStages = 3;
 
-__global__ void __launch_bounds__(kRtThreads, 1)
-    router_logits_kernel(const __nv_bfloat16 *__restrict__ x,
-                         const __nv_bfloat16 *__restrict__ w_r, int T, int d, int E,
-                         float *__restrict__ logits) {
-  extern __shared__ __align__(16) float rsm[];
-  float *xs = rsm;                   // [slice][j][token]
-  float *ws = rsm + 32 * kXsStride;  // [slice][j][expert]
-  const int t0 = blockIdx.x * kRtTok;
-  const int e0 = blockIdx.y * kRtExp;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int tb = (warp & 1) * 8;
-  const int eb = (warp >> 1) * 16;
-  const bool e_vec = (E % 8) == 0;
+template <int LT, int LE, int CE, int NT>
+struct RtCfg {
+  static constexpr int NW = NT / 32;        // warps
+  static constexpr int SW = 32 / NW;        // slices per warp
+  static constexpr int EG = CE / LE;        // lane groups along experts
+  static constexpr int TG = 32 / EG;        // lane groups along tokens
+  static constexpr int CT = TG * LT;        // tokens per CTA
+  static constexpr int XS = 8 * CT + 4;     // floats per slice, x tile
+  static constexpr int WS = 8 * CE + 8;     // bf16 per slice, w tile
+  static constexpr int XBYTES = 32 * XS * 4;
+  static constexpr int STAGE = XBYTES + 32 * WS * 2;  // bytes per stage
+  static constexpr int RED = 32 * CT * CE * 4;       // bytes of the final exchange
+  static constexpr int SMEM = (kRtStages * STAGE > RED ? kRtStages * STAGE : RED);
+  static constexpr int XCH = CT * 32 / NT;      // 16-byte x chunks per thread
+  static constexpr int WCHUNKS = 256 * CE / 8;  // 16-byte w chunks per round
+  static constexpr int WCH = (WCHUNKS + NT - 1) / NT;  // per thread
+  static constexpr int OUT = (CT * CE + NT - 1) / NT;  // outputs reduced per thread
+  static_assert(EG * TG == 32 && LE == 8 && (LT == 1 || LT == 2 || LT == 4), "lane tile");
+  static_assert(NW * SW == 32, "slices");
+  static_assert(XCH >= 1 && WCH >= 1 && CT % 8 == 0 && CE % 8 == 0, "tile shape");
+  static_assert(STAGE % 16 == 0 && SMEM <= 227 * 1024, "shared memory");
+};
 
-  float acc[8][16];
-#pragma unroll
-  for (int a = 0; a < 8; ++a)
-#pragma unroll
-    for (int b = 0; b < 16; ++b) acc[a][b] = 0.0f;
+// Padded bf16 copy of the router weight: rows rounded up to a whole round,
+// columns to 64 experts, zeros outside [d, E).
+__host__ __device__ inline int router_e_pad(int E) { return (E + 63) / 64 * 64; }
+__host__ __device__ inline int router_d_pad(int d) { return (d + 255) / 256 * 256; }
 
-  const int rounds = (d + 255) / 256;
-  for (int r = 0; r < rounds; ++r) {
-    __syncthreads();
-    // x tile: 16 tokens x 32 chunks of 8 bf16
-    for (int q = threadIdx.x; q < kRtTok * 32; q += kRtThreads) {
-      const int t = q >> 5, c = q & 31;
-      const int i0 = r * 256 + c * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (t0 + t < T && i0 < d)
-        v = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + t) * d + i0));
-      float *dst = xs + c * kXsStride + t;
-      dst[0 * kRtTok] = bf16lo(v.x);
-      dst[1 * kRtTok] = bf16hi(v.x);
-      dst[2 * kRtTok] = bf16lo(v.y);
-      dst[3 * kRtTok] = bf16hi(v.y);
-      dst[4 * kRtTok] = bf16lo(v.z);
-      dst[5 * kRtTok] = bf16hi(v.z);
-      dst[6 * kRtTok] = bf16lo(v.w);
-      dst[7 * kRtTok] = bf16hi(v.w);
-    }
-    // w tile: 256 rows x 64 experts
-    for (int q = threadIdx.x; q < 256 * 8; q += kRtThreads) {
-      const int ii = q >> 3, ec = (q & 7) * 8;
-      const int i = r * 256 + ii;
-      float vals[8];
-      if (e_vec && i < d && e0 + ec + 8 <= E) {
-        uint4 v = __ldg(reinterpret_cast<const uint4 *>(w_r + (size_t)i * E + e0 + ec));
-        vals[0] = bf16lo(v.x); vals[1] = bf16hi(v.x);
-        vals[2] = bf16lo(v.y); vals[3] = bf16hi(v.y);
-        vals[4] = bf16lo(v.z); vals[5] = bf16hi(v.z);
-        vals[6] = bf16lo(v.w); vals[7] = bf16hi(v.w);
-      } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          vals[u] = (i < d && e0 + ec + u < E)
-                        ? __bfloat162float(w_r[(size_t)i * E + e0 + ec + u])
-                        : 0.0f;
-      }
-      float *dst = ws + (ii >> 3) * kWsStride + (ii & 7) * kRtExp + ec;
-      *reinterpret_cast<float4 *>(dst) = make_float4(vals[0], vals[1], vals[2], vals[3]);
-      *reinterpret_cast<float4 *>(dst + 4) = make_float4(vals[4], vals[5], vals[6], vals[7]);
-    }
-    __syncthreads();
-    const float *xsl = xs + lane * kXsStride + tb;
-    const float *wsl = ws + lane * kWsStride + eb;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float xv[8], wv[16];
-      *reinterpret_cast<float4 *>(&xv[0]) = *reinterpret_cast<const float4 *>(xsl + j * kRtTok);
-      *reinterpret_cast<float4 *>(&xv[4]) =
-          *reinterpret_cast<const float4 *>(xsl + j * kRtTok + 4);
-#pragma unroll
-      for (int b4 = 0; b4 < 4; ++b4)
-        *reinterpret_cast<float4 *>(&wv[b4 * 4]) =
-            *reinterpret_cast<const float4 *>(wsl + j * kRtExp + b4 * 4);
-#pragma unroll
-      for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int b = 0; b < 16; ++b) acc[a][b] = __fmaf_rn(xv[a], wv[b], acc[a][b]);
-    }
+__global__ void router_pad_kernel(const uint16_t *__restrict__ w_r, int d, int E,
+                                  uint16_t *__restrict__ wp) {
+  const int ep = router_e_pad(E);
+  const int64_t n = static_cast<int64_t>(router_d_pad(d)) * ep;
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const int i = static_cast<int>(q / ep), e = static_cast<int>(q % ep);
+    wp[q] = (i < d && e < E) ? w_r[(size_t)i * E + e] : static_cast<uint16_t>(0);
   }
+}
 
-  // xor butterfly across the 32 slices; every lane ends with the same value
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// fp32 pair (lo, hi) of a packed bf16 pair
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t v) {
+  uint64_t r;
+  asm("{\n\t.reg .b32 lo, hi;\n\tshl.b32 lo, %1, 16;\n\tand.b32 hi, %1, 0xFFFF0000;\n\t"
+      "mov.b64 %0, {lo, hi};\n\t}"
+      : "=l"(r)
+      : "r"(v));
+  return r;
+}
+
+template <int LT, int LE, int CE, int NT>
+__global__ void __launch_bounds__(NT, 1)
+    router_logits_kernel(const __nv_bfloat16 *__restrict__ x, const uint16_t *__restrict__ wpad,
+                         int T, int d, int E, float *__restrict__ logits) {
+  using C = RtCfg<LT, LE, CE, NT>;
+  constexpr int SW = C::SW;
+  extern __shared__ __align__(16) uint8_t rsm_raw[];
+  const int t0 = blockIdx.x * C::CT;
+  const int e0 = blockIdx.y * CE;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int tl = (lane / C::EG) * LT;  // first token of this lane
+  const int el = (lane % C::EG) * LE;  // first expert of this lane
+  const int rounds = (d + 255) / 256;
+  const int ep = router_e_pad(E);
+  const bool full_tokens = t0 + C::CT <= T;
+  auto xbuf = [&](int st) { return reinterpret_cast<float *>(rsm_raw + st * C::STAGE); };
+  auto wbuf = [&](int st) {
+    return reinterpret_cast<uint16_t *>(rsm_raw + st * C::STAGE + C::XBYTES);
+  };
+
+  uint4 xr[C::XCH];
+
+  // x chunk m of this thread: 8 chunks x 4 tokens per warp-sized group, so
+  // that the scalar shared stores below hit 32 distinct banks
+  auto x_coord = [&](int m, int &t, int &c) {
+    const int q = tid + NT * m;
+    const int g = q >> 5, l = q & 31;
+    c = (g & 3) * 8 + (l & 7);
+    t = (g >> 2) * 4 + (l >> 3);
+  };
+  auto load_x = [&](int r) {
+    const bool full = full_tokens && (r + 1) * 256 <= d;
 #pragma unroll
-  for (int a = 0; a < 8; ++a)
-#pragma unroll
-    for (int b = 0; b < 16; ++b) {
-      float v = acc[a][b];
-      v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 8));
-      v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 4));
-      v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 2));
-      v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 1));
-      acc[a][b] = v;
+    for (int m = 0; m < C::XCH; ++m) {
+      int t, c;
+      x_coord(m, t, c);
+      const int i0 = r * 256 + c * 8;
+      if (full || (t0 + t < T && i0 < d))
+        xr[m] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + t) * d + i0));
+      else
+        xr[m] = make_uint4(0u, 0u, 0u, 0u);
     }
-  // lane l stores the outputs whose flat index is congruent to l mod 32
+  };
+  auto store_x = [&](float *xs) {
 #pragma unroll
-  for (int a = 0; a < 8; ++a)
+    for (int m = 0; m < C::XCH; ++m) {
+      int t, c;
+      x_coord(m, t, c);
+      float *dst = xs + c * C::XS + t;
+      const uint4 v = xr[m];
+      dst[0 * C::CT] = bf16lo(v.x);
+      dst[1 * C::CT] = bf16hi(v.x);
+      dst[2 * C::CT] = bf16lo(v.y);
+      dst[3 * C::CT] = bf16hi(v.y);
+      dst[4 * C::CT] = bf16lo(v.z);
+      dst[5 * C::CT] = bf16hi(v.z);
+      dst[6 * C::CT] = bf16lo(v.w);
+      dst[7 * C::CT] = bf16hi(v.w);
+    }
+  };
+  // w tile of round r: 256 rows x CE experts (bf16) of the padded copy; one
+  // commit group per round (empty groups past the last round keep the count)
+  auto issue_w = [&](int r) {
+    if (r < rounds) {
+      uint16_t *ws = wbuf(r % kRtStages);
 #pragma unroll
-    for (int b = 0; b < 16; ++b) {
-      if (((a * 16 + b) & 31) == lane) {
-        const int t = t0 + tb + a, e = e0 + eb + b;
-        if (t < T && e < E) logits[(size_t)t * E + e] = acc[a][b];
+      for (int m = 0; m < C::WCH; ++m) {
+        const int q = tid + NT * m;
+        if (C::WCHUNKS % NT != 0 && q >= C::WCHUNKS) break;
+        const int ii = q / (CE / 8), ec = (q % (CE / 8)) * 8;
+        cp_async_16(ws + (ii >> 3) * C::WS + (ii & 7) * CE + ec,
+                    wpad + (size_t)(r * 256 + ii) * ep + e0 + ec);
       }
     }
+    cp_async_commit();
+  };
+
+  // acc2[s][a][b]: slice SW*warp+s, token tl+a, experts el+2b and el+2b+1
+  uint64_t acc2[SW][LT][LE / 2];
+#pragma unroll
+  for (int s4 = 0; s4 < SW; ++s4)
+#pragma unroll
+    for (int a = 0; a < LT; ++a)
+#pragma unroll
+      for (int b = 0; b < LE / 2; ++b) acc2[s4][a][b] = 0ull;
+
+#pragma unroll
+  for (int r = 0; r < kRtStages - 1; ++r) issue_w(r);
+  load_x(0);
+  store_x(xbuf(0));
+  cp_async_wait<kRtStages - 2>();
+  __syncthreads();
+  for (int r = 0; r < rounds; ++r) {
+    issue_w(r + kRtStages - 1);
+    if (r + 1 < rounds) load_x(r + 1);
+    const float *xs = xbuf(r % kRtStages);
+    const uint16_t *ws = wbuf(r % kRtStages);
+    float xv[2][LT];
+    uint4 wv[2];
+    // operands of step q = s * 8 + j: slice SW*warp + s, input j of its chunk
+    auto ld = [&](int q, int slot) {
+      const int c = SW * warp + (q >> 3), j = q & 7;
+      const float *xp = xs + c * C::XS + j * C::CT + tl;
+      if (LT == 4) {
+        *reinterpret_cast<float4 *>(&xv[slot][0]) = *reinterpret_cast<const float4 *>(xp);
+      } else if (LT == 2) {
+        *reinterpret_cast<float2 *>(&xv[slot][0]) = *reinterpret_cast<const float2 *>(xp);
+      } else {
+        xv[slot][0] = *xp;
+      }
+      wv[slot] = *reinterpret_cast<const uint4 *>(ws + c * C::WS + j * CE + el);
+    };
+    ld(0, 0);
+#pragma unroll
+    for (int q = 0; q < 8 * SW; ++q) {
+      if (q + 1 < 8 * SW) ld(q + 1, (q + 1) & 1);
+      const uint4 w = wv[q & 1];
+      const uint64_t wp[4] = {bf16x2_to_f32x2(w.x), bf16x2_to_f32x2(w.y), bf16x2_to_f32x2(w.z),
+                              bf16x2_to_f32x2(w.w)};
+#pragma unroll
+      for (int a = 0; a < LT; ++a) {
+        uint64_t xd;
+        asm("mov.b64 %0, {%1, %1};" : "=l"(xd) : "f"(xv[q & 1][a]));
+#pragma unroll
+        for (int b = 0; b < LE / 2; ++b)
+          asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[q >> 3][a][b]) : "l"(xd), "l"(wp[b]));
+      }
+    }
+    if (r + 1 < rounds) store_x(xbuf((r + 1) % kRtStages));
+    cp_async_wait<kRtStages - 2>();
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // exchange: red[slice][o], o = token * CE + expert (tile-relative)
+  float *red = reinterpret_cast<float *>(rsm_raw);
+#pragma unroll
+  for (int s4 = 0; s4 < SW; ++s4)
+#pragma unroll
+    for (int a = 0; a < LT; ++a)
+#pragma unroll
+      for (int b = 0; b < LE / 2; ++b) {
+        float lo, hi;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc2[s4][a][b]));
+        float *dst = red + (size_t)(SW * warp + s4) * (C::CT * CE) + (tl + a) * CE + el + 2 * b;
+        *reinterpret_cast<float2 *>(dst) = make_float2(lo, hi);
+      }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < C::OUT; ++k) {
+    const int o = tid + k * NT;
+    if (o >= C::CT * CE) break;
+    float v[32];
+#pragma unroll
+    for (int l = 0; l < 32; ++l) v[l] = red[(size_t)l * (C::CT * CE) + o];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+      for (int l = 0; l < off; ++l) v[l] = __fadd_rn(v[l], v[l + off]);
+    const int t = t0 + o / CE, e = e0 + o % CE;
+    if (t < T && e < E) logits[(size_t)t * E + e] = v[0];
+  }
+}
+
+template <int LT, int LE, int CE, int NT>
+cudaError_t run_logits(const void *x, const uint16_t *wpad, int T, int d, int E, float *logits,
+                       cudaStream_t s) {
+  using C = RtCfg<LT, LE, CE, NT>;
+  auto kern = router_logits_kernel<LT, LE, CE, NT>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (err != cudaSuccess) return err;
+  dim3 grid((T + C::CT - 1) / C::CT, (E + CE - 1) / CE);
+  kern<<<grid, NT, C::SMEM, s>>>(static_cast<const __nv_bfloat16 *>(x), wpad, T, d, E, logits);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -307,18 +454,27 @@ __global__ void __launch_bounds__(kSelWarps * 32)
 
 }  // namespace
 
+size_t router_scratch_bytes(int d, int E) {
+  return static_cast<size_t>(router_d_pad(d)) * router_e_pad(E) * sizeof(uint16_t);
+}
+
 cudaError_t launch_router_logits(const void *x, const void *w_r, int T, int d, int E,
-                                 float *logits, cudaStream_t s) {
+                                 float *logits, void *w_scratch, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  cudaError_t err = cudaFuncSetAttribute(router_logits_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kRtSmemBytes);
+  const int64_t n = static_cast<int64_t>(router_d_pad(d)) * router_e_pad(E);
+  const int64_t want = (n + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  uint16_t *wpad = static_cast<uint16_t *>(w_scratch);
+  router_pad_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, s>>>(
+      static_cast<const uint16_t *>(w_r), d, E, wpad);
+  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  dim3 grid((T + kRtTok - 1) / kRtTok, (E + kRtExp - 1) / kRtExp);
-  router_logits_kernel<<<grid, kRtThreads, kRtSmemBytes, s>>>(
-      static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(w_r), T, d, E,
-      logits);
-  return cudaGetLastError();
+  // tile shapes (tokens x experts): E <= 8: 32 x 8; <= 16: 32 x 16;
+  // <= 32: 32 x 32; otherwise 16 x 64; 16 warps, 2 slices per warp
+  if (E <= 8) return run_logits<1, 8, 8, 512>(x, wpad, T, d, E, logits, s);
+  if (E <= 16) return run_logits<2, 8, 16, 512>(x, wpad, T, d, E, logits, s);
+  if (E <= 32) return run_logits<4, 8, 32, 512>(x, wpad, T, d, E, logits, s);
+  return run_logits<4, 8, 64, 512>(x, wpad, T, d, E, logits, s);
 }
 
 cudaError_t launch_router_select(const float *logits, const float *bias, int T, int E, int G,

@@ -133,7 +133,7 @@ def test_zero_tokens_is_a_noop(lib):
                        None, 0, None, None)
     assert st == 0
     assert lib.moe_layer_launch_count(ctypes.byref(s)) == 0
-    assert lib.moe_layer_launch_count(ctypes.byref(_shape())) == 9
+    assert lib.moe_layer_launch_count(ctypes.byref(_shape())) == 10
 
 
 def test_masked_layout_arguments(lib):
