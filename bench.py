@@ -455,6 +455,99 @@ def run_gpu(args, c):
     return 0
 
 
+# --------------------------------------------------------------------------
+# masked per-rank expert slices (expert FFN only)
+# --------------------------------------------------------------------------
+
+def run_masked(args):
+    """Time the masked expert FFN on a per-rank slice (its own JSON line).
+
+    Token counts come from routing 4096 tokens through the decode router on
+    the GPU (moe_route + moe_dispatch); "ep" keeps experts 0-7 of the decode
+    weights (d=7168, inter=2048), "tp" keeps all 256 experts with the SwiGLU
+    width sliced to 64 (gate_up N=128), the same weight bytes.  Reported:
+    gate_up+SwiGLU alone and the whole FFN (gate_up + down), in microseconds
+    and as a fraction of the HBM roofline of the weight bytes.
+    """
+    import torch
+    import dispatch_combine_gb300 as moe
+    from moe_inputs import (MASKED_EP_EXPERTS, MASKED_ROUTE_TOKENS, MASKED_TP_INTER,
+                            make_layer_tensors)
+    torch.cuda.set_device(0)
+    cfg = CONFIGS["decode"]
+    t = make_layer_tensors(cfg, device="cuda", seed=0, n_tokens=MASKED_ROUTE_TOKENS)
+    rshape = cfg.replace(T=MASKED_ROUTE_TOKENS).shape()
+    ws = moe.Workspace(moe.moe_workspace_size(rshape))
+    ids, _, _ = moe.moe_route(rshape, t["x"], t["w_r"], t["bias"], ws)
+    counts, offsets, src, _, _ = moe.moe_dispatch(rshape, ids, None, ws)
+    counts_h, offsets_h = counts.cpu(), offsets.cpu()
+    if args.masked == "ep":
+        experts = list(range(MASKED_EP_EXPERTS))
+        w_gu = t["w_gate_up"][:MASKED_EP_EXPERTS].contiguous()
+        w_down = t["w_down"][:MASKED_EP_EXPERTS].contiguous()
+        inter = cfg.inter
+    else:
+        experts = list(range(cfg.E))
+        i0 = MASKED_TP_INTER
+        w_gu = torch.cat([t["w_gate_up"][:, :i0], t["w_gate_up"][:, cfg.inter:cfg.inter + i0]],
+                         dim=1).contiguous()
+        w_down = t["w_down"][:, :, :i0].contiguous()
+        inter = i0
+    del t["w_gate_up"], t["w_down"]
+    mm_h = counts_h[experts]
+    M_max = max(128, int((int(mm_h.max()) + 127) // 128 * 128))
+    buf = torch.zeros(len(experts), M_max, cfg.d, dtype=torch.bfloat16, device="cuda")
+    for i, e in enumerate(experts):
+        rows = src[int(offsets_h[e]):int(offsets_h[e + 1])].long()
+        buf[i, :rows.numel()] = t["x"][rows]
+    mm = mm_h.to(torch.int32).cuda()
+    shape = dict(T=1, d=cfg.d, E=len(experts), G=1, topk_group=1, k=1, inter=inter, score=1,
+                 bias_scale=0.15)
+    fws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_MASKED, M_max))
+    h = torch.empty(len(experts), M_max, inter, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(len(experts), M_max, cfg.d, dtype=torch.float32, device="cuda")
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000.0 / args.steps
+
+    us_gu = timed(lambda: moe.moe_expert_gate_up(shape, moe.MOE_LAYOUT_MASKED, buf, mm, M_max,
+                                                 w_gu, fws, h_out=h))
+    us_ffn = timed(lambda: moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_MASKED, buf, mm, M_max,
+                                              w_gu, w_down, fws, y_out=y))
+    if moe.moe_get_device_status(fws) != 0:
+        raise SystemExit("device status error")
+    peaks, src_p = load_peaks()
+    touched = [i for i, e in enumerate(experts) if int(mm_h[i]) > 0]
+    gu_bytes = len(touched) * 2 * inter * cfg.d * 2
+    dn_bytes = len(touched) * cfg.d * inter * 2
+    rows = int(mm_h.sum())
+    line = {
+        "metric": f"masked expert FFN ({args.masked}) us", "impl": "gb300",
+        "value": us_ffn, "unit": "us", "higher_is_better": False, "steps": args.steps,
+        "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": (f"masked per-rank slice '{args.masked}': {len(experts)} experts, "
+                                f"d={cfg.d}, inter={inter} (gate_up N={2 * inter}), M_max={M_max}"),
+                   "rows": rows, "masked_m_min": int(mm_h.min()), "masked_m_max": int(mm_h.max()),
+                   "masked_m_mean": float(mm_h.float().mean()), "touched_experts": len(touched)},
+        "gate_up_us": us_gu,
+        "gate_up_hbm_frac": gu_bytes / (peaks["hbm_gbs"] * 1e9) / (us_gu * 1e-6),
+        "ffn_hbm_frac": (gu_bytes + dn_bytes) / (peaks["hbm_gbs"] * 1e9) / (us_ffn * 1e-6),
+        "weight_bytes": gu_bytes + dn_bytes, "peak_source": src_p,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,6 +558,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-sample-s", type=float, default=15.0,
                     help="seconds of CPU oracle work for cpu_baseline (0 = skip)")
+    ap.add_argument("--masked", choices=["ep", "tp"], default=None,
+                    help="time the masked expert FFN of a per-rank slice instead")
     ap.add_argument("--ref-step-s", type=float, default=4.0,
                     help="seconds of oracle work per step of --impl reference")
     return ap.parse_args(argv)
@@ -473,6 +568,8 @@ def parse_args(argv=None):
 def main(argv=None):
     args = parse_args(argv)
     c = CONFIGS[args.config]
+    if args.masked:
+        return run_masked(args)
     if args.impl == "reference":
         return run_reference(args, c)
     return run_gpu(args, c)
