@@ -123,6 +123,13 @@ moe_status_t ffn_rows(const moe_shape_t *s, int32_t layout, int32_t M_max, int64
 
 // gate_up + SwiGLU (and optionally down) over `rows` rows with mtile_base
 // already computed in the workspace.
+// Pair (2-CTA, 256-row) tiles for the contiguous layout when experts
+// average at least kPairRowsPerExpert rows.
+bool use_pair(const moe_shape_t *s, int32_t layout) {
+  return layout == MOE_LAYOUT_CONTIGUOUS && s->inter % 128 == 0 && s->d % 256 == 0 &&
+         static_cast<int64_t>(s->T) * s->k >= moe::kPairRowsPerExpert * s->E;
+}
+
 moe_status_t run_gate_up(const moe_shape_t *s, int32_t layout, const void *x_in,
                          const int32_t *seg, int32_t M_max, int64_t rows, const int32_t *mtile,
                          const void *w_gate_up, void *h, uint32_t *status, cudaStream_t st) {
@@ -141,6 +148,7 @@ moe_status_t run_gate_up(const moe_shape_t *s, int32_t layout, const void *x_in,
   p.b_rows = 2 * s->inter;
   p.out = h;
   p.status = status;
+  p.pair = use_pair(s, layout);
   return cuda_status(moe::launch_gemm_gate_up_swiglu(p, st));
 }
 
@@ -162,6 +170,7 @@ moe_status_t run_down(const moe_shape_t *s, int32_t layout, const void *h, const
   p.b_rows = s->d;
   p.out = y;
   p.status = status;
+  p.pair = use_pair(s, layout);
   return cuda_status(moe::launch_gemm_down(p, st));
 }
 
@@ -281,7 +290,7 @@ moe_status_t moe_dispatch(const moe_shape_t *shape, const int32_t *topk_ids, con
   MOE_TRY(check_ws(ws, ws_bytes, L.end_dispatch));
   return cuda_status(moe::launch_dispatch(topk_ids, s.T, s.k, s.E, x, s.d, counts, offsets,
                                           src_token, dest, x_perm, at<int32_t>(ws, L.chunk),
-                                          nullptr, at<uint32_t>(ws, L.status), stream));
+                                          nullptr, 128, at<uint32_t>(ws, L.status), stream));
 }
 
 static moe_status_t ffn_common(const moe_shape_t *shape, int32_t layout, const void *x_in,
@@ -311,7 +320,9 @@ moe_status_t moe_expert_ffn(const moe_shape_t *shape, int32_t layout, const void
   uint32_t *status = at<uint32_t>(ws, L.status);
   int32_t *mtile = at<int32_t>(ws, L.mtile);
   void *h = at<void>(ws, L.h);
-  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max, mtile, status, stream)));
+  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max,
+                                            use_pair(shape, layout) ? 256 : 128, mtile, status,
+                                            stream)));
   MOE_TRY(run_gate_up(shape, layout, x_in, seg, M_max, rows, mtile, w_gate_up, h, status,
                       stream));
   return run_down(shape, layout, h, seg, M_max, rows, mtile, w_down, y_out, status, stream);
@@ -329,7 +340,9 @@ moe_status_t moe_expert_gate_up(const moe_shape_t *shape, int32_t layout, const 
   if (rows == 0) return MOE_OK;
   uint32_t *status = at<uint32_t>(ws, L.status);
   int32_t *mtile = at<int32_t>(ws, L.mtile);
-  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max, mtile, status, stream)));
+  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max,
+                                            use_pair(shape, layout) ? 256 : 128, mtile, status,
+                                            stream)));
   return run_gate_up(shape, layout, x_in, seg, M_max, rows, mtile, w_gate_up, h_out, status,
                      stream);
 }
@@ -346,7 +359,9 @@ moe_status_t moe_expert_down(const moe_shape_t *shape, int32_t layout, const voi
   if (rows == 0) return MOE_OK;
   uint32_t *status = at<uint32_t>(ws, L.status);
   int32_t *mtile = at<int32_t>(ws, L.mtile);
-  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max, mtile, status, stream)));
+  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max,
+                                            use_pair(shape, layout) ? 256 : 128, mtile, status,
+                                            stream)));
   return run_down(shape, layout, h_in, seg, M_max, rows, mtile, w_down, y_out, status, stream);
 }
 
@@ -400,8 +415,9 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
                                                 s.score, s.bias_scale, 0, ids, w, stream)));
   MOE_TRY(mark(1));
   MOE_TRY(cuda_status(moe::launch_dispatch(ids, s.T, s.k, s.E, x, s.d, cnt, offsets, src, dest,
-                                           x_perm, at<int32_t>(ws, L.chunk), mtile, status,
-                                           stream)));
+                                           x_perm, at<int32_t>(ws, L.chunk), mtile,
+                                           use_pair(shape, MOE_LAYOUT_CONTIGUOUS) ? 256 : 128,
+                                           status, stream)));
   MOE_TRY(mark(2));
   MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_perm, offsets, 0, n, mtile, w_gate_up, h,
                       status, stream));

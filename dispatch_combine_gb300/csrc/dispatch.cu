@@ -79,7 +79,7 @@ __device__ int block_exclusive_scan(int v, int *total) {
 __global__ void __launch_bounds__(1024)
     dispatch_scan_kernel(int32_t *__restrict__ chunk_counts, int nchunks, int E,
                          int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
-                         int32_t *__restrict__ mtile_base) {
+                         int32_t *__restrict__ mtile_base, int tile_rows) {
   const int e = threadIdx.x;
   int run = 0;
   if (e < E) {
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(1024)
   if (e == 0) offsets[E] = total;
   if (mtile_base) {
     int mt_total = 0;
-    const int mt = (e < E) ? (run + 127) / 128 : 0;
+    const int mt = (e < E) ? (run + tile_rows - 1) / tile_rows : 0;
     const int mt_excl = block_exclusive_scan(mt, &mt_total);
     if (e < E) mtile_base[e] = mt_excl;
     if (e == 0) mtile_base[E] = mt_total;
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
 // mtile_base from offsets (layout 0) or masked_m clamped to M_max (layout 1)
 __global__ void __launch_bounds__(1024)
     ffn_tiles_kernel(const int32_t *__restrict__ seg, int layout, int E, int M_max,
-                     int32_t *__restrict__ mtile_base, uint32_t *status) {
+                     int tile_rows, int32_t *__restrict__ mtile_base, uint32_t *status) {
   const int e = threadIdx.x;
   int rows = 0;
   if (e < E) {
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(1024)
     }
   }
   int total = 0;
-  const int excl = block_exclusive_scan((rows + 127) / 128, &total);
+  const int excl = block_exclusive_scan((rows + tile_rows - 1) / tile_rows, &total);
   if (e < E) mtile_base[e] = excl;
   if (e == 0) mtile_base[E] = total;
 }
@@ -208,7 +208,8 @@ __global__ void __launch_bounds__(1024)
 cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void *x, int d,
                             int32_t *counts, int32_t *offsets, int32_t *src_token,
                             int32_t *dest, void *x_perm, int32_t *chunk_scratch,
-                            int32_t *mtile_base, uint32_t *status, cudaStream_t s) {
+                            int32_t *mtile_base, int tile_rows, uint32_t *status,
+                            cudaStream_t s) {
   const int64_t n = (int64_t)T * k;
   const int64_t nchunks = dispatch_num_chunks(n);
   if (n == 0) return cudaSuccess;
@@ -217,7 +218,7 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_scratch, (int)nchunks, E, counts, offsets,
-                                          mtile_base);
+                                          mtile_base, tile_rows);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const unsigned sblocks = (unsigned)((nchunks + kScatterWarps - 1) / kScatterWarps);
@@ -237,9 +238,9 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
   return err;
 }
 
-cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max,
+cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,
                              int32_t *mtile_base, uint32_t *status, cudaStream_t s) {
-  ffn_tiles_kernel<<<1, 1024, 0, s>>>(seg, layout, E, M_max, mtile_base, status);
+  ffn_tiles_kernel<<<1, 1024, 0, s>>>(seg, layout, E, M_max, tile_rows, mtile_base, status);
   return cudaGetLastError();
 }
 

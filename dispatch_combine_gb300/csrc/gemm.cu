@@ -76,6 +76,7 @@ struct KArgs {
   uint64_t wait_limit_ns;
 };
 
+template <int TILE_M = kBM>
 __device__ __forceinline__ Tile decode_tile(const KArgs &a, const int32_t *mt, int u) {
   Tile t;
   const int q = u / a.n_tiles;
@@ -108,8 +109,8 @@ __device__ __forceinline__ Tile decode_tile(const KArgs &a, const int32_t *mt, i
     start = t.e * a.M_max;
     rows = min(max(a.seg[t.e], 0), a.M_max);
   }
-  t.row0 = start + t.m * kBM;
-  t.rows_valid = min(kBM, rows - t.m * kBM);
+  t.row0 = start + t.m * TILE_M;
+  t.rows_valid = min(TILE_M, rows - t.m * TILE_M);
   return t;
 }
 
@@ -342,6 +343,264 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Pair variant (cta_group::2): a cluster of two CTAs on two SMs computes a
+// 256-row tile.  Each CTA loads its own 128 rows of A and half (BN/2 rows) of
+// the B tile; the even CTA issues the pair MMAs (M=256, N=BN), which read A
+// and B from both CTAs' shared memory and leave rows 0-127 of the
+// accumulator in its TMEM and rows 128-255 in the peer's.  Per SM this halves
+// the B bytes per FLOP and, with 32 KB stages, gives a 6-stage ring.
+//   full[s]       in the even CTA, completed by both CTAs' TMA bytes;
+//   empty[s]      in both CTAs, the pair MMA commit arrives on both;
+//   tmem_full[b]  in both CTAs, the pair MMA commit arrives on both;
+//   tmem_empty[b] in the even CTA, all 8 epilogue warps of the pair arrive.
+// ---------------------------------------------------------------------------
+template <int BN, bool SWIGLU>
+struct Cfg2 {
+  static constexpr int A_BYTES = 128 * kBK * 2;
+  static constexpr int B_BYTES = (BN / 2) * kBK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = kStageBudget / STAGE_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BN_OUT = SWIGLU ? BN / 2 : BN;
+  static constexpr int HALF = BN / 2;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int MT_OFF = MISC_OFF + 16;
+  static constexpr int SMEM_BYTES = MT_OFF + (kMaxE + 1) * 4 + 1024;
+  static_assert(BN == 256 || BN == 128, "pair tile width");
+  static_assert(STAGES >= 4, "pipeline depth");
+};
+
+template <int BN, bool SWIGLU>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, const KArgs args) {
+  using C = Cfg2<BN, SWIGLU>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *smA = smem;
+  uint8_t *smB = smem + C::STAGES * C::A_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + C::STAGES;
+  uint64_t *tmem_full = bars + 2 * C::STAGES;
+  uint64_t *tmem_empty = tmem_full + 2;
+  uint64_t *drain = tmem_full + 4;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+  int32_t *mt = reinterpret_cast<int32_t *>(smem + C::MT_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool even = rank == 0;
+  const int cid = static_cast<int>(blockIdx.x >> 1);
+  const int ncl = static_cast<int>(gridDim.x >> 1);
+
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) mt[i] = args.mtile_base[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  cluster_sync_all();  // both CTAs' barriers exist before any remote use
+  const int total = mt[args.E] * args.n_tiles;
+  if (cid >= total) return;  // uniform across the pair
+
+  if (warp == 1) tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int kblocks = args.K / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[C::STAGES];
+      bool issued[C::STAGES];
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) issued[s] = false;
+      for (int u = cid; u < total && !*abort_flag; u += ncl) {
+        const Tile t = decode_tile<256>(args, mt, u);
+        const int a_row = t.row0 + 128 * static_cast<int>(rank);
+        int b_row;
+        if (SWIGLU)  // even CTA: gate rows, odd CTA: the matching up rows
+          b_row = t.e * args.b_rows + (even ? 0 : args.up_off) + t.n * C::HALF;
+        else
+          b_row = t.e * args.b_rows + t.n * BN + static_cast<int>(rank) * C::HALF;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
+                                 args.wait_limit_ns))
+            break;
+          if (even) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+          const uint32_t fbar = mapa_shared(&full[stage], 0);
+          tma_load_2d_pair(smA + stage * C::A_BYTES, &tmA, fbar, kb * kBK, a_row);
+          tma_load_2d_pair(smB + stage * C::B_BYTES, &tmB, fbar, kb * kBK, b_row);
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // drain: the even CTA sees its full barriers; the odd CTA knows its
+      // copies landed once the pair MMA that read them released the slot
+      for (int s = 0; s < C::STAGES; ++s)
+        if (issued[s]) {
+          if (even)
+            wait_drain(&full[s], issued_phase[s], args.wait_limit_ns);
+          else
+            wait_drain(&empty[s], issued_phase[s], args.wait_limit_ns);
+        }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && even) {
+      // ---------------- pair MMA issuer (even CTA) ----------------
+      constexpr uint32_t kIdesc = mma_idesc_bf16_f32(256, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool any_mma = false;
+      for (int u = cid; u < total && !*abort_flag; u += ncl) {
+        if (!mbar_wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, args.status,
+                               args.wait_limit_ns))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.status,
+                                 args.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(smA + stage * C::A_BYTES));
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16_ss_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, kIdesc,
+                             (kb | kk) != 0 ? 1u : 0u);
+          any_mma = true;
+          mma_commit_pair(&empty[stage], 0x3);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&tmem_full[acc], 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (any_mma) {
+        mma_commit_pair(drain, 0x1);
+        wait_drain(drain, 0, args.wait_limit_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;               // TMEM lane = row in this CTA's half
+    const int prow = static_cast<int>(rank) * 128 + row;  // row within the 256-row tile
+    const uint32_t empty_even = mapa_shared(&tmem_empty[0], 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = cid; u < total; u += ncl) {
+      const Tile t = decode_tile<256>(args, mt, u);
+      const bool waited = mbar_wait_bounded(&tmem_full[acc], acc_phase, abort_flag,
+                                            args.status, args.wait_limit_ns);
+      if (!__all_sync(0xffffffffu, waited)) break;
+      tc_fence_after();
+      const uint32_t tb =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const int64_t grow = static_cast<int64_t>(t.row0) + prow;
+      const bool ok = prow < t.rows_valid && grow >= 0 && grow < args.rows_total;
+      if (SWIGLU) {
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(args.out) + grow * args.ldo +
+                             static_cast<int64_t>(t.n) * C::BN_OUT;
+#pragma unroll 1
+        for (int c = 0; c < C::BN_OUT / 32; ++c) {
+          uint32_t g[32], v[32];
+          tmem_ld_32x32b_x32(tb + c * 32, g);
+          tmem_ld_32x32b_x32(tb + C::HALF + c * 32, v);
+          tmem_ld_wait();
+          tmem_regs_fence(g);
+          tmem_regs_fence(v);
+          if (ok) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+              const float u0 = __uint_as_float(v[2 * i]), u1 = __uint_as_float(v[2 * i + 1]);
+              const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+              const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+              packed[i] = pack_bf16x2(h0, h1);
+            }
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                 packed[4 * i + 3]);
+          }
+        }
+      } else {
+        float *dst = static_cast<float *>(args.out) + grow * args.ldo +
+                     static_cast<int64_t>(t.n) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + c * 32, v);
+          tmem_ld_wait();
+          tmem_regs_fence(v);
+          if (ok) {
+            float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (even)
+          mbar_arrive(&tmem_empty[acc]);
+        else
+          mbar_arrive_remote(empty_even + static_cast<uint32_t>(acc) * 8u);
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // no CTA leaves while its peer may still use its memory
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
 // bounded-wait self test: one thread waits on a barrier nobody arrives on
 // ---------------------------------------------------------------------------
 __global__ void wait_selftest_kernel(uint32_t *status, uint64_t limit_ns) {
@@ -431,6 +690,61 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int BN, bool SWIGLU>
+cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
+  using C = Cfg2<BN, SWIGLU>;
+  CUtensorMap tmA, tmB;
+  if (!make_tmap(&tmA, p.a, static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.rows_total),
+                 128))
+    return cudaErrorInvalidValue;
+  if (!make_tmap(&tmB, p.b, static_cast<uint64_t>(p.K),
+                 static_cast<uint64_t>(p.E) * static_cast<uint64_t>(p.b_rows), C::HALF))
+    return cudaErrorInvalidValue;
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<BN, SWIGLU>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  KArgs a;
+  a.E = p.E;
+  a.K = p.K;
+  a.n_tiles = p.n_out / C::BN_OUT;
+  a.layout = p.layout;
+  a.M_max = p.M_max;
+  a.b_rows = p.b_rows;
+  a.up_off = up_off;
+  a.seg = p.seg;
+  a.mtile_base = p.mtile_base;
+  a.out = p.out;
+  a.ldo = p.n_out;
+  a.rows_total = p.rows_total;
+  a.m_block = static_cast<int>((24ll << 20) / (512ll * p.K));
+  if (a.m_block < 1) a.m_block = 1;
+  a.status = p.status;
+  a.wait_limit_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitLimitNs;
+  // persistent grid: as many CTA pairs as can be resident at once
+  int clusters = 0;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_pair_kernel<BN, SWIGLU>, &cfg);
+    if (err != cudaSuccess) return err;
+  }
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  grouped_gemm_pair_kernel<BN, SWIGLU><<<2 * clusters, kGemmThreads, C::SMEM_BYTES, s>>>(
+      tmA, tmB, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int num_sms() {
@@ -446,6 +760,10 @@ int num_sms() {
 
 cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s) {
   // p.n_out = inter, p.b_rows = 2*inter, K = d
+  if (p.pair) {
+    if (p.n_out % 128 == 0) return run_gemm_pair<256, true>(p, p.n_out, s);
+    return cudaErrorInvalidValue;
+  }
   if (p.n_out % 128 == 0) return run_gemm<256, true>(p, p.n_out, s);
   if (p.n_out % 64 == 0) return run_gemm<128, true>(p, p.n_out, s);
   return cudaErrorInvalidValue;
@@ -453,6 +771,10 @@ cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s) {
 
 cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s) {
   // p.n_out = d, p.b_rows = d, K = inter
+  if (p.pair) {
+    if (p.n_out % 256 == 0) return run_gemm_pair<256, false>(p, 0, s);
+    return cudaErrorInvalidValue;
+  }
   if (p.n_out % 256 == 0) return run_gemm<256, false>(p, 0, s);
   if (p.n_out % 128 == 0) return run_gemm<128, false>(p, 0, s);
   if (p.n_out % 64 == 0) return run_gemm<64, false>(p, 0, s);

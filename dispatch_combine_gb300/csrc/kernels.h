@@ -29,11 +29,17 @@ inline int64_t dispatch_num_chunks(int64_t n) {
 cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void *x, int d,
                             int32_t *counts, int32_t *offsets, int32_t *src_token,
                             int32_t *dest, void *x_perm, int32_t *chunk_scratch,
-                            int32_t *mtile_base, uint32_t *status, cudaStream_t s);
-// mtile_base[e] = sum_{e'<e} ceil(M_e'/128) for the contiguous (seg = offsets)
-// or masked (seg = masked_m, clamped to M_max) layout.
-cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max,
+                            int32_t *mtile_base, int tile_rows, uint32_t *status,
+                            cudaStream_t s);
+// mtile_base[e] = sum_{e'<e} ceil(M_e'/tile_rows) for the contiguous (seg =
+// offsets) or masked (seg = masked_m, clamped to M_max) layout.
+cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,
                              int32_t *mtile_base, uint32_t *status, cudaStream_t s);
+// Expert GEMMs run on CTA pairs with 256-row tiles when the average number
+// of rows per expert reaches this.  Below it, the MMA work wasted on each
+// expert's last, partly filled 256-row tile outweighs the halved B traffic
+// per SM (measured at 512 rows per expert: no gain).
+constexpr int64_t kPairRowsPerExpert = 1024;
 
 // combine.cu
 cudaError_t launch_combine(const float *y_perm, const int32_t *dest, const float *w, int T,
@@ -55,6 +61,7 @@ struct GemmProblem {
   void *out;                 // bf16 h [rows, inter] or fp32 y [rows, d]
   uint32_t *status;
   uint64_t wait_limit_ns;
+  bool pair;  // 256-row tiles on CTA pairs (mtile_base counts 256-row tiles)
 };
 cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s);
 cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s);

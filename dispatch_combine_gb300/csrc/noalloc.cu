@@ -68,6 +68,6 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_shape_t *shape, const int
   if (ast != MOE_OK) return ast;
   const cudaError_t err = moe::launch_dispatch(topk_ids, shape->T, shape->k, shape->E, x,
                                                shape->d, counts, offsets, src_token, dest, x_perm,
-                                               scratch, nullptr, nullptr, stream);
+                                               scratch, nullptr, 128, nullptr, stream);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -452,6 +452,108 @@ __global__ void __launch_bounds__(kSelWarps * 32)
   if (lane < k) weights[(size_t)t * k + lane] = __fdiv_rn(v, sum);
 }
 
+// Fast path of the selection: lane l holds the PER consecutive experts
+// l*PER .. l*PER+PER-1, so a group of gs experts spans gs/PER lanes and all
+// groups' top-2 reduce at once; a group's rank (how many groups beat it,
+// ties to the lower index) comes from G independent broadcasts.  Same
+// decisions as router_select_kernel; requires G == 1 or gs a power-of-two
+// multiple of PER.
+template <int PER>
+__global__ void __launch_bounds__(kSelWarps * 32)
+    router_select_fast_kernel(const float *__restrict__ logits, const float *__restrict__ bias,
+                              int T, int E, int G, int topk_group, int k, int score,
+                              float bias_scale, int mode, int32_t *__restrict__ ids,
+                              float *__restrict__ weights) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float *lt = logits + (size_t)t * E;
+  const float kNegInf = -__int_as_float(0x7f800000);
+  const int e0 = lane * PER;
+
+  float s[PER];
+#pragma unroll
+  for (int m = 0; m < PER; ++m) {
+    const int e = e0 + m;
+    s[m] = kNegInf;
+    if (e < E) {
+      const float l = lt[e];
+      if (mode == 1 || score == MOE_SCORE_SOFTMAX)
+        s[m] = l;
+      else
+        s[m] = __fadd_rn(canon_sigmoid(l), __fmul_rn(bias_scale, bias[e]));
+    }
+  }
+  uint32_t eligible = 0;
+#pragma unroll
+  for (int m = 0; m < PER; ++m)
+    if (e0 + m < E) eligible |= 1u << m;
+
+  if (G > 1) {
+    const int gs = E / G;
+    const int lpg = gs / PER;  // lanes per group (power of two)
+    float m1 = kNegInf, m2 = kNegInf;
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      const float v = s[m];
+      if (v > m1) {
+        m2 = m1;
+        m1 = v;
+      } else if (v > m2) {
+        m2 = v;
+      }
+    }
+    for (int off = 1; off < lpg; off <<= 1) {
+      const float o1 = __shfl_xor_sync(0xffffffffu, m1, off);
+      const float o2 = __shfl_xor_sync(0xffffffffu, m2, off);
+      if (m1 >= o1) {
+        m2 = fmaxf(m2, o1);
+      } else {
+        m2 = fmaxf(m1, o2);
+        m1 = o1;
+      }
+    }
+    const float mine = (gs >= 2) ? __fadd_rn(m1, m2) : m1;
+    const int my_group = (e0 < E) ? e0 / gs : G;
+    int rank = 0;
+    for (int g = 0; g < G; ++g) {
+      const float o = __shfl_sync(0xffffffffu, mine, g * lpg);
+      rank += (o > mine || (o == mine && g < my_group)) ? 1 : 0;
+    }
+    if (my_group >= G || rank >= topk_group) eligible = 0;
+  }
+
+  int my_id = -1;
+  for (int j = 0; j < k; ++j) {
+    float bv = kNegInf;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      if ((eligible >> m) & 1u) {
+        if (s[m] > bv || bi == 0x7fffffff) {
+          bv = s[m];
+          bi = e0 + m;
+        }
+      }
+    }
+    warp_argmax(bv, bi);
+    if (bi != 0x7fffffff && bi / PER == lane) eligible &= ~(1u << (bi - e0));
+    if (lane == j) my_id = bi;
+  }
+
+  if (lane < k) ids[(size_t)t * k + lane] = my_id;
+  if (mode == 1) return;
+  const float l0 = __shfl_sync(0xffffffffu, (lane < k) ? lt[my_id] : 0.0f, 0);
+  float v = 0.0f;
+  if (lane < k) {
+    const float l = lt[my_id];
+    v = (score == MOE_SCORE_SOFTMAX) ? canon_exp(__fsub_rn(l, l0)) : canon_sigmoid(l);
+  }
+  float sum = __shfl_sync(0xffffffffu, v, 0);
+  for (int j = 1; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, v, j));
+  if (lane < k) weights[(size_t)t * k + lane] = __fdiv_rn(v, sum);
+}
+
 }  // namespace
 
 size_t router_scratch_bytes(int d, int E) {
@@ -482,6 +584,32 @@ cudaError_t launch_router_select(const float *logits, const float *bias, int T, 
                                  int32_t *ids, float *weights, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int grid = (T + kSelWarps - 1) / kSelWarps;
+  int per = 1;
+  while (per * 32 < E) per *= 2;
+  bool fast = per <= 32;
+  if (fast && G > 1) {
+    const int gs = E / G;
+    const int lpg = gs / per;
+    fast = gs % per == 0 && lpg >= 1 && lpg <= 32 && (lpg & (lpg - 1)) == 0;
+  }
+  if (fast) {
+#define MOE_SELECT_FAST(P)                                                                  \
+  case P:                                                                                   \
+    router_select_fast_kernel<P><<<grid, kSelWarps * 32, 0, s>>>(                           \
+        logits, bias, T, E, G, topk_group, k, score, bias_scale, mode, ids, weights);       \
+    return cudaGetLastError();
+    switch (per) {
+      MOE_SELECT_FAST(1)
+      MOE_SELECT_FAST(2)
+      MOE_SELECT_FAST(4)
+      MOE_SELECT_FAST(8)
+      MOE_SELECT_FAST(16)
+      MOE_SELECT_FAST(32)
+      default:
+        break;
+    }
+#undef MOE_SELECT_FAST
+  }
   router_select_kernel<<<grid, kSelWarps * 32, 0, s>>>(logits, bias, T, E, G, topk_group, k,
                                                        score, bias_scale, mode, ids, weights);
   return cudaGetLastError();

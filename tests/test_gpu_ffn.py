@@ -68,6 +68,28 @@ def test_ffn_contiguous(counts, d, inter):
     check_ffn(y.cpu().numpy(), bits(x), row_e, bits(w_gu), bits(w_down), "y")
 
 
+@pytest.mark.parametrize("counts,d,inter", [
+    ([1100, 1000], 512, 256),      # ragged pair tiles; the odd CTA of one has no rows
+    ([0, 2561, 768], 1024, 384),   # empty expert, exact multiples of 256
+    ([4000, 40, 300, 700], 256, 128),
+])
+def test_ffn_pair_tiles(counts, d, inter):
+    # T*k >= 1024 rows per expert selects the CTA-pair (cta_group::2) kernels
+    ensure_lib()
+    E = len(counts)
+    assert sum(counts) >= 1024 * E
+    w_gu, w_down = _weights(E, d, inter, seed=d * 3 + inter)
+    x, offsets, row_e = _contiguous_case(counts, d, inter, seed=d + 7)
+    shape = _shape(E, d, inter, T=x.shape[0], k=1)
+    ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    y = torch.full((x.shape[0], d), float("nan"), dtype=torch.float32, device="cuda")
+    moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_CONTIGUOUS, x.cuda(), offsets.cuda(), 0,
+                       w_gu.cuda(), w_down.cuda(), ws, y_out=y)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    check_ffn(y.cpu().numpy(), bits(x), row_e, bits(w_gu), bits(w_down), "y (pair)")
+
+
 def test_gate_up_alone_matches_oracle_h():
     ensure_lib()
     counts = [17, 129, 0, 256]
