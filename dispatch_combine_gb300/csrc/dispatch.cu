@@ -22,13 +22,13 @@ namespace {
 constexpr int kCountThreads = 256;
 
 __global__ void __launch_bounds__(kCountThreads)
-    dispatch_count_kernel(const int32_t *__restrict__ ids, int64_t n, int E,
+    dispatch_count_kernel(const int32_t *__restrict__ ids, int64_t n, int E, int chunk,
                           int32_t *__restrict__ chunk_counts, uint32_t *status) {
   extern __shared__ int hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  const int64_t a0 = (int64_t)blockIdx.x * kDispatchChunk;
-  for (int q = threadIdx.x; q < kDispatchChunk; q += blockDim.x) {
+  const int64_t a0 = (int64_t)blockIdx.x * chunk;
+  for (int q = threadIdx.x; q < chunk; q += blockDim.x) {
     const int64_t a = a0 + q;
     if (a < n) {
       const int id = ids[a];
@@ -75,20 +75,45 @@ __device__ int block_exclusive_scan(int v, int *total) {
   return res;
 }
 
-// one CTA of 1024 threads, thread e owns expert e (E <= 1024)
+// One CTA of 1024 threads (E <= 1024).  The chunks of expert e are split in
+// Q consecutive ranges, Q = 1024 / (E rounded up to a power of two); thread
+// (q, e) sums range q, the range sums are scanned in shared memory, then
+// every thread rewrites its range as exclusive running counts.
 __global__ void __launch_bounds__(1024)
     dispatch_scan_kernel(int32_t *__restrict__ chunk_counts, int nchunks, int E,
                          int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                          int32_t *__restrict__ mtile_base, int tile_rows) {
-  const int e = threadIdx.x;
-  int run = 0;
-  if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = chunk_counts[(size_t)c * E + e];
-      chunk_counts[(size_t)c * E + e] = run;
-      run += v;
+  __shared__ int part[1024];
+  int ep = 1;
+  while (ep < E) ep <<= 1;
+  const int Q = 1024 / ep;
+  const int eq = threadIdx.x % ep, q = threadIdx.x / ep;
+  const int per = (nchunks + Q - 1) / Q;
+  const int c0 = q * per, c1 = min(nchunks, c0 + per);
+  int local = 0;
+  if (eq < E) {
+#pragma unroll 8
+    for (int c = c0; c < c1; ++c) local += chunk_counts[(size_t)c * E + eq];
+  }
+  part[threadIdx.x] = local;
+  __syncthreads();
+  int base = 0, run = 0;
+  for (int q2 = 0; q2 < Q; ++q2) {
+    const int v = part[q2 * ep + eq];
+    if (q2 < q) base += v;
+    run += v;
+  }
+  if (eq < E) {
+    int r = base;
+    for (int c = c0; c < c1; ++c) {
+      const int v = chunk_counts[(size_t)c * E + eq];
+      chunk_counts[(size_t)c * E + eq] = r;
+      r += v;
     }
   }
+  // thread e < E (range q == 0 of expert e) carries expert e's total
+  const int e = threadIdx.x;
+  if (e >= E) run = 0;
   int total = 0;
   const int excl = block_exclusive_scan(e < E ? run : 0, &total);
   if (e < E) {
@@ -108,20 +133,20 @@ __global__ void __launch_bounds__(1024)
 constexpr int kScatterWarps = 4;
 
 __global__ void __launch_bounds__(kScatterWarps * 32)
-    dispatch_scatter_kernel(const int32_t *__restrict__ ids, int64_t n, int k, int E,
+    dispatch_scatter_kernel(const int32_t *__restrict__ ids, int64_t n, int k, int E, int chunk,
                             int64_t nchunks, const int32_t *__restrict__ chunk_base,
                             const int32_t *__restrict__ offsets, int32_t *__restrict__ dest,
                             int32_t *__restrict__ src_token) {
   extern __shared__ int cursor_all[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t chunk = (int64_t)blockIdx.x * kScatterWarps + warp;
-  if (chunk >= nchunks) return;
+  const int64_t ci = (int64_t)blockIdx.x * kScatterWarps + warp;
+  if (ci >= nchunks) return;
   int *cursor = cursor_all + warp * E;
-  for (int e = lane; e < E; e += 32) cursor[e] = chunk_base[chunk * E + e] + offsets[e];
+  for (int e = lane; e < E; e += 32) cursor[e] = chunk_base[ci * E + e] + offsets[e];
   __syncwarp();
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int s = 0; s < kDispatchChunk / 32; ++s) {
-    const int64_t a = chunk * kDispatchChunk + s * 32 + lane;
+  for (int s = 0; s < chunk / 32; ++s) {
+    const int64_t a = ci * chunk + s * 32 + lane;
     int id = (a < n) ? ids[a] : -1;
     const bool valid = id >= 0 && id < E;
     if (!valid) id = -1;
@@ -145,6 +170,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
 
 constexpr int kGatherWarps = 8;
 
+// Warp per row; each lane moves up to 8 16-byte vectors per pass with all
+// loads issued before the stores.
 __global__ void __launch_bounds__(kGatherWarps * 32)
     dispatch_gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ src_token,
                            const int32_t *__restrict__ offsets_end, int64_t n, int T,
@@ -159,16 +186,19 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
     if (t < 0 || t >= T) continue;
     const uint4 *src = x + (size_t)t * vec_per_row;
     uint4 *dst = x_perm + (size_t)row * vec_per_row;
-    int v = lane;
-    for (; v + 96 < vec_per_row; v += 128) {
-      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
-                  d = __ldg(src + v + 96);
-      dst[v] = a;
-      dst[v + 32] = b;
-      dst[v + 64] = c;
-      dst[v + 96] = d;
+    for (int v0 = 0; v0 < vec_per_row; v0 += 256) {
+      uint4 r[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec_per_row) r[u] = __ldg(src + v);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec_per_row) dst[v] = r[u];
+      }
     }
-    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
   }
 }
 
@@ -212,9 +242,10 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
                             cudaStream_t s) {
   const int64_t n = (int64_t)T * k;
   const int64_t nchunks = dispatch_num_chunks(n);
+  const int chunk = dispatch_chunk(n);
   if (n == 0) return cudaSuccess;
   dispatch_count_kernel<<<(unsigned)nchunks, kCountThreads, E * sizeof(int), s>>>(
-      ids, n, E, chunk_scratch, status);
+      ids, n, E, chunk, chunk_scratch, status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_scratch, (int)nchunks, E, counts, offsets,
@@ -223,7 +254,7 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
   if (err != cudaSuccess) return err;
   const unsigned sblocks = (unsigned)((nchunks + kScatterWarps - 1) / kScatterWarps);
   dispatch_scatter_kernel<<<sblocks, kScatterWarps * 32, kScatterWarps * E * sizeof(int), s>>>(
-      ids, n, k, E, nchunks, chunk_scratch, offsets, dest, src_token);
+      ids, n, k, E, chunk, nchunks, chunk_scratch, offsets, dest, src_token);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (x != nullptr && x_perm != nullptr) {

@@ -67,6 +67,7 @@ struct Tile {
 struct KArgs {
   int E, K, n_tiles, layout, M_max, b_rows, up_off;
   int m_block;  // m-tiles per rasterization block (A rows of a block stay in L2)
+  int out_v8;   // output base 32-byte aligned: 32-byte stores
   int64_t rows_total;
   const int32_t *seg;
   const int32_t *mtile_base;
@@ -303,11 +304,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
               packed[i] = pack_bf16x2(h0, h1);
             }
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+            if (args.out_v8) {
+              // each lane writes whole 32-byte sectors of its row
+              uint32_t w8[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                 packed[4 * i + 3]);
+              for (int i = 0; i < 8; ++i) w8[i] = packed[i];
+              st_global_v8(dst + c * 32, w8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w8[i] = packed[8 + i];
+              st_global_v8(dst + c * 32 + 16, w8);
+            } else {
+              uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                   packed[4 * i + 3]);
+            }
           }
         }
       } else {
@@ -320,11 +332,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld_wait();
           tmem_regs_fence(v);
           if (ok) {
-            float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+            if (args.out_v8) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) w8[j] = v[8 * i + j];
+                st_global_v8(dst + c * 32 + 8 * i, w8);
+              }
+            } else {
+              float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            }
           }
         }
       }
@@ -556,11 +578,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
               const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
               packed[i] = pack_bf16x2(h0, h1);
             }
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+            if (args.out_v8) {
+              // each lane writes whole 32-byte sectors of its row
+              uint32_t w8[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                 packed[4 * i + 3]);
+              for (int i = 0; i < 8; ++i) w8[i] = packed[i];
+              st_global_v8(dst + c * 32, w8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w8[i] = packed[8 + i];
+              st_global_v8(dst + c * 32 + 16, w8);
+            } else {
+              uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                   packed[4 * i + 3]);
+            }
           }
         }
       } else {
@@ -573,11 +606,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           tmem_ld_wait();
           tmem_regs_fence(v);
           if (ok) {
-            float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+            if (args.out_v8) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) w8[j] = v[8 * i + j];
+                st_global_v8(dst + c * 32 + 8 * i, w8);
+              }
+            } else {
+              float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            }
           }
         }
       }
@@ -681,6 +724,7 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.out = p.out;
   a.ldo = p.n_out;
   a.rows_total = p.rows_total;
+  a.out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
   // A rows of one block: about 24 MB (a 128-row tile holds 256*K bytes)
   a.m_block = static_cast<int>((24ll << 20) / (256ll * p.K));
   if (a.m_block < 1) a.m_block = 1;
@@ -717,6 +761,7 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.out = p.out;
   a.ldo = p.n_out;
   a.rows_total = p.rows_total;
+  a.out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
   a.m_block = static_cast<int>((24ll << 20) / (512ll * p.K));
   if (a.m_block < 1) a.m_block = 1;
   a.status = p.status;

@@ -22,9 +22,12 @@ cudaError_t launch_router_select(const float *logits, const float *bias, int T, 
                                  int32_t *ids, float *weights, cudaStream_t s);
 
 // dispatch.cu
-constexpr int kDispatchChunk = 512;
+// Assignments per dispatch chunk: 128 up to 32768 assignments (enough chunks
+// to spread the ordered scatter over many warps), 512 above.
+inline int dispatch_chunk(int64_t n) { return n <= 32768 ? 128 : 512; }
 inline int64_t dispatch_num_chunks(int64_t n) {
-  return (n + kDispatchChunk - 1) / kDispatchChunk;
+  const int c = dispatch_chunk(n);
+  return (n + c - 1) / c;
 }
 cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void *x, int d,
                             int32_t *counts, int32_t *offsets, int32_t *src_token,

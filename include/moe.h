@@ -228,7 +228,8 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
  *   Arguments and outputs are those of moe_dispatch minus the workspace.
  *   The per-chunk expert histograms live in a 1 MiB device array inside the
  *   library (every GPU that loads the library holds it until exit), which
- *   limits ceil(T*k / 512) * E to 262144 entries (T*k <= 524288 at E = 256);
+ *   limits ceil(T*k / c) * E to 262144 entries, c being the assignments per
+ *   chunk (128 up to T*k = 32768, 512 beyond; so T*k <= 524288 at E = 256);
  *   larger shapes return MOE_ERR_UNSUPPORTED.  Nothing is allocated.
  *   The first call on a device looks up the array's device address (no
  *   allocation); make that first call before any stream capture.

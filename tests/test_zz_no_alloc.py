@@ -48,7 +48,7 @@ def test_noalloc_dispatch_equals_workspace_dispatch_twice():
 
 def test_noalloc_dispatch_rejects_shapes_beyond_its_array():
     ensure_lib()
-    # ceil(T*k/512) * E = 1025 * 256 > 262144 entries
+    # ceil(T*k/512) * E = 1025 * 256 > 262144 entries (512 per chunk above 32768)
     T, k, E = 65600, 8, 256
     shape = _shape(T, 8, E, k)
     ids = torch.zeros(T, k, dtype=torch.int32, device="cuda")
