@@ -350,6 +350,8 @@ def run_gpu(args, c):
     n_touched = int((cnt > 0).sum())
     mean = float(cnt.float().mean())
     r_imb = float(cnt.max()) / mean if mean > 0 else 0.0
+    m_tiles = int(((cnt + 127) // 128).sum())
+    tile_fill = float(cnt.sum()) / (128.0 * m_tiles) if m_tiles else 0.0
 
     peaks, peak_src = load_peaks()
     hbm = peaks["hbm_gbs"] * 1e9
@@ -441,7 +443,8 @@ def run_gpu(args, c):
         "roofline": roof,
         "stages": stages,
         "ffn": {"us": ffn_sec * 1e6, "frac": ffn_bound / ffn_sec,
-                "n_touched_experts": n_touched, "r_imbalance": r_imb},
+                "n_touched_experts": n_touched, "r_imbalance": r_imb,
+                "m_tiles_128": m_tiles, "tile_fill": tile_fill},
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": moe.moe_layer_launch_count(shape) * K,

@@ -12,9 +12,11 @@ namespace moe {
 namespace {
 
 constexpr int kCombineThreads = 256;
+constexpr int kCombineVec = 2;  // 16-byte column vectors per thread
 
-// One CTA per (token, 1024-column segment): every thread keeps k 16-byte
-// loads in flight, so even a few hundred tokens fill the GPU.
+// One CTA per (token, kCombineVec * 1024-column segment): every thread keeps
+// kCombineVec * k 16-byte loads in flight, so even a few hundred tokens fill
+// the GPU.
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__ dest,
                    const float *__restrict__ w, int T, int k, int d4, int segs,
@@ -32,18 +34,34 @@ __global__ void __launch_bounds__(kCombineThreads)
     s_w[threadIdx.x] = in ? w[(size_t)t * k + threadIdx.x] : 0.0f;
   }
   __syncthreads();
-  const int v = seg * kCombineThreads + threadIdx.x;
-  if (v >= d4) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int v0 = seg * kCombineThreads * kCombineVec + threadIdx.x;
+  float4 acc[kCombineVec];
+#pragma unroll
+  for (int u = 0; u < kCombineVec; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int j = 0; j < k; ++j) {
     const float wj = s_w[j];
-    const float4 yv = __ldg(y_perm + (size_t)s_row[j] * d4 + v);
-    acc.x = fmaf(wj, yv.x, acc.x);
-    acc.y = fmaf(wj, yv.y, acc.y);
-    acc.z = fmaf(wj, yv.z, acc.z);
-    acc.w = fmaf(wj, yv.w, acc.w);
+    const float4 *row = y_perm + (size_t)s_row[j] * d4;
+    float4 yv[kCombineVec];
+#pragma unroll
+    for (int u = 0; u < kCombineVec; ++u) {
+      const int v = v0 + u * kCombineThreads;
+      yv[u] = (v < d4) ? __ldg(row + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kCombineVec; ++u) {
+      acc[u].x = fmaf(wj, yv[u].x, acc[u].x);
+      acc[u].y = fmaf(wj, yv[u].y, acc[u].y);
+      acc[u].z = fmaf(wj, yv[u].z, acc[u].z);
+      acc[u].w = fmaf(wj, yv[u].w, acc[u].w);
+    }
   }
-  y[(size_t)t * d4 + v] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+#pragma unroll
+  for (int u = 0; u < kCombineVec; ++u) {
+    const int v = v0 + u * kCombineThreads;
+    if (v < d4)
+      y[(size_t)t * d4 + v] =
+          make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+  }
 }
 
 }  // namespace
@@ -52,7 +70,7 @@ cudaError_t launch_combine(const float *y_perm, const int32_t *dest, const float
                            int k, int d, void *y, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int d4 = d / 4;
-  const int segs = (d4 + kCombineThreads - 1) / kCombineThreads;
+  const int segs = (d4 + kCombineThreads * kCombineVec - 1) / (kCombineThreads * kCombineVec);
   const int64_t blocks = static_cast<int64_t>(T) * segs;
   combine_kernel<<<static_cast<unsigned>(blocks), kCombineThreads, 0, s>>>(
       reinterpret_cast<const float4 *>(y_perm), dest, w, T, k, d4, segs,

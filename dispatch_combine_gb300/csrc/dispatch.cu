@@ -86,7 +86,8 @@ __global__ void __launch_bounds__(1024)
   __shared__ int part[1024];
   int ep = 1;
   while (ep < E) ep <<= 1;
-  const int Q = 1024 / ep;
+  // ranges per expert: enough to keep each range short, no more
+  const int Q = min(1024 / ep, max(1, nchunks / 8));
   const int eq = threadIdx.x % ep, q = threadIdx.x / ep;
   const int per = (nchunks + Q - 1) / Q;
   const int c0 = q * per, c1 = min(nchunks, c0 + per);

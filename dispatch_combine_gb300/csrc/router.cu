@@ -277,6 +277,160 @@ __global__ void __launch_bounds__(NT, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Small E (W_r fits in shared memory): a persistent kernel keeps all of W_r
+// (bf16, d x EP) in shared memory and streams x.  Warp = TT tokens, lane =
+// slice, so lane l sums the inputs of its chunks in order, exactly as above;
+// the 32 slice sums meet in the xor butterfly.  W row i sits at
+// i + (i / 8) rows of 16 bytes (EP = 8) -- one padding row per chunk -- so
+// the 32 lanes, which read rows 8 apart, hit distinct banks.
+// ---------------------------------------------------------------------------
+constexpr int kSmallWarps = 8;
+constexpr int kSmallTT = 2;  // tokens per warp
+constexpr int kSmallPF = 4;  // rounds of x in flight per lane
+
+template <int EP>
+struct SmallCfg {
+  static constexpr int ROWB = EP * 2;  // bytes per W row
+  static constexpr int CHUNKB = 9 * ROWB;  // 8 rows + 1 padding row per chunk
+};
+
+// whole rounds of 32 chunks are staged (zeros past d), so every lane of the
+// last round reads inside the buffer
+__host__ inline size_t router_small_smem(int d, int EP) {
+  const int chunks = (d + 255) / 256 * 32;
+  return static_cast<size_t>(chunks) * 9 * EP * 2;
+}
+
+template <int EP>
+__global__ void __launch_bounds__(kSmallWarps * 32)
+    router_logits_small_kernel(const __nv_bfloat16 *__restrict__ x,
+                               const uint16_t *__restrict__ w_r, int T, int d, int E,
+                               float *__restrict__ logits) {
+  using C = SmallCfg<EP>;
+  extern __shared__ __align__(16) uint8_t wsm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int chunks = (d + 255) / 256 * 32;
+  // stage W_r: chunk c, row j -> wsm + c * CHUNKB + j * ROWB; zeros for
+  // experts >= E and inputs >= d
+  // one thread per row of 8 experts: a 16-byte load when the row is aligned
+  const bool vec = (E % 8) == 0;
+  for (int q = threadIdx.x; q < chunks * 8 * (EP / 8); q += blockDim.x) {
+    const int i = q / (EP / 8), e8 = (q % (EP / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (i < d) {
+      if (vec && e8 + 8 <= E) {
+        v = __ldg(reinterpret_cast<const uint4 *>(w_r + (size_t)i * E + e8));
+      } else {
+        uint16_t h[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) h[u] = (e8 + u < E) ? w_r[(size_t)i * E + e8 + u] : 0;
+        v = make_uint4(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16),
+                       h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
+      }
+    }
+    *reinterpret_cast<uint4 *>(wsm + (i >> 3) * C::CHUNKB + (i & 7) * C::ROWB + e8 * 2) = v;
+  }
+  __syncthreads();
+  const int rounds = (d + 255) / 256;
+  const int groups = (T + kSmallTT - 1) / kSmallTT;
+  for (int grp = blockIdx.x * kSmallWarps + warp; grp < groups;
+       grp += gridDim.x * kSmallWarps) {
+    const int t0 = grp * kSmallTT;
+    float acc[kSmallTT][EP];
+#pragma unroll
+    for (int a = 0; a < kSmallTT; ++a)
+#pragma unroll
+      for (int e = 0; e < EP; ++e) acc[a][e] = 0.0f;
+    // ring of kSmallPF rounds of this lane's x chunks
+    uint4 xr[kSmallPF][kSmallTT];
+    auto load = [&](int r, int slot) {
+      const int i0 = r * 256 + lane * 8;
+#pragma unroll
+      for (int a = 0; a < kSmallTT; ++a)
+        xr[slot][a] =
+            (r < rounds && t0 + a < T && i0 < d)
+                ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + a) * d + i0))
+                : make_uint4(0u, 0u, 0u, 0u);
+    };
+#pragma unroll
+    for (int u = 0; u < kSmallPF; ++u) load(u, u);
+    for (int r0 = 0; r0 < rounds; r0 += kSmallPF) {
+#pragma unroll
+      for (int u = 0; u < kSmallPF; ++u) {
+        const int r = r0 + u;
+        if (r < rounds) {
+          float xv[kSmallTT][8];
+#pragma unroll
+          for (int a = 0; a < kSmallTT; ++a) {
+            const uint4 v = xr[u][a];
+            xv[a][0] = bf16lo(v.x); xv[a][1] = bf16hi(v.x);
+            xv[a][2] = bf16lo(v.y); xv[a][3] = bf16hi(v.y);
+            xv[a][4] = bf16lo(v.z); xv[a][5] = bf16hi(v.z);
+            xv[a][6] = bf16lo(v.w); xv[a][7] = bf16hi(v.w);
+          }
+          load(r + kSmallPF, u);
+          const uint8_t *wc = wsm + (r * 32 + lane) * C::CHUNKB;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float wv[EP];
+#pragma unroll
+            for (int e8 = 0; e8 < EP / 8; ++e8) {
+              const uint4 w = *reinterpret_cast<const uint4 *>(wc + j * C::ROWB + e8 * 16);
+              wv[e8 * 8 + 0] = bf16lo(w.x); wv[e8 * 8 + 1] = bf16hi(w.x);
+              wv[e8 * 8 + 2] = bf16lo(w.y); wv[e8 * 8 + 3] = bf16hi(w.y);
+              wv[e8 * 8 + 4] = bf16lo(w.z); wv[e8 * 8 + 5] = bf16hi(w.z);
+              wv[e8 * 8 + 6] = bf16lo(w.w); wv[e8 * 8 + 7] = bf16hi(w.w);
+            }
+#pragma unroll
+            for (int a = 0; a < kSmallTT; ++a)
+#pragma unroll
+              for (int e = 0; e < EP; ++e) acc[a][e] = __fmaf_rn(xv[a][j], wv[e], acc[a][e]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < kSmallTT; ++a)
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        float v = acc[a][e];
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 2));
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 1));
+        acc[a][e] = v;
+      }
+#pragma unroll
+    for (int a = 0; a < kSmallTT; ++a)
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (((a * EP + e) & 31) == lane && t0 + a < T && e < E)
+          logits[(size_t)(t0 + a) * E + e] = acc[a][e];
+  }
+}
+
+template <int EP>
+cudaError_t run_logits_small(const void *x, const void *w_r, int T, int d, int E,
+                             float *logits, cudaStream_t s) {
+  const size_t smem = router_small_smem(d, EP);
+  auto kern = router_logits_small_kernel<EP>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const int groups = (T + kSmallTT - 1) / kSmallTT;
+  const int want = (groups + kSmallWarps - 1) / kSmallWarps;
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSmallWarps * 32, smem);
+  if (per_sm < 1) per_sm = 1;
+  const int cap = num_sms() * per_sm;
+  const int grid = want < cap ? want : cap;
+  kern<<<grid, kSmallWarps * 32, smem, s>>>(static_cast<const __nv_bfloat16 *>(x),
+                                            static_cast<const uint16_t *>(w_r), T, d, E, logits);
+  return cudaGetLastError();
+}
+
 template <int LT, int LE, int CE, int NT>
 cudaError_t run_logits(const void *x, const uint16_t *wpad, int T, int d, int E, float *logits,
                        cudaStream_t s) {
@@ -563,6 +717,12 @@ size_t router_scratch_bytes(int d, int E) {
 cudaError_t launch_router_logits(const void *x, const void *w_r, int T, int d, int E,
                                  float *logits, void *w_scratch, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  // W_r resident in shared memory when it fits
+  constexpr size_t kSmallSmemMax = 200 * 1024;
+  if (E <= 8 && router_small_smem(d, 8) <= kSmallSmemMax)
+    return run_logits_small<8>(x, w_r, T, d, E, logits, s);
+  if (E <= 16 && router_small_smem(d, 16) <= kSmallSmemMax)
+    return run_logits_small<16>(x, w_r, T, d, E, logits, s);
   const int64_t n = static_cast<int64_t>(router_d_pad(d)) * router_e_pad(E);
   const int64_t want = (n + 255) / 256;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;

@@ -45,6 +45,36 @@ def test_route_bit_exact_full_size(name):
     assert np.all(np.abs(w.astype(np.float64).sum(1) - 1.0) <= cfg.k * 2.0 ** -23)
 
 
+@pytest.mark.parametrize("T,d,E,G,tg,k,score", [
+    (37, 776, 3, 1, 1, 2, SCORE_SOFTMAX),        # small-E kernel, ragged d, E not % 8
+    (5, 8, 1, 1, 1, 1, SCORE_SOFTMAX),           # one round, one expert
+    (129, 7168, 8, 1, 1, 2, SCORE_SOFTMAX),      # small-E kernel, W_r 129 KB resident
+    (300, 2048, 16, 4, 2, 4, SCORE_SIGMOID_BIAS),
+    (64, 1024, 24, 3, 2, 3, SCORE_SIGMOID_BIAS),  # tiled 32 x 32 tiles
+    (100, 512, 64, 8, 4, 6, SCORE_SIGMOID_BIAS),  # tiled 16 x 64 tiles
+    (33, 264, 200, 8, 3, 5, SCORE_SIGMOID_BIAS),  # ragged d and E
+    (1000, 4096, 32, 1, 1, 8, SCORE_SOFTMAX),
+])
+def test_route_bit_exact_shapes(T, d, E, G, tg, k, score):
+    ensure_lib()
+    import moe_inputs
+    tns = moe_inputs.make_tensors_for_shape(T, d, E, 64, device="cuda", seed=T + d + E)
+    shape = dict(T=T, d=d, E=E, G=G, topk_group=tg, k=k, inter=64, score=score,
+                 bias_scale=0.15)
+    ws = moe.Workspace(moe.moe_workspace_size(shape))
+    bias = tns["bias"] if score == SCORE_SIGMOID_BIAS else None
+    ids, w, logits = moe.moe_route(shape, tns["x"], tns["w_r"], bias, ws, want_logits=True)
+    torch.cuda.synchronize()
+    from tests.gpu_common import bits
+    ref_logits = oracle.router_logits(bits(tns["x"]), bits(tns["w_r"]))
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), ref_logits.view(np.uint32))
+    ref_ids, ref_w, _ = oracle.route_from_logits(ref_logits, tns["bias"].cpu().numpy(), G, tg, k,
+                                                 score, 0.15)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    gw = w.cpu().numpy()
+    assert np.all(np.abs(gw - ref_w) <= 1e-6 * np.abs(ref_w))
+
+
 def _rand_logits(T, E, seed, kind):
     g = np.random.default_rng(seed)
     if kind == "normal":
