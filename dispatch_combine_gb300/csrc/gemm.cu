@@ -394,10 +394,26 @@ struct Cfg2 {
   static_assert(STAGES >= 4, "pipeline depth");
 };
 
+// An expert's last 256-row tile that holds at most 128 rows runs swapped
+// (BN = 256 only): the 256 weight rows of the n-tile are the pair MMA's M
+// side (128 per CTA, in the A slots), the tile's token rows are its N side
+// (N = rows rounded up to 16, N/2 rows per CTA from a 64-row box, in the B
+// slots).  The tile then costs the weight bytes plus its own rows instead
+// of a full 256-row tile.  For gate_up each CTA's 128 M rows are 4 groups of
+// [16 gate rows, the 16 matching up rows] (a 4-D tensor map), so a warp's
+// 32 TMEM lanes hold both factors of 16 intermediate columns.
+constexpr int kSwapBoxRows = 64;
+constexpr int kSwapXBytes = kSwapBoxRows * kBK * 2;
+__device__ __forceinline__ int pair_swap_n(const Tile &t) {
+  return (t.rows_valid <= 2 * kSwapBoxRows) ? ((t.rows_valid + 15) & ~15) : 0;
+}
+
 template <int BN, bool SWIGLU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                             const __grid_constant__ CUtensorMap tmB, const KArgs args) {
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmX,
+                             const __grid_constant__ CUtensorMap tmW, const KArgs args) {
   using C = Cfg2<BN, SWIGLU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -457,22 +473,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       bool issued[C::STAGES];
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) issued[s] = false;
+      tma_prefetch_desc(&tmX);
+      if (SWIGLU) tma_prefetch_desc(&tmW);
       for (int u = cid; u < total && !*abort_flag; u += ncl) {
         const Tile t = decode_tile<256>(args, mt, u);
+        const int sn = (BN == 256) ? pair_swap_n(t) : 0;
         const int a_row = t.row0 + 128 * static_cast<int>(rank);
         int b_row;
         if (SWIGLU)  // even CTA: gate rows, odd CTA: the matching up rows
           b_row = t.e * args.b_rows + (even ? 0 : args.up_off) + t.n * C::HALF;
         else
           b_row = t.e * args.b_rows + t.n * BN + static_cast<int>(rank) * C::HALF;
+        // swapped tile: this CTA's token rows, and (gate_up) its 16-row group
+        // index in the 4-D weight map
+        const int x_row = t.row0 + static_cast<int>(rank) * (sn >> 1);
+        const int w_grp = (t.e * args.b_rows + t.n * C::BN_OUT + static_cast<int>(rank) * 64) >> 4;
+        const uint32_t tx = sn ? 2u * (C::A_BYTES + kSwapXBytes) : 2u * C::STAGE_BYTES;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
                                  args.wait_limit_ns))
             break;
-          if (even) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+          if (even) mbar_arrive_expect_tx(&full[stage], tx);
           const uint32_t fbar = mapa_shared(&full[stage], 0);
-          tma_load_2d_pair(smA + stage * C::A_BYTES, &tmA, fbar, kb * kBK, a_row);
-          tma_load_2d_pair(smB + stage * C::B_BYTES, &tmB, fbar, kb * kBK, b_row);
+          if (sn == 0) {
+            tma_load_2d_pair(smA + stage * C::A_BYTES, &tmA, fbar, kb * kBK, a_row);
+            tma_load_2d_pair(smB + stage * C::B_BYTES, &tmB, fbar, kb * kBK, b_row);
+          } else {
+            if (SWIGLU)
+              tma_load_4d_pair(smA + stage * C::A_BYTES, &tmW, fbar, kb * kBK, 0, 0, w_grp);
+            else
+              tma_load_2d_pair(smA + stage * C::A_BYTES, &tmB, fbar, kb * kBK, b_row);
+            tma_load_2d_pair(smB + stage * C::B_BYTES, &tmX, fbar, kb * kBK, x_row);
+          }
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == C::STAGES) {
@@ -502,6 +534,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool any_mma = false;
       for (int u = cid; u < total && !*abort_flag; u += ncl) {
+        const int sn = (BN == 256) ? pair_swap_n(decode_tile<256>(args, mt, u)) : 0;
+        // swapped: the A slots hold weight rows (M) and the B slots token rows (N)
+        const uint32_t idesc = sn ? mma_idesc_bf16_f32(256, sn) : kIdesc;
         if (!mbar_wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, args.status,
                                args.wait_limit_ns))
           break;
@@ -519,7 +554,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const uint64_t bd = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ss_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, kIdesc,
+            mma_bf16_ss_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
                              (kb | kk) != 0 ? 1u : 0u);
           any_mma = true;
           mma_commit_pair(&empty[stage], 0x3);
@@ -557,7 +592,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
       const int64_t grow = static_cast<int64_t>(t.row0) + prow;
       const bool ok = prow < t.rows_valid && grow >= 0 && grow < args.rows_total;
-      if (SWIGLU) {
+      const int sn = (BN == 256) ? pair_swap_n(t) : 0;
+      if (sn > 0) {
+        // swapped tile: TMEM lane = weight row of this CTA's half, column =
+        // token row of the tile
+#pragma unroll 1
+        for (int c0 = 0; c0 < sn; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tb + c0, v);
+          tmem_ld_wait();
+          tmem_regs_fence16(v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int r = c0 + i;
+            const int64_t gr = static_cast<int64_t>(t.row0) + r;
+            const bool rok = r < t.rows_valid && gr >= 0 && gr < args.rows_total;
+            if (SWIGLU) {
+              // lanes 0-15: gate of intermediate column j, lanes 16-31: its up
+              const float mine = __uint_as_float(v[i]);
+              const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+              if (lane < 16 && rok) {
+                const int j = t.n * C::BN_OUT + static_cast<int>(rank) * 64 + quad * 16 + lane;
+                const float h = __fdividef(mine, 1.0f + __expf(-mine)) * other;
+                static_cast<__nv_bfloat16 *>(args.out)[gr * args.ldo + j] =
+                    __float2bfloat16_rn(h);
+              }
+            } else if (rok) {
+              const int col = t.n * BN + static_cast<int>(rank) * 128 + quad * 32 + lane;
+              static_cast<float *>(args.out)[gr * args.ldo + col] = __uint_as_float(v[i]);
+            }
+          }
+        }
+      } else if (SWIGLU) {
         __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(args.out) + grow * args.ldo +
                              static_cast<int64_t>(t.n) * C::BN_OUT;
 #pragma unroll 1
@@ -681,6 +747,25 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Gate/up weights [E * 2 inter, K] seen as 4-D (k, row in group of 16,
+// gate|up, group of 16 rows), box 64 x 16 x 2 x 4: one box holds 4 x [16 gate
+// rows, the 16 up rows up_off further] of K columns [k, k + 64).  The group
+// extent stops up_off rows short, so every element the map can address lies
+// inside the weight tensor.
+bool make_tmap_gate_up_groups(CUtensorMap *map, const void *base, uint64_t K, uint64_t rows,
+                              uint64_t up_off) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= up_off || (rows - up_off) % 16 != 0) return false;
+  const cuuint64_t dims[4] = {K, 16, 2, (rows - up_off) / 16};
+  const cuuint64_t strides[3] = {K * 2, up_off * K * 2, 16 * K * 2};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(kBK), 16, 2, 4};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2D bf16 tensor [rows, inner] row-major; box = box_rows x 64 elements,
 // 128-byte swizzle, out-of-bounds rows read as zero.
 bool make_tmap(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
@@ -737,13 +822,23 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
 template <int BN, bool SWIGLU>
 cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   using C = Cfg2<BN, SWIGLU>;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmX, tmW;
+  const uint64_t w_rows = static_cast<uint64_t>(p.E) * static_cast<uint64_t>(p.b_rows);
   if (!make_tmap(&tmA, p.a, static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.rows_total),
                  128))
     return cudaErrorInvalidValue;
-  if (!make_tmap(&tmB, p.b, static_cast<uint64_t>(p.K),
-                 static_cast<uint64_t>(p.E) * static_cast<uint64_t>(p.b_rows), C::HALF))
+  if (!make_tmap(&tmB, p.b, static_cast<uint64_t>(p.K), w_rows, C::HALF))
     return cudaErrorInvalidValue;
+  if (!make_tmap(&tmX, p.a, static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.rows_total),
+                 kSwapBoxRows))
+    return cudaErrorInvalidValue;
+  if (SWIGLU) {
+    if (!make_tmap_gate_up_groups(&tmW, p.b, static_cast<uint64_t>(p.K), w_rows,
+                                  static_cast<uint64_t>(up_off)))
+      return cudaErrorInvalidValue;
+  } else {
+    tmW = tmB;
+  }
   cudaError_t err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<BN, SWIGLU>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
@@ -786,7 +881,7 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   }
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   grouped_gemm_pair_kernel<BN, SWIGLU><<<2 * clusters, kGemmThreads, C::SMEM_BYTES, s>>>(
-      tmA, tmB, a);
+      tmA, tmB, tmX, tmW, a);
   return cudaGetLastError();
 }
 

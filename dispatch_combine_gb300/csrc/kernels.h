@@ -39,10 +39,13 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
 cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,
                              int32_t *mtile_base, uint32_t *status, cudaStream_t s);
 // Expert GEMMs run on CTA pairs with 256-row tiles when the average number
-// of rows per expert reaches this.  Below it, the MMA work wasted on each
-// expert's last, partly filled 256-row tile outweighs the halved B traffic
-// per SM (measured at 512 rows per expert: no gain).
-constexpr int64_t kPairRowsPerExpert = 1024;
+// of rows per expert reaches this.  A full pair tile moves half the B bytes
+// per FLOP through each SM's shared memory, which bounds the single-CTA
+// 128x256 tile (about 1.2x faster on full tiles), and an expert's last tile
+// of at most 128 rows runs swapped, costing about its weight bytes.  Below
+// this most tiles are such tails, and the single-CTA kernel already streams
+// the weights at HBM speed.
+constexpr int64_t kPairRowsPerExpert = 256;
 
 // combine.cu
 cudaError_t launch_combine(const float *y_perm, const int32_t *dest, const float *w, int T,

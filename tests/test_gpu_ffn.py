@@ -72,12 +72,16 @@ def test_ffn_contiguous(counts, d, inter):
     ([1100, 1000], 512, 256),      # ragged pair tiles; the odd CTA of one has no rows
     ([0, 2561, 768], 1024, 384),   # empty expert, exact multiples of 256
     ([4000, 40, 300, 700], 256, 128),
+    # last tiles of 1, 16, 17, 100, 128 rows run swapped; 129 and 255 do not
+    ([257, 272, 273, 356, 384, 385, 511, 0], 512, 256),
+    ([1, 16, 600, 900], 256, 384),  # experts made of one swapped tile
+    ([700, 300], 4096, 1024),       # long K
 ])
 def test_ffn_pair_tiles(counts, d, inter):
-    # T*k >= 1024 rows per expert selects the CTA-pair (cta_group::2) kernels
+    # T*k >= 256 rows per expert selects the CTA-pair (cta_group::2) kernels
     ensure_lib()
     E = len(counts)
-    assert sum(counts) >= 1024 * E
+    assert sum(counts) >= 256 * E
     w_gu, w_down = _weights(E, d, inter, seed=d * 3 + inter)
     x, offsets, row_e = _contiguous_case(counts, d, inter, seed=d + 7)
     shape = _shape(E, d, inter, T=x.shape[0], k=1)
@@ -90,9 +94,12 @@ def test_ffn_pair_tiles(counts, d, inter):
     check_ffn(y.cpu().numpy(), bits(x), row_e, bits(w_gu), bits(w_down), "y (pair)")
 
 
-def test_gate_up_alone_matches_oracle_h():
+@pytest.mark.parametrize("counts", [
+    [17, 129, 0, 256],     # single-CTA tiles
+    [17, 300, 129, 600],   # pair tiles; last tiles of 17, 44 and 88 rows swapped
+])
+def test_gate_up_alone_matches_oracle_h(counts):
     ensure_lib()
-    counts = [17, 129, 0, 256]
     E, d, inter = 4, 512, 256
     w_gu, w_down = _weights(E, d, inter, seed=3)
     x, offsets, row_e = _contiguous_case(counts, d, inter, seed=4)
