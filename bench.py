@@ -91,6 +91,44 @@ def load_peaks() -> tuple[dict, str]:
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# DRAM traffic of one launch of a kernel, from an ncu capture summarised in
+# profiles/dram_traffic.md; valid only while the kernel's sources are the
+# ones the capture was taken from.
+KERNEL_SOURCES = {
+    "gate_up": ["gemm.cu", "common.cuh"], "down": ["gemm.cu", "common.cuh"],
+    "router": ["router.cu", "common.cuh"], "dispatch": ["dispatch.cu", "common.cuh"],
+    "combine": ["combine.cu", "common.cuh"],
+}
+
+
+def kernel_source_hash(stage: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[stage]:
+        with open(os.path.join(ROOT, "dispatch_combine_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, stage: str):
+    """Bytes per launch (DRAM read + write) if profiles/dram_traffic.md holds a
+    capture of this stage's kernel at this workload from the current sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    try:
+        rows = open(path).read().splitlines()
+    except OSError:
+        return None
+    want = kernel_source_hash(stage)
+    for ln in rows:
+        cells = [x.strip().strip("`") for x in ln.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == workload and cells[1] == stage and cells[2] == want:
+            try:
+                return float(cells[3])
+            except ValueError:
+                return None
+    return None
+
+
 def workload_desc(c) -> str:
     score = "sigmoid+0.15*bias" if c.score == SCORE_SIGMOID_BIAS else "softmax"
     g = f"E={c.E} in G={c.G} groups, topk_group={c.topk_group}" if c.G > 1 else f"E={c.E}, G=1"
@@ -117,7 +155,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -387,6 +425,7 @@ def run_gpu(args, c):
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"], "traffic": None}
     roof["kernel"] = dominant
+    roof["traffic"] = measured_traffic(c.name, dominant)
     roof["peak_source"] = (f"{peak_src} ({'bf16 sustained' if roof['bound'] == 'tensor' else 'HBM copy'})")
 
     # end to end through the C ABI with host buffers
@@ -554,7 +593,7 @@ def run_masked(args):
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", choices=sorted(CONFIGS), default=DEFAULT_CONFIG)
