@@ -82,6 +82,10 @@ def _load():
             "oracle_combine": (None, [P, P, P, I, I, I, P]),
             "oracle_layer_tokens": (None, [P, P, P, P, P, I, I, I, I, I, I, I, I, F,
                                            P, I, P, P, P]),
+            "oracle_layer_tokens_keep": (None, [P, P, P, P, P, I, I, I, I, I, I, I, I, F,
+                                                P, I, P, P, P, P]),
+            "oracle_expert_capacity": (I, [I, I, I, ctypes.c_double]),
+            "oracle_dispatch_capacity": (I, [P, I, I, I, I, I, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -246,8 +250,31 @@ def combine(y_perm, dest, w, T: int, k: int) -> np.ndarray:
     return y
 
 
-def layer_tokens(x, w_r, bias, w_gu, w_down, shape: dict, tokens):
-    """Whole layer for the listed tokens; returns (y [n,d] f64, ids, weights)."""
+def expert_capacity(T, k, E, c):
+    """C = ceil(c * T * k / E) (capacity per expert)."""
+    return int(_load().oracle_expert_capacity(int(T), int(k), int(E), float(c)))
+
+
+def dispatch_capacity(ids, E, C, policy):
+    """Capacity dispatch (policy 0 drop, 1 second round); returns
+    (counts, kept, ovf_offsets, dest, src_row)."""
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    counts = np.empty(E, np.int32)
+    kept = np.empty(E, np.int32)
+    ovf = np.empty(E + 1, np.int32)
+    dest = np.empty(T * k, np.int32)
+    src = np.empty(E * C + T * k, np.int32)
+    rc = _load().oracle_dispatch_capacity(_p(ids), T, k, E, int(C), int(policy), _p(counts),
+                                          _p(kept), _p(ovf), _p(dest), _p(src))
+    if rc != 0:
+        raise ValueError("expert id out of range")
+    return counts, kept, ovf, dest, src
+
+
+def layer_tokens(x, w_r, bias, w_gu, w_down, shape: dict, tokens, keep=None):
+    """Whole layer for the listed tokens; returns (y [n,d] f64, ids, weights).
+    keep [n, k] (optional): assignments that add their term (capacity drop)."""
     x = _u16(x)
     w_r = _u16(w_r)
     w_gu = _u16(w_gu)
@@ -262,9 +289,11 @@ def layer_tokens(x, w_r, bias, w_gu, w_down, shape: dict, tokens):
     ids = np.empty((n, k), dtype=np.int32)
     wts = np.empty((n, k), dtype=np.float32)
     y = np.empty((n, d), dtype=np.float64)
+    kp = None if keep is None else _c(keep, np.uint8)
     if n:
-        _load().oracle_layer_tokens(_p(x), _p(w_r), _p(b), _p(w_gu), _p(w_down), T, d,
-                                    E, shape["G"], shape["topk_group"], k, inter,
-                                    shape["score"], float(shape.get("bias_scale", 0.15)),
-                                    _p(tokens), n, _p(ids), _p(wts), _p(y))
+        _load().oracle_layer_tokens_keep(_p(x), _p(w_r), _p(b), _p(w_gu), _p(w_down), T, d,
+                                         E, shape["G"], shape["topk_group"], k, inter,
+                                         shape["score"], float(shape.get("bias_scale", 0.15)),
+                                         _p(tokens), n, None if kp is None else _p(kp),
+                                         _p(ids), _p(wts), _p(y))
     return y, ids, wts

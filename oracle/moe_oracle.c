@@ -43,6 +43,10 @@
  *   R8  dispatch is a stable counting sort of the flat assignments a = t*k+j.
  *   R9  expert FFN: h = silu(x.Wg) * (x.Wu), y = h.Wd, accumulated in fp64.
  *   R10 combine: y[t] = sum_j w[t,j] * y_perm[dest[t*k+j]], j ascending.
+ *   R11 capacity: the first C assignments of an expert in increasing
+ *       a = t*k + j keep their place; later ones overflow.  Dropped ones add
+ *       nothing (weights are not renormalised); second-round ones are
+ *       computed like any other.
  *
  * Compile with -O2 -ffp-contract=off, no fast-math, so that every floating
  * point operation is exactly the one written.
@@ -335,6 +339,66 @@ int oracle_dispatch(const int32_t *ids, int T, int k, int E, int32_t *counts,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Capacity ([ch15] 4.3 "Capacity Factor" and its overflow table)            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * C = ceil(c * T * k / E), the page's per-expert capacity for capacity factor
+ * c, evaluated in double.  (Its example: T = 5600, k = 16, E = 896, c = 1.2
+ * gives 120 with a mean of 100.)
+ */
+int oracle_expert_capacity(int T, int k, int E, double c) {
+  double mean = (double)T * (double)k / (double)E;
+  return (int)ceil(c * mean);
+}
+
+/*
+ * Dispatch with a capacity of C rows per expert.  The assignments a = t*k+j
+ * are taken in increasing a (R11: first come, first served); the first C
+ * assignments of expert e get the padded row e*C + r (r = their rank at e).
+ * A later one overflows: with policy 1 ("second round": the overflow is run
+ * after the first round, same expert) it gets row E*C + ovf_offsets[e] +
+ * (r - C); with policy 0 ("drop") it gets no row, dest = -1.
+ * counts[e] = n_e, kept[e] = min(n_e, C), ovf_offsets = exclusive prefix sum
+ * of n_e - kept[e] (E+1 entries).  src_row has E*C + T*k entries: the token
+ * of every used row, -1 for the others.  Returns 0, or -1 for a bad id.
+ */
+int oracle_dispatch_capacity(const int32_t *ids, int T, int k, int E, int C, int policy,
+                             int32_t *counts, int32_t *kept, int32_t *ovf_offsets,
+                             int32_t *dest, int32_t *src_row) {
+  if (E <= 0 || C < 0) return -1;
+  int64_t n = (int64_t)T * k;
+  int64_t rows = (int64_t)E * C + n;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int64_t a = 0; a < n; ++a) {
+    if (ids[a] < 0 || ids[a] >= E) return -1;
+    counts[ids[a]] += 1;
+  }
+  ovf_offsets[0] = 0;
+  for (int e = 0; e < E; ++e) {
+    kept[e] = counts[e] < C ? counts[e] : C;
+    ovf_offsets[e + 1] = ovf_offsets[e] + (counts[e] - kept[e]);
+  }
+  for (int64_t r = 0; r < rows; ++r) src_row[r] = -1;
+  int32_t *rank = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+  for (int64_t a = 0; a < n; ++a) {
+    int e = ids[a];
+    int32_t r = rank[e]++;
+    int64_t row;
+    if (r < C)
+      row = (int64_t)e * C + r;
+    else if (policy == 1)
+      row = (int64_t)E * C + ovf_offsets[e] + (r - C);
+    else
+      row = -1;
+    dest[a] = (int32_t)row;
+    if (row >= 0) src_row[row] = (int32_t)(a / k);
+  }
+  free(rank);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* R9: SwiGLU expert FFN, row by row                                         */
 /* ------------------------------------------------------------------------ */
 
@@ -420,11 +484,34 @@ void oracle_combine(const float *y_perm, const int32_t *dest, const float *w, in
  * row and combine (R10).  Tokens are independent, so any subset can be
  * checked one by one.  y: [n_tok, d] fp64.  ids/weights: [n_tok, k].
  */
+void oracle_layer_tokens_keep(const uint16_t *x, const uint16_t *w_r, const float *bias,
+                              const uint16_t *w_gu, const uint16_t *w_down, int T, int d,
+                              int E, int G, int topk_group, int k, int inter,
+                              int score_kind, float bias_scale, const int32_t *tokens,
+                              int n_tok, const uint8_t *keep, int32_t *ids, float *weights,
+                              double *y);
+
 void oracle_layer_tokens(const uint16_t *x, const uint16_t *w_r, const float *bias,
                          const uint16_t *w_gu, const uint16_t *w_down, int T, int d,
                          int E, int G, int topk_group, int k, int inter,
                          int score_kind, float bias_scale, const int32_t *tokens,
                          int n_tok, int32_t *ids, float *weights, double *y) {
+  oracle_layer_tokens_keep(x, w_r, bias, w_gu, w_down, T, d, E, G, topk_group, k, inter,
+                           score_kind, bias_scale, tokens, n_tok, NULL, ids, weights, y);
+}
+
+/*
+ * As oracle_layer_tokens, but assignment (q, j) of listed token q only adds
+ * its term when keep[q*k + j] != 0 (keep == NULL: every assignment) -- the
+ * layer output under the "drop" overflow policy, where a dropped assignment
+ * contributes nothing ([ch15] 4.3 overflow table: drop / residual path).
+ */
+void oracle_layer_tokens_keep(const uint16_t *x, const uint16_t *w_r, const float *bias,
+                              const uint16_t *w_gu, const uint16_t *w_down, int T, int d,
+                              int E, int G, int topk_group, int k, int inter,
+                              int score_kind, float bias_scale, const int32_t *tokens,
+                              int n_tok, const uint8_t *keep, int32_t *ids, float *weights,
+                              double *y) {
   if (n_tok <= 0) return;
   uint16_t *xs = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n_tok * d);
   for (int q = 0; q < n_tok; ++q)
@@ -446,7 +533,8 @@ void oracle_layer_tokens(const uint16_t *x, const uint16_t *w_r, const float *bi
     for (int c = 0; c < d; ++c) {
       double acc = 0.0;
       for (int j = 0; j < k; ++j)
-        acc += (double)weights[q * k + j] * (double)yr[(size_t)(q * k + j) * d + c];
+        if (!keep || keep[q * k + j])
+          acc += (double)weights[q * k + j] * (double)yr[(size_t)(q * k + j) * d + c];
       y[(size_t)q * d + c] = acc;
     }
   free(yr);

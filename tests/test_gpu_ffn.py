@@ -74,6 +74,8 @@ def test_ffn_contiguous(counts, d, inter):
     ([4000, 40, 300, 700], 256, 128),
     # last tiles of 1, 16, 17, 100, 128 rows run swapped; 129 and 255 do not
     ([257, 272, 273, 356, 384, 385, 511, 0], 512, 256),
+    # swapped tails of 63, 64, 65 rows (N rounded up to 64, 64, 80)
+    ([320, 319, 321, 575, 576, 1], 512, 256),
     ([1, 16, 600, 900], 256, 384),  # experts made of one swapped tile
     ([700, 300], 4096, 1024),       # long K
 ])
