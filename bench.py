@@ -600,6 +600,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-sample-s", type=float, default=15.0,
                     help="seconds of CPU oracle work for cpu_baseline (0 = skip)")
+    ap.add_argument("--capacity", type=float, default=None,
+                    help="time the capacity variant with this capacity factor (own line)")
+    ap.add_argument("--overflow", choices=["drop", "second"], default="drop")
     ap.add_argument("--masked", choices=["ep", "tp"], default=None,
                     help="time the masked expert FFN of a per-rank slice instead")
     ap.add_argument("--ref-step-s", type=float, default=4.0,
@@ -607,9 +610,62 @@ def parse_args(argv=None):
     return ap.parse_args(argv)
 
 
+def run_capacity(args):
+    """Time the capacity variant of the layer (its own JSON line): capacity
+    C = ceil(c*T*k/E) per expert, overflow dropped or run in a second round."""
+    import torch
+    import dispatch_combine_gb300 as moe
+    from moe_inputs import make_layer_tensors
+    torch.cuda.set_device(0)
+    c = CONFIGS[args.config]
+    t = make_layer_tensors(c, device="cuda", seed=0)
+    bias = t["bias"] if c.score == SCORE_SIGMOID_BIAS else None
+    shape = c.shape()
+    C = moe.moe_expert_capacity(c.T, c.k, c.E, args.capacity)
+    policy = moe.MOE_OVERFLOW_DROP if args.overflow == "drop" else moe.MOE_OVERFLOW_SECOND_ROUND
+    ws = moe.Workspace(moe.moe_layer_capacity_workspace_size(shape, C))
+    y = torch.empty(c.T, c.d, dtype=torch.bfloat16, device="cuda")
+    counts = torch.empty(c.E, dtype=torch.int32, device="cuda")
+    kept = torch.empty(c.E, dtype=torch.int32, device="cuda")
+
+    def step():
+        moe.moe_layer_capacity(shape, C, policy, t["x"], t["w_r"], bias, t["w_gate_up"],
+                               t["w_down"], ws, y=y, counts=counts, kept=kept)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status error")
+    ms = e0.elapsed_time(e1) / args.steps
+    n = c.T * c.k
+    dropped = int((counts - kept).sum()) if policy == moe.MOE_OVERFLOW_DROP else 0
+    line = {
+        "metric": METRIC + f" (capacity factor {args.capacity}, overflow {args.overflow})",
+        "impl": "gb300", "value": c.T / (ms / 1000.0), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(c), "capacity": C, "capacity_factor": args.capacity,
+                   "overflow": args.overflow, "padded_rows": c.E * C,
+                   "overflow_rows": int((counts - kept).sum()),
+                   "dropped_fraction": dropped / n},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     c = CONFIGS[args.config]
+    if args.capacity is not None:
+        return run_capacity(args)
     if args.masked:
         return run_masked(args)
     if args.impl == "reference":

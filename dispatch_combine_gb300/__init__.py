@@ -9,6 +9,8 @@ from ._lib import (  # noqa: F401
     LIB_PATH,
     MOE_LAYOUT_CONTIGUOUS,
     MOE_LAYOUT_MASKED,
+    MOE_OVERFLOW_DROP,
+    MOE_OVERFLOW_SECOND_ROUND,
     MOE_SCORE_SIGMOID_BIAS,
     MOE_SCORE_SOFTMAX,
     SIGNATURES,
@@ -20,7 +22,9 @@ from ._lib import (  # noqa: F401
     lib,
     moe_combine,
     moe_dispatch,
+    moe_dispatch_capacity,
     moe_dispatch_noalloc,
+    moe_expert_capacity,
     moe_expert_down,
     moe_expert_ffn,
     moe_expert_ffn_workspace_size,
@@ -28,6 +32,8 @@ from ._lib import (  # noqa: F401
     moe_get_device_status,
     moe_group_topk,
     moe_layer,
+    moe_layer_capacity,
+    moe_layer_capacity_workspace_size,
     moe_layer_launch_count,
     moe_route,
     moe_route_from_logits,

@@ -60,6 +60,12 @@ SIGNATURES = {
     "moe_group_topk": (_I32, [_PS, _P, _P, _P]),
     "moe_dispatch": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_noalloc": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_expert_capacity": (_I32, [_I32, _I32, _I32, ctypes.c_double]),
+    "moe_dispatch_capacity": (_I32, [_PS, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                     _SZ, _P]),
+    "moe_layer_capacity_workspace_size": (_I32, [_PS, _I32, ctypes.POINTER(_SZ)]),
+    "moe_layer_capacity": (_I32, [_PS, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                  _P]),
     "moe_expert_ffn": (_I32, [_PS, _I32, _P, _P, _I32, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_gate_up": (_I32, [_PS, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
     "moe_expert_down": (_I32, [_PS, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
@@ -375,6 +381,65 @@ def moe_layer(shape, x, w_r, bias, w_gate_up, w_down, ws: Workspace, y=None,
                                         _ptr(topk_ids), _ptr(topk_w), _ptr(counts),
                                         ws.c_ptr, ws.nbytes, _event_array(stage_events),
                                         _stream(stream)))
+    return y
+
+
+MOE_OVERFLOW_DROP = 0
+MOE_OVERFLOW_SECOND_ROUND = 1
+
+
+def moe_expert_capacity(T: int, k: int, E: int, c: float) -> int:
+    """C = ceil(c * T * k / E)."""
+    return int(lib().moe_expert_capacity(int(T), int(k), int(E), float(c)))
+
+
+def moe_dispatch_capacity(shape, capacity, overflow, topk_ids, x, ws: Workspace, stream=None):
+    """Returns (counts [E], kept [E], ovf_offsets [E+1], dest [T*k],
+    src_row [E*C + T*k], x_rows [E*C + T*k, d] or None)."""
+    s = as_shape(shape)
+    dev = topk_ids.device
+    n = s.T * s.k
+    rows = s.E * int(capacity) + n
+    _expect(topk_ids, torch.int32, (s.T, s.k), "topk_ids")
+    counts = torch.empty(s.E, dtype=torch.int32, device=dev)
+    kept = torch.empty(s.E, dtype=torch.int32, device=dev)
+    ovf = torch.empty(s.E + 1, dtype=torch.int32, device=dev)
+    dest = torch.empty(n, dtype=torch.int32, device=dev)
+    src = torch.full((rows,), -1, dtype=torch.int32, device=dev)
+    x_rows = None
+    if x is not None:
+        _expect(x, torch.bfloat16, (s.T, s.d), "x")
+        x_rows = torch.empty((rows, s.d), dtype=torch.bfloat16, device=dev)
+    _check("moe_dispatch_capacity",
+           lib().moe_dispatch_capacity(ctypes.byref(s), int(capacity), int(overflow),
+                                       _ptr(topk_ids), _ptr(x), _ptr(counts), _ptr(kept),
+                                       _ptr(ovf), _ptr(dest), _ptr(src), _ptr(x_rows),
+                                       ws.c_ptr, ws.nbytes, _stream(stream)))
+    return counts, kept, ovf, dest, src, x_rows
+
+
+def moe_layer_capacity_workspace_size(shape, capacity) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_layer_capacity_workspace_size",
+           lib().moe_layer_capacity_workspace_size(ctypes.byref(as_shape(shape)), int(capacity),
+                                                   ctypes.byref(out)))
+    return int(out.value)
+
+
+def moe_layer_capacity(shape, capacity, overflow, x, w_r, bias, w_gate_up, w_down,
+                       ws: Workspace, y=None, counts=None, kept=None, stream=None):
+    s = as_shape(shape)
+    _expect(x, torch.bfloat16, (s.T, s.d), "x")
+    _expect(w_r, torch.bfloat16, (s.d, s.E), "w_r")
+    _expect(w_gate_up, torch.bfloat16, (s.E, 2 * s.inter, s.d), "w_gate_up")
+    _expect(w_down, torch.bfloat16, (s.E, s.d, s.inter), "w_down")
+    if y is None:
+        y = torch.empty((s.T, s.d), dtype=torch.bfloat16, device=x.device)
+    _check("moe_layer_capacity",
+           lib().moe_layer_capacity(ctypes.byref(s), int(capacity), int(overflow), _ptr(x),
+                                    _ptr(w_r), _ptr(bias), _ptr(w_gate_up), _ptr(w_down),
+                                    _ptr(y), _ptr(counts), _ptr(kept), ws.c_ptr, ws.nbytes,
+                                    _stream(stream)))
     return y
 
 

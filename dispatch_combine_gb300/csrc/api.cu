@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libmoe: argument validation, workspace layout and
 // the launch sequence of each entry point.  Nothing here allocates device
 // memory; every buffer is the caller's.
+#include <cmath>
 #include <cstring>
 
 #include "common.cuh"
@@ -22,18 +23,27 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 //   (layer only) ids [T*k] | w [T*k] | counts [E] | offsets [E+1] |
 //   dest [T*k] | src [T*k] | x_perm [T*k*d] bf16 | y_perm [T*k*d] f32
 struct Layout {
-  size_t status, mtile, chunk, logits, wr32, h, ids, w, counts, offsets, dest, src, x_perm,
-      y_perm;
+  size_t status, mtile, doff, kept, ovf, chunk, logits, wr32, h, ids, w, counts, offsets, dest,
+      src, x_perm, y_perm;
   size_t end_route, end_dispatch, end_ffn, end_layer;
 };
 
-Layout make_layout(const moe_shape_t &s, int64_t h_rows) {
+// h_rows: rows of h; perm_rows: rows of x_perm / y_perm / src (T*k, or
+// E*C + T*k for the capacity layer)
+Layout make_layout(const moe_shape_t &s, int64_t h_rows, int64_t perm_rows = -1) {
   Layout L;
   const int64_t n = static_cast<int64_t>(s.T) * s.k;
+  if (perm_rows < 0) perm_rows = n;
   size_t off = 0;
   L.status = off;
   off = align_up(off + 4);
   L.mtile = off;
+  off = align_up(off + 4 * static_cast<size_t>(s.E + 1));
+  L.doff = off;  // expert offsets of the capacity dispatch
+  off = align_up(off + 4 * static_cast<size_t>(s.E + 1));
+  L.kept = off;
+  off = align_up(off + 4 * static_cast<size_t>(s.E));
+  L.ovf = off;
   off = align_up(off + 4 * static_cast<size_t>(s.E + 1));
   L.chunk = off;
   off = align_up(off + 4 * static_cast<size_t>(moe::dispatch_num_chunks(n)) * s.E);
@@ -57,11 +67,11 @@ Layout make_layout(const moe_shape_t &s, int64_t h_rows) {
   L.dest = off;
   off = align_up(off + 4 * static_cast<size_t>(n));
   L.src = off;
-  off = align_up(off + 4 * static_cast<size_t>(n));
+  off = align_up(off + 4 * static_cast<size_t>(perm_rows));
   L.x_perm = off;
-  off = align_up(off + 2 * static_cast<size_t>(n) * s.d);
+  off = align_up(off + 2 * static_cast<size_t>(perm_rows) * s.d);
   L.y_perm = off;
-  off = align_up(off + 4 * static_cast<size_t>(n) * s.d);
+  off = align_up(off + 4 * static_cast<size_t>(perm_rows) * s.d);
   L.end_layer = off;
   return L;
 }
@@ -129,6 +139,7 @@ bool use_pair(const moe_shape_t *s, int32_t layout) {
   return layout == MOE_LAYOUT_CONTIGUOUS && s->inter % 128 == 0 && s->d % 256 == 0 &&
          static_cast<int64_t>(s->T) * s->k >= moe::kPairRowsPerExpert * s->E;
 }
+int tile_rows_for(const moe_shape_t *s, int32_t layout) { return use_pair(s, layout) ? 256 : 128; }
 
 moe_status_t run_gate_up(const moe_shape_t *s, int32_t layout, const void *x_in,
                          const int32_t *seg, int32_t M_max, int64_t rows, const int32_t *mtile,
@@ -372,7 +383,8 @@ moe_status_t moe_combine(const moe_shape_t *shape, const float *y_perm, const in
   if (!y_perm || !dest || !topk_w || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
   return cuda_status(
-      moe::launch_combine(y_perm, dest, topk_w, shape->T, shape->k, shape->d, y, stream));
+      moe::launch_combine(y_perm, static_cast<int64_t>(shape->T) * shape->k, dest, topk_w,
+                          shape->T, shape->k, shape->d, y, stream));
 }
 
 moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
@@ -425,8 +437,132 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
   MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, offsets, 0, n, mtile, w_down, y_perm, status,
                    stream));
   MOE_TRY(mark(4));
-  MOE_TRY(cuda_status(moe::launch_combine(y_perm, dest, w, s.T, s.k, s.d, y, stream)));
+  MOE_TRY(cuda_status(moe::launch_combine(y_perm, n, dest, w, s.T, s.k, s.d, y, stream)));
   return mark(5);
+}
+
+// ---------------------------------------------------------------------------
+// capacity variant
+// ---------------------------------------------------------------------------
+
+int32_t moe_expert_capacity(int32_t T, int32_t k, int32_t E, double c) {
+  if (T < 0 || k < 1 || E < 1 || !(c >= 0.0) || !std::isfinite(c)) return -1;
+  const double v = std::ceil(c * (static_cast<double>(T) * k / E));
+  if (v >= 2147483647.0) return -1;
+  return static_cast<int32_t>(v);
+}
+
+static moe_status_t check_capacity(const moe_shape_t *s, int32_t capacity, int32_t overflow) {
+  if (capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (overflow != MOE_OVERFLOW_DROP && overflow != MOE_OVERFLOW_SECOND_ROUND)
+    return MOE_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(s->E) * capacity + static_cast<int64_t>(s->T) * s->k;
+  if (rows >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t moe_dispatch_capacity(const moe_shape_t *shape, int32_t capacity,
+                                   int32_t overflow, const int32_t *topk_ids, const void *x,
+                                   int32_t *counts, int32_t *kept, int32_t *ovf_offsets,
+                                   int32_t *dest, int32_t *src_row, void *x_rows, void *ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  MOE_TRY(check_capacity(shape, capacity, overflow));
+  const moe_shape_t &s = *shape;
+  if (!topk_ids || !counts || !kept || !ovf_offsets || !dest || !src_row)
+    return MOE_ERR_INVALID_ARG;
+  if (x && !x_rows) return MOE_ERR_INVALID_ARG;
+  if (x && (!aligned16(x) || !aligned16(x_rows))) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(s, 0);
+  MOE_TRY(check_ws(ws, ws_bytes, L.end_dispatch));
+  if (s.T == 0) {
+    // no assignments: every count is zero
+    MOE_TRY(cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * s.E, stream)));
+    MOE_TRY(cuda_status(cudaMemsetAsync(kept, 0, sizeof(int32_t) * s.E, stream)));
+    return cuda_status(cudaMemsetAsync(ovf_offsets, 0, sizeof(int32_t) * (s.E + 1), stream));
+  }
+  moe::CapacityArgs cap{capacity, overflow, s.E, kept, ovf_offsets};
+  return cuda_status(moe::launch_dispatch(topk_ids, s.T, s.k, s.E, x, s.d, counts,
+                                          at<int32_t>(ws, L.doff), src_row, dest, x_rows,
+                                          at<int32_t>(ws, L.chunk), nullptr, 128,
+                                          at<uint32_t>(ws, L.status), stream, cap));
+}
+
+static Layout capacity_layout(const moe_shape_t &s, int32_t capacity) {
+  const int64_t rows = static_cast<int64_t>(s.E) * capacity + static_cast<int64_t>(s.T) * s.k;
+  return make_layout(s, rows, rows);
+}
+
+moe_status_t moe_layer_capacity_workspace_size(const moe_shape_t *shape, int32_t capacity,
+                                               size_t *bytes) {
+  MOE_TRY(check_shape(shape));
+  MOE_TRY(check_capacity(shape, capacity, MOE_OVERFLOW_DROP));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = capacity_layout(*shape, capacity).end_layer;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int32_t overflow,
+                                const void *x, const void *w_r, const float *bias,
+                                const void *w_gate_up, const void *w_down, void *y,
+                                int32_t *counts, int32_t *kept, void *ws, size_t ws_bytes,
+                                moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  MOE_TRY(check_capacity(shape, capacity, overflow));
+  if (shape->T == 0) return MOE_OK;
+  MOE_TRY(check_ffn_shape(shape));
+  const moe_shape_t &s = *shape;
+  if (!x || !w_r || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (s.score == MOE_SCORE_SIGMOID_BIAS && !bias) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_r) || !aligned16(w_gate_up) || !aligned16(w_down) ||
+      !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t n = static_cast<int64_t>(s.T) * s.k;
+  const int64_t pad = static_cast<int64_t>(s.E) * capacity;
+  const Layout L = capacity_layout(s, capacity);
+  MOE_TRY(check_ws(ws, ws_bytes, L.end_layer));
+  uint32_t *status = at<uint32_t>(ws, L.status);
+  int32_t *ids = at<int32_t>(ws, L.ids);
+  float *w = at<float>(ws, L.w);
+  int32_t *cnt = counts ? counts : at<int32_t>(ws, L.counts);
+  int32_t *kp = kept ? kept : at<int32_t>(ws, L.kept);
+  int32_t *ovf = at<int32_t>(ws, L.ovf);
+  int32_t *mtile = at<int32_t>(ws, L.mtile);
+  int32_t *dest = at<int32_t>(ws, L.dest);
+  uint8_t *x_rows = at<uint8_t>(ws, L.x_perm);
+  float *y_rows = at<float>(ws, L.y_perm);
+  uint8_t *h = at<uint8_t>(ws, L.h);
+  float *logits = at<float>(ws, L.logits);
+
+  MOE_TRY(cuda_status(
+      moe::launch_router_logits(x, w_r, s.T, s.d, s.E, logits, at<void>(ws, L.wr32), stream)));
+  MOE_TRY(cuda_status(moe::launch_router_select(logits, bias, s.T, s.E, s.G, s.topk_group, s.k,
+                                                s.score, s.bias_scale, 0, ids, w, stream)));
+  moe::CapacityArgs cap{capacity, overflow, s.E, kp, ovf};
+  MOE_TRY(cuda_status(moe::launch_dispatch(ids, s.T, s.k, s.E, x, s.d, cnt,
+                                           at<int32_t>(ws, L.doff), at<int32_t>(ws, L.src),
+                                           dest, x_rows, at<int32_t>(ws, L.chunk), nullptr,
+                                           128, status, stream, cap)));
+  // first round: the padded rows, masked layout with M_max = C
+  if (capacity > 0) {
+    MOE_TRY(cuda_status(moe::launch_ffn_tiles(kp, MOE_LAYOUT_MASKED, s.E, capacity, 128, mtile,
+                                              status, stream)));
+    MOE_TRY(run_gate_up(shape, MOE_LAYOUT_MASKED, x_rows, kp, capacity, pad, mtile, w_gate_up,
+                        h, status, stream));
+    MOE_TRY(run_down(shape, MOE_LAYOUT_MASKED, h, kp, capacity, pad, mtile, w_down, y_rows,
+                     status, stream));
+  }
+  // second round: the overflow rows, contiguous with offsets ovf_offsets
+  if (overflow == MOE_OVERFLOW_SECOND_ROUND) {
+    MOE_TRY(cuda_status(moe::launch_ffn_tiles(ovf, MOE_LAYOUT_CONTIGUOUS, s.E, 0,
+                                              tile_rows_for(shape, MOE_LAYOUT_CONTIGUOUS), mtile,
+                                              status, stream)));
+    MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_rows + pad * s.d * 2, ovf, 0, n, mtile,
+                        w_gate_up, h, status, stream));
+    MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, ovf, 0, n, mtile, w_down,
+                     y_rows + pad * s.d, status, stream));
+  }
+  return cuda_status(moe::launch_combine(y_rows, pad + n, dest, w, s.T, s.k, s.d, y, stream));
 }
 
 int32_t moe_layer_launch_count(const moe_shape_t *shape) {

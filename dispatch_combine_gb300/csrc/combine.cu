@@ -18,18 +18,18 @@ constexpr int kCombineVec = 2;  // 16-byte column vectors per thread
 // kCombineVec * k 16-byte loads in flight, so even a few hundred tokens fill
 // the GPU.
 __global__ void __launch_bounds__(kCombineThreads)
-    combine_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__ dest,
-                   const float *__restrict__ w, int T, int k, int d4, int segs,
-                   uint2 *__restrict__ y) {
+    combine_kernel(const float4 *__restrict__ y_perm, int64_t y_rows,
+                   const int32_t *__restrict__ dest, const float *__restrict__ w, int T, int k,
+                   int d4, int segs, uint2 *__restrict__ y) {
   __shared__ int s_row[32];
   __shared__ float s_w[32];
   const int t = blockIdx.x / segs;
   const int seg = blockIdx.x - t * segs;
   if (threadIdx.x < k) {
-    // a row outside [0, T*k) (a caller-supplied dest that is not a
-    // permutation) contributes nothing instead of reading out of bounds
+    // a row outside [0, y_rows) (a dropped assignment, or a caller-supplied
+    // dest that is not a permutation) contributes nothing
     const int r = dest[(size_t)t * k + threadIdx.x];
-    const bool in = r >= 0 && static_cast<int64_t>(r) < static_cast<int64_t>(T) * k;
+    const bool in = r >= 0 && static_cast<int64_t>(r) < y_rows;
     s_row[threadIdx.x] = in ? r : 0;
     s_w[threadIdx.x] = in ? w[(size_t)t * k + threadIdx.x] : 0.0f;
   }
@@ -66,14 +66,14 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 }  // namespace
 
-cudaError_t launch_combine(const float *y_perm, const int32_t *dest, const float *w, int T,
-                           int k, int d, void *y, cudaStream_t s) {
+cudaError_t launch_combine(const float *y_perm, int64_t y_rows, const int32_t *dest,
+                           const float *w, int T, int k, int d, void *y, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int d4 = d / 4;
   const int segs = (d4 + kCombineThreads * kCombineVec - 1) / (kCombineThreads * kCombineVec);
   const int64_t blocks = static_cast<int64_t>(T) * segs;
   combine_kernel<<<static_cast<unsigned>(blocks), kCombineThreads, 0, s>>>(
-      reinterpret_cast<const float4 *>(y_perm), dest, w, T, k, d4, segs,
+      reinterpret_cast<const float4 *>(y_perm), y_rows, dest, w, T, k, d4, segs,
       static_cast<uint2 *>(y));
   return cudaGetLastError();
 }

@@ -82,7 +82,7 @@ __device__ int block_exclusive_scan(int v, int *total) {
 __global__ void __launch_bounds__(1024)
     dispatch_scan_kernel(int32_t *__restrict__ chunk_counts, int nchunks, int E,
                          int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
-                         int32_t *__restrict__ mtile_base, int tile_rows) {
+                         int32_t *__restrict__ mtile_base, int tile_rows, CapacityArgs cap) {
   __shared__ int part[1024];
   int ep = 1;
   while (ep < E) ep <<= 1;
@@ -122,6 +122,17 @@ __global__ void __launch_bounds__(1024)
     offsets[e] = excl;
   }
   if (e == 0) offsets[E] = total;
+  if (cap.kept) {
+    // capacity: the first C rows of an expert stay, the rest overflow
+    const int kept = (e < E) ? min(run, cap.capacity) : 0;
+    int ovf_total = 0;
+    const int ovf_excl = block_exclusive_scan((e < E) ? run - kept : 0, &ovf_total);
+    if (e < E) {
+      cap.kept[e] = kept;
+      cap.ovf_offsets[e] = ovf_excl;
+    }
+    if (e == 0) cap.ovf_offsets[E] = ovf_total;
+  }
   if (mtile_base) {
     int mt_total = 0;
     const int mt = (e < E) ? (run + tile_rows - 1) / tile_rows : 0;
@@ -137,7 +148,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
     dispatch_scatter_kernel(const int32_t *__restrict__ ids, int64_t n, int k, int E, int chunk,
                             int64_t nchunks, const int32_t *__restrict__ chunk_base,
                             const int32_t *__restrict__ offsets, int32_t *__restrict__ dest,
-                            int32_t *__restrict__ src_token) {
+                            int32_t *__restrict__ src_token, CapacityArgs cap) {
   extern __shared__ int cursor_all[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t ci = (int64_t)blockIdx.x * kScatterWarps + warp;
@@ -162,9 +173,20 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
     base = __shfl_sync(0xffffffffu, base, leader);
     __syncwarp();
     if (valid) {
-      const int p = base + rank;
+      int p = base + rank;
+      if (cap.kept) {
+        // rank r inside the expert: padded row e*C + r, or an overflow row
+        // (second round) after all padded rows, or none (drop)
+        const int r = p - offsets[id];
+        if (r < cap.capacity)
+          p = id * cap.capacity + r;
+        else if (cap.policy == MOE_OVERFLOW_SECOND_ROUND)
+          p = E * cap.capacity + cap.ovf_offsets[id] + (r - cap.capacity);
+        else
+          p = -1;
+      }
       dest[a] = p;
-      src_token[p] = static_cast<int32_t>(a / k);
+      if (p >= 0) src_token[p] = static_cast<int32_t>(a / k);
     }
   }
 }
@@ -176,13 +198,21 @@ constexpr int kGatherWarps = 8;
 __global__ void __launch_bounds__(kGatherWarps * 32)
     dispatch_gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ src_token,
                            const int32_t *__restrict__ offsets_end, int64_t n, int T,
-                           int vec_per_row, uint4 *__restrict__ x_perm) {
+                           int vec_per_row, uint4 *__restrict__ x_perm, CapacityArgs cap) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // rows past offsets[E] exist only if some ids were invalid; they have no
-  // source token and are left untouched
-  const int64_t rows = min(n, static_cast<int64_t>(*offsets_end));
+  // source token and are left untouched.  With a capacity the rows are the
+  // E*C padded rows (row r of expert e used if r < kept[e]) and then the
+  // overflow rows.
+  const int64_t pad = cap.kept ? static_cast<int64_t>(cap.E) * cap.capacity : 0;
+  const int64_t rows = cap.kept ? pad + cap.ovf_offsets[cap.E]
+                                : min(n, static_cast<int64_t>(*offsets_end));
   for (int64_t row = (int64_t)blockIdx.x * kGatherWarps + warp; row < rows;
        row += (int64_t)gridDim.x * kGatherWarps) {
+    if (cap.kept && row < pad) {
+      const int e = static_cast<int>(row / cap.capacity);
+      if (row - static_cast<int64_t>(e) * cap.capacity >= cap.kept[e]) continue;
+    }
     const int t = src_token[row];
     if (t < 0 || t >= T) continue;
     const uint4 *src = x + (size_t)t * vec_per_row;
@@ -240,7 +270,8 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
                             int32_t *counts, int32_t *offsets, int32_t *src_token,
                             int32_t *dest, void *x_perm, int32_t *chunk_scratch,
                             int32_t *mtile_base, int tile_rows, uint32_t *status,
-                            cudaStream_t s) {
+                            cudaStream_t s, CapacityArgs cap) {
+  cap.E = E;
   const int64_t n = (int64_t)T * k;
   const int64_t nchunks = dispatch_num_chunks(n);
   const int chunk = dispatch_chunk(n);
@@ -250,21 +281,22 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_scratch, (int)nchunks, E, counts, offsets,
-                                          mtile_base, tile_rows);
+                                          mtile_base, tile_rows, cap);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const unsigned sblocks = (unsigned)((nchunks + kScatterWarps - 1) / kScatterWarps);
   dispatch_scatter_kernel<<<sblocks, kScatterWarps * 32, kScatterWarps * E * sizeof(int), s>>>(
-      ids, n, k, E, chunk, nchunks, chunk_scratch, offsets, dest, src_token);
+      ids, n, k, E, chunk, nchunks, chunk_scratch, offsets, dest, src_token, cap);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (x != nullptr && x_perm != nullptr) {
-    const int64_t want = (n + kGatherWarps - 1) / kGatherWarps;
-    const int64_t cap = (int64_t)num_sms() * 8;
-    const unsigned gblocks = (unsigned)(want < cap ? want : cap);
+    const int64_t max_rows = cap.kept ? static_cast<int64_t>(E) * cap.capacity + n : n;
+    const int64_t want = (max_rows + kGatherWarps - 1) / kGatherWarps;
+    const int64_t grid_cap = (int64_t)num_sms() * 8;
+    const unsigned gblocks = (unsigned)(want < grid_cap ? want : grid_cap);
     dispatch_gather_kernel<<<gblocks, kGatherWarps * 32, 0, s>>>(
         static_cast<const uint4 *>(x), src_token, offsets + E, n, T, d / 8,
-        static_cast<uint4 *>(x_perm));
+        static_cast<uint4 *>(x_perm), cap);
     err = cudaGetLastError();
   }
   return err;

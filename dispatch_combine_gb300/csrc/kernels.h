@@ -29,11 +29,23 @@ inline int64_t dispatch_num_chunks(int64_t n) {
   const int c = dispatch_chunk(n);
   return (n + c - 1) / c;
 }
+// Capacity variant of the dispatch: kept == nullptr turns it off.  With it,
+// expert e keeps its first `capacity` assignments (in increasing t*k+j) in
+// padded rows e*capacity + r; later ones go to overflow rows
+// E*capacity + ovf_offsets[e] + (r - capacity) (second round) or nowhere,
+// dest = -1 (drop).  kept[e] = min(n_e, capacity), ovf_offsets [E+1].
+struct CapacityArgs {
+  int capacity;
+  int policy;  // moe_overflow_t
+  int E;       // set by launch_dispatch
+  int32_t *kept;
+  int32_t *ovf_offsets;
+};
 cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void *x, int d,
                             int32_t *counts, int32_t *offsets, int32_t *src_token,
                             int32_t *dest, void *x_perm, int32_t *chunk_scratch,
                             int32_t *mtile_base, int tile_rows, uint32_t *status,
-                            cudaStream_t s);
+                            cudaStream_t s, CapacityArgs cap = CapacityArgs{0, 0, 0, nullptr, nullptr});
 // mtile_base[e] = sum_{e'<e} ceil(M_e'/tile_rows) for the contiguous (seg =
 // offsets) or masked (seg = masked_m, clamped to M_max) layout.
 cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,
@@ -48,8 +60,9 @@ cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, i
 constexpr int64_t kPairRowsPerExpert = 256;
 
 // combine.cu
-cudaError_t launch_combine(const float *y_perm, const int32_t *dest, const float *w, int T,
-                           int k, int d, void *y, cudaStream_t s);
+// y[t] = sum_j w[t,j] * y_perm[dest[t*k+j]]; rows outside [0, y_rows) add nothing
+cudaError_t launch_combine(const float *y_perm, int64_t y_rows, const int32_t *dest,
+                           const float *w, int T, int k, int d, void *y, cudaStream_t s);
 
 // gemm.cu
 struct GemmProblem {

@@ -77,6 +77,11 @@ typedef enum {
 
 typedef enum { MOE_LAYOUT_CONTIGUOUS = 0, MOE_LAYOUT_MASKED = 1 } moe_layout_t;
 
+/* What happens to assignments past an expert's capacity ("第十五章" section
+ * 4.3, overflow table): dropped (they add nothing to the output), or run in a
+ * second round on the same expert after the first. */
+typedef enum { MOE_OVERFLOW_DROP = 0, MOE_OVERFLOW_SECOND_ROUND = 1 } moe_overflow_t;
+
 /* Shape limits (MOE_ERR_INVALID_ARG beyond them unless noted):
  *   E % G == 0, 1 <= topk_group <= G <= 32, 1 <= k <= min(32, topk_group*E/G),
  *   E <= 1024, d % 8 == 0, T*k < 2^31.
@@ -242,6 +247,55 @@ moe_status_t moe_dispatch_noalloc(const moe_shape_t *shape, const int32_t *topk_
                                   const void *x, int32_t *counts, int32_t *offsets,
                                   int32_t *src_token, int32_t *dest, void *x_perm,
                                   moe_stream_t stream);
+
+/*
+ * Capacity variant ("第十五章：多节点大模型推理" section 4.3, "Capacity Factor"):
+ * each expert takes at most C assignments per batch.
+ *
+ * moe_expert_capacity returns C = ceil(c * T * k / E) (evaluated in double;
+ * the page's example T = 5600, k = 16, E = 896, c = 1.2 gives 120), or -1
+ * for T < 0, k < 1, E < 1 or c not finite and >= 0.
+ */
+int32_t moe_expert_capacity(int32_t T, int32_t k, int32_t E, double c);
+
+/*
+ * Dispatch with capacity C >= 0.  Assignments a = t*k + j of each expert are
+ * taken in increasing a; the first C keep a padded row e*C + r (r = rank at
+ * the expert); later ones go, by `overflow`, to row
+ * E*C + ovf_offsets[e] + (r - C) (MOE_OVERFLOW_SECOND_ROUND) or nowhere
+ * (MOE_OVERFLOW_DROP: dest = -1).
+ * Outputs (device, caller-owned): counts [E] = n_e, kept [E] = min(n_e, C),
+ *   ovf_offsets [E+1] = exclusive prefix sum of n_e - kept[e],
+ *   dest [T*k] int32, src_row [E*C + T*k] int32 (token of each used row;
+ *   other entries are not written), x_rows [(E*C + T*k), d] bf16 (NULL to
+ *   skip the gather; rows not used are not written).  The padded rows
+ *   [0, E*C) form the masked layout of moe_expert_ffn with masked_m = kept,
+ *   M_max = C; the overflow rows are contiguous with offsets ovf_offsets.
+ * Workspace: as moe_dispatch.  E*C + T*k must be < 2^31.
+ */
+moe_status_t moe_dispatch_capacity(const moe_shape_t *shape, int32_t capacity,
+                                   int32_t overflow, const int32_t *topk_ids, const void *x,
+                                   int32_t *counts, int32_t *kept, int32_t *ovf_offsets,
+                                   int32_t *dest, int32_t *src_row, void *x_rows, void *ws,
+                                   size_t ws_bytes, moe_stream_t stream);
+
+/* Workspace bytes for moe_layer_capacity with this shape and capacity. */
+moe_status_t moe_layer_capacity_workspace_size(const moe_shape_t *shape, int32_t capacity,
+                                               size_t *bytes);
+
+/*
+ * The layer with capacity C: route, capacity dispatch, the expert FFN over
+ * the padded rows (masked layout, M_max = C), with MOE_OVERFLOW_SECOND_ROUND
+ * a second expert FFN over the overflow rows, then the combine over the
+ * assignments that have a row (dropped ones add nothing; weights are not
+ * renormalised).  Arguments as moe_layer; kept [E] (optional) receives
+ * min(n_e, C).  With the second round the output is the uncapped layer's.
+ */
+moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int32_t overflow,
+                                const void *x, const void *w_r, const float *bias,
+                                const void *w_gate_up, const void *w_down, void *y,
+                                int32_t *counts, int32_t *kept, void *ws, size_t ws_bytes,
+                                moe_stream_t stream);
 
 /*
  * Number of kernels moe_layer launches per call for this shape (for launch
