@@ -85,6 +85,7 @@ def _load():
             "oracle_layer_tokens_keep": (None, [P, P, P, P, P, I, I, I, I, I, I, I, I, F,
                                                 P, I, P, P, P, P]),
             "oracle_expert_capacity": (I, [I, I, I, ctypes.c_double]),
+            "oracle_eplb_place": (I, [P, I, I, I, I, I, P, P]),
             "oracle_dispatch_capacity": (I, [P, I, I, I, I, I, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -270,6 +271,20 @@ def dispatch_capacity(ids, E, C, policy):
     if rc != 0:
         raise ValueError("expert id out of range")
     return counts, kept, ovf, dest, src
+
+
+def eplb_place(load, groups, nodes, gpus, phys):
+    """Expert placement (nodes = 0: global).  Returns (gpu_slots [gpus, phys//gpus]
+    logical expert ids, replicas [E])."""
+    load = _c(load, np.float64)
+    E = load.size
+    slots = np.empty(phys, np.int32)
+    reps = np.empty(E, np.int32)
+    rc = _load().oracle_eplb_place(_p(load), E, int(groups), int(nodes), int(gpus), int(phys),
+                                   _p(slots), _p(reps))
+    if rc != 0:
+        raise ValueError("sizes do not divide")
+    return slots.reshape(gpus, phys // gpus), reps
 
 
 def layer_tokens(x, w_r, bias, w_gu, w_down, shape: dict, tokens, keep=None):

@@ -399,6 +399,125 @@ int oracle_dispatch_capacity(const int32_t *ids, int T, int k, int E, int C, int
 }
 
 /* ------------------------------------------------------------------------ */
+/* Expert placement ([ep] "EPLB 与路由约束"): the three greedy steps         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Balanced packing of n items with weights w into n_packs packs of n/n_packs
+ * items each: items in order of decreasing weight (equal weights: lower
+ * index first); each goes to the pack with the smallest running sum among
+ * the packs that are not full (equal sums: lower pack index).
+ * packs[p * per + q] = q-th item put in pack p.
+ */
+static void eplb_pack(const double *w, int n, int n_packs, int32_t *packs) {
+  int per = n / n_packs;
+  int32_t *order = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+  int32_t *fill = (int32_t *)calloc((size_t)n_packs, sizeof(int32_t));
+  double *sum = (double *)calloc((size_t)n_packs, sizeof(double));
+  for (int i = 0; i < n; ++i) order[i] = i;
+  /* insertion sort: decreasing weight, stable */
+  for (int i = 1; i < n; ++i) {
+    int32_t v = order[i];
+    int j = i - 1;
+    while (j >= 0 && w[order[j]] < w[v]) {
+      order[j + 1] = order[j];
+      --j;
+    }
+    order[j + 1] = v;
+  }
+  for (int q = 0; q < n; ++q) {
+    int it = order[q], best = -1;
+    for (int p = 0; p < n_packs; ++p)
+      if (fill[p] < per && (best < 0 || sum[p] < sum[best])) best = p;
+    packs[best * per + fill[best]] = it;
+    fill[best] += 1;
+    sum[best] += w[it];
+  }
+  free(sum);
+  free(fill);
+  free(order);
+}
+
+/*
+ * Place E logical experts with per-expert loads on `gpus` GPUs as `phys`
+ * physical experts.
+ *   hierarchical (nodes > 0): (1) pack the expert groups (E/groups
+ *   consecutive experts each) onto the nodes by group load, the same number
+ *   of groups per node; (2) inside each node, add replicas one at a time to
+ *   the expert with the largest load per replica (equal: first in the node's
+ *   order) until the node has phys * (its experts) / E physical experts;
+ *   (3) pack the node's physical experts, weight load / replicas, onto its
+ *   gpus * (its experts) / E GPUs.
+ *   global (nodes == 0): the whole cluster is one node.
+ * A node's experts are its groups' experts, groups in the order they were
+ * packed.  gpu_slots[g * (phys/gpus) + q] = logical expert of the q-th
+ * physical expert of GPU g; replicas[e] = number of physical copies of e.
+ * Returns 0, or -1 when the sizes do not divide as required.
+ */
+int oracle_eplb_place(const double *load, int E, int groups, int nodes, int gpus, int phys,
+                      int32_t *gpu_slots, int32_t *replicas) {
+  int n_nodes = nodes > 0 ? nodes : 1;
+  if (E <= 0 || groups <= 0 || E % groups || groups % n_nodes || gpus % n_nodes ||
+      phys % gpus || phys < E)
+    return -1;
+  int gsize = E / groups;
+  int per_node_e = E / n_nodes;
+  int node_phys = phys / n_nodes, node_gpus = gpus / n_nodes;
+  int per_gpu = phys / gpus;
+  if (node_phys * n_nodes != phys || node_gpus * per_gpu != node_phys) return -1;
+  int32_t *node_experts = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+  if (nodes > 0) {
+    double *gload = (double *)calloc((size_t)groups, sizeof(double));
+    for (int g = 0; g < groups; ++g)
+      for (int i = 0; i < gsize; ++i) gload[g] += load[g * gsize + i];
+    int32_t *gpack = (int32_t *)malloc(sizeof(int32_t) * (size_t)groups);
+    eplb_pack(gload, groups, nodes, gpack);
+    int per_node_g = groups / nodes;
+    for (int nd = 0; nd < nodes; ++nd)
+      for (int q = 0; q < per_node_g; ++q) {
+        int g = gpack[nd * per_node_g + q];
+        for (int i = 0; i < gsize; ++i)
+          node_experts[nd * per_node_e + q * gsize + i] = g * gsize + i;
+      }
+    free(gpack);
+    free(gload);
+  } else {
+    for (int e = 0; e < E; ++e) node_experts[e] = e;
+  }
+  int32_t *cnt = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+  int32_t *pl = (int32_t *)malloc(sizeof(int32_t) * (size_t)node_phys);
+  double *pw = (double *)malloc(sizeof(double) * (size_t)node_phys);
+  int32_t *packs = (int32_t *)malloc(sizeof(int32_t) * (size_t)node_phys);
+  for (int nd = 0; nd < n_nodes; ++nd) {
+    const int32_t *ids = node_experts + nd * per_node_e;
+    for (int i = 0; i < per_node_e; ++i) cnt[ids[i]] = 1;
+    for (int r = per_node_e; r < node_phys; ++r) {
+      int best = 0;
+      for (int i = 1; i < per_node_e; ++i)
+        if (load[ids[i]] / cnt[ids[i]] > load[ids[best]] / cnt[ids[best]]) best = i;
+      cnt[ids[best]] += 1;
+    }
+    int m = 0;
+    for (int i = 0; i < per_node_e; ++i)
+      for (int c = 0; c < cnt[ids[i]]; ++c) {
+        pl[m] = ids[i];
+        pw[m] = load[ids[i]] / cnt[ids[i]];
+        ++m;
+      }
+    eplb_pack(pw, node_phys, node_gpus, packs);
+    for (int q = 0; q < node_phys; ++q)
+      gpu_slots[nd * node_phys + q] = pl[packs[q]];
+    for (int i = 0; i < per_node_e; ++i) replicas[ids[i]] = cnt[ids[i]];
+  }
+  free(packs);
+  free(pw);
+  free(pl);
+  free(cnt);
+  free(node_experts);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* R9: SwiGLU expert FFN, row by row                                         */
 /* ------------------------------------------------------------------------ */
 
