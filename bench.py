@@ -600,6 +600,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-sample-s", type=float, default=15.0,
                     help="seconds of CPU oracle work for cpu_baseline (0 = skip)")
+    ap.add_argument("--eplb", action="store_true",
+                    help="plan expert placements on the routed loads (own line)")
     ap.add_argument("--capacity", type=float, default=None,
                     help="time the capacity variant with this capacity factor (own line)")
     ap.add_argument("--overflow", choices=["drop", "second"], default="drop")
@@ -661,9 +663,50 @@ def run_capacity(args):
     return 0
 
 
+def run_eplb(args):
+    """Expert placement on the loads of a routed batch (its own JSON line):
+    route the workload's tokens on the GPU, count assignments per expert,
+    plan global and hierarchical placements on the host (moe_eplb_plan) and
+    report the planner time and the busiest/mean GPU load."""
+    import torch
+    import dispatch_combine_gb300 as moe
+    from moe_inputs import make_layer_tensors
+    torch.cuda.set_device(0)
+    c = CONFIGS[args.config]
+    t = make_layer_tensors(c, device="cuda", seed=0)
+    ws = moe.Workspace(moe.moe_workspace_size(c.shape()))
+    bias = t["bias"] if c.score == SCORE_SIGMOID_BIAS else None
+    ids, _, _ = moe.moe_route(c.shape(), t["x"], t["w_r"], bias, ws)
+    counts = torch.bincount(ids.flatten().long(), minlength=c.E).double().cpu().numpy()
+    results = []
+    for nodes, gpus, phys in ((4, 32, c.E + 32), (8, 64, c.E + 64)):
+        for hier in (0, 1):
+            if c.G % nodes or c.E % gpus:
+                continue
+            reps = max(1, args.steps)
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                slots, rep = moe.moe_eplb_plan(counts, c.G, nodes if hier else 0, gpus, phys)
+            us = (time.perf_counter() - t0) / reps * 1e6
+            per_gpu = [sum(counts[e] / rep[e] for e in row) for row in slots]
+            results.append({"nodes": nodes, "gpus": gpus, "physical": phys,
+                            "placement": "hierarchical" if hier else "global",
+                            "plan_us": us,
+                            "busiest_over_mean": max(per_gpu) / (sum(per_gpu) / len(per_gpu))})
+    line = {"metric": "EPLB plan time (host) and busiest/mean GPU load", "impl": "gb300",
+            "value": max(r["plan_us"] for r in results) if results else None, "unit": "us",
+            "higher_is_better": False, "steps": args.steps, "data": "synthetic",
+            "config": {"workload": workload_desc(c), "loads": "assignment counts of the routed batch"},
+            "plans": results}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     c = CONFIGS[args.config]
+    if args.eplb:
+        return run_eplb(args)
     if args.capacity is not None:
         return run_capacity(args)
     if args.masked:

@@ -24,6 +24,7 @@ from ._lib import (  # noqa: F401
     moe_dispatch,
     moe_dispatch_capacity,
     moe_dispatch_noalloc,
+    moe_eplb_plan,
     moe_expert_capacity,
     moe_expert_down,
     moe_expert_ffn,

@@ -61,6 +61,7 @@ SIGNATURES = {
     "moe_dispatch": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_noalloc": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_capacity": (_I32, [_I32, _I32, _I32, ctypes.c_double]),
+    "moe_eplb_plan": (_I32, [_P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
     "moe_dispatch_capacity": (_I32, [_PS, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                      _SZ, _P]),
     "moe_layer_capacity_workspace_size": (_I32, [_PS, _I32, ctypes.POINTER(_SZ)]),
@@ -441,6 +442,22 @@ def moe_layer_capacity(shape, capacity, overflow, x, w_r, bias, w_gate_up, w_dow
                                     _ptr(y), _ptr(counts), _ptr(kept), ws.c_ptr, ws.nbytes,
                                     _stream(stream)))
     return y
+
+
+def moe_eplb_plan(load, num_groups: int, num_nodes: int, num_gpus: int, num_physical: int):
+    """Expert placement (host).  load: per-expert loads (numpy).  Returns
+    (gpu_slots [num_gpus, num_physical // num_gpus], replicas [E]) as numpy."""
+    import numpy as np
+    load = np.ascontiguousarray(load, dtype=np.float64)
+    E = load.size
+    slots = np.empty(num_physical, dtype=np.int32)
+    reps = np.empty(E, dtype=np.int32)
+    _check("moe_eplb_plan",
+           lib().moe_eplb_plan(load.ctypes.data_as(ctypes.c_void_p), E, int(num_groups),
+                               int(num_nodes), int(num_gpus), int(num_physical),
+                               slots.ctypes.data_as(ctypes.c_void_p),
+                               reps.ctypes.data_as(ctypes.c_void_p)))
+    return slots.reshape(num_gpus, num_physical // num_gpus), reps
 
 
 def moe_selftest_wait_timeout(ws: Workspace, limit_ns: int, stream=None):

@@ -298,6 +298,31 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
                                 moe_stream_t stream);
 
 /*
+ * Expert placement planner ("ep-deploy" handbook page, section "EPLB 与路由约束",
+ * host code, no GPU): places num_experts logical experts, given their loads
+ * (load [E] host doubles, >= 0), on num_gpus GPUs as num_physical physical
+ * experts (num_physical - E redundant copies).
+ *   num_nodes > 0 (hierarchical): the expert groups (E / num_groups
+ *   consecutive experts) are packed onto the nodes by group load, the same
+ *   number per node, so no group spans nodes; inside each node, copies are
+ *   added one at a time to the expert with the largest load per copy (equal:
+ *   the one first in the node's order) until the node has num_physical/nodes
+ *   physical experts; these (weight load / copies) are packed onto the
+ *   node's GPUs.  num_nodes = 0 (global): the cluster is one node.
+ *   Packing: heaviest item first (equal: lower index), into the lightest
+ *   pack with room (equal: lower pack index); every pack gets the same count.
+ * Outputs (host, caller-owned): gpu_slots [num_physical], GPU g holding the
+ *   logical experts gpu_slots[g * P/G .. (g+1) * P/G) (P = num_physical,
+ *   G = num_gpus); replicas [E] copies per expert.
+ * Errors: MOE_ERR_INVALID_ARG when E % num_groups, num_groups % nodes,
+ *   num_gpus % nodes or num_physical % num_gpus is not zero, num_physical < E,
+ *   or a load is negative or not finite.
+ */
+moe_status_t moe_eplb_plan(const double *load, int32_t num_experts, int32_t num_groups,
+                           int32_t num_nodes, int32_t num_gpus, int32_t num_physical,
+                           int32_t *gpu_slots, int32_t *replicas);
+
+/*
  * Number of kernels moe_layer launches per call for this shape (for launch
  * accounting).
  */
