@@ -86,6 +86,11 @@ def _load():
                                                 P, I, P, P, P, P]),
             "oracle_expert_capacity": (I, [I, I, I, ctypes.c_double]),
             "oracle_eplb_place": (I, [P, I, I, I, I, I, P, P]),
+            "oracle_e4m3_to_float": (F, [ctypes.c_uint8]),
+            "oracle_float_to_e4m3": (ctypes.c_uint8, [F]),
+            "oracle_quantize_rows_fp8": (None, [P, ctypes.c_int64, I, P, P]),
+            "oracle_quantize_blocks_fp8": (None, [P, I, I, I, P, P]),
+            "oracle_expert_ffn_rows_fp8": (None, [P, P, P, I, I, I, P, P, P, P, P, P]),
             "oracle_dispatch_capacity": (I, [P, I, I, I, I, I, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -271,6 +276,50 @@ def dispatch_capacity(ids, E, C, policy):
     if rc != 0:
         raise ValueError("expert id out of range")
     return counts, kept, ovf, dest, src
+
+
+def e4m3_to_float(code: int) -> float:
+    return float(_load().oracle_e4m3_to_float(int(code)))
+
+
+def float_to_e4m3(x: float) -> int:
+    return int(_load().oracle_float_to_e4m3(float(x)))
+
+
+def quantize_rows_fp8(x_bits):
+    """Per (row, 128 columns) e4m3 codes and fp32 scales of bf16 rows."""
+    x = _u16(x_bits)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows, cols // 128), np.float32)
+    _load().oracle_quantize_rows_fp8(_p(x), rows, cols, _p(q), _p(s))
+    return q, s
+
+
+def quantize_blocks_fp8(w_bits):
+    """Per 128 x 128 block e4m3 codes and fp32 scales of [mats, rows, cols] bf16."""
+    w = _u16(w_bits)
+    mats, rows, cols = w.shape
+    q = np.empty((mats, rows, cols), np.uint8)
+    s = np.empty((mats, rows // 128, cols // 128), np.float32)
+    _load().oracle_quantize_blocks_fp8(_p(w), mats, rows, cols, _p(q), _p(s))
+    return q, s
+
+
+def expert_ffn_rows_fp8(xq, xs, row_expert, wgu_q, wgu_s, wd_q, wd_s, return_h=False):
+    """FP8 SwiGLU FFN of each row; returns y [n,d] fp32 (and h as fp32 of its bf16)."""
+    xq = _c(xq, np.uint8)
+    xs = _c(xs, np.float32)
+    row_expert = _c(row_expert, np.int32)
+    n, d = xq.shape
+    inter = wgu_q.shape[1] // 2
+    y = np.empty((n, d), np.float32)
+    h = np.empty((n, inter), np.float32) if return_h else None
+    _load().oracle_expert_ffn_rows_fp8(_p(xq), _p(xs), _p(row_expert), n, d, inter,
+                                       _p(_c(wgu_q, np.uint8)), _p(_c(wgu_s, np.float32)),
+                                       _p(_c(wd_q, np.uint8)), _p(_c(wd_s, np.float32)),
+                                       None if h is None else _p(h), _p(y))
+    return (y, h) if return_h else y
 
 
 def eplb_place(load, groups, nodes, gpus, phys):

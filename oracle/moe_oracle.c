@@ -43,6 +43,10 @@
  *   R8  dispatch is a stable counting sort of the flat assignments a = t*k+j.
  *   R9  expert FFN: h = silu(x.Wg) * (x.Wu), y = h.Wd, accumulated in fp64.
  *   R10 combine: y[t] = sum_j w[t,j] * y_perm[dest[t*k+j]], j ascending.
+ *   R13 FP8: e4m3 codes with fp32 block scales, one per (row, 128 columns)
+ *       of an activation and per 128 x 128 block of a weight;
+ *       s = amax / 448 (1 for an all-zero block), q = round-to-nearest-even
+ *       e4m3 of x / s (IEEE fp32 division), saturating at 448.
  *   R11 capacity: the first C assignments of an expert in increasing
  *       a = t*k + j keep their place; later ones overflow.  Dropped ones add
  *       nothing (weights are not renormalised); second-round ones are
@@ -336,6 +340,173 @@ int oracle_dispatch(const int32_t *ids, int T, int k, int E, int32_t *counts,
   }
   free(cursor);
   return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 (e4m3) with block scales ([par02] "DeepGEMM masked, FP8"; [ep] "the    */
+/* dispatch sends FP8 with scales", 7168 + 224 bytes per token)              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * e4m3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent field 0
+ * holds the subnormals m/8 * 2^-6; 0x7f / 0xff are NaN; the largest finite
+ * value is 448.  No infinities.
+ */
+float oracle_e4m3_to_float(uint8_t c) {
+  int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  float v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexpf((float)m, -9); /* m/8 * 2^-6 */
+  else
+    v = ldexpf((float)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+  return s ? -v : v;
+}
+
+/*
+ * Nearest e4m3 value to x, ties to the even mantissa code, magnitudes past
+ * 448 saturating to 448 (R13).  |x| < 2^-6: the subnormal code is
+ * |x| * 2^9 rounded to nearest even (8 meaning the smallest normal);
+ * otherwise |x| = f * 2^p with f in [1, 2): mantissa (f - 1) * 8 rounded to
+ * nearest even, carrying into the exponent.  (Both products are exact in
+ * double, and nearbyint rounds half to even.)
+ */
+uint8_t oracle_float_to_e4m3(float x) {
+  double a = fabs((double)x);
+  int code;
+  if (a >= 448.0) {
+    code = 126;
+  } else if (a < ldexp(1.0, -6)) {
+    code = (int)nearbyint(a * 512.0); /* 0..8 */
+  } else {
+    int p;
+    double f = frexp(a, &p) * 2.0; /* a = f * 2^(p-1), f in [1,2) */
+    int e = p - 1;                 /* unbiased exponent, -6..8 */
+    int m = (int)nearbyint((f - 1.0) * 8.0);
+    if (m == 8) {
+      m = 0;
+      e += 1;
+    }
+    code = ((e + 7) << 3) | m;
+    if (code > 126) code = 126; /* saturate */
+  }
+  return (uint8_t)(code | (signbit(x) ? 0x80 : 0));
+}
+
+/* scale of a block with largest magnitude amax: amax / 448 in fp32, 1 when
+   the block is all zeros (R13) */
+static float fp8_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
+
+/*
+ * Activations, per row and 128-column block (R13): s = amax / 448,
+ * q = e4m3(x / s) with IEEE fp32 division.  x: [rows, cols] bf16, cols a
+ * multiple of 128; q: [rows, cols] codes; scales: [rows, cols/128] fp32.
+ */
+void oracle_quantize_rows_fp8(const uint16_t *x, int64_t rows, int cols, uint8_t *q,
+                              float *scales) {
+  int nb = cols / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int b = 0; b < nb; ++b) {
+      const uint16_t *xb = x + (size_t)r * cols + (size_t)b * 128;
+      float amax = 0.0f;
+      for (int i = 0; i < 128; ++i) {
+        float v = fabsf(bf16_value(xb[i]));
+        if (v > amax) amax = v;
+      }
+      float s = fp8_scale(amax);
+      scales[(size_t)r * nb + b] = s;
+      for (int i = 0; i < 128; ++i)
+        q[(size_t)r * cols + (size_t)b * 128 + i] = oracle_float_to_e4m3(bf16_value(xb[i]) / s);
+    }
+}
+
+/*
+ * Weights [mats, rows, cols] bf16, per 128 x 128 block (R13): one scale per
+ * block, scales [mats, rows/128, cols/128].
+ */
+void oracle_quantize_blocks_fp8(const uint16_t *w, int mats, int rows, int cols, uint8_t *q,
+                                float *scales) {
+  int rb = rows / 128, cb = cols / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t blk = 0; blk < (int64_t)mats * rb * cb; ++blk) {
+    int64_t m = blk / ((int64_t)rb * cb);
+    int i = (int)((blk / cb) % rb), j = (int)(blk % cb);
+    const uint16_t *base = w + (size_t)m * rows * cols;
+    float amax = 0.0f;
+    for (int r = 0; r < 128; ++r)
+      for (int c = 0; c < 128; ++c) {
+        float v = fabsf(bf16_value(base[(size_t)(i * 128 + r) * cols + j * 128 + c]));
+        if (v > amax) amax = v;
+      }
+    float s = fp8_scale(amax);
+    scales[blk] = s;
+    for (int r = 0; r < 128; ++r)
+      for (int c = 0; c < 128; ++c) {
+        size_t o = (size_t)m * rows * cols + (size_t)(i * 128 + r) * cols + j * 128 + c;
+        q[o] = oracle_float_to_e4m3(bf16_value(w[o]) / s);
+      }
+  }
+}
+
+/*
+ * FP8 SwiGLU FFN of each row (R13): with x~ = q_x * s_x (per 128 block) and
+ * W~ = q_W * s_W (per 128 x 128 block), g, u = x~ . W~gu, h = silu(g) * u in
+ * fp64; h is rounded to bf16 (its storage format) and quantized per 128
+ * block like an activation; y = h~ . W~d^T in fp64.
+ */
+void oracle_expert_ffn_rows_fp8(const uint8_t *xq, const float *xs, const int32_t *row_expert,
+                                int n, int d, int inter, const uint8_t *wgu_q,
+                                const float *wgu_s, const uint8_t *wd_q, const float *wd_s,
+                                float *h_out, float *y_out) {
+  int db = d / 128, ib = inter / 128;
+#pragma omp parallel
+  {
+    double *xv = (double *)malloc(sizeof(double) * (size_t)d);
+    uint16_t *hb = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)inter);
+    uint8_t *hq = (uint8_t *)malloc((size_t)inter);
+    float *hs = (float *)malloc(sizeof(float) * (size_t)ib);
+    double *hv = (double *)malloc(sizeof(double) * (size_t)inter);
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < n; ++r) {
+      int e = row_expert[r];
+      for (int i = 0; i < d; ++i)
+        xv[i] = (double)oracle_e4m3_to_float(xq[(size_t)r * d + i]) * (double)xs[(size_t)r * db + i / 128];
+      const uint8_t *wg = wgu_q + (size_t)e * 2 * inter * d;
+      const float *sg = wgu_s + (size_t)e * (2 * inter / 128) * db;
+      for (int j = 0; j < inter; ++j) {
+        double g = 0.0, u = 0.0;
+        for (int i = 0; i < d; ++i) {
+          double wgv = (double)oracle_e4m3_to_float(wg[(size_t)j * d + i]) *
+                       (double)sg[(size_t)(j / 128) * db + i / 128];
+          double wuv = (double)oracle_e4m3_to_float(wg[(size_t)(inter + j) * d + i]) *
+                       (double)sg[(size_t)((inter + j) / 128) * db + i / 128];
+          g += xv[i] * wgv;
+          u += xv[i] * wuv;
+        }
+        double h = g / (1.0 + exp(-g)) * u;
+        hb[j] = bf16_round((float)h);
+        if (h_out) h_out[(size_t)r * inter + j] = bf16_value(hb[j]);
+      }
+      oracle_quantize_rows_fp8(hb, 1, inter, hq, hs);
+      for (int j = 0; j < inter; ++j)
+        hv[j] = (double)oracle_e4m3_to_float(hq[j]) * (double)hs[j / 128];
+      const uint8_t *wd = wd_q + (size_t)e * d * inter;
+      const float *sd = wd_s + (size_t)e * db * ib;
+      for (int c = 0; c < d; ++c) {
+        double y = 0.0;
+        for (int j = 0; j < inter; ++j)
+          y += hv[j] * (double)oracle_e4m3_to_float(wd[(size_t)c * inter + j]) *
+               (double)sd[(size_t)(c / 128) * ib + j / 128];
+        y_out[(size_t)r * d + c] = (float)y;
+      }
+    }
+    free(hv);
+    free(hs);
+    free(hq);
+    free(hb);
+    free(xv);
+  }
 }
 
 /* ------------------------------------------------------------------------ */
