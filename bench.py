@@ -600,6 +600,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-sample-s", type=float, default=15.0,
                     help="seconds of CPU oracle work for cpu_baseline (0 = skip)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the layer with FP8 experts (own line)")
     ap.add_argument("--eplb", action="store_true",
                     help="plan expert placements on the routed loads (own line)")
     ap.add_argument("--capacity", type=float, default=None,
@@ -663,6 +665,69 @@ def run_capacity(args):
     return 0
 
 
+def run_fp8(args):
+    """Time the FP8 layer (its own JSON line): e4m3 weights with 128 x 128
+    block scales (quantized once, outside the timed region), activations
+    quantized per row and 128 columns inside the layer."""
+    import torch
+    import dispatch_combine_gb300 as moe
+    from moe_inputs import make_layer_tensors
+    torch.cuda.set_device(0)
+    c = CONFIGS[args.config]
+    t = make_layer_tensors(c, device="cuda", seed=0)
+    bias = t["bias"] if c.score == SCORE_SIGMOID_BIAS else None
+    shape = c.shape()
+    gq, gs = moe.moe_quantize_fp8_blocks(t["w_gate_up"])
+    dq, ds = moe.moe_quantize_fp8_blocks(t["w_down"])
+    del t["w_gate_up"], t["w_down"]
+    ws = moe.Workspace(moe.moe_layer_fp8_workspace_size(shape))
+    y = torch.empty(c.T, c.d, dtype=torch.bfloat16, device="cuda")
+    counts = torch.empty(c.E, dtype=torch.int32, device="cuda")
+
+    def step():
+        moe.moe_layer_fp8(shape, t["x"], t["w_r"], bias, gq, gs, dq, ds, ws, y=y, counts=counts)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark("t_start")
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    sampler.mark("t_end")
+    clocks = sampler.stop()
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status error")
+    ms = e0.elapsed_time(e1) / args.steps
+    cnt = counts.cpu()
+    touched = int((cnt > 0).sum())
+    w_bytes = touched * 3 * c.d * c.inter          # e4m3: one byte per weight
+    flops = 6.0 * c.T * c.k * c.d * c.inter
+    peaks, peak_src = load_peaks()
+    line = {
+        "metric": METRIC + " (FP8 e4m3 experts, block scales)", "impl": "gb300",
+        "value": c.T / (ms / 1000.0), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(c), "weights": "e4m3, fp32 scale per 128x128 block",
+                   "activations": "e4m3, fp32 scale per row and 128 columns",
+                   "touched_experts": touched},
+        "layer_weight_bytes_fp8": w_bytes,
+        "layer_hbm_fraction_of_weights": w_bytes / (ms / 1000.0) / (peaks["hbm_gbs"] * 1e9),
+        "layer_tflops": flops / (ms / 1000.0) / 1e12,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_eplb(args):
     """Expert placement on the loads of a routed batch (its own JSON line):
     route the workload's tokens on the GPU, count assignments per expert,
@@ -705,6 +770,8 @@ def run_eplb(args):
 def main(argv=None):
     args = parse_args(argv)
     c = CONFIGS[args.config]
+    if args.fp8:
+        return run_fp8(args)
     if args.eplb:
         return run_eplb(args)
     if args.capacity is not None:

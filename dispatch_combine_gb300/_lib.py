@@ -62,6 +62,13 @@ SIGNATURES = {
     "moe_dispatch_noalloc": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_capacity": (_I32, [_I32, _I32, _I32, ctypes.c_double]),
     "moe_eplb_plan": (_I32, [_P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
+    "moe_quantize_fp8_rows": (_I32, [_P, ctypes.c_int64, _I32, _P, _P, _P]),
+    "moe_expert_ffn_fp8_workspace_size": (_I32, [_PS, _I32, _I32, ctypes.POINTER(_SZ)]),
+    "moe_expert_ffn_fp8": (_I32, [_PS, _I32, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _SZ,
+                                  _P]),
+    "moe_layer_fp8_workspace_size": (_I32, [_PS, ctypes.POINTER(_SZ)]),
+    "moe_layer_fp8": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_quantize_fp8_blocks": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "moe_dispatch_capacity": (_I32, [_PS, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                      _SZ, _P]),
     "moe_layer_capacity_workspace_size": (_I32, [_PS, _I32, ctypes.POINTER(_SZ)]),
@@ -458,6 +465,73 @@ def moe_eplb_plan(load, num_groups: int, num_nodes: int, num_gpus: int, num_phys
                                slots.ctypes.data_as(ctypes.c_void_p),
                                reps.ctypes.data_as(ctypes.c_void_p)))
     return slots.reshape(num_gpus, num_physical // num_gpus), reps
+
+
+def moe_quantize_fp8_rows(x, stream=None):
+    """x [rows, cols] bf16 -> (q [rows, cols] uint8 e4m3 codes, scales [rows, cols/128] fp32)."""
+    rows, cols = x.shape
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    sc = torch.empty((rows, cols // 128), dtype=torch.float32, device=x.device)
+    _check("moe_quantize_fp8_rows",
+           lib().moe_quantize_fp8_rows(_ptr(x), rows, cols, _ptr(q), _ptr(sc), _stream(stream)))
+    return q, sc
+
+
+def moe_quantize_fp8_blocks(w, stream=None):
+    """w [mats, rows, cols] bf16 -> (q uint8 codes, scales [mats, rows/128, cols/128] fp32)."""
+    mats, rows, cols = w.shape
+    q = torch.empty((mats, rows, cols), dtype=torch.uint8, device=w.device)
+    sc = torch.empty((mats, rows // 128, cols // 128), dtype=torch.float32, device=w.device)
+    _check("moe_quantize_fp8_blocks",
+           lib().moe_quantize_fp8_blocks(_ptr(w), mats, rows, cols, _ptr(q), _ptr(sc),
+                                         _stream(stream)))
+    return q, sc
+
+
+def moe_expert_ffn_fp8_workspace_size(shape, layout, M_max=0) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_expert_ffn_fp8_workspace_size",
+           lib().moe_expert_ffn_fp8_workspace_size(ctypes.byref(as_shape(shape)), int(layout),
+                                                   int(M_max), ctypes.byref(out)))
+    return int(out.value)
+
+
+def moe_expert_ffn_fp8(shape, layout, x_q, x_scale, seg, M_max, w_gu_q, w_gu_s, w_dn_q,
+                       w_dn_s, ws: Workspace, y_out=None, stream=None):
+    s = as_shape(shape)
+    rows = x_q.shape[0] if x_q.dim() == 2 else x_q.shape[0] * x_q.shape[1]
+    if y_out is None:
+        y_out = torch.empty(tuple(x_q.shape[:-1]) + (s.d,), dtype=torch.float32,
+                            device=x_q.device)
+    _check("moe_expert_ffn_fp8",
+           lib().moe_expert_ffn_fp8(ctypes.byref(s), int(layout), _ptr(x_q), _ptr(x_scale),
+                                    _ptr(seg), int(M_max), _ptr(w_gu_q), _ptr(w_gu_s),
+                                    _ptr(w_dn_q), _ptr(w_dn_s), _ptr(y_out), ws.c_ptr,
+                                    ws.nbytes, _stream(stream)))
+    return y_out
+
+
+def moe_layer_fp8_workspace_size(shape) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_layer_fp8_workspace_size",
+           lib().moe_layer_fp8_workspace_size(ctypes.byref(as_shape(shape)), ctypes.byref(out)))
+    return int(out.value)
+
+
+def moe_layer_fp8(shape, x, w_r, bias, w_gu_q, w_gu_s, w_dn_q, w_dn_s, ws: Workspace, y=None,
+                  counts=None, stream=None):
+    s = as_shape(shape)
+    _expect(x, torch.bfloat16, (s.T, s.d), "x")
+    _expect(w_r, torch.bfloat16, (s.d, s.E), "w_r")
+    _expect(w_gu_q, torch.uint8, (s.E, 2 * s.inter, s.d), "w_gate_up_q")
+    _expect(w_dn_q, torch.uint8, (s.E, s.d, s.inter), "w_down_q")
+    if y is None:
+        y = torch.empty((s.T, s.d), dtype=torch.bfloat16, device=x.device)
+    _check("moe_layer_fp8",
+           lib().moe_layer_fp8(ctypes.byref(s), _ptr(x), _ptr(w_r), _ptr(bias), _ptr(w_gu_q),
+                               _ptr(w_gu_s), _ptr(w_dn_q), _ptr(w_dn_s), _ptr(y), _ptr(counts),
+                               ws.c_ptr, ws.nbytes, _stream(stream)))
+    return y
 
 
 def moe_selftest_wait_timeout(ws: Workspace, limit_ns: int, stream=None):

@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["router.cu", "dispatch.cu", "combine.cu", "gemm.cu", "api.cu", "noalloc.cu",
-           "eplb.cpp"]
+           "quant.cu", "eplb.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -442,6 +442,202 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
 }
 
 // ---------------------------------------------------------------------------
+// FP8 quantization
+// ---------------------------------------------------------------------------
+
+moe_status_t moe_quantize_fp8_rows(const void *x, int64_t rows, int32_t cols, void *q,
+                                   float *scales, moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !q || !scales || !aligned16(x) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_quantize_rows_fp8(x, rows, cols, q, scales, stream));
+}
+
+moe_status_t moe_quantize_fp8_blocks(const void *w, int32_t mats, int32_t rows, int32_t cols,
+                                     void *q, float *scales, moe_stream_t stream) {
+  if (mats < 0 || rows < 0 || cols <= 0 || rows % 128 != 0 || cols % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (mats == 0 || rows == 0) return MOE_OK;
+  if (!w || !q || !scales || !aligned16(w) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_quantize_blocks_fp8(w, mats, rows, cols, q, scales, stream));
+}
+
+// ---------------------------------------------------------------------------
+// FP8 expert FFN and layer
+// ---------------------------------------------------------------------------
+
+struct LayoutF8 {
+  size_t status, mtile, chunk, logits, wr32, h, hq, hs, ids, w, counts, offsets, dest, src, xq,
+      xs, xq_perm, xs_perm, y_perm;
+  size_t end_ffn, end_layer;
+};
+
+// FFN part (h in bf16, then its FP8 codes and scales) for `rows` rows; the
+// layer part adds routing, dispatch and the FP8 activations
+LayoutF8 make_fp8_layout(const moe_shape_t &s, int64_t rows) {
+  LayoutF8 L;
+  const int64_t n = static_cast<int64_t>(s.T) * s.k;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at_ = off;
+    off = align_up(off + bytes);
+    return at_;
+  };
+  L.status = take(4);
+  L.mtile = take(4 * static_cast<size_t>(s.E + 1));
+  L.h = take(2 * static_cast<size_t>(rows) * s.inter);
+  L.hq = take(static_cast<size_t>(rows) * s.inter);
+  L.hs = take(4 * static_cast<size_t>(rows) * (s.inter / 128));
+  L.end_ffn = off;
+  L.chunk = take(4 * static_cast<size_t>(moe::dispatch_num_chunks(n)) * s.E);
+  L.logits = take(4 * static_cast<size_t>(s.T) * s.E);
+  L.wr32 = take(moe::router_scratch_bytes(s.d, s.E));
+  L.ids = take(4 * static_cast<size_t>(n));
+  L.w = take(4 * static_cast<size_t>(n));
+  L.counts = take(4 * static_cast<size_t>(s.E));
+  L.offsets = take(4 * static_cast<size_t>(s.E + 1));
+  L.dest = take(4 * static_cast<size_t>(n));
+  L.src = take(4 * static_cast<size_t>(n));
+  L.xq = take(static_cast<size_t>(s.T) * s.d);
+  L.xs = take(4 * static_cast<size_t>(s.T) * (s.d / 128));
+  L.xq_perm = take(static_cast<size_t>(n) * s.d);
+  L.xs_perm = take(4 * static_cast<size_t>(n) * (s.d / 128));
+  L.y_perm = take(4 * static_cast<size_t>(n) * s.d);
+  L.end_layer = off;
+  return L;
+}
+
+moe_status_t check_fp8_shape(const moe_shape_t *s) {
+  if (s->d % 128 != 0 || s->inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// FP8 gate_up + SwiGLU -> h (bf16) -> FP8 codes of h -> FP8 down, over rows
+// whose m-tile prefix (128-row tiles) is in the workspace
+moe_status_t run_ffn_fp8(const moe_shape_t *s, int32_t layout, const void *xq, const float *xs,
+                         const int32_t *seg, int32_t M_max, int64_t rows, int32_t *mtile,
+                         const void *wgu_q, const float *wgu_s, const void *wd_q,
+                         const float *wd_s, float *y, void *ws, const LayoutF8 &L,
+                         cudaStream_t st) {
+  uint32_t *status = at<uint32_t>(ws, L.status);
+  GemmProblem p;
+  std::memset(&p, 0, sizeof p);
+  p.E = s->E;
+  p.layout = layout;
+  p.seg = seg;
+  p.M_max = M_max;
+  p.rows_total = rows;
+  p.mtile_base = mtile;
+  p.status = status;
+  p.K = s->d;
+  p.n_out = s->inter;
+  p.a = xq;
+  p.b = wgu_q;
+  p.b_rows = 2 * s->inter;
+  p.out = at<void>(ws, L.h);
+  MOE_TRY(cuda_status(moe::launch_gemm_fp8_gate_up_swiglu(p, xs, wgu_s, st)));
+  MOE_TRY(cuda_status(moe::launch_quantize_rows_fp8(at<void>(ws, L.h), rows, s->inter,
+                                                    at<void>(ws, L.hq), at<float>(ws, L.hs),
+                                                    st)));
+  p.K = s->inter;
+  p.n_out = s->d;
+  p.a = at<void>(ws, L.hq);
+  p.b = wd_q;
+  p.b_rows = s->d;
+  p.out = y;
+  return cuda_status(moe::launch_gemm_fp8_down(p, at<float>(ws, L.hs), wd_s, st));
+}
+
+moe_status_t moe_expert_ffn_fp8_workspace_size(const moe_shape_t *shape, int32_t layout,
+                                               int32_t M_max, size_t *bytes) {
+  MOE_TRY(check_shape(shape));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  int64_t rows = 0;
+  MOE_TRY(ffn_rows(shape, layout, M_max, &rows));
+  *bytes = make_fp8_layout(*shape, rows).end_ffn;
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_ffn_fp8(const moe_shape_t *shape, int32_t layout, const void *x_q,
+                                const float *x_scale, const int32_t *seg, int32_t M_max,
+                                const void *w_gate_up_q, const float *w_gate_up_scale,
+                                const void *w_down_q, const float *w_down_scale, float *y_out,
+                                void *ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  MOE_TRY(check_fp8_shape(shape));
+  int64_t rows = 0;
+  MOE_TRY(ffn_rows(shape, layout, M_max, &rows));
+  if (rows == 0) return MOE_OK;
+  if (!x_q || !x_scale || !seg || !w_gate_up_q || !w_gate_up_scale || !w_down_q ||
+      !w_down_scale || !y_out)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_q) || !aligned16(w_gate_up_q) || !aligned16(w_down_q) || !aligned16(y_out))
+    return MOE_ERR_INVALID_ARG;
+  const LayoutF8 L = make_fp8_layout(*shape, rows);
+  MOE_TRY(check_ws(ws, ws_bytes, L.end_ffn));
+  int32_t *mtile = at<int32_t>(ws, L.mtile);
+  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max, 128, mtile,
+                                            at<uint32_t>(ws, L.status), stream)));
+  return run_ffn_fp8(shape, layout, x_q, x_scale, seg, M_max, rows, mtile, w_gate_up_q,
+                     w_gate_up_scale, w_down_q, w_down_scale, y_out, ws, L, stream);
+}
+
+moe_status_t moe_layer_fp8_workspace_size(const moe_shape_t *shape, size_t *bytes) {
+  MOE_TRY(check_shape(shape));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_fp8_layout(*shape, static_cast<int64_t>(shape->T) * shape->k).end_layer;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_fp8(const moe_shape_t *shape, const void *x, const void *w_r,
+                           const float *bias, const void *w_gate_up_q,
+                           const float *w_gate_up_scale, const void *w_down_q,
+                           const float *w_down_scale, void *y, int32_t *counts, void *ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  if (shape->T == 0) return MOE_OK;
+  MOE_TRY(check_fp8_shape(shape));
+  const moe_shape_t &s = *shape;
+  if (!x || !w_r || !w_gate_up_q || !w_gate_up_scale || !w_down_q || !w_down_scale || !y)
+    return MOE_ERR_INVALID_ARG;
+  if (s.score == MOE_SCORE_SIGMOID_BIAS && !bias) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_r) || !aligned16(w_gate_up_q) || !aligned16(w_down_q) ||
+      !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t n = static_cast<int64_t>(s.T) * s.k;
+  const LayoutF8 L = make_fp8_layout(s, n);
+  MOE_TRY(check_ws(ws, ws_bytes, L.end_layer));
+  uint32_t *status = at<uint32_t>(ws, L.status);
+  int32_t *ids = at<int32_t>(ws, L.ids);
+  float *w = at<float>(ws, L.w);
+  int32_t *cnt = counts ? counts : at<int32_t>(ws, L.counts);
+  int32_t *offsets = at<int32_t>(ws, L.offsets);
+  int32_t *mtile = at<int32_t>(ws, L.mtile);
+  int32_t *dest = at<int32_t>(ws, L.dest);
+  int32_t *src = at<int32_t>(ws, L.src);
+  float *y_perm = at<float>(ws, L.y_perm);
+  MOE_TRY(cuda_status(moe::launch_router_logits(x, w_r, s.T, s.d, s.E, at<float>(ws, L.logits),
+                                                at<void>(ws, L.wr32), stream)));
+  MOE_TRY(cuda_status(moe::launch_router_select(at<float>(ws, L.logits), bias, s.T, s.E, s.G,
+                                                s.topk_group, s.k, s.score, s.bias_scale, 0,
+                                                ids, w, stream)));
+  // the dispatch moves FP8 rows and their scales
+  MOE_TRY(cuda_status(moe::launch_quantize_rows_fp8(x, s.T, s.d, at<void>(ws, L.xq),
+                                                    at<float>(ws, L.xs), stream)));
+  MOE_TRY(cuda_status(moe::launch_dispatch(ids, s.T, s.k, s.E, nullptr, s.d, cnt, offsets, src,
+                                           dest, nullptr, at<int32_t>(ws, L.chunk), mtile, 128,
+                                           status, stream)));
+  MOE_TRY(cuda_status(moe::launch_gather_rows(at<void>(ws, L.xq), s.d, at<float>(ws, L.xs),
+                                              s.d / 128, src, offsets + s.E, n, s.T,
+                                              at<void>(ws, L.xq_perm), at<float>(ws, L.xs_perm),
+                                              stream)));
+  MOE_TRY(run_ffn_fp8(shape, MOE_LAYOUT_CONTIGUOUS, at<void>(ws, L.xq_perm),
+                      at<float>(ws, L.xs_perm), offsets, 0, n, mtile, w_gate_up_q,
+                      w_gate_up_scale, w_down_q, w_down_scale, y_perm, ws, L, stream));
+  return cuda_status(moe::launch_combine(y_perm, n, dest, w, s.T, s.k, s.d, y, stream));
+}
+
+// ---------------------------------------------------------------------------
 // capacity variant
 // ---------------------------------------------------------------------------
 

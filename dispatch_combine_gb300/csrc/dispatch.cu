@@ -233,6 +233,22 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
   }
 }
 
+// per-row fp32 block scales follow their row: dst[p, b] = src[src_token[p], b]
+__global__ void __launch_bounds__(256)
+    gather_scales_kernel(const float *__restrict__ src, const int32_t *__restrict__ src_token,
+                         const int32_t *__restrict__ offsets_end, int64_t n, int T, int per_row,
+                         float *__restrict__ dst) {
+  const int64_t rows = min(n, static_cast<int64_t>(*offsets_end));
+  const int64_t total = rows * per_row;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / per_row;
+    const int t = src_token[row];
+    if (t < 0 || t >= T) continue;
+    dst[i] = src[static_cast<int64_t>(t) * per_row + (i - row * per_row)];
+  }
+}
+
 // mtile_base from offsets (layout 0) or masked_m clamped to M_max (layout 1)
 __global__ void __launch_bounds__(1024)
     ffn_tiles_kernel(const int32_t *__restrict__ seg, int layout, int E, int M_max,
@@ -300,6 +316,26 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
     err = cudaGetLastError();
   }
   return err;
+}
+
+cudaError_t launch_gather_rows(const void *src, int row_bytes, const float *src_scale,
+                               int scales_per_row, const int32_t *src_token,
+                               const int32_t *offsets_end, int64_t n, int T, void *dst,
+                               float *dst_scale, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int64_t want = (n + kGatherWarps - 1) / kGatherWarps;
+  const int64_t grid_cap = (int64_t)num_sms() * 8;
+  dispatch_gather_kernel<<<(unsigned)(want < grid_cap ? want : grid_cap), kGatherWarps * 32, 0,
+                           s>>>(static_cast<const uint4 *>(src), src_token, offsets_end, n, T,
+                                row_bytes / 16, static_cast<uint4 *>(dst),
+                                CapacityArgs{0, 0, 0, nullptr, nullptr});
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || !src_scale) return err;
+  const int64_t items = n * scales_per_row;
+  const int64_t blocks = (items + 255) / 256;
+  gather_scales_kernel<<<(unsigned)(blocks < grid_cap ? blocks : grid_cap), 256, 0, s>>>(
+      src_scale, src_token, offsets_end, n, T, scales_per_row, dst_scale);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,

@@ -710,6 +710,277 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// FP8 (e4m3) grouped GEMM with block scales.  A rows carry one fp32 scale per
+// 128 columns, B (weights) one per 128 x 128 block; a k-block is 128
+// columns, i.e. one scale block and one 128-byte swizzle row.  The MMA warp
+// issues kind::f8f6f4 MMAs (M=128, N=128, K=32) for one k-block into one of
+// two TMEM partial accumulators; the four epilogue warps (thread = row) read
+// the partial, multiply it by the two scales and add it into fp32 registers
+// (128 per thread), then release the partial.  After the last k-block they
+// apply SwiGLU (gate_up: columns 0-63 gate, 64-127 the matching up) or write
+// fp32 (down) straight from registers.
+//   full/empty[s]    stage ring (producer <-> MMA);
+//   pfull/pempty[b]  partial accumulator b (MMA <-> epilogue warps).
+// ---------------------------------------------------------------------------
+constexpr int kF8BK = 128;  // e4m3 per k-block = bytes per swizzle row
+constexpr int kF8BN = 128;
+constexpr int kF8Stages = 6;
+
+template <bool SWIGLU>
+struct CfgF8 {
+  static constexpr int A_BYTES = kBM * kF8BK;
+  static constexpr int B_BYTES = kF8BN * kF8BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = kF8Stages;
+  static constexpr int BN_OUT = SWIGLU ? kF8BN / 2 : kF8BN;
+  static constexpr int TMEM_COLS = 2 * kF8BN;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int MT_OFF = MISC_OFF + 16;
+  static constexpr int SMEM_BYTES = MT_OFF + (kMaxE + 1) * 4 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "227 KB of shared memory per CTA");
+};
+
+struct F8Args {
+  KArgs k;              // tiles, layout, output (k.K = reduction length)
+  const float *a_scale;  // [rows_total, K/128]
+  const float *b_scale;  // [E, b_rows/128, K/128]
+};
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB, const F8Args fa) {
+  using C = CfgF8<SWIGLU>;
+  const KArgs &args = fa.k;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *smA = smem;
+  uint8_t *smB = smem + C::STAGES * C::A_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + C::STAGES;
+  uint64_t *pfull = bars + 2 * C::STAGES;
+  uint64_t *pempty = pfull + 2;
+  uint64_t *drain = pfull + 4;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+  int32_t *mt = reinterpret_cast<int32_t *>(smem + C::MT_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) mt[i] = args.mtile_base[i];
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < C::STAGES; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pfull[b], 1);
+      mbar_init(&pempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int total = mt[args.E] * args.n_tiles;
+  if (blockIdx.x >= total) return;
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int kblocks = args.K / kF8BK;
+  const int kbs = kblocks;  // scale blocks along K
+  const int b_blocks = args.b_rows / 128;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[C::STAGES];
+      bool issued[C::STAGES];
+#pragma unroll
+      for (int st = 0; st < C::STAGES; ++st) issued[st] = false;
+      for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x) {
+        const Tile t = decode_tile(args, mt, u);
+        int b0, b1;
+        if (SWIGLU) {
+          b0 = t.e * args.b_rows + t.n * C::BN_OUT;
+          b1 = t.e * args.b_rows + args.up_off + t.n * C::BN_OUT;
+        } else {
+          b0 = t.e * args.b_rows + t.n * kF8BN;
+          b1 = b0 + kF8BN / 2;
+        }
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
+                                 args.wait_limit_ns))
+            break;
+          uint8_t *a_dst = smA + stage * C::A_BYTES;
+          uint8_t *b_dst = smB + stage * C::B_BYTES;
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_2d(a_dst, &tmA, &full[stage], kb * kF8BK, t.row0);
+          tma_load_2d(b_dst, &tmB, &full[stage], kb * kF8BK, b0);
+          tma_load_2d(b_dst + (kF8BN / 2) * kF8BK, &tmB, &full[stage], kb * kF8BK, b1);
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int st = 0; st < C::STAGES; ++st)
+        if (issued[st]) wait_drain(&full[st], issued_phase[st], args.wait_limit_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t kIdesc = mma_idesc_e4m3_f32(kBM, kF8BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t q = 0;  // k-blocks issued so far: partial q & 1, its use q >> 1
+      bool any_mma = false;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok && !*abort_flag; u += gridDim.x) {
+        for (int kb = 0; kb < kblocks; ++kb, ++q) {
+          const int p = static_cast<int>(q & 1u);
+          if (!mbar_wait_bounded(&pempty[p], ((q >> 1) & 1u) ^ 1u, abort_flag, args.status,
+                                 args.wait_limit_ns) ||
+              !mbar_wait_bounded(&full[stage], phase, abort_flag, args.status,
+                                 args.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(p * kF8BN);
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(smA + stage * C::A_BYTES));
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < kF8BK / 32; ++kk)  // +32 bytes = 32 e4m3 along K
+            mma_e4m3_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, kIdesc, kk != 0 ? 1u : 0u);
+          any_mma = true;
+          mma_commit(&empty[stage]);
+          mma_commit(&pfull[p]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (any_mma) {
+        mma_commit(drain);
+        wait_drain(drain, 0, args.wait_limit_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- promotion + epilogue (warps 2..5) ----------------
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t q = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Tile t = decode_tile(args, mt, u);
+      const int64_t grow = static_cast<int64_t>(t.row0) + row;
+      const bool rok = row < t.rows_valid && grow >= 0 && grow < args.rows_total;
+      const float *as = fa.a_scale + (rok ? grow : 0) * kbs;
+      const float *bs0, *bs1;
+      if (SWIGLU) {
+        bs0 = fa.b_scale + (static_cast<int64_t>(t.e) * b_blocks + (t.n * C::BN_OUT) / 128) * kbs;
+        bs1 = fa.b_scale +
+              (static_cast<int64_t>(t.e) * b_blocks + (args.up_off + t.n * C::BN_OUT) / 128) * kbs;
+      } else {
+        bs0 = bs1 = fa.b_scale + (static_cast<int64_t>(t.e) * b_blocks + t.n) * kbs;
+      }
+      float acc[kF8BN];
+#pragma unroll
+      for (int c = 0; c < kF8BN; ++c) acc[c] = 0.0f;
+      float sa = rok ? __ldg(as) : 0.0f;
+      for (int kb = 0; kb < kblocks; ++kb, ++q) {
+        const int p = static_cast<int>(q & 1u);
+        const float s0 = sa * __ldg(bs0 + kb), s1 = sa * __ldg(bs1 + kb);
+        sa = (rok && kb + 1 < kblocks) ? __ldg(as + kb + 1) : 0.0f;
+        const bool waited = mbar_wait_bounded(&pfull[p], (q >> 1) & 1u, abort_flag, args.status,
+                                              args.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, waited)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tp = tmem_base + lane_off + static_cast<uint32_t>(p * kF8BN);
+#pragma unroll
+        for (int c = 0; c < kF8BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tp + c * 32, v);
+          tmem_ld_wait();
+          tmem_regs_fence(v);
+          const float sc = (c < kF8BN / 64) ? s0 : s1;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(__uint_as_float(v[j]), sc, acc[c * 32 + j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pempty[p]);
+      }
+      if (!ok || !rok) continue;
+      if (SWIGLU) {
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(args.out) + grow * args.ldo +
+                             static_cast<int64_t>(t.n) * C::BN_OUT;
+#pragma unroll
+        for (int c = 0; c < C::BN_OUT / 16; ++c) {
+          uint32_t w8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int j = c * 16 + 2 * i;
+            const float g0 = acc[j], g1 = acc[j + 1];
+            const float u0 = acc[C::BN_OUT + j], u1 = acc[C::BN_OUT + j + 1];
+            w8[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
+                                __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+          }
+          if (args.out_v8) {
+            st_global_v8(dst + c * 16, w8);
+          } else {
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 16);
+            d4[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+            d4[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+          }
+        }
+      } else {
+        float *dst = static_cast<float *>(args.out) + grow * args.ldo +
+                     static_cast<int64_t>(t.n) * kF8BN;
+#pragma unroll
+        for (int c = 0; c < kF8BN / 8; ++c) {
+          uint32_t w8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w8[i] = __float_as_uint(acc[c * 8 + i]);
+          if (args.out_v8) {
+            st_global_v8(dst + c * 8, w8);
+          } else {
+            float4 *d4 = reinterpret_cast<float4 *>(dst + c * 8);
+            d4[0] = make_float4(acc[c * 8], acc[c * 8 + 1], acc[c * 8 + 2], acc[c * 8 + 3]);
+            d4[1] = make_float4(acc[c * 8 + 4], acc[c * 8 + 5], acc[c * 8 + 6], acc[c * 8 + 7]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
 // bounded-wait self test: one thread waits on a barrier nobody arrives on
 // ---------------------------------------------------------------------------
 __global__ void wait_selftest_kernel(uint32_t *status, uint64_t limit_ns) {
@@ -780,6 +1051,62 @@ bool make_tmap(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D e4m3 (byte) tensor [rows, inner]; box = box_rows x 128 bytes, 128-byte
+// swizzle, out-of-bounds rows read as zero.
+bool make_tmap_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                  uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kF8BK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool SWIGLU>
+cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float *b_scale,
+                         int up_off, cudaStream_t s) {
+  using C = CfgF8<SWIGLU>;
+  CUtensorMap tmA, tmB;
+  if (!make_tmap_u8(&tmA, p.a, static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.rows_total),
+                    kBM))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_u8(&tmB, p.b, static_cast<uint64_t>(p.K),
+                    static_cast<uint64_t>(p.E) * static_cast<uint64_t>(p.b_rows), kF8BN / 2))
+    return cudaErrorInvalidValue;
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_fp8_kernel<SWIGLU>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  F8Args fa;
+  KArgs &a = fa.k;
+  a.E = p.E;
+  a.K = p.K;
+  a.n_tiles = p.n_out / C::BN_OUT;
+  a.layout = p.layout;
+  a.M_max = p.M_max;
+  a.b_rows = p.b_rows;
+  a.up_off = up_off;
+  a.seg = p.seg;
+  a.mtile_base = p.mtile_base;
+  a.out = p.out;
+  a.ldo = p.n_out;
+  a.rows_total = p.rows_total;
+  a.out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+  // A rows of one block: about 24 MB (a 128-row tile holds 128*K bytes)
+  a.m_block = static_cast<int>((24ll << 20) / (128ll * p.K));
+  if (a.m_block < 1) a.m_block = 1;
+  a.status = p.status;
+  a.wait_limit_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitLimitNs;
+  fa.a_scale = a_scale;
+  fa.b_scale = b_scale;
+  grouped_gemm_fp8_kernel<SWIGLU><<<num_sms(), kGemmThreads, C::SMEM_BYTES, s>>>(tmA, tmB, fa);
+  return cudaGetLastError();
 }
 
 template <int BN, bool SWIGLU>
@@ -919,6 +1246,20 @@ cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s) {
   if (p.n_out % 128 == 0) return run_gemm<128, false>(p, 0, s);
   if (p.n_out % 64 == 0) return run_gemm<64, false>(p, 0, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_fp8_gate_up_swiglu(const GemmProblem &p, const float *a_scale,
+                                           const float *b_scale, cudaStream_t s) {
+  // p.n_out = inter, p.b_rows = 2*inter, K = d; inter and d multiples of 128
+  if (p.n_out % 128 != 0 || p.K % kF8BK != 0) return cudaErrorInvalidValue;
+  return run_gemm_fp8<true>(p, a_scale, b_scale, p.n_out, s);
+}
+
+cudaError_t launch_gemm_fp8_down(const GemmProblem &p, const float *a_scale,
+                                 const float *b_scale, cudaStream_t s) {
+  // p.n_out = d, p.b_rows = d, K = inter
+  if (p.n_out % kF8BN != 0 || p.K % kF8BK != 0) return cudaErrorInvalidValue;
+  return run_gemm_fp8<false>(p, a_scale, b_scale, 0, s);
 }
 
 cudaError_t launch_wait_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t s) {

@@ -41,6 +41,13 @@ struct CapacityArgs {
   int32_t *kept;
   int32_t *ovf_offsets;
 };
+// x_perm-style gather of byte rows (row_bytes a multiple of 16) and,
+// optionally, of per-row fp32 scales: dst[p] = src[src_token[p]] for
+// p < min(n, *offsets_end)
+cudaError_t launch_gather_rows(const void *src, int row_bytes, const float *src_scale,
+                               int scales_per_row, const int32_t *src_token,
+                               const int32_t *offsets_end, int64_t n, int T, void *dst,
+                               float *dst_scale, cudaStream_t s);
 cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void *x, int d,
                             int32_t *counts, int32_t *offsets, int32_t *src_token,
                             int32_t *dest, void *x_perm, int32_t *chunk_scratch,
@@ -58,6 +65,13 @@ cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, i
 // this most tiles are such tails, and the single-CTA kernel already streams
 // the weights at HBM speed.
 constexpr int64_t kPairRowsPerExpert = 256;
+
+// quant.cu: e4m3 codes with fp32 scales, per (row, 128 columns) of [rows,
+// cols] bf16, or per 128 x 128 block of [mats, rows, cols] bf16
+cudaError_t launch_quantize_rows_fp8(const void *x, int64_t rows, int cols, void *q,
+                                     float *scales, cudaStream_t s);
+cudaError_t launch_quantize_blocks_fp8(const void *w, int mats, int rows, int cols, void *q,
+                                       float *scales, cudaStream_t s);
 
 // combine.cu
 // y[t] = sum_j w[t,j] * y_perm[dest[t*k+j]]; rows outside [0, y_rows) add nothing
@@ -84,6 +98,12 @@ struct GemmProblem {
 };
 cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s);
 cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s);
+// FP8 forms: p.a / p.b hold e4m3 codes; a_scale [rows_total, K/128] and
+// b_scale [E, b_rows/128, K/128] fp32 block scales
+cudaError_t launch_gemm_fp8_gate_up_swiglu(const GemmProblem &p, const float *a_scale,
+                                           const float *b_scale, cudaStream_t s);
+cudaError_t launch_gemm_fp8_down(const GemmProblem &p, const float *a_scale,
+                                 const float *b_scale, cudaStream_t s);
 // one CTA waits on an mbarrier nobody completes, bounded by limit_ns
 cudaError_t launch_wait_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t s);
 

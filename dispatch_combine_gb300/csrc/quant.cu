@@ -1,0 +1,120 @@
+// quant.cu -- FP8 (e4m3) quantization with block scales.
+//
+// The MoE path of "ep-deploy" (its cost model: "the dispatch sends FP8 with
+// scales", 7168 + 224 bytes per token) and the FP8 grouped GEMM of
+// "推理INFRA方法论-02-parallelism" ("DeepGEMM masked, FP8") use e4m3 values
+// with fp32 scales: one per (row, 128 columns) of an activation and one per
+// 128 x 128 block of a weight.  Here: s = amax / 448 (1 for an all-zero
+// block), q = e4m3(x / s) rounded to nearest even with saturation at 448,
+// both divisions in IEEE fp32, so the codes are reproducible bit for bit.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ float fp8_block_scale(float amax) {
+  return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+}
+
+// two fp32 -> two e4m3 codes (lo in bits 0-7), round to nearest even,
+// saturating to +-448
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// One warp per (row, 128-column block): 4 values per lane.
+__global__ void __launch_bounds__(256)
+    quantize_rows_kernel(const __nv_bfloat16 *__restrict__ x, int64_t rows, int cols,
+                         uint8_t *__restrict__ q, float *__restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int nb = cols / 128;
+  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= rows * nb) return;
+  const int64_t r = item / nb;
+  const int b = static_cast<int>(item - r * nb);
+  const size_t o = static_cast<size_t>(r) * cols + static_cast<size_t>(b) * 128 + lane * 4;
+  const uint2 raw = *reinterpret_cast<const uint2 *>(x + o);
+  const float v0 = bf16lo(raw.x), v1 = bf16hi(raw.x), v2 = bf16lo(raw.y), v3 = bf16hi(raw.y);
+  float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+  for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float s = fp8_block_scale(amax);
+  const uint32_t packed = static_cast<uint32_t>(e4m3x2(__fdiv_rn(v0, s), __fdiv_rn(v1, s))) |
+                          (static_cast<uint32_t>(e4m3x2(__fdiv_rn(v2, s), __fdiv_rn(v3, s))) << 16);
+  *reinterpret_cast<uint32_t *>(q + o) = packed;
+  if (lane == 0) scales[r * nb + b] = s;
+}
+
+// One CTA of 256 threads per 128 x 128 block: each thread 64 values.
+__global__ void __launch_bounds__(256)
+    quantize_blocks_kernel(const __nv_bfloat16 *__restrict__ w, int rows, int cols,
+                           uint8_t *__restrict__ q, float *__restrict__ scales) {
+  __shared__ float red[8];
+  const int rb = rows / 128, cb = cols / 128;
+  const int64_t blk = blockIdx.x;
+  const int64_t m = blk / (static_cast<int64_t>(rb) * cb);
+  const int i = static_cast<int>((blk / cb) % rb), j = static_cast<int>(blk % cb);
+  const __nv_bfloat16 *base = w + static_cast<size_t>(m) * rows * cols;
+  // thread t: row (t / 2) of the block, columns (t % 2) * 64 .. +63
+  const int br = threadIdx.x >> 1, bc = (threadIdx.x & 1) * 64;
+  const size_t o = static_cast<size_t>(i * 128 + br) * cols + j * 128 + bc;
+  uint4 raw[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) raw[u] = *reinterpret_cast<const uint4 *>(base + o + u * 8);
+  float amax = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(wv[t])), fabsf(bf16hi(wv[t]))));
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int t = 1; t < 8; ++t) amax = fmaxf(amax, red[t]);
+  const float s = fp8_block_scale(amax);
+  uint8_t *qo = q + static_cast<size_t>(m) * rows * cols + o;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+    uint32_t out[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t a = wv[2 * t], b = wv[2 * t + 1];
+      out[t] = static_cast<uint32_t>(e4m3x2(__fdiv_rn(bf16lo(a), s), __fdiv_rn(bf16hi(a), s))) |
+               (static_cast<uint32_t>(e4m3x2(__fdiv_rn(bf16lo(b), s), __fdiv_rn(bf16hi(b), s)))
+                << 16);
+    }
+    *reinterpret_cast<uint2 *>(qo + u * 8) = make_uint2(out[0], out[1]);
+  }
+  if (threadIdx.x == 0) scales[blk] = s;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_rows_fp8(const void *x, int64_t rows, int cols, void *q,
+                                     float *scales, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int64_t warps = rows * (cols / 128);
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  quantize_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16 *>(x), rows, cols, static_cast<uint8_t *>(q), scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_blocks_fp8(const void *w, int mats, int rows, int cols, void *q,
+                                       float *scales, cudaStream_t s) {
+  const int64_t blocks = static_cast<int64_t>(mats) * (rows / 128) * (cols / 128);
+  if (blocks == 0) return cudaSuccess;
+  quantize_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16 *>(w), rows, cols, static_cast<uint8_t *>(q), scales);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

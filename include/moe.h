@@ -298,6 +298,59 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
                                 moe_stream_t stream);
 
 /*
+ * FP8 quantization (e4m3 with fp32 block scales; the "ep-deploy" page's
+ * cost model dispatches FP8 with scales, 7168 + 224 bytes per token, and
+ * "推理INFRA方法论-02-parallelism" measures the FP8 grouped expert GEMM):
+ *   s = amax / 448 of the block (1 when the block is all zeros),
+ *   q = e4m3(x / s), IEEE fp32 division, round to nearest even, saturating
+ *   at 448.
+ * moe_quantize_fp8_rows: x [rows, cols] bf16 -> q [rows, cols] e4m3 codes,
+ *   scales [rows, cols/128] fp32 (one per row and 128 columns).
+ * moe_quantize_fp8_blocks: w [mats, rows, cols] bf16 -> q [mats, rows, cols],
+ *   scales [mats, rows/128, cols/128] (one per 128 x 128 block).
+ * rows (blocks: rows too) and cols must be multiples of 128 (rows of the
+ * row form: any); all pointers device, 16-byte aligned.
+ */
+moe_status_t moe_quantize_fp8_rows(const void *x, int64_t rows, int32_t cols, void *q,
+                                   float *scales, moe_stream_t stream);
+moe_status_t moe_quantize_fp8_blocks(const void *w, int32_t mats, int32_t rows, int32_t cols,
+                                     void *q, float *scales, moe_stream_t stream);
+
+/*
+ * FP8 expert FFN: moe_expert_ffn with e4m3 operands and block scales.
+ *   x_q [rows, d] e4m3 codes, x_scale [rows, d/128] fp32 (per row and 128
+ *   columns, as moe_quantize_fp8_rows); w_gate_up_q [E, 2*inter, d] and
+ *   w_down_q [E, d, inter] e4m3 codes with w_*_scale [E, rows/128, cols/128]
+ *   fp32 (per 128 x 128 block, as moe_quantize_fp8_blocks); seg, M_max and
+ *   the layouts as moe_expert_ffn; y_out [rows, d] fp32.
+ *   Each 128-column k-block is multiplied on the tensor core in fp32 and
+ *   added with its two scales; h = silu(g) * u is stored in bf16, quantized
+ *   per row and 128 columns, and multiplied by w_down the same way.
+ *   d and inter must be multiples of 128 (MOE_ERR_UNSUPPORTED otherwise).
+ */
+moe_status_t moe_expert_ffn_fp8_workspace_size(const moe_shape_t *shape, int32_t layout,
+                                               int32_t M_max, size_t *bytes);
+moe_status_t moe_expert_ffn_fp8(const moe_shape_t *shape, int32_t layout, const void *x_q,
+                                const float *x_scale, const int32_t *seg, int32_t M_max,
+                                const void *w_gate_up_q, const float *w_gate_up_scale,
+                                const void *w_down_q, const float *w_down_scale, float *y_out,
+                                void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * The layer with FP8 experts: route (from bf16 x, as moe_layer), quantize x
+ * per row and 128 columns, dispatch the FP8 rows with their scales (the
+ * "ep-deploy" page's FP8 dispatch: d + 4*d/128 bytes per row), the FP8
+ * expert FFN, and the combine (fp32, as moe_layer).  Weights as
+ * moe_expert_ffn_fp8; y [T,d] bf16; counts [E] optional.
+ */
+moe_status_t moe_layer_fp8_workspace_size(const moe_shape_t *shape, size_t *bytes);
+moe_status_t moe_layer_fp8(const moe_shape_t *shape, const void *x, const void *w_r,
+                           const float *bias, const void *w_gate_up_q,
+                           const float *w_gate_up_scale, const void *w_down_q,
+                           const float *w_down_scale, void *y, int32_t *counts, void *ws,
+                           size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Expert placement planner ("ep-deploy" handbook page, section "EPLB 与路由约束",
  * host code, no GPU): places num_experts logical experts, given their loads
  * (load [E] host doubles, >= 0), on num_gpus GPUs as num_physical physical

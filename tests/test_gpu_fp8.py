@@ -1,0 +1,147 @@
+"""FP8 path (e4m3 codes with fp32 block scales) against the oracle: the
+quantizers bit-exact, the FP8 expert FFN (contiguous and masked layouts,
+ragged tiles) and the FP8 layer within the stated tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import dispatch_combine_gb300 as moe
+import oracle
+from moe_inputs import CONFIGS, SCORE_SIGMOID_BIAS
+from tests.gpu_common import bf16_to_f64, bits, check_close, ensure_lib, host_bits, layer_inputs
+from tests.test_gpu_layer import oracle_routing
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand_bf16(shape, seed, scale_cols=None):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(*shape, generator=g)
+    if scale_cols is not None:
+        x = x * scale_cols
+    return x.to(torch.bfloat16)
+
+
+def test_quantize_rows_bit_exact():
+    ensure_lib()
+    mags = torch.tensor([1e-4, 1.0, 300.0, 1e3]).repeat_interleave(128)
+    x = _rand_bf16((333, 512), 1, mags)
+    x[7, 128:256] = 0                       # all-zero block: scale 1
+    x[9, 0] = 448.0                         # exact code boundaries
+    q, s = moe.moe_quantize_fp8_rows(x.cuda())
+    rq, rs = oracle.quantize_rows_fp8(bits(x))
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(s.cpu().numpy(), rs)
+
+
+def test_quantize_blocks_bit_exact():
+    ensure_lib()
+    w = _rand_bf16((3, 256, 384), 2) * 0.02
+    w[1, :128, 128:256] = 0
+    q, s = moe.moe_quantize_fp8_blocks(w.cuda())
+    rq, rs = oracle.quantize_blocks_fp8(bits(w))
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(s.cpu().numpy(), rs)
+
+
+def _weights_fp8(E, d, inter, seed):
+    w_gu = _rand_bf16((E, 2 * inter, d), seed) / d ** 0.5
+    w_dn = _rand_bf16((E, d, inter), seed + 1) / inter ** 0.5
+    gq, gs = moe.moe_quantize_fp8_blocks(w_gu.cuda())
+    dq, ds = moe.moe_quantize_fp8_blocks(w_dn.cuda())
+    rgq, rgs = oracle.quantize_blocks_fp8(bits(w_gu))
+    rdq, rds = oracle.quantize_blocks_fp8(bits(w_dn))
+    assert np.array_equal(gq.cpu().numpy(), rgq) and np.array_equal(dq.cpu().numpy(), rdq)
+    return (gq, gs, dq, ds), (rgq, rgs, rdq, rds)
+
+
+def _shape(E, d, inter, T):
+    return dict(T=T, d=d, E=E, G=1, topk_group=1, k=1, inter=inter, score=1, bias_scale=0.15)
+
+
+@pytest.mark.parametrize("counts,d,inter", [
+    ([0, 1, 127, 128, 129, 300], 256, 128),
+    ([5, 0, 260], 512, 256),
+    ([40, 300, 1], 384, 384),
+    ([3, 200], 4096, 1024),                 # long K in both GEMMs
+])
+def test_ffn_fp8_contiguous(counts, d, inter):
+    ensure_lib()
+    E = len(counts)
+    rows = sum(counts)
+    x = _rand_bf16((rows, d), d + inter)
+    (gq, gs, dq, ds), (rgq, rgs, rdq, rds) = _weights_fp8(E, d, inter, seed=d)
+    xq, xs = moe.moe_quantize_fp8_rows(x.cuda())
+    offsets = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32).cuda()
+    shape = _shape(E, d, inter, rows)
+    ws = moe.Workspace(moe.moe_expert_ffn_fp8_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    y = moe.moe_expert_ffn_fp8(shape, moe.MOE_LAYOUT_CONTIGUOUS, xq, xs, offsets, 0, gq, gs, dq,
+                               ds, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    rxq, rxs = oracle.quantize_rows_fp8(bits(x))
+    row_e = np.repeat(np.arange(E), counts).astype(np.int32)
+    ref = oracle.expert_ffn_rows_fp8(rxq, rxs, row_e, rgq, rgs, rdq, rds)
+    check_close(y.cpu().numpy(), ref, bf16_output=False, what="y (fp8)")
+
+
+def test_ffn_fp8_masked():
+    ensure_lib()
+    E, d, inter, M_max = 3, 256, 256, 256
+    masked_m = [0, 5, 256]
+    x = _rand_bf16((E, M_max, d), 11)
+    (gq, gs, dq, ds), (rgq, rgs, rdq, rds) = _weights_fp8(E, d, inter, seed=12)
+    xq, xs = moe.moe_quantize_fp8_rows(x.reshape(E * M_max, d).cuda())
+    shape = _shape(E, d, inter, 1)
+    ws = moe.Workspace(moe.moe_expert_ffn_fp8_workspace_size(shape, moe.MOE_LAYOUT_MASKED, M_max))
+    mm = torch.tensor(masked_m, dtype=torch.int32).cuda()
+    y = torch.full((E * M_max, d), float("nan"), dtype=torch.float32, device="cuda")
+    moe.moe_expert_ffn_fp8(shape, moe.MOE_LAYOUT_MASKED, xq, xs, mm, M_max, gq, gs, dq, ds, ws,
+                           y_out=y)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    rxq, rxs = oracle.quantize_rows_fp8(bits(x.reshape(E * M_max, d)))
+    yc = y.cpu().numpy()
+    for e, m in enumerate(masked_m):
+        if m == 0:
+            assert np.isnan(yc[e * M_max:(e + 1) * M_max]).all()
+            continue
+        rows = slice(e * M_max, e * M_max + m)
+        ref = oracle.expert_ffn_rows_fp8(rxq[rows], rxs[rows], np.full(m, e, np.int32), rgq, rgs,
+                                         rdq, rds)
+        check_close(yc[rows], ref, bf16_output=False, what=f"expert {e}")
+        assert np.isnan(yc[e * M_max + m:(e + 1) * M_max]).all()
+
+
+@pytest.mark.parametrize("name,n_samples", [("tiny", None), ("decode", 4), ("few_large", 3)])
+def test_layer_fp8_matches_oracle(name, n_samples):
+    ensure_lib()
+    cfg = CONFIGS[name]
+    t = layer_inputs(name)
+    gq, gs = moe.moe_quantize_fp8_blocks(t["w_gate_up"])
+    dq, ds = moe.moe_quantize_fp8_blocks(t["w_down"])
+    ws = moe.Workspace(moe.moe_layer_fp8_workspace_size(cfg.shape()))
+    bias = t["bias"] if cfg.score == SCORE_SIGMOID_BIAS else None
+    y = moe.moe_layer_fp8(cfg.shape(), t["x"], t["w_r"], bias, gq, gs, dq, ds, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    ids, w = oracle_routing(name)
+    if n_samples is None:
+        toks = np.arange(cfg.T)
+    else:
+        toks = np.sort(np.random.default_rng(2).choice(cfg.T, n_samples, replace=False))
+    experts = np.unique(ids[toks])
+    # the oracle quantizes what it needs itself: the sampled rows and the
+    # weights of the experts they reach
+    xq, xs = oracle.quantize_rows_fp8(host_bits(name, "x")[toks])
+    wgu, wdn = host_bits(name, "w_gate_up"), host_bits(name, "w_down")
+    rgq, rgs = oracle.quantize_blocks_fp8(np.ascontiguousarray(wgu[experts]))
+    rdq, rds = oracle.quantize_blocks_fp8(np.ascontiguousarray(wdn[experts]))
+    local = {int(e): i for i, e in enumerate(experts)}
+    rows_x = np.repeat(np.arange(toks.size), cfg.k)
+    row_e = np.array([local[int(e)] for e in ids[toks].ravel()], np.int32)
+    yr = oracle.expert_ffn_rows_fp8(xq[rows_x], xs[rows_x], row_e, rgq, rgs, rdq, rds)
+    ref = (yr.astype(np.float64).reshape(toks.size, cfg.k, cfg.d) *
+           w[toks].astype(np.float64)[:, :, None]).sum(1)
+    got = bf16_to_f64(y[torch.from_numpy(toks).cuda().long()])
+    check_close(got, ref, bf16_output=True, what=f"{name} fp8 layer")
