@@ -725,6 +725,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 constexpr int kF8BK = 128;  // e4m3 per k-block = bytes per swizzle row
 constexpr int kF8BN = 128;
 constexpr int kF8Stages = 6;
+constexpr int kF8Parts = 4;  // TMEM partial accumulators: the MMA runs up to 3 k-blocks ahead
 
 template <bool SWIGLU>
 struct CfgF8 {
@@ -733,9 +734,9 @@ struct CfgF8 {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = kF8Stages;
   static constexpr int BN_OUT = SWIGLU ? kF8BN / 2 : kF8BN;
-  static constexpr int TMEM_COLS = 2 * kF8BN;
+  static constexpr int TMEM_COLS = kF8Parts * kF8BN;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * kF8Parts + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int MT_OFF = MISC_OFF + 16;
   static constexpr int SMEM_BYTES = MT_OFF + (kMaxE + 1) * 4 + 1024;
@@ -748,9 +749,15 @@ struct F8Args {
   const float *b_scale;  // [E, b_rows/128, K/128]
 };
 
+// A tile of fewer than 128 rows loads only ceil(rows / 32) boxes of 32 rows;
+// the shared-memory rows past them are stale and only feed accumulator rows
+// that are never written.
+constexpr int kF8SubRows = 32;
+
 template <bool SWIGLU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmA32,
                             const __grid_constant__ CUtensorMap tmB, const F8Args fa) {
   using C = CfgF8<SWIGLU>;
   const KArgs &args = fa.k;
@@ -763,8 +770,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t *full = bars;
   uint64_t *empty = bars + C::STAGES;
   uint64_t *pfull = bars + 2 * C::STAGES;
-  uint64_t *pempty = pfull + 2;
-  uint64_t *drain = pfull + 4;
+  uint64_t *pempty = pfull + kF8Parts;
+  uint64_t *drain = pempty + kF8Parts;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
   int32_t *mt = reinterpret_cast<int32_t *>(smem + C::MT_OFF);
@@ -777,7 +784,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[st], 1);
       mbar_init(&empty[st], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kF8Parts; ++b) {
       mbar_init(&pfull[b], 1);
       mbar_init(&pempty[b], 4);
     }
@@ -801,6 +808,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmA32);
       tma_prefetch_desc(&tmB);
       int stage = 0;
       uint32_t phase = 0;
@@ -810,6 +818,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int st = 0; st < C::STAGES; ++st) issued[st] = false;
       for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x) {
         const Tile t = decode_tile(args, mt, u);
+        const int subs = (t.rows_valid + kF8SubRows - 1) / kF8SubRows;  // 1..4
+        const uint32_t tx = C::B_BYTES + (subs < kBM / kF8SubRows ? subs * kF8SubRows * kF8BK
+                                                                  : C::A_BYTES);
         int b0, b1;
         if (SWIGLU) {
           b0 = t.e * args.b_rows + t.n * C::BN_OUT;
@@ -824,8 +835,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           uint8_t *a_dst = smA + stage * C::A_BYTES;
           uint8_t *b_dst = smB + stage * C::B_BYTES;
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(a_dst, &tmA, &full[stage], kb * kF8BK, t.row0);
+          mbar_arrive_expect_tx(&full[stage], tx);
+          if (subs < kBM / kF8SubRows) {
+            for (int i = 0; i < subs; ++i)
+              tma_load_2d(a_dst + i * kF8SubRows * kF8BK, &tmA32, &full[stage], kb * kF8BK,
+                          t.row0 + i * kF8SubRows);
+          } else {
+            tma_load_2d(a_dst, &tmA, &full[stage], kb * kF8BK, t.row0);
+          }
           tma_load_2d(b_dst, &tmB, &full[stage], kb * kF8BK, b0);
           tma_load_2d(b_dst + (kF8BN / 2) * kF8BK, &tmB, &full[stage], kb * kF8BK, b1);
           issued[stage] = true;
@@ -846,13 +863,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       constexpr uint32_t kIdesc = mma_idesc_e4m3_f32(kBM, kF8BN);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t q = 0;  // k-blocks issued so far: partial q & 1, its use q >> 1
+      uint32_t q = 0;  // k-blocks issued so far: partial q % kF8Parts, its use q / kF8Parts
       bool any_mma = false;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok && !*abort_flag; u += gridDim.x) {
         for (int kb = 0; kb < kblocks; ++kb, ++q) {
-          const int p = static_cast<int>(q & 1u);
-          if (!mbar_wait_bounded(&pempty[p], ((q >> 1) & 1u) ^ 1u, abort_flag, args.status,
+          const int p = static_cast<int>(q % kF8Parts);
+          if (!mbar_wait_bounded(&pempty[p], ((q / kF8Parts) & 1u) ^ 1u, abort_flag, args.status,
                                  args.wait_limit_ns) ||
               !mbar_wait_bounded(&full[stage], phase, abort_flag, args.status,
                                  args.wait_limit_ns)) {
@@ -905,27 +922,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
       for (int c = 0; c < kF8BN; ++c) acc[c] = 0.0f;
       float sa = rok ? __ldg(as) : 0.0f;
+      // a warp whose 32 rows are all past the tile's rows only keeps the
+      // partial ring moving
+      const bool warp_rows = quad * 32 < t.rows_valid;
       for (int kb = 0; kb < kblocks; ++kb, ++q) {
-        const int p = static_cast<int>(q & 1u);
+        const int p = static_cast<int>(q % kF8Parts);
         const float s0 = sa * __ldg(bs0 + kb), s1 = sa * __ldg(bs1 + kb);
         sa = (rok && kb + 1 < kblocks) ? __ldg(as + kb + 1) : 0.0f;
-        const bool waited = mbar_wait_bounded(&pfull[p], (q >> 1) & 1u, abort_flag, args.status,
-                                              args.wait_limit_ns);
+        const bool waited = mbar_wait_bounded(&pfull[p], (q / kF8Parts) & 1u, abort_flag,
+                                              args.status, args.wait_limit_ns);
         if (!__all_sync(0xffffffffu, waited)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t tp = tmem_base + lane_off + static_cast<uint32_t>(p * kF8BN);
+        if (warp_rows) {
 #pragma unroll
-        for (int c = 0; c < kF8BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tp + c * 32, v);
-          tmem_ld_wait();
-          tmem_regs_fence(v);
-          const float sc = (c < kF8BN / 64) ? s0 : s1;
+          for (int c = 0; c < kF8BN / 64; ++c) {
+            // two 32-column loads per wait
+            uint32_t v[32], w[32];
+            tmem_ld_32x32b_x32(tp + c * 64, v);
+            tmem_ld_32x32b_x32(tp + c * 64 + 32, w);
+            tmem_ld_wait();
+            tmem_regs_fence(v);
+            tmem_regs_fence(w);
+            const float sc = (c < kF8BN / 128) ? s0 : s1;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(__uint_as_float(v[j]), sc, acc[c * 32 + j]);
+            for (int j = 0; j < 32; ++j) {
+              acc[c * 64 + j] = fmaf(__uint_as_float(v[j]), sc, acc[c * 64 + j]);
+              acc[c * 64 + 32 + j] = fmaf(__uint_as_float(w[j]), sc, acc[c * 64 + 32 + j]);
+            }
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -1065,16 +1093,18 @@ bool make_tmap_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t r
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool SWIGLU>
 cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float *b_scale,
                          int up_off, cudaStream_t s) {
   using C = CfgF8<SWIGLU>;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmA32, tmB;
   if (!make_tmap_u8(&tmA, p.a, static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.rows_total),
-                    kBM))
+                    kBM) ||
+      !make_tmap_u8(&tmA32, p.a, static_cast<uint64_t>(p.K),
+                    static_cast<uint64_t>(p.rows_total), kF8SubRows))
     return cudaErrorInvalidValue;
   if (!make_tmap_u8(&tmB, p.b, static_cast<uint64_t>(p.K),
                     static_cast<uint64_t>(p.E) * static_cast<uint64_t>(p.b_rows), kF8BN / 2))
@@ -1105,7 +1135,8 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   a.wait_limit_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitLimitNs;
   fa.a_scale = a_scale;
   fa.b_scale = b_scale;
-  grouped_gemm_fp8_kernel<SWIGLU><<<num_sms(), kGemmThreads, C::SMEM_BYTES, s>>>(tmA, tmB, fa);
+  grouped_gemm_fp8_kernel<SWIGLU><<<num_sms(), kGemmThreads, C::SMEM_BYTES, s>>>(tmA, tmA32,
+                                                                                tmB, fa);
   return cudaGetLastError();
 }
 
