@@ -763,9 +763,9 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
 
 int32_t moe_layer_launch_count(const moe_shape_t *shape) {
   if (check_shape(shape) != MOE_OK || shape->T == 0) return 0;
-  // router widen, logits, select, count, scan, scatter, gather, gate_up, down,
-  // combine
-  return 10;
+  // router logits (1 or 2), select, count, scan, scatter, gather, gate_up,
+  // down, combine
+  return moe::router_logits_launches(shape->d, shape->E) + 8;
 }
 
 moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, uint64_t limit_ns,

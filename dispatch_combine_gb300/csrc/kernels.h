@@ -13,6 +13,8 @@ namespace moe {
 // w_scratch: router_scratch_bytes(d, E) bytes of workspace (a zero-padded
 // copy of w_r made by the first of the two kernels launched here)
 size_t router_scratch_bytes(int d, int E);
+// kernels launch_router_logits launches (1: weights resident; 2: padded copy + tiled)
+int router_logits_launches(int d, int E);
 cudaError_t launch_router_logits(const void *x, const void *w_r, int T, int d, int E,
                                  float *logits, void *w_scratch, cudaStream_t s);
 // mode 0: scores from logits (score kind); mode 1: the input already holds

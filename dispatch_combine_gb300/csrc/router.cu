@@ -714,11 +714,18 @@ size_t router_scratch_bytes(int d, int E) {
   return static_cast<size_t>(router_d_pad(d)) * router_e_pad(E) * sizeof(uint16_t);
 }
 
+// W_r resident in shared memory when it fits
+constexpr size_t kSmallSmemMax = 200 * 1024;
+bool router_resident(int d, int E) {
+  return (E <= 8 && router_small_smem(d, 8) <= kSmallSmemMax) ||
+         (E <= 16 && router_small_smem(d, 16) <= kSmallSmemMax);
+}
+
+int router_logits_launches(int d, int E) { return router_resident(d, E) ? 1 : 2; }
+
 cudaError_t launch_router_logits(const void *x, const void *w_r, int T, int d, int E,
                                  float *logits, void *w_scratch, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  // W_r resident in shared memory when it fits
-  constexpr size_t kSmallSmemMax = 200 * 1024;
   if (E <= 8 && router_small_smem(d, 8) <= kSmallSmemMax)
     return run_logits_small<8>(x, w_r, T, d, E, logits, s);
   if (E <= 16 && router_small_smem(d, 16) <= kSmallSmemMax)
