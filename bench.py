@@ -41,6 +41,9 @@ UNIT = "tokens/s"
 DEFAULT_CONFIG = "few_large"
 L2_BYTES = 126 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# fp32 FMA peak from the unit counts: 152 SMs x 128 fp32 lanes x 2 FLOP per
+# fused multiply-add x 2.07 GHz (the maximum SM clock)
+FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 # --------------------------------------------------------------------------
@@ -401,6 +404,15 @@ def run_gpu(args, c):
         sec = stage_ms[n] / 1000.0
         stages[n] = {"us": stage_ms[n] * 1000.0, "bound": "hbm", "bytes": sb[n],
                      "achieved_gbs": sb[n] / sec / 1e9, "frac": sb[n] / hbm / sec}
+    # the router logits are fp32 multiply-adds on CUDA cores (fixed order):
+    # at large T they bound the stage, not its bytes
+    r_flops = 2.0 * c.T * c.d * c.E
+    if r_flops / (FP32_TFLOPS * 1e12) > sb["router"] / hbm:
+        sec = stage_ms["router"] / 1000.0
+        stages["router"].update({"bound": "alu", "flops": r_flops,
+                                 "achieved_tflops": r_flops / sec / 1e12,
+                                 "peak_tflops_fp32": FP32_TFLOPS,
+                                 "frac": r_flops / sec / (FP32_TFLOPS * 1e12)})
     for n in ("gate_up", "down"):
         sec = stage_ms[n] / 1000.0
         t_hbm, t_tc = fw[n]["bytes"] / hbm, fw[n]["flops"] / tensor

@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(NT, 1)
 // the 32 lanes, which read rows 8 apart, hit distinct banks.
 // ---------------------------------------------------------------------------
 constexpr int kSmallWarps = 8;
-constexpr int kSmallTT = 2;  // tokens per warp
+constexpr int kSmallTT = 1;  // tokens per warp
 constexpr int kSmallPF = 4;  // rounds of x in flight per lane
 
 template <int EP>
@@ -313,15 +313,19 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
   const int chunks = (d + 255) / 256 * 32;
   // stage W_r: chunk c, row j -> wsm + c * CHUNKB + j * ROWB; zeros for
   // experts >= E and inputs >= d
-  // one thread per row of 8 experts: a 16-byte load when the row is aligned
+  // one thread per row of 8 experts: aligned full rows are copied
+  // asynchronously (all in flight at once), the others through registers
   const bool vec = (E % 8) == 0;
   for (int q = threadIdx.x; q < chunks * 8 * (EP / 8); q += blockDim.x) {
     const int i = q / (EP / 8), e8 = (q % (EP / 8)) * 8;
+    uint8_t *dst = wsm + (i >> 3) * C::CHUNKB + (i & 7) * C::ROWB + e8 * 2;
+    if (i < d && vec && e8 + 8 <= E) {
+      cp_async_16(dst, w_r + (size_t)i * E + e8);
+      continue;
+    }
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (i < d) {
-      if (vec && e8 + 8 <= E) {
-        v = __ldg(reinterpret_cast<const uint4 *>(w_r + (size_t)i * E + e8));
-      } else {
+      {
         uint16_t h[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) h[u] = (e8 + u < E) ? w_r[(size_t)i * E + e8 + u] : 0;
@@ -329,8 +333,10 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
                        h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
       }
     }
-    *reinterpret_cast<uint4 *>(wsm + (i >> 3) * C::CHUNKB + (i & 7) * C::ROWB + e8 * 2) = v;
+    *reinterpret_cast<uint4 *>(dst) = v;
   }
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncthreads();
   const int rounds = (d + 255) / 256;
   const int groups = (T + kSmallTT - 1) / kSmallTT;
