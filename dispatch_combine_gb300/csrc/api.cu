@@ -133,13 +133,19 @@ moe_status_t ffn_rows(const moe_shape_t *s, int32_t layout, int32_t M_max, int64
 
 // gate_up + SwiGLU (and optionally down) over `rows` rows with mtile_base
 // already computed in the workspace.
-// Pair (2-CTA, 256-row) tiles for the contiguous layout when experts
-// average at least kPairRowsPerExpert rows.
-bool use_pair(const moe_shape_t *s, int32_t layout) {
-  return layout == MOE_LAYOUT_CONTIGUOUS && s->inter % 128 == 0 && s->d % 256 == 0 &&
-         static_cast<int64_t>(s->T) * s->k >= moe::kPairRowsPerExpert * s->E;
+// Pair (2-CTA, 256-row) tiles when the T*k routed rows average at least
+// kPairRowsPerExpert per expert; for the masked layout the slabs must also
+// hold that many rows (M_max >= kPairRowsPerExpert).
+bool use_pair(const moe_shape_t *s, int32_t layout, int32_t M_max) {
+  if (s->inter % 128 != 0 || s->d % 256 != 0) return false;
+  if (static_cast<int64_t>(s->T) * s->k < static_cast<int64_t>(moe::kPairRowsPerExpert) * s->E)
+    return false;
+  if (layout == MOE_LAYOUT_CONTIGUOUS) return true;
+  return layout == MOE_LAYOUT_MASKED && M_max >= moe::kPairRowsPerExpert;
 }
-int tile_rows_for(const moe_shape_t *s, int32_t layout) { return use_pair(s, layout) ? 256 : 128; }
+int tile_rows_for(const moe_shape_t *s, int32_t layout, int32_t M_max) {
+  return use_pair(s, layout, M_max) ? 256 : 128;
+}
 
 moe_status_t run_gate_up(const moe_shape_t *s, int32_t layout, const void *x_in,
                          const int32_t *seg, int32_t M_max, int64_t rows, const int32_t *mtile,
@@ -159,7 +165,7 @@ moe_status_t run_gate_up(const moe_shape_t *s, int32_t layout, const void *x_in,
   p.b_rows = 2 * s->inter;
   p.out = h;
   p.status = status;
-  p.pair = use_pair(s, layout);
+  p.pair = use_pair(s, layout, M_max);
   return cuda_status(moe::launch_gemm_gate_up_swiglu(p, st));
 }
 
@@ -181,7 +187,7 @@ moe_status_t run_down(const moe_shape_t *s, int32_t layout, const void *h, const
   p.b_rows = s->d;
   p.out = y;
   p.status = status;
-  p.pair = use_pair(s, layout);
+  p.pair = use_pair(s, layout, M_max);
   return cuda_status(moe::launch_gemm_down(p, st));
 }
 
@@ -332,7 +338,7 @@ moe_status_t moe_expert_ffn(const moe_shape_t *shape, int32_t layout, const void
   int32_t *mtile = at<int32_t>(ws, L.mtile);
   void *h = at<void>(ws, L.h);
   MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max,
-                                            use_pair(shape, layout) ? 256 : 128, mtile, status,
+                                            tile_rows_for(shape, layout, M_max), mtile, status,
                                             stream)));
   MOE_TRY(run_gate_up(shape, layout, x_in, seg, M_max, rows, mtile, w_gate_up, h, status,
                       stream));
@@ -352,7 +358,7 @@ moe_status_t moe_expert_gate_up(const moe_shape_t *shape, int32_t layout, const 
   uint32_t *status = at<uint32_t>(ws, L.status);
   int32_t *mtile = at<int32_t>(ws, L.mtile);
   MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max,
-                                            use_pair(shape, layout) ? 256 : 128, mtile, status,
+                                            tile_rows_for(shape, layout, M_max), mtile, status,
                                             stream)));
   return run_gate_up(shape, layout, x_in, seg, M_max, rows, mtile, w_gate_up, h_out, status,
                      stream);
@@ -371,7 +377,7 @@ moe_status_t moe_expert_down(const moe_shape_t *shape, int32_t layout, const voi
   uint32_t *status = at<uint32_t>(ws, L.status);
   int32_t *mtile = at<int32_t>(ws, L.mtile);
   MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max,
-                                            use_pair(shape, layout) ? 256 : 128, mtile, status,
+                                            tile_rows_for(shape, layout, M_max), mtile, status,
                                             stream)));
   return run_down(shape, layout, h_in, seg, M_max, rows, mtile, w_down, y_out, status, stream);
 }
@@ -428,7 +434,7 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
   MOE_TRY(mark(1));
   MOE_TRY(cuda_status(moe::launch_dispatch(ids, s.T, s.k, s.E, x, s.d, cnt, offsets, src, dest,
                                            x_perm, at<int32_t>(ws, L.chunk), mtile,
-                                           use_pair(shape, MOE_LAYOUT_CONTIGUOUS) ? 256 : 128,
+                                           tile_rows_for(shape, MOE_LAYOUT_CONTIGUOUS, 0),
                                            status, stream)));
   MOE_TRY(mark(2));
   MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_perm, offsets, 0, n, mtile, w_gate_up, h,
@@ -741,8 +747,9 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
                                            128, status, stream, cap)));
   // first round: the padded rows, masked layout with M_max = C
   if (capacity > 0) {
-    MOE_TRY(cuda_status(moe::launch_ffn_tiles(kp, MOE_LAYOUT_MASKED, s.E, capacity, 128, mtile,
-                                              status, stream)));
+    MOE_TRY(cuda_status(moe::launch_ffn_tiles(kp, MOE_LAYOUT_MASKED, s.E, capacity,
+                                              tile_rows_for(shape, MOE_LAYOUT_MASKED, capacity),
+                                              mtile, status, stream)));
     MOE_TRY(run_gate_up(shape, MOE_LAYOUT_MASKED, x_rows, kp, capacity, pad, mtile, w_gate_up,
                         h, status, stream));
     MOE_TRY(run_down(shape, MOE_LAYOUT_MASKED, h, kp, capacity, pad, mtile, w_down, y_rows,
@@ -751,7 +758,7 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
   // second round: the overflow rows, contiguous with offsets ovf_offsets
   if (overflow == MOE_OVERFLOW_SECOND_ROUND) {
     MOE_TRY(cuda_status(moe::launch_ffn_tiles(ovf, MOE_LAYOUT_CONTIGUOUS, s.E, 0,
-                                              tile_rows_for(shape, MOE_LAYOUT_CONTIGUOUS), mtile,
+                                              tile_rows_for(shape, MOE_LAYOUT_CONTIGUOUS, 0), mtile,
                                               status, stream)));
     MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_rows + pad * s.d * 2, ovf, 0, n, mtile,
                         w_gate_up, h, status, stream));

@@ -121,17 +121,20 @@ def test_gate_up_alone_matches_oracle_h(counts):
     assert np.abs(y.cpu().numpy() - ref_y).max() < 1e-3
 
 
-@pytest.mark.parametrize("masked_m,M_max,d,inter", [
-    ([0, 5, 256, 130], 256, 256, 128),
-    ([64, 1, 128], 128, 512, 64),
+@pytest.mark.parametrize("masked_m,M_max,d,inter,T", [
+    ([0, 5, 256, 130], 256, 256, 128, 1),
+    ([64, 1, 128], 128, 512, 64, 1),
+    # CTA-pair tiles (T*k >= 256 rows per expert, M_max >= 256): full 256-row
+    # tiles, a 44-row swapped tail, a 5-row swapped expert, a 200-row plain tail
+    ([0, 5, 300, 512, 456], 512, 256, 128, 1280),
 ])
-def test_ffn_masked(masked_m, M_max, d, inter):
+def test_ffn_masked(masked_m, M_max, d, inter, T):
     ensure_lib()
     E = len(masked_m)
     w_gu, w_down = _weights(E, d, inter, seed=9)
     g = torch.Generator().manual_seed(10)
     x = torch.randn(E, M_max, d, generator=g).to(torch.bfloat16)
-    shape = _shape(E, d, inter)
+    shape = _shape(E, d, inter, T=T)
     ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_MASKED, M_max))
     y = torch.full((E, M_max, d), float("nan"), dtype=torch.float32, device="cuda")
     mm = torch.tensor(masked_m, dtype=torch.int32)
