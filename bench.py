@@ -387,6 +387,7 @@ def run_gpu(args, c):
             stage_ms[n] += row[i].elapsed_time(row[i + 1])
     stage_ms = {n: v / K for n, v in stage_ms.items()}
 
+    n_flagged = moe.moe_route_screened_count(shape, ws)
     cnt = counts.cpu()
     n_touched = int((cnt > 0).sum())
     mean = float(cnt.float().mean())
@@ -404,10 +405,17 @@ def run_gpu(args, c):
         sec = stage_ms[n] / 1000.0
         stages[n] = {"us": stage_ms[n] * 1000.0, "bound": "hbm", "bytes": sb[n],
                      "achieved_gbs": sb[n] / sec / 1e9, "frac": sb[n] / hbm / sec}
-    # the router logits are fp32 multiply-adds on CUDA cores (fixed order):
-    # at large T they bound the stage, not its bytes
+    # screened router: tensor-core logits, then the fixed-order logits of the
+    # k selected experts per token (their weight rows come from L2) and all
+    # E for the flagged tokens; its HBM bytes stay those of the stage
     r_flops = 2.0 * c.T * c.d * c.E
-    if r_flops / (FP32_TFLOPS * 1e12) > sb["router"] / hbm:
+    if n_flagged >= 0:
+        stages["router"].update({"screened": True, "flagged_tokens": n_flagged,
+                                 "tc_flops": r_flops,
+                                 "refine_l2_bytes": c.T * c.k * c.d * 2 + n_flagged * c.E * c.d * 2})
+    # otherwise the logits are fp32 multiply-adds on CUDA cores (fixed order):
+    # at large T they bound the stage, not its bytes
+    elif r_flops / (FP32_TFLOPS * 1e12) > sb["router"] / hbm:
         sec = stage_ms["router"] / 1000.0
         stages["router"].update({"bound": "alu", "flops": r_flops,
                                  "achieved_tflops": r_flops / sec / 1e12,

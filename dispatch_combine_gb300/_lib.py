@@ -80,6 +80,7 @@ SIGNATURES = {
     "moe_combine": (_I32, [_PS, _P, _P, _P, _P, _P]),
     "moe_layer": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_layer_launch_count": (_I32, [_PS]),
+    "moe_route_screened_count": (_I32, [_PS, _P, _SZ, _P, _P]),
     "moe_selftest_wait_timeout": (_I32, [_P, _SZ, _U64, _P]),
 }
 
@@ -212,6 +213,16 @@ def moe_status_string(status: int) -> str:
 
 def moe_layer_launch_count(shape) -> int:
     return int(lib().moe_layer_launch_count(ctypes.byref(as_shape(shape))))
+
+
+def moe_route_screened_count(shape, ws: Workspace, stream=None) -> int:
+    """Tokens the last screened routing in ws sent to the full fixed-order
+    path (-1: the shape is not screened).  Synchronises the stream."""
+    out = torch.empty(1, dtype=torch.int32, device="cuda")
+    _check("moe_route_screened_count",
+           lib().moe_route_screened_count(ctypes.byref(as_shape(shape)), ws.c_ptr, ws.nbytes,
+                                          _ptr(out), _stream(stream)))
+    return int(out.item())
 
 
 # --------------------------------------------------------------------------

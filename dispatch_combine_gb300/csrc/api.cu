@@ -51,7 +51,7 @@ Layout make_layout(const moe_shape_t &s, int64_t h_rows, int64_t perm_rows = -1)
   L.logits = off;
   off = align_up(off + 4 * static_cast<size_t>(s.T) * s.E);
   L.wr32 = off;
-  off = align_up(off + moe::router_scratch_bytes(s.d, s.E));
+  off = align_up(off + moe::router_scratch_bytes(s.T, s.d, s.E));
   L.end_route = off;
   L.h = off;
   off = align_up(off + 2 * static_cast<size_t>(h_rows) * s.inter);
@@ -262,10 +262,14 @@ moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *w_r,
   if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
   const Layout L = make_layout(s, 0);
   MOE_TRY(check_ws(ws, ws_bytes, L.end_route));
-  float *lg = logits ? logits : at<float>(ws, L.logits);
+  if (!logits)
+    return cuda_status(moe::launch_router(x, w_r, bias, s.T, s.d, s.E, s.G, s.topk_group, s.k,
+                                          s.score, s.bias_scale, at<float>(ws, L.logits),
+                                          topk_ids, topk_w, at<void>(ws, L.wr32),
+                                          at<uint32_t>(ws, L.status), stream));
   MOE_TRY(cuda_status(
-      moe::launch_router_logits(x, w_r, s.T, s.d, s.E, lg, at<void>(ws, L.wr32), stream)));
-  return cuda_status(moe::launch_router_select(lg, bias, s.T, s.E, s.G, s.topk_group, s.k,
+      moe::launch_router_logits(x, w_r, s.T, s.d, s.E, logits, at<void>(ws, L.wr32), stream)));
+  return cuda_status(moe::launch_router_select(logits, bias, s.T, s.E, s.G, s.topk_group, s.k,
                                                s.score, s.bias_scale, 0, topk_ids, topk_w,
                                                stream));
 }
@@ -427,10 +431,9 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
     return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), stream));
   };
   MOE_TRY(mark(0));
-  MOE_TRY(cuda_status(
-      moe::launch_router_logits(x, w_r, s.T, s.d, s.E, logits, at<void>(ws, L.wr32), stream)));
-  MOE_TRY(cuda_status(moe::launch_router_select(logits, bias, s.T, s.E, s.G, s.topk_group, s.k,
-                                                s.score, s.bias_scale, 0, ids, w, stream)));
+  MOE_TRY(cuda_status(moe::launch_router(x, w_r, bias, s.T, s.d, s.E, s.G, s.topk_group, s.k,
+                                         s.score, s.bias_scale, logits, ids, w,
+                                         at<void>(ws, L.wr32), status, stream)));
   MOE_TRY(mark(1));
   MOE_TRY(cuda_status(moe::launch_dispatch(ids, s.T, s.k, s.E, x, s.d, cnt, offsets, src, dest,
                                            x_perm, at<int32_t>(ws, L.chunk), mtile,
@@ -497,7 +500,7 @@ LayoutF8 make_fp8_layout(const moe_shape_t &s, int64_t rows) {
   L.end_ffn = off;
   L.chunk = take(4 * static_cast<size_t>(moe::dispatch_num_chunks(n)) * s.E);
   L.logits = take(4 * static_cast<size_t>(s.T) * s.E);
-  L.wr32 = take(moe::router_scratch_bytes(s.d, s.E));
+  L.wr32 = take(moe::router_scratch_bytes(s.T, s.d, s.E));
   L.ids = take(4 * static_cast<size_t>(n));
   L.w = take(4 * static_cast<size_t>(n));
   L.counts = take(4 * static_cast<size_t>(s.E));
@@ -622,11 +625,9 @@ moe_status_t moe_layer_fp8(const moe_shape_t *shape, const void *x, const void *
   int32_t *dest = at<int32_t>(ws, L.dest);
   int32_t *src = at<int32_t>(ws, L.src);
   float *y_perm = at<float>(ws, L.y_perm);
-  MOE_TRY(cuda_status(moe::launch_router_logits(x, w_r, s.T, s.d, s.E, at<float>(ws, L.logits),
-                                                at<void>(ws, L.wr32), stream)));
-  MOE_TRY(cuda_status(moe::launch_router_select(at<float>(ws, L.logits), bias, s.T, s.E, s.G,
-                                                s.topk_group, s.k, s.score, s.bias_scale, 0,
-                                                ids, w, stream)));
+  MOE_TRY(cuda_status(moe::launch_router(x, w_r, bias, s.T, s.d, s.E, s.G, s.topk_group, s.k,
+                                         s.score, s.bias_scale, at<float>(ws, L.logits), ids, w,
+                                         at<void>(ws, L.wr32), status, stream)));
   // the dispatch moves FP8 rows and their scales
   MOE_TRY(cuda_status(moe::launch_quantize_rows_fp8(x, s.T, s.d, at<void>(ws, L.xq),
                                                     at<float>(ws, L.xs), stream)));
@@ -736,10 +737,9 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
   uint8_t *h = at<uint8_t>(ws, L.h);
   float *logits = at<float>(ws, L.logits);
 
-  MOE_TRY(cuda_status(
-      moe::launch_router_logits(x, w_r, s.T, s.d, s.E, logits, at<void>(ws, L.wr32), stream)));
-  MOE_TRY(cuda_status(moe::launch_router_select(logits, bias, s.T, s.E, s.G, s.topk_group, s.k,
-                                                s.score, s.bias_scale, 0, ids, w, stream)));
+  MOE_TRY(cuda_status(moe::launch_router(x, w_r, bias, s.T, s.d, s.E, s.G, s.topk_group, s.k,
+                                         s.score, s.bias_scale, logits, ids, w,
+                                         at<void>(ws, L.wr32), status, stream)));
   moe::CapacityArgs cap{capacity, overflow, s.E, kp, ovf};
   MOE_TRY(cuda_status(moe::launch_dispatch(ids, s.T, s.k, s.E, x, s.d, cnt,
                                            at<int32_t>(ws, L.doff), at<int32_t>(ws, L.src),
@@ -770,9 +770,23 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
 
 int32_t moe_layer_launch_count(const moe_shape_t *shape) {
   if (check_shape(shape) != MOE_OK || shape->T == 0) return 0;
-  // router logits (1 or 2), select, count, scan, scatter, gather, gate_up,
-  // down, combine
-  return moe::router_logits_launches(shape->d, shape->E) + 8;
+  // router (screened: 5; else logits 1 or 2 + select), count, scan,
+  // scatter, gather, gate_up, down, combine
+  return moe::router_launches(shape->T, shape->d, shape->E, shape->G, shape->k) + 7;
+}
+
+moe_status_t moe_route_screened_count(const moe_shape_t *shape, const void *ws, size_t ws_bytes,
+                                      int32_t *count, moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  if (!count) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*shape, 0);
+  MOE_TRY(check_ws(const_cast<void *>(ws), ws_bytes, L.end_route));
+  const int32_t *src = moe::router_flagged_count(at<void>(const_cast<void *>(ws), L.wr32),
+                                                 shape->T, shape->d, shape->E, shape->G,
+                                                 shape->k);
+  if (!src) return cuda_status(cudaMemsetAsync(count, 0xff, sizeof(int32_t), stream));
+  return cuda_status(cudaMemcpyAsync(count, src, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                                     stream));
 }
 
 moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, uint64_t limit_ns,

@@ -66,6 +66,7 @@ struct Tile {
 
 struct KArgs {
   int E, K, n_tiles, layout, M_max, b_rows, up_off;
+  int ksplit;   // 1-CTA down form: K pieces per tile, summed into a zeroed out (1: none)
   int m_block;  // m-tiles per rasterization block (A rows of a block stay in L2)
   int out_v8;   // output base 32-byte aligned: 32-byte stores
   int64_t rows_total;
@@ -163,7 +164,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
-  const int total = mt[args.E] * args.n_tiles;
+  const int ksplit = SWIGLU ? 1 : args.ksplit;
+  const int total = mt[args.E] * args.n_tiles * ksplit;
   if (static_cast<int>(blockIdx.x) >= total) return;  // uniform across the CTA
 
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -172,6 +174,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int kblocks = args.K / kBK;
+  // k-blocks [kb_lo, kb_hi) of piece u % ksplit
+  auto kb_lo = [&](int u) { return (u % ksplit) * kblocks / ksplit; };
+  auto kb_hi = [&](int u) { return (u % ksplit + 1) * kblocks / ksplit; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -185,7 +190,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) issued[s] = false;
       for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x) {
-        const Tile t = decode_tile(args, mt, u);
+        const Tile t = decode_tile(args, mt, u / ksplit);
         int b0, b1;
         if (SWIGLU) {
           b0 = t.e * args.b_rows + t.n * C::HALF;
@@ -194,7 +199,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           b0 = t.e * args.b_rows + t.n * BN;
           b1 = b0 + C::HALF;
         }
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb_lo(u); kb < kb_hi(u); ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
                                  args.wait_limit_ns))
             break;
@@ -233,7 +238,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const int kb0 = kb_lo(u);
+        for (int kb = kb0; kb < kb_hi(u); ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.status,
                                  args.wait_limit_ns)) {
             ok = false;
@@ -245,7 +251,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // +32 bytes along K inside the 128-byte swizzle row
-            mma_bf16_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            mma_bf16_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, kIdesc,
+                        (kb != kb0 || kk != 0) ? 1u : 0u);
           }
           any_mma = true;
           mma_commit(&empty[stage]);
@@ -272,7 +279,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Tile t = decode_tile(args, mt, u);
+      const Tile t = decode_tile(args, mt, u / ksplit);
       const bool waited = mbar_wait_bounded(&tmem_full[acc], acc_phase, abort_flag,
                                             args.status, args.wait_limit_ns);
       // the tcgen05.ld below is warp-collective: leave together if any lane gave up
@@ -331,7 +338,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld_32x32b_x32(tb + c * 32, v);
           tmem_ld_wait();
           tmem_regs_fence(v);
-          if (ok) {
+          if (ok && ksplit > 1) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              red_add_v4(dst + c * 32 + 4 * i, __uint_as_float(v[4 * i]),
+                         __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                         __uint_as_float(v[4 * i + 3]));
+          } else if (ok) {
             if (args.out_v8) {
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
@@ -1133,6 +1146,7 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   if (a.m_block < 1) a.m_block = 1;
   a.status = p.status;
   a.wait_limit_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitLimitNs;
+  a.ksplit = 1;
   fa.a_scale = a_scale;
   fa.b_scale = b_scale;
   grouped_gemm_fp8_kernel<SWIGLU><<<num_sms(), kGemmThreads, C::SMEM_BYTES, s>>>(tmA, tmA32,
@@ -1173,6 +1187,7 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
   if (a.m_block < 1) a.m_block = 1;
   a.status = p.status;
   a.wait_limit_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitLimitNs;
+  a.ksplit = (!SWIGLU && p.ksplit > 1) ? p.ksplit : 1;
   grouped_gemm_kernel<BN, SWIGLU><<<num_sms(), kGemmThreads, C::SMEM_BYTES, s>>>(tmA, tmB, a);
   return cudaGetLastError();
 }
@@ -1219,6 +1234,7 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   if (a.m_block < 1) a.m_block = 1;
   a.status = p.status;
   a.wait_limit_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitLimitNs;
+  a.ksplit = 1;
   // persistent grid: as many CTA pairs as can be resident at once
   int clusters = 0;
   {
@@ -1271,6 +1287,13 @@ cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s) {
   // p.n_out = d, p.b_rows = d, K = inter
   if (p.pair) {
     if (p.n_out % 256 == 0) return run_gemm_pair<256, false>(p, 0, s);
+    return cudaErrorInvalidValue;
+  }
+  if (p.bn != 0) {
+    if (p.n_out % p.bn != 0) return cudaErrorInvalidValue;
+    if (p.bn == 256) return run_gemm<256, false>(p, 0, s);
+    if (p.bn == 128) return run_gemm<128, false>(p, 0, s);
+    if (p.bn == 64) return run_gemm<64, false>(p, 0, s);
     return cudaErrorInvalidValue;
   }
   if (p.n_out % 256 == 0) return run_gemm<256, false>(p, 0, s);

@@ -10,9 +10,10 @@
 namespace moe {
 
 // router.cu
-// w_scratch: router_scratch_bytes(d, E) bytes of workspace (a zero-padded
-// copy of w_r made by the first of the two kernels launched here)
-size_t router_scratch_bytes(int d, int E);
+// w_scratch: router_scratch_bytes(T, d, E) bytes of workspace (a zero-padded
+// copy of w_r for launch_router_logits; the transposed copy, the token list
+// and the GEMM tile table for launch_router)
+size_t router_scratch_bytes(int T, int d, int E);
 // kernels launch_router_logits launches (1: weights resident; 2: padded copy + tiled)
 int router_logits_launches(int d, int E);
 cudaError_t launch_router_logits(const void *x, const void *w_r, int T, int d, int E,
@@ -22,6 +23,21 @@ cudaError_t launch_router_logits(const void *x, const void *w_r, int T, int d, i
 cudaError_t launch_router_select(const float *logits, const float *bias, int T, int E, int G,
                                  int topk_group, int k, int score, float bias_scale, int mode,
                                  int32_t *ids, float *weights, cudaStream_t s);
+// Routing without a logits output: ids [T,k] and weights [T,k], the same
+// values as launch_router_logits + launch_router_select.  Where the shape
+// allows (router_screened) the logits come from the tensor cores and only
+// the selected ones, or every logit of a token whose selection margin is
+// below kScreenDelta, are recomputed in the canonical order; logits [T,E]
+// is scratch.  status receives the GEMM's wait errors.
+bool router_screened(int T, int d, int E, int G, int k);
+int router_launches(int T, int d, int E, int G, int k);
+cudaError_t launch_router(const void *x, const void *w_r, const float *bias, int T, int d, int E,
+                          int G, int topk_group, int k, int score, float bias_scale,
+                          float *logits, int32_t *ids, float *weights, void *w_scratch,
+                          uint32_t *status, cudaStream_t s);
+// tokens of the last launch_router call that took the canonical path
+// (device int in the router scratch; nullptr when the call was not screened)
+const int32_t *router_flagged_count(const void *w_scratch, int T, int d, int E, int G, int k);
 
 // dispatch.cu
 // Assignments per dispatch chunk: 128 up to 32768 assignments (enough chunks
@@ -67,6 +83,8 @@ cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, i
 // this most tiles are such tails, and the single-CTA kernel already streams
 // the weights at HBM speed.
 constexpr int64_t kPairRowsPerExpert = 256;
+// rows of a 1-CTA GEMM tile (the unit mtile_base counts when pair is false)
+constexpr int kGemmTileRows = 128;
 
 // quant.cu: e4m3 codes with fp32 scales, per (row, 128 columns) of [rows,
 // cols] bf16, or per 128 x 128 block of [mats, rows, cols] bf16
@@ -97,6 +115,8 @@ struct GemmProblem {
   uint32_t *status;
   uint64_t wait_limit_ns;
   bool pair;  // 256-row tiles on CTA pairs (mtile_base counts 256-row tiles)
+  int bn;     // 1-CTA down form: output tile width 64, 128 or 256 (0: widest dividing n_out)
+  int ksplit; // 1-CTA down form: K pieces per tile added into out, which must hold zeros (0, 1: none)
 };
 cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s);
 cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s);

@@ -124,6 +124,15 @@ moe_status_t moe_get_device_status(void *ws, size_t ws_bytes, moe_stream_t strea
  * owns the 8-element chunks c with c mod 32 == l and sums them in order; the
  * 32 lane sums are combined by an xor butterfly), and sigmoid/exp use a
  * fixed Cody-Waite + Taylor evaluation, so ids are reproducible bit-exactly.
+ * With logits == NULL, d % 64 == 0, d <= 16384 and E % 64 == 0 the call is
+ * screened: the logits are first taken on the tensor cores; a token whose
+ * margins (last kept group score minus best dropped one, k-th selected score
+ * minus the best unselected eligible one; scores are the logits for softmax)
+ * are both >= 1e-3 keeps that selection, with its order and weights from the
+ * fixed-order logits of its k experts; every other token gets all E
+ * fixed-order logits.  The outputs are those of the fixed order whenever
+ * every tensor-core logit is within 2.5e-4 of it (moe_route_screened_count
+ * reports the fallbacks).
  */
 moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *w_r,
                        const float *bias, int32_t *topk_ids, float *topk_w,
@@ -380,6 +389,15 @@ moe_status_t moe_eplb_plan(const double *load, int32_t num_experts, int32_t num_
  * accounting).
  */
 int32_t moe_layer_launch_count(const moe_shape_t *shape);
+
+/*
+ * Tokens that the last screened routing in `ws` (moe_route without logits,
+ * moe_layer, moe_layer_capacity, moe_layer_fp8 of this shape) sent to the
+ * full fixed-order path: copies one int32 to device memory `count` on
+ * `stream` (asynchronous); -1 when the shape is not screened.
+ */
+moe_status_t moe_route_screened_count(const moe_shape_t *shape, const void *ws, size_t ws_bytes,
+                                      int32_t *count, moe_stream_t stream);
 
 /*
  * Self-test of the bounded wait used by every device-side spin: launches one

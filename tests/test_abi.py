@@ -133,16 +133,19 @@ def test_zero_tokens_is_a_noop(lib):
                        None, 0, None, None)
     assert st == 0
     assert lib.moe_layer_launch_count(ctypes.byref(s)) == 0
-    # router logits (1 with the weights resident in shared memory, else a
-    # padded copy + the tiled kernel), select, count, scan, scatter, gather,
-    # gate_up, down, combine
+    # router: screened (d, E multiples of 64: transpose, tensor-core logits,
+    # screen, listed logits, listed selection) or logits (1 with the weights
+    # resident in shared memory, else a padded copy + the tiled kernel) +
+    # select; then count, scan, scatter, gather, gate_up, down, combine
     assert lib.moe_layer_launch_count(ctypes.byref(_shape())) == 9
     decode = _shape(T=512, d=7168, E=256, G=8, topk_group=4, k=8, inter=2048, score=1)
     prefill = _shape(T=16384, d=7168, E=256, G=8, topk_group=4, k=8, inter=2048, score=1)
     few_large = _shape(T=2048, d=4096, E=8, G=1, topk_group=1, k=2, inter=14336)
-    assert lib.moe_layer_launch_count(ctypes.byref(decode)) == 10
-    assert lib.moe_layer_launch_count(ctypes.byref(prefill)) == 10
+    e32 = _shape(T=100, d=512, E=32, G=1, topk_group=1, k=4, inter=128)
+    assert lib.moe_layer_launch_count(ctypes.byref(decode)) == 12
+    assert lib.moe_layer_launch_count(ctypes.byref(prefill)) == 12
     assert lib.moe_layer_launch_count(ctypes.byref(few_large)) == 9
+    assert lib.moe_layer_launch_count(ctypes.byref(e32)) == 10
 
 
 def test_masked_layout_arguments(lib):

@@ -128,3 +128,107 @@ def test_group_topk_reproduces_ep_deploy_simulation():
     for nodes, gpus, place, ratio, ntok in _golden_rows():
         if place == "by_number":
             assert placement_stats(ids, 256, nodes, gpus) == (ratio, ntok)
+
+
+# --------------------------------------------------------------------------
+# Screened routing (moe_route without logits; d and E multiples of 64): ids
+# equal to the fixed-order path's, weights bit for bit.
+# --------------------------------------------------------------------------
+
+def _screened_vs_fixed(shape, x, w_r, bias):
+    ws = moe.Workspace(moe.moe_workspace_size(shape))
+    b = bias if shape["score"] == SCORE_SIGMOID_BIAS else None
+    ids_s, w_s, _ = moe.moe_route(shape, x, w_r, b, ws)
+    n_flag = moe.moe_route_screened_count(shape, ws)
+    ids_f, w_f, logits = moe.moe_route(shape, x, w_r, b, ws, want_logits=True)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    ids_s, w_s = ids_s.cpu().numpy(), w_s.cpu().numpy()
+    assert np.array_equal(ids_s, ids_f.cpu().numpy())
+    assert np.array_equal(w_s.view(np.uint32), w_f.cpu().numpy().view(np.uint32))
+    return ids_s, w_s, logits.cpu().numpy(), n_flag
+
+
+@pytest.mark.parametrize("T,d,E,G,tg,k,score", [
+    (300, 512, 64, 1, 1, 6, SCORE_SIGMOID_BIAS),
+    (257, 1024, 128, 4, 2, 8, SCORE_SIGMOID_BIAS),
+    (1000, 256, 256, 8, 4, 8, SCORE_SIGMOID_BIAS),
+    (64, 7168, 256, 8, 4, 8, SCORE_SIGMOID_BIAS),
+    (500, 512, 128, 1, 1, 4, SCORE_SOFTMAX),
+    (33, 128, 1024, 32, 8, 32, SCORE_SIGMOID_BIAS),   # 32 experts per lane, k = 32
+    (1, 64, 64, 2, 1, 1, SCORE_SIGMOID_BIAS),
+    (4100, 2048, 192, 3, 2, 8, SCORE_SIGMOID_BIAS),   # 33 m-tiles, ragged last tile
+])
+def test_screened_route_matches_oracle(T, d, E, G, tg, k, score):
+    ensure_lib()
+    import moe_inputs
+    from tests.gpu_common import bits
+    tns = moe_inputs.make_tensors_for_shape(T, d, E, 64, device="cuda", seed=3 * T + d + E)
+    shape = dict(T=T, d=d, E=E, G=G, topk_group=tg, k=k, inter=64, score=score,
+                 bias_scale=0.15)
+    ids, w, logits, n_flag = _screened_vs_fixed(shape, tns["x"], tns["w_r"], tns["bias"])
+    assert 0 <= n_flag <= T
+    ref_logits = oracle.router_logits(bits(tns["x"]), bits(tns["w_r"]))
+    assert np.array_equal(logits.view(np.uint32), ref_logits.view(np.uint32))
+    ref_ids, ref_w, _ = oracle.route_from_logits(ref_logits, tns["bias"].cpu().numpy(), G, tg, k,
+                                                 score, 0.15)
+    assert np.array_equal(ids, ref_ids)
+    assert np.all(np.abs(w - ref_w) <= 1e-6 * np.abs(ref_w))
+
+
+def test_screened_route_all_ties_take_the_fixed_order_path():
+    # zero router weight and bias: every score ties, no token is screened
+    ensure_lib()
+    T, d, E, G, tg, k = 200, 256, 128, 8, 3, 6
+    shape = dict(T=T, d=d, E=E, G=G, topk_group=tg, k=k, inter=64, score=SCORE_SIGMOID_BIAS,
+                 bias_scale=0.15)
+    x = torch.randn(T, d, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
+    w_r = torch.zeros(d, E, dtype=torch.bfloat16, device="cuda")
+    bias = torch.zeros(E, dtype=torch.float32, device="cuda")
+    ids, w, _, n_flag = _screened_vs_fixed(shape, x, w_r, bias)
+    assert n_flag == T
+    # ties go to the lower group, then the lower expert; equal weights
+    assert np.array_equal(ids, np.tile(np.arange(k, dtype=np.int32), (T, 1)))
+    _, ref_w, _ = oracle.route_from_logits(np.zeros((T, E), np.float32), np.zeros(E), G, tg, k,
+                                           SCORE_SIGMOID_BIAS, 0.15)
+    assert np.array_equal(w, ref_w)
+
+
+def test_screened_route_duplicate_experts_tie_exactly():
+    # experts 2j and 2j+1 share a weight column: exact ties in every token;
+    # the pair split at the selection boundary is flagged, pairs inside keep
+    # lower index first
+    ensure_lib()
+    from tests.gpu_common import bits
+    T, d, E, G, tg, k = 512, 1024, 64, 4, 2, 5
+    g = torch.Generator().manual_seed(11)
+    half = (torch.randn(d, E // 2, generator=g) * 0.05).to(torch.bfloat16)
+    w_r = half.repeat_interleave(2, dim=1).contiguous()
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    bias = torch.zeros(E, dtype=torch.float32)
+    shape = dict(T=T, d=d, E=E, G=G, topk_group=tg, k=k, inter=64, score=SCORE_SIGMOID_BIAS,
+                 bias_scale=0.15)
+    ids, w, _, n_flag = _screened_vs_fixed(shape, x.cuda(), w_r.cuda(), bias.cuda())
+    assert n_flag == T   # k odd: the k-th and (k+1)-th experts always tie
+    ref_ids, ref_w, _ = oracle.route(bits(x), bits(w_r), bias.numpy(), G, tg, k,
+                                     SCORE_SIGMOID_BIAS)
+    assert np.array_equal(ids, ref_ids)
+    k2 = 4
+    shape["k"] = k2
+    ids, w, _, n_flag = _screened_vs_fixed(shape, x.cuda(), w_r.cuda(), bias.cuda())
+    assert n_flag < T
+    ref_ids, ref_w, _ = oracle.route(bits(x), bits(w_r), bias.numpy(), G, tg, k2,
+                                     SCORE_SIGMOID_BIAS)
+    assert np.array_equal(ids, ref_ids)
+    assert np.all(np.abs(w - ref_w) <= 1e-6 * np.abs(ref_w))
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_screened_route_full_size(name):
+    ensure_lib()
+    cfg = CONFIGS[name]
+    t = layer_inputs(name)
+    ids, w, logits, n_flag = _screened_vs_fixed(cfg.shape(), t["x"], t["w_r"], t["bias"])
+    # the fixed-order path itself is pinned to the oracle in
+    # test_route_bit_exact_full_size; the screen sends a small share back
+    assert 0 <= n_flag < cfg.T // 5
