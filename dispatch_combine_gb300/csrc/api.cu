@@ -635,7 +635,8 @@ moe_status_t moe_layer_fp8(const moe_shape_t *shape, const void *x, const void *
                                            dest, nullptr, at<int32_t>(ws, L.chunk), mtile, 128,
                                            status, stream)));
   MOE_TRY(cuda_status(moe::launch_gather_rows(at<void>(ws, L.xq), s.d, at<float>(ws, L.xs),
-                                              s.d / 128, src, offsets + s.E, n, s.T,
+                                              s.d / 128, ids, dest, s.k, s.E, src,
+                                              offsets + s.E, n, s.T,
                                               at<void>(ws, L.xq_perm), at<float>(ws, L.xs_perm),
                                               stream)));
   MOE_TRY(run_ffn_fp8(shape, MOE_LAYOUT_CONTIGUOUS, at<void>(ws, L.xq_perm),

@@ -193,37 +193,47 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
 
 constexpr int kGatherWarps = 8;
 
-// Warp per row; each lane moves up to 8 16-byte vectors per pass with all
-// loads issued before the stores.
 __global__ void __launch_bounds__(kGatherWarps * 32)
-    dispatch_gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ src_token,
-                           const int32_t *__restrict__ offsets_end, int64_t n, int T,
-                           int vec_per_row, uint4 *__restrict__ x_perm, CapacityArgs cap) {
+    dispatch_gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ ids,
+                           const int32_t *__restrict__ dest, int T, int k, int E,
+                           const int32_t *__restrict__ offsets_end, int64_t n, int vec_per_row,
+                           uint4 *__restrict__ x_perm, CapacityArgs cap) {
+  // Token-major: warp item (t, s) reads 4 KB segment s of x[t] once and
+  // writes it to the rows dest[t*k + j] of the token's valid assignments, so
+  // x is read once however many experts a token has.  Valid rows are
+  // [0, offsets[E]) (with a capacity: the E*C padded rows, then the
+  // overflow rows); assignments with an invalid id or no row (dropped) are
+  // skipped, and rows without an assignment are left untouched.
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // rows past offsets[E] exist only if some ids were invalid; they have no
-  // source token and are left untouched.  With a capacity the rows are the
-  // E*C padded rows (row r of expert e used if r < kept[e]) and then the
-  // overflow rows.
   const int64_t pad = cap.kept ? static_cast<int64_t>(cap.E) * cap.capacity : 0;
   const int64_t rows = cap.kept ? pad + cap.ovf_offsets[cap.E]
                                 : min(n, static_cast<int64_t>(*offsets_end));
-  for (int64_t row = (int64_t)blockIdx.x * kGatherWarps + warp; row < rows;
-       row += (int64_t)gridDim.x * kGatherWarps) {
-    if (cap.kept && row < pad) {
-      const int e = static_cast<int>(row / cap.capacity);
-      if (row - static_cast<int64_t>(e) * cap.capacity >= cap.kept[e]) continue;
-    }
-    const int t = src_token[row];
-    if (t < 0 || t >= T) continue;
-    const uint4 *src = x + (size_t)t * vec_per_row;
-    uint4 *dst = x_perm + (size_t)row * vec_per_row;
-    for (int v0 = 0; v0 < vec_per_row; v0 += 256) {
-      uint4 r[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int v = v0 + u * 32 + lane;
-        if (v < vec_per_row) r[u] = __ldg(src + v);
+  const int segs = (vec_per_row + 255) / 256;
+  const int64_t items = static_cast<int64_t>(T) * segs;
+  for (int64_t it = (int64_t)blockIdx.x * kGatherWarps + warp; it < items;
+       it += (int64_t)gridDim.x * kGatherWarps) {
+    const int t = static_cast<int>(it / segs);
+    const int v0 = static_cast<int>(it - static_cast<int64_t>(t) * segs) * 256;
+    int p = -1;
+    if (lane < k) {
+      const int64_t a = static_cast<int64_t>(t) * k + lane;
+      const int id = ids[a];
+      if (id >= 0 && id < E) {
+        const int q = dest[a];
+        if (q >= 0 && q < rows) p = q;
       }
+    }
+    const uint4 *src = x + (size_t)t * vec_per_row;
+    uint4 r[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int v = v0 + u * 32 + lane;
+      if (v < vec_per_row) r[u] = __ldg(src + v);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int pj = __shfl_sync(0xffffffffu, p, j);
+      if (pj < 0) continue;
+      uint4 *dst = x_perm + (size_t)pj * vec_per_row;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int v = v0 + u * 32 + lane;
@@ -306,12 +316,13 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (x != nullptr && x_perm != nullptr) {
-    const int64_t max_rows = cap.kept ? static_cast<int64_t>(E) * cap.capacity + n : n;
-    const int64_t want = (max_rows + kGatherWarps - 1) / kGatherWarps;
+    const int vec = d / 8;
+    const int64_t items = static_cast<int64_t>(T) * ((vec + 255) / 256);
+    const int64_t want = (items + kGatherWarps - 1) / kGatherWarps;
     const int64_t grid_cap = (int64_t)num_sms() * 8;
     const unsigned gblocks = (unsigned)(want < grid_cap ? want : grid_cap);
     dispatch_gather_kernel<<<gblocks, kGatherWarps * 32, 0, s>>>(
-        static_cast<const uint4 *>(x), src_token, offsets + E, n, T, d / 8,
+        static_cast<const uint4 *>(x), ids, dest, T, k, E, offsets + E, n, vec,
         static_cast<uint4 *>(x_perm), cap);
     err = cudaGetLastError();
   }
@@ -319,20 +330,23 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
 }
 
 cudaError_t launch_gather_rows(const void *src, int row_bytes, const float *src_scale,
-                               int scales_per_row, const int32_t *src_token,
+                               int scales_per_row, const int32_t *ids, const int32_t *dest,
+                               int k, int E, const int32_t *src_token,
                                const int32_t *offsets_end, int64_t n, int T, void *dst,
                                float *dst_scale, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  const int64_t want = (n + kGatherWarps - 1) / kGatherWarps;
+  const int vec = row_bytes / 16;
+  const int64_t items = static_cast<int64_t>(T) * ((vec + 255) / 256);
+  const int64_t want = (items + kGatherWarps - 1) / kGatherWarps;
   const int64_t grid_cap = (int64_t)num_sms() * 8;
   dispatch_gather_kernel<<<(unsigned)(want < grid_cap ? want : grid_cap), kGatherWarps * 32, 0,
-                           s>>>(static_cast<const uint4 *>(src), src_token, offsets_end, n, T,
-                                row_bytes / 16, static_cast<uint4 *>(dst),
+                           s>>>(static_cast<const uint4 *>(src), ids, dest, T, k, E,
+                                offsets_end, n, vec, static_cast<uint4 *>(dst),
                                 CapacityArgs{0, 0, 0, nullptr, nullptr});
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || !src_scale) return err;
-  const int64_t items = n * scales_per_row;
-  const int64_t blocks = (items + 255) / 256;
+  const int64_t scale_items = n * scales_per_row;
+  const int64_t blocks = (scale_items + 255) / 256;
   gather_scales_kernel<<<(unsigned)(blocks < grid_cap ? blocks : grid_cap), 256, 0, s>>>(
       src_scale, src_token, offsets_end, n, T, scales_per_row, dst_scale);
   return cudaGetLastError();

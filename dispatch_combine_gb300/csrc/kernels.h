@@ -60,10 +60,12 @@ struct CapacityArgs {
   int32_t *ovf_offsets;
 };
 // x_perm-style gather of byte rows (row_bytes a multiple of 16) and,
-// optionally, of per-row fp32 scales: dst[p] = src[src_token[p]] for
-// p < min(n, *offsets_end)
+// optionally, of per-row fp32 scales: row t of src goes to the rows
+// dest[t*k + j] < min(n, *offsets_end) of its valid assignments (ids in
+// [0, E)); scales by src_token: dst_scale[p] = src_scale[src_token[p]]
 cudaError_t launch_gather_rows(const void *src, int row_bytes, const float *src_scale,
-                               int scales_per_row, const int32_t *src_token,
+                               int scales_per_row, const int32_t *ids, const int32_t *dest,
+                               int k, int E, const int32_t *src_token,
                                const int32_t *offsets_end, int64_t n, int T, void *dst,
                                float *dst_scale, cudaStream_t s);
 cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void *x, int d,
