@@ -78,6 +78,11 @@ def test_ffn_contiguous(counts, d, inter):
     ([320, 319, 321, 575, 576, 1], 512, 256),
     ([1, 16, 600, 900], 256, 384),  # experts made of one swapped tile
     ([700, 300], 4096, 1024),       # long K
+    # down: 15 m-tiles x 16 n-tiles = 240 tiles on 76 pairs, the last 12
+    # (swapped tails among them) split in 4 pieces of 64 columns
+    ([520, 520, 520, 520, 530], 4096, 256),
+    # 192 tiles: a last wave of 40 tiles, not split
+    ([2000, 1000], 4096, 256),
 ])
 def test_ffn_pair_tiles(counts, d, inter):
     # T*k >= 256 rows per expert selects the CTA-pair (cta_group::2) kernels
