@@ -727,11 +727,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 // 128 columns, B (weights) one per 128 x 128 block; a k-block is 128
 // columns, i.e. one scale block and one 128-byte swizzle row.  The MMA warp
 // issues kind::f8f6f4 MMAs (M=128, N=128, K=32) for one k-block into one of
-// two TMEM partial accumulators; the four epilogue warps (thread = row) read
-// the partial, multiply it by the two scales and add it into fp32 registers
-// (128 per thread), then release the partial.  After the last k-block they
-// apply SwiGLU (gate_up: columns 0-63 gate, 64-127 the matching up) or write
-// fp32 (down) straight from registers.
+// four TMEM partial accumulators; eight promotion warps (two per TMEM lane
+// quadrant, thread = row, each half of the columns) read the partial in one
+// wait, multiply it by the two scales and add it into fp32 registers (64 per
+// thread), then release the partial.  After the last k-block they apply
+// SwiGLU (gate_up: columns 0-63 gate, 64-127 the matching up; a warp holds
+// 32 gate columns and their up columns) or write fp32 (down) straight from
+// registers.
 //   full/empty[s]    stage ring (producer <-> MMA);
 //   pfull/pempty[b]  partial accumulator b (MMA <-> epilogue warps).
 // ---------------------------------------------------------------------------
@@ -739,6 +741,7 @@ constexpr int kF8BK = 128;  // e4m3 per k-block = bytes per swizzle row
 constexpr int kF8BN = 128;
 constexpr int kF8Stages = 6;
 constexpr int kF8Parts = 4;  // TMEM partial accumulators: the MMA runs up to 3 k-blocks ahead
+constexpr int kF8Threads = 320;  // producer, MMA issuer, 8 promotion warps
 
 template <bool SWIGLU>
 struct CfgF8 {
@@ -768,7 +771,7 @@ struct F8Args {
 constexpr int kF8SubRows = 32;
 
 template <bool SWIGLU>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kF8Threads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmA32,
                             const __grid_constant__ CUtensorMap tmB, const F8Args fa) {
@@ -799,7 +802,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < kF8Parts; ++b) {
       mbar_init(&pfull[b], 1);
-      mbar_init(&pempty[b], 4);
+      mbar_init(&pempty[b], 8);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -912,10 +915,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- promotion + epilogue (warps 2..5) ----------------
+    // ---------------- promotion + epilogue (warps 2..9) ----------------
+    // Warp w handles TMEM lane quadrant w % 4 and column half h = (w - 2) / 4:
+    // gate_up: gate columns 32h .. 32h+31 and the matching up columns
+    // 64 + 32h .. (so SwiGLU stays in the thread); down: columns 64h .. 64h+63.
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int col0 = SWIGLU ? 32 * half : 64 * half;            // first TMEM column
+    const int col1 = SWIGLU ? kF8BN / 2 + 32 * half : col0 + 32;  // second 32-column run
     uint32_t q = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
@@ -931,9 +940,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else {
         bs0 = bs1 = fa.b_scale + (static_cast<int64_t>(t.e) * b_blocks + t.n) * kbs;
       }
-      float acc[kF8BN];
+      // acc2[i]: this warp's columns 2i, 2i+1 of its two runs (0..15 the
+      // first run, 16..31 the second); promoted with fma.rn.f32x2 (two IEEE
+      // fused multiply-adds, rounded as scalar ones)
+      uint64_t acc2[32];
 #pragma unroll
-      for (int c = 0; c < kF8BN; ++c) acc[c] = 0.0f;
+      for (int c = 0; c < 32; ++c) acc2[c] = 0ull;
       float sa = rok ? __ldg(as) : 0.0f;
       // a warp whose 32 rows are all past the tile's rows only keeps the
       // partial ring moving
@@ -951,21 +963,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t tp = tmem_base + lane_off + static_cast<uint32_t>(p * kF8BN);
         if (warp_rows) {
+          // both 32-column runs in one wait
+          uint32_t v[32], w[32];
+          tmem_ld_32x32b_x32(tp + col0, v);
+          tmem_ld_32x32b_x32(tp + col1, w);
+          tmem_ld_wait();
+          tmem_regs_fence(v);
+          tmem_regs_fence(w);
+          // down: one weight block, s0 == s1; gate_up: gate run s0, up run s1
+          uint64_t sc0, sc1;
+          asm("mov.b64 %0, {%1, %1};" : "=l"(sc0) : "f"(s0));
+          asm("mov.b64 %0, {%1, %1};" : "=l"(sc1) : "f"(s1));
 #pragma unroll
-          for (int c = 0; c < kF8BN / 64; ++c) {
-            // two 32-column loads per wait
-            uint32_t v[32], w[32];
-            tmem_ld_32x32b_x32(tp + c * 64, v);
-            tmem_ld_32x32b_x32(tp + c * 64 + 32, w);
-            tmem_ld_wait();
-            tmem_regs_fence(v);
-            tmem_regs_fence(w);
-            const float sc = (c < kF8BN / 128) ? s0 : s1;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              acc[c * 64 + j] = fmaf(__uint_as_float(v[j]), sc, acc[c * 64 + j]);
-              acc[c * 64 + 32 + j] = fmaf(__uint_as_float(w[j]), sc, acc[c * 64 + 32 + j]);
-            }
+          for (int j = 0; j < 16; ++j) {
+            uint64_t pv, pw;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(pv) : "r"(v[2 * j]), "r"(v[2 * j + 1]));
+            asm("mov.b64 %0, {%1, %2};" : "=l"(pw) : "r"(w[2 * j]), "r"(w[2 * j + 1]));
+            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[j]) : "l"(pv), "l"(sc0));
+            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[16 + j]) : "l"(pw), "l"(sc1));
           }
         }
         tc_fence_before();
@@ -973,17 +988,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) mbar_arrive(&pempty[p]);
       }
       if (!ok || !rok) continue;
-      if (SWIGLU) {
-        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(args.out) + grow * args.ldo +
-                             static_cast<int64_t>(t.n) * C::BN_OUT;
+      float acc[64];
 #pragma unroll
-        for (int c = 0; c < C::BN_OUT / 16; ++c) {
+      for (int c = 0; c < 32; ++c)
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[2 * c]), "=f"(acc[2 * c + 1]) : "l"(acc2[c]));
+      if (SWIGLU) {
+        // intermediate columns t.n * 64 + 32h .. +31: gate acc[0..31], up acc[32..63]
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(args.out) + grow * args.ldo +
+                             static_cast<int64_t>(t.n) * C::BN_OUT + 32 * half;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
           uint32_t w8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int j = c * 16 + 2 * i;
             const float g0 = acc[j], g1 = acc[j + 1];
-            const float u0 = acc[C::BN_OUT + j], u1 = acc[C::BN_OUT + j + 1];
+            const float u0 = acc[32 + j], u1 = acc[32 + j + 1];
             w8[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
                                 __fdividef(g1, 1.0f + __expf(-g1)) * u1);
           }
@@ -997,9 +1017,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       } else {
         float *dst = static_cast<float *>(args.out) + grow * args.ldo +
-                     static_cast<int64_t>(t.n) * kF8BN;
+                     static_cast<int64_t>(t.n) * kF8BN + 64 * half;
 #pragma unroll
-        for (int c = 0; c < kF8BN / 8; ++c) {
+        for (int c = 0; c < 8; ++c) {
           uint32_t w8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) w8[i] = __float_as_uint(acc[c * 8 + i]);
@@ -1149,7 +1169,7 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   a.ksplit = 1;
   fa.a_scale = a_scale;
   fa.b_scale = b_scale;
-  grouped_gemm_fp8_kernel<SWIGLU><<<num_sms(), kGemmThreads, C::SMEM_BYTES, s>>>(tmA, tmA32,
+  grouped_gemm_fp8_kernel<SWIGLU><<<num_sms(), kF8Threads, C::SMEM_BYTES, s>>>(tmA, tmA32,
                                                                                 tmB, fa);
   return cudaGetLastError();
 }
