@@ -962,7 +962,16 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
         tc_fence_after();
         const uint32_t tp = tmem_base + lane_off + static_cast<uint32_t>(p * kF8BN);
-        if (warp_rows) {
+        // the partial is released as soon as its values are in registers, so
+        // the MMA can refill it while the scales are applied
+        auto release = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pempty[p]);
+        };
+        if (!warp_rows) {
+          release();
+        } else {
           // both 32-column runs in one wait
           uint32_t v[32], w[32];
           tmem_ld_32x32b_x32(tp + col0, v);
@@ -970,6 +979,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           tmem_ld_wait();
           tmem_regs_fence(v);
           tmem_regs_fence(w);
+          release();
           // down: one weight block, s0 == s1; gate_up: gate run s0, up run s1
           uint64_t sc0, sc1;
           asm("mov.b64 %0, {%1, %1};" : "=l"(sc0) : "f"(s0));
@@ -983,9 +993,6 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[16 + j]) : "l"(pw), "l"(sc1));
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pempty[p]);
       }
       if (!ok || !rok) continue;
       float acc[64];

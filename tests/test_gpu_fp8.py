@@ -64,6 +64,11 @@ def _shape(E, d, inter, T):
     ([5, 0, 260], 512, 256),
     ([40, 300, 1], 384, 384),
     ([3, 200], 4096, 1024),                 # long K in both GEMMs
+    # >= 256 rows per expert: CTA-pair tiles of 256 rows (an expert of 5 rows
+    # and tails of 1 and 255 rows leave the odd CTA of the pair empty or short)
+    ([300, 700, 5, 600], 512, 256),
+    ([256, 257, 511, 512, 1], 256, 128),
+    ([1000, 1100], 1024, 512),
 ])
 def test_ffn_fp8_contiguous(counts, d, inter):
     ensure_lib()
@@ -85,14 +90,17 @@ def test_ffn_fp8_contiguous(counts, d, inter):
     check_close(y.cpu().numpy(), ref, bf16_output=False, what="y (fp8)")
 
 
-def test_ffn_fp8_masked():
+@pytest.mark.parametrize("masked_m,M_max,T", [
+    ([0, 5, 256], 256, 1),
+    ([0, 5, 300, 512], 512, 1300),   # T*k >= 256 per expert and M_max >= 256: pair tiles
+])
+def test_ffn_fp8_masked(masked_m, M_max, T):
     ensure_lib()
-    E, d, inter, M_max = 3, 256, 256, 256
-    masked_m = [0, 5, 256]
+    E, d, inter = len(masked_m), 256, 256
     x = _rand_bf16((E, M_max, d), 11)
     (gq, gs, dq, ds), (rgq, rgs, rdq, rds) = _weights_fp8(E, d, inter, seed=12)
     xq, xs = moe.moe_quantize_fp8_rows(x.reshape(E * M_max, d).cuda())
-    shape = _shape(E, d, inter, 1)
+    shape = _shape(E, d, inter, T)
     ws = moe.Workspace(moe.moe_expert_ffn_fp8_workspace_size(shape, moe.MOE_LAYOUT_MASKED, M_max))
     mm = torch.tensor(masked_m, dtype=torch.int32).cuda()
     y = torch.full((E * M_max, d), float("nan"), dtype=torch.float32, device="cuda")
