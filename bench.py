@@ -265,11 +265,12 @@ def time_oracle(c, host: dict, n_tokens: int, seed: int = 0) -> dict:
             "cores": oracle.num_threads()}
 
 
-def oracle_sample_size(c, seconds: float, threads: int) -> int:
-    """Tokens of oracle work that take about `seconds` on `threads` cores."""
-    flops_per_token = ffn_flops_per_row(c) * c.k + 2 * c.d * c.E
-    rate = 0.6e9 * max(threads, 1)  # plain fp64 loops, order of magnitude
-    return max(1, int(seconds * rate / flops_per_token))
+def oracle_sample_size(c, host: dict, seconds: float) -> int:
+    """Tokens of oracle work that take about `seconds` on this host: an
+    8-token sample is timed first and the count scaled from it."""
+    probe = time_oracle(c, host, 8, seed=999)
+    per_token = probe["seconds"] / max(probe["tokens"], 1)
+    return max(1, min(c.T, int(seconds / per_token)))
 
 
 def host_inputs(t: dict) -> dict:
@@ -288,7 +289,7 @@ def run_reference(args, c):
     from moe_inputs import make_layer_tensors
     t = make_layer_tensors(c, device="cpu", seed=0)
     host = host_inputs(t)
-    n = oracle_sample_size(c, args.ref_step_s, oracle.num_threads())
+    n = oracle_sample_size(c, host, args.ref_step_s)
     for w in range(args.warmup):  # untimed warm-up steps (one token each)
         time_oracle(c, host, 1, seed=1000 + w)
     total_s, total_tok = 0.0, 0
@@ -481,7 +482,7 @@ def run_gpu(args, c):
     if rank == 0 and world == 1 and args.cpu_sample_s > 0:
         import oracle
         host = host_inputs(t)
-        n = oracle_sample_size(c, args.cpu_sample_s, oracle.num_threads())
+        n = oracle_sample_size(c, host, args.cpu_sample_s)
         r = time_oracle(c, host, n)
         cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                "sample": f"{r['tokens']} of {c.T} tokens (seeded), full layer per token, "
