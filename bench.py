@@ -632,7 +632,76 @@ def parse_args(argv=None):
                     help="time the masked expert FFN of a per-rank slice instead")
     ap.add_argument("--ref-step-s", type=float, default=4.0,
                     help="seconds of oracle work per step of --impl reference")
+    ap.add_argument("--ffn-rows", default=None, metavar="E,R",
+                    help="time the expert FFN alone on E experts x R rows at the workload's "
+                         "d and inter (bf16, or FP8 with --fp8; own line)")
     return ap.parse_args(argv)
+
+
+def run_ffn_only(args):
+    """Expert FFN alone (gate_up + SwiGLU, down) on E experts of R rows each,
+    contiguous layout, at the workload's d and inter: the GEMM kernels
+    without routing or dispatch, with a small device footprint (own line)."""
+    import torch
+    import dispatch_combine_gb300 as moe
+    torch.cuda.set_device(0)
+    c = CONFIGS[args.config]
+    E, R = (int(v) for v in args.ffn_rows.split(","))
+    d, inter = c.d, c.inter
+    g = torch.Generator(device="cuda").manual_seed(0)
+    w_gu = (torch.randn(E, 2 * inter, d, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    w_dn = (torch.randn(E, d, inter, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    x = torch.randn(E * R, d, device="cuda", generator=g).to(torch.bfloat16)
+    offsets = torch.arange(E + 1, dtype=torch.int32, device="cuda") * R
+    shape = dict(T=E * R, d=d, E=E, G=1, topk_group=1, k=1, inter=inter, score=1,
+                 bias_scale=0.15)
+    y = torch.empty(E * R, d, dtype=torch.float32, device="cuda")
+    if args.fp8:
+        gq, gs = moe.moe_quantize_fp8_blocks(w_gu)
+        dq, ds = moe.moe_quantize_fp8_blocks(w_dn)
+        del w_gu, w_dn
+        xq, xs = moe.moe_quantize_fp8_rows(x)
+        ws = moe.Workspace(moe.moe_expert_ffn_fp8_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+
+        def step():
+            moe.moe_expert_ffn_fp8(shape, moe.MOE_LAYOUT_CONTIGUOUS, xq, xs, offsets, 0, gq, gs,
+                                   dq, ds, ws, y_out=y)
+        wbytes = E * 3 * d * inter
+    else:
+        ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+
+        def step():
+            moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_CONTIGUOUS, x, offsets, 0, w_gu, w_dn, ws,
+                               y_out=y)
+        wbytes = E * 3 * d * inter * 2
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status error")
+    sec = e0.elapsed_time(e1) / 1000.0 / args.steps
+    flops = 6.0 * E * R * d * inter
+    peaks, peak_src = load_peaks()
+    line = {
+        "metric": "expert FFN alone: weight GB/s and TFLOP/s", "impl": "gb300",
+        "value": wbytes / sec / 1e9, "unit": "GB/s", "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "us_per_step": sec * 1e6,
+        "dtype": "e4m3" if args.fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": f"{E} experts x {R} rows, d={d}, inter={inter} "
+                               f"(from {c.name})", "weight_bytes": wbytes},
+        "tflops": flops / sec / 1e12,
+        "hbm_fraction": wbytes / sec / (peaks["hbm_gbs"] * 1e9),
+        "peak_source": peak_src,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def run_capacity(args):
@@ -791,6 +860,8 @@ def run_eplb(args):
 def main(argv=None):
     args = parse_args(argv)
     c = CONFIGS[args.config]
+    if args.ffn_rows:
+        return run_ffn_only(args)
     if args.fp8:
         return run_fp8(args)
     if args.eplb:
