@@ -55,6 +55,10 @@ def expert_weight_bytes(c) -> int:
     return 3 * c.d * c.inter * 2
 
 
+# timed steps that carry the six stage events (every STAGE_EVERY-th)
+STAGE_EVERY = 8
+
+
 def ffn_flops_per_row(c) -> int:
     """gate_up (2*d*2*inter) + down (2*inter*d) per routed row."""
     return 6 * c.d * c.inter
@@ -352,8 +356,12 @@ def run_gpu(args, c):
         raise SystemExit("device status error during warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
-    for row in evs:  # create the events before the timed region
+    # stage events on every STAGE_EVERY-th timed step (an event between two
+    # kernels stops the next one from launching early, so the other steps
+    # run without them); the stage times are the averages over those steps
+    sampled = list(range(0, K, STAGE_EVERY))
+    evs = {s: [torch.cuda.Event(enable_timing=True) for _ in range(6)] for s in sampled}
+    for row in evs.values():  # create the events before the timed region
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
@@ -368,7 +376,7 @@ def run_gpu(args, c):
     sampler.mark("t_start")
     start.record(stream)
     for s in range(K):
-        step(evs[s])
+        step(evs.get(s))
     end.record(stream)
     torch.cuda.synchronize()
     sampler.mark("t_end")
@@ -383,10 +391,10 @@ def run_gpu(args, c):
     # per-stage durations (events recorded on the launching stream)
     names = ["router", "dispatch", "gate_up", "down", "combine"]
     stage_ms = {n: 0.0 for n in names}
-    for row in evs:
+    for row in evs.values():
         for i, n in enumerate(names):
             stage_ms[n] += row[i].elapsed_time(row[i + 1])
-    stage_ms = {n: v / K for n, v in stage_ms.items()}
+    stage_ms = {n: v / len(evs) for n, v in stage_ms.items()}
 
     n_flagged = moe.moe_route_screened_count(shape, ws)
     cnt = counts.cpu()

@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float4 *__restrict__ y_perm, int64_t y_rows,
                    const int32_t *__restrict__ dest, const float *__restrict__ w, int T, int k,
                    int d4, int segs, uint2 *__restrict__ y) {
+  pdl_begin();
   __shared__ int s_row[32];
   __shared__ float s_w[32];
   const int t = blockIdx.x / segs;
@@ -72,7 +73,7 @@ cudaError_t launch_combine(const float *y_perm, int64_t y_rows, const int32_t *d
   const int d4 = d / 4;
   const int segs = (d4 + kCombineThreads * kCombineVec - 1) / (kCombineThreads * kCombineVec);
   const int64_t blocks = static_cast<int64_t>(T) * segs;
-  combine_kernel<<<static_cast<unsigned>(blocks), kCombineThreads, 0, s>>>(
+  MOE_LAUNCH_PDL(combine_kernel, static_cast<unsigned>(blocks), kCombineThreads, 0, s, 
       reinterpret_cast<const float4 *>(y_perm), y_rows, dest, w, T, k, d4, segs,
       static_cast<uint2 *>(y));
   return cudaGetLastError();

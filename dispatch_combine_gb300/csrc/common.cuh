@@ -19,6 +19,43 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization (launch_pdl) and starts with
+// pdl_begin(): it waits until the previous kernel of the stream has
+// completed and its writes are visible, then lets the next kernel launch.
+// So a kernel's launch and set-up overlap its predecessor's tail, and, since
+// every kernel waits, completion stays ordered along the whole stream.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// kernel, grid, block, dynamic shared bytes, stream, arguments: launches with
+// launch_pdl and returns its error from the enclosing function
+#define MOE_LAUNCH_PDL(...)                                  \
+  do {                                                       \
+    const cudaError_t moe_launch_err_ = ::moe::launch_pdl(__VA_ARGS__); \
+    if (moe_launch_err_ != cudaSuccess) return moe_launch_err_; \
+  } while (0)
+
+// ---------------------------------------------------------------------------
 // status word (first 4 bytes of the workspace)
 // ---------------------------------------------------------------------------
 

@@ -24,6 +24,7 @@ constexpr int kCountThreads = 256;
 __global__ void __launch_bounds__(kCountThreads)
     dispatch_count_kernel(const int32_t *__restrict__ ids, int64_t n, int E, int chunk,
                           int32_t *__restrict__ chunk_counts, uint32_t *status) {
+  pdl_begin();
   extern __shared__ int hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(1024)
     dispatch_scan_kernel(int32_t *__restrict__ chunk_counts, int nchunks, int E,
                          int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                          int32_t *__restrict__ mtile_base, int tile_rows, CapacityArgs cap) {
+  pdl_begin();
   __shared__ int part[1024];
   int ep = 1;
   while (ep < E) ep <<= 1;
@@ -149,6 +151,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
                             int64_t nchunks, const int32_t *__restrict__ chunk_base,
                             const int32_t *__restrict__ offsets, int32_t *__restrict__ dest,
                             int32_t *__restrict__ src_token, CapacityArgs cap) {
+  pdl_begin();
   extern __shared__ int cursor_all[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t ci = (int64_t)blockIdx.x * kScatterWarps + warp;
@@ -198,6 +201,7 @@ __global__ void __launch_bounds__(kGatherWarps * 32)
                            const int32_t *__restrict__ dest, int T, int k, int E,
                            const int32_t *__restrict__ offsets_end, int64_t n, int vec_per_row,
                            uint4 *__restrict__ x_perm, CapacityArgs cap) {
+  pdl_begin();
   // Token-major: warp item (t, s) reads 4 KB segment s of x[t] once and
   // writes it to the rows dest[t*k + j] of the token's valid assignments, so
   // x is read once however many experts a token has.  Valid rows are
@@ -248,6 +252,7 @@ __global__ void __launch_bounds__(256)
     gather_scales_kernel(const float *__restrict__ src, const int32_t *__restrict__ src_token,
                          const int32_t *__restrict__ offsets_end, int64_t n, int T, int per_row,
                          float *__restrict__ dst) {
+  pdl_begin();
   const int64_t rows = min(n, static_cast<int64_t>(*offsets_end));
   const int64_t total = rows * per_row;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -263,6 +268,7 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(1024)
     ffn_tiles_kernel(const int32_t *__restrict__ seg, int layout, int E, int M_max,
                      int tile_rows, int32_t *__restrict__ mtile_base, uint32_t *status) {
+  pdl_begin();
   const int e = threadIdx.x;
   int rows = 0;
   if (e < E) {
@@ -302,16 +308,16 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
   const int64_t nchunks = dispatch_num_chunks(n);
   const int chunk = dispatch_chunk(n);
   if (n == 0) return cudaSuccess;
-  dispatch_count_kernel<<<(unsigned)nchunks, kCountThreads, E * sizeof(int), s>>>(
+  MOE_LAUNCH_PDL(dispatch_count_kernel, (unsigned)nchunks, kCountThreads, E * sizeof(int), s, 
       ids, n, E, chunk, chunk_scratch, status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_scratch, (int)nchunks, E, counts, offsets,
+  MOE_LAUNCH_PDL(dispatch_scan_kernel, 1, 1024, 0, s, chunk_scratch, (int)nchunks, E, counts, offsets,
                                           mtile_base, tile_rows, cap);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const unsigned sblocks = (unsigned)((nchunks + kScatterWarps - 1) / kScatterWarps);
-  dispatch_scatter_kernel<<<sblocks, kScatterWarps * 32, kScatterWarps * E * sizeof(int), s>>>(
+  MOE_LAUNCH_PDL(dispatch_scatter_kernel, sblocks, kScatterWarps * 32, kScatterWarps * E * sizeof(int), s, 
       ids, n, k, E, chunk, nchunks, chunk_scratch, offsets, dest, src_token, cap);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -321,7 +327,7 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
     const int64_t want = (items + kGatherWarps - 1) / kGatherWarps;
     const int64_t grid_cap = (int64_t)num_sms() * 8;
     const unsigned gblocks = (unsigned)(want < grid_cap ? want : grid_cap);
-    dispatch_gather_kernel<<<gblocks, kGatherWarps * 32, 0, s>>>(
+    MOE_LAUNCH_PDL(dispatch_gather_kernel, gblocks, kGatherWarps * 32, 0, s, 
         static_cast<const uint4 *>(x), ids, dest, T, k, E, offsets + E, n, vec,
         static_cast<uint4 *>(x_perm), cap);
     err = cudaGetLastError();
@@ -339,22 +345,22 @@ cudaError_t launch_gather_rows(const void *src, int row_bytes, const float *src_
   const int64_t items = static_cast<int64_t>(T) * ((vec + 255) / 256);
   const int64_t want = (items + kGatherWarps - 1) / kGatherWarps;
   const int64_t grid_cap = (int64_t)num_sms() * 8;
-  dispatch_gather_kernel<<<(unsigned)(want < grid_cap ? want : grid_cap), kGatherWarps * 32, 0,
-                           s>>>(static_cast<const uint4 *>(src), ids, dest, T, k, E,
+  MOE_LAUNCH_PDL(dispatch_gather_kernel, (unsigned)(want < grid_cap ? want : grid_cap), kGatherWarps * 32, 0,
+                           s, static_cast<const uint4 *>(src), ids, dest, T, k, E,
                                 offsets_end, n, vec, static_cast<uint4 *>(dst),
                                 CapacityArgs{0, 0, 0, nullptr, nullptr});
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || !src_scale) return err;
   const int64_t scale_items = n * scales_per_row;
   const int64_t blocks = (scale_items + 255) / 256;
-  gather_scales_kernel<<<(unsigned)(blocks < grid_cap ? blocks : grid_cap), 256, 0, s>>>(
+  MOE_LAUNCH_PDL(gather_scales_kernel, (unsigned)(blocks < grid_cap ? blocks : grid_cap), 256, 0, s, 
       src_scale, src_token, offsets_end, n, T, scales_per_row, dst_scale);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,
                              int32_t *mtile_base, uint32_t *status, cudaStream_t s) {
-  ffn_tiles_kernel<<<1, 1024, 0, s>>>(seg, layout, E, M_max, tile_rows, mtile_base, status);
+  MOE_LAUNCH_PDL(ffn_tiles_kernel, 1, 1024, 0, s, seg, layout, E, M_max, tile_rows, mtile_base, status);
   return cudaGetLastError();
 }
 

@@ -130,6 +130,7 @@ template <int BN, bool SWIGLU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const KArgs args) {
+  pdl_begin();
   using C = Cfg<BN, SWIGLU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -427,6 +428,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmX,
                              const __grid_constant__ CUtensorMap tmW, const KArgs args) {
+  pdl_begin();
   using C = Cfg2<BN, SWIGLU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -775,6 +777,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmA32,
                             const __grid_constant__ CUtensorMap tmB, const F8Args fa) {
+  pdl_begin();
   using C = CfgF8<SWIGLU>;
   const KArgs &args = fa.k;
   extern __shared__ uint8_t smem_raw[];
@@ -1052,6 +1055,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 // bounded-wait self test: one thread waits on a barrier nobody arrives on
 // ---------------------------------------------------------------------------
 __global__ void wait_selftest_kernel(uint32_t *status, uint64_t limit_ns) {
+  pdl_begin();
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -1176,7 +1180,7 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   a.ksplit = 1;
   fa.a_scale = a_scale;
   fa.b_scale = b_scale;
-  grouped_gemm_fp8_kernel<SWIGLU><<<num_sms(), kF8Threads, C::SMEM_BYTES, s>>>(tmA, tmA32,
+  MOE_LAUNCH_PDL(grouped_gemm_fp8_kernel<SWIGLU>, num_sms(), kF8Threads, C::SMEM_BYTES, s, tmA, tmA32,
                                                                                 tmB, fa);
   return cudaGetLastError();
 }
@@ -1215,7 +1219,7 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.status = p.status;
   a.wait_limit_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitLimitNs;
   a.ksplit = (!SWIGLU && p.ksplit > 1) ? p.ksplit : 1;
-  grouped_gemm_kernel<BN, SWIGLU><<<num_sms(), kGemmThreads, C::SMEM_BYTES, s>>>(tmA, tmB, a);
+  MOE_LAUNCH_PDL(grouped_gemm_kernel<BN, SWIGLU>, num_sms(), kGemmThreads, C::SMEM_BYTES, s, tmA, tmB, a);
   return cudaGetLastError();
 }
 
@@ -1281,7 +1285,7 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
     if (err != cudaSuccess) return err;
   }
   if (clusters < 1) return cudaErrorInvalidConfiguration;
-  grouped_gemm_pair_kernel<BN, SWIGLU><<<2 * clusters, kGemmThreads, C::SMEM_BYTES, s>>>(
+  MOE_LAUNCH_PDL(grouped_gemm_pair_kernel<BN, SWIGLU>, 2 * clusters, kGemmThreads, C::SMEM_BYTES, s, 
       tmA, tmB, tmX, tmW, a);
   return cudaGetLastError();
 }
@@ -1344,7 +1348,7 @@ cudaError_t launch_gemm_fp8_down(const GemmProblem &p, const float *a_scale,
 }
 
 cudaError_t launch_wait_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t s) {
-  wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  MOE_LAUNCH_PDL(wait_selftest_kernel, 1, 32, 0, s, status, limit_ns);
   return cudaGetLastError();
 }
 

@@ -29,6 +29,7 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
 __global__ void __launch_bounds__(256)
     quantize_rows_kernel(const __nv_bfloat16 *__restrict__ x, int64_t rows, int cols,
                          uint8_t *__restrict__ q, float *__restrict__ scales) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int nb = cols / 128;
   const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -52,6 +53,7 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     quantize_blocks_kernel(const __nv_bfloat16 *__restrict__ w, int rows, int cols,
                            uint8_t *__restrict__ q, float *__restrict__ scales) {
+  pdl_begin();
   __shared__ float red[8];
   const int rb = rows / 128, cb = cols / 128;
   const int64_t blk = blockIdx.x;
@@ -103,7 +105,7 @@ cudaError_t launch_quantize_rows_fp8(const void *x, int64_t rows, int cols, void
   if (rows == 0) return cudaSuccess;
   const int64_t warps = rows * (cols / 128);
   const int64_t blocks = (warps * 32 + 255) / 256;
-  quantize_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+  MOE_LAUNCH_PDL(quantize_rows_kernel, static_cast<unsigned>(blocks), 256, 0, s, 
       static_cast<const __nv_bfloat16 *>(x), rows, cols, static_cast<uint8_t *>(q), scales);
   return cudaGetLastError();
 }
@@ -112,7 +114,7 @@ cudaError_t launch_quantize_blocks_fp8(const void *w, int mats, int rows, int co
                                        float *scales, cudaStream_t s) {
   const int64_t blocks = static_cast<int64_t>(mats) * (rows / 128) * (cols / 128);
   if (blocks == 0) return cudaSuccess;
-  quantize_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+  MOE_LAUNCH_PDL(quantize_blocks_kernel, static_cast<unsigned>(blocks), 256, 0, s, 
       static_cast<const __nv_bfloat16 *>(w), rows, cols, static_cast<uint8_t *>(q), scales);
   return cudaGetLastError();
 }

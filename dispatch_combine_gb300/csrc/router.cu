@@ -80,6 +80,7 @@ __host__ __device__ inline int router_d_pad(int d) { return (d + 255) / 256 * 25
 
 __global__ void router_pad_kernel(const uint16_t *__restrict__ w_r, int d, int E,
                                   uint16_t *__restrict__ wp) {
+  pdl_begin();
   const int ep = router_e_pad(E);
   const int64_t n = static_cast<int64_t>(router_d_pad(d)) * ep;
   for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n;
@@ -116,6 +117,7 @@ template <int LT, int LE, int CE, int NT>
 __global__ void __launch_bounds__(NT, 1)
     router_logits_kernel(const __nv_bfloat16 *__restrict__ x, const uint16_t *__restrict__ wpad,
                          int T, int d, int E, float *__restrict__ logits) {
+  pdl_begin();
   using C = RtCfg<LT, LE, CE, NT>;
   constexpr int SW = C::SW;
   extern __shared__ __align__(16) uint8_t rsm_raw[];
@@ -309,6 +311,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
     router_logits_small_kernel(const __nv_bfloat16 *__restrict__ x,
                                const uint16_t *__restrict__ w_r, int T, int d, int E,
                                float *__restrict__ logits) {
+  pdl_begin();
   using C = SmallCfg<EP>;
   extern __shared__ __align__(16) uint8_t wsm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -434,7 +437,7 @@ cudaError_t run_logits_small(const void *x, const void *w_r, int T, int d, int E
   if (per_sm < 1) per_sm = 1;
   const int cap = num_sms() * per_sm;
   const int grid = want < cap ? want : cap;
-  kern<<<grid, kSmallWarps * 32, smem, s>>>(static_cast<const __nv_bfloat16 *>(x),
+  MOE_LAUNCH_PDL(kern, grid, kSmallWarps * 32, smem, s, static_cast<const __nv_bfloat16 *>(x),
                                             static_cast<const uint16_t *>(w_r), T, d, E, logits);
   return cudaGetLastError();
 }
@@ -448,7 +451,7 @@ cudaError_t run_logits(const void *x, const uint16_t *wpad, int T, int d, int E,
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
   dim3 grid((T + C::CT - 1) / C::CT, (E + CE - 1) / CE);
-  kern<<<grid, NT, C::SMEM, s>>>(static_cast<const __nv_bfloat16 *>(x), wpad, T, d, E, logits);
+  MOE_LAUNCH_PDL(kern, grid, NT, C::SMEM, s, static_cast<const __nv_bfloat16 *>(x), wpad, T, d, E, logits);
   return cudaGetLastError();
 }
 
@@ -504,6 +507,7 @@ __global__ void __launch_bounds__(kSelWarps * 32)
                          int E, int G, int topk_group, int k, int score, float bias_scale,
                          int mode, int32_t *__restrict__ ids, float *__restrict__ weights,
                          const int32_t *__restrict__ list, const int32_t *__restrict__ count) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
   if (list) {
@@ -632,6 +636,7 @@ __global__ void __launch_bounds__(kSelWarps * 32)
                               float bias_scale, int mode, int32_t *__restrict__ ids,
                               float *__restrict__ weights, const int32_t *__restrict__ list,
                               const int32_t *__restrict__ count) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
   if (list) {
@@ -752,6 +757,7 @@ __global__ void __launch_bounds__(256)
                           uint16_t *__restrict__ wt, int32_t *__restrict__ seg,
                           int32_t *__restrict__ mtile, int32_t *__restrict__ count,
                           float *__restrict__ zero, int64_t n_zero) {
+  pdl_begin();
   // 64 x 64 tile (d and E are multiples of 64), 16-byte loads and stores
   __shared__ __align__(16) uint16_t tile[64][72];
   const int e0 = blockIdx.x * 64, i0 = blockIdx.y * 64;
@@ -852,6 +858,7 @@ __global__ void __launch_bounds__(kScreenWarps * 32)
                          float bias_scale, int32_t *__restrict__ ids,
                          float *__restrict__ weights, int32_t *__restrict__ list,
                          int32_t *__restrict__ count) {
+  pdl_begin();
   __shared__ int32_t sh_id[32];
   __shared__ float sh_l[32];
   __shared__ int sh_ok;
@@ -1016,6 +1023,7 @@ __global__ void __launch_bounds__(256, 2)
     router_list_logits_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wt,
                               int d, int E, const int32_t *__restrict__ list,
                               const int32_t *__restrict__ count, float *__restrict__ logits) {
+  pdl_begin();
   constexpr int kListSlice = 8 * EPW;
   extern __shared__ uint4 sh_xl[];  // [kListTok][d / 8]
   const int n = *count;
@@ -1137,7 +1145,7 @@ cudaError_t launch_router_logits(const void *x, const void *w_r, int T, int d, i
   const int64_t want = (n + 255) / 256;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   uint16_t *wpad = static_cast<uint16_t *>(w_scratch);
-  router_pad_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, s>>>(
+  MOE_LAUNCH_PDL(router_pad_kernel, static_cast<unsigned>(want < cap ? want : cap), 256, 0, s, 
       static_cast<const uint16_t *>(w_r), d, E, wpad);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -1160,7 +1168,7 @@ cudaError_t select_impl(const float *logits, const float *bias, int T, int E, in
   if (per != 0) {
 #define MOE_SELECT_FAST(P)                                                                  \
   case P:                                                                                   \
-    router_select_fast_kernel<P><<<grid, kSelWarps * 32, 0, s>>>(                           \
+    MOE_LAUNCH_PDL(router_select_fast_kernel<P>, grid, kSelWarps * 32, 0, s,                            \
         logits, bias, T, E, G, topk_group, k, score, bias_scale, mode, ids, weights, list,  \
         count);                                                                             \
     return cudaGetLastError();
@@ -1176,7 +1184,7 @@ cudaError_t select_impl(const float *logits, const float *bias, int T, int E, in
     }
 #undef MOE_SELECT_FAST
   }
-  router_select_kernel<<<grid, kSelWarps * 32, 0, s>>>(logits, bias, T, E, G, topk_group, k,
+  MOE_LAUNCH_PDL(router_select_kernel, grid, kSelWarps * 32, 0, s, logits, bias, T, E, G, topk_group, k,
                                                        score, bias_scale, mode, ids, weights,
                                                        list, count);
   return cudaGetLastError();
@@ -1242,7 +1250,7 @@ cudaError_t launch_router(const void *x, const void *w_r, const float *bias, int
     ksplit = static_cast<int>(by_sms < by_k ? by_sms : by_k);
     if (ksplit < 1) ksplit = 1;
   }
-  router_tc_prep_kernel<<<dim3(E / 64, d / 64), 256, 0, s>>>(
+  MOE_LAUNCH_PDL(router_tc_prep_kernel, dim3(E / 64, d / 64), 256, 0, s, 
       static_cast<const uint16_t *>(w_r), d, E, T, wt, seg, mtile, count, logits,
       ksplit > 1 ? static_cast<int64_t>(T) * E : 0);
   cudaError_t err = cudaGetLastError();
@@ -1286,7 +1294,7 @@ cudaError_t launch_router(const void *x, const void *w_r, const float *bias, int
   switch (select_per(E, G)) {
 #define MOE_SCREEN(P)                                                                      \
   case P:                                                                                  \
-    router_screen_kernel<P><<<T, kScreenWarps * 32, xbytes, s>>>(logits, bias, xs, wt, T, d, E, G, \
+    MOE_LAUNCH_PDL(router_screen_kernel<P>, T, kScreenWarps * 32, xbytes, s, logits, bias, xs, wt, T, d, E, G, \
                                                             topk_group, k, score,          \
                                                             bias_scale, ids, weights, list, \
                                                             count);                        \
@@ -1315,7 +1323,7 @@ cudaError_t launch_router(const void *x, const void *w_r, const float *bias, int
                                static_cast<int>(lbytes));
     if (err != cudaSuccess) return err;
   }
-  list_kernel<<<static_cast<unsigned>(items < cap ? items : cap), 256, lbytes, s>>>(
+  MOE_LAUNCH_PDL(list_kernel, static_cast<unsigned>(items < cap ? items : cap), 256, lbytes, s, 
       xs, wt, d, E, list, count, logits);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
