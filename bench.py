@@ -457,27 +457,55 @@ def run_gpu(args, c):
     roof["traffic"] = measured_traffic(c.name, dominant)
     roof["peak_source"] = (f"{peak_src} ({'bf16 sustained' if roof['bound'] == 'tensor' else 'HBM copy'})")
 
-    # end to end through the C ABI with host buffers
+    # end to end through the C ABI with host buffers: every step copies its
+    # x from pinned host memory and reads its y back, on two copy streams
+    # with double-buffered device tensors, so step s+1's upload and step
+    # s-1's read-back overlap step s's layer; all copies lie inside the
+    # timed region
     e2e = None
     if args.e2e_steps > 0:
         x_host = t["x"].cpu().pin_memory()
-        y_host = torch.empty(c.T, c.d, dtype=torch.bfloat16).pin_memory()
-        x_dev = torch.empty_like(t["x"])
+        y_host = [torch.empty(c.T, c.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        x_dev = [torch.empty_like(t["x"]) for _ in range(2)]
+        y_dev = [torch.empty_like(y) for _ in range(2)]
+        h2d = torch.cuda.Stream(device)
+        d2h = torch.cuda.Stream(device)
+        ev_up = [torch.cuda.Event() for _ in range(2)]     # x_dev[b] filled
+        ev_done = [torch.cuda.Event() for _ in range(2)]   # layer on buffer b done
+        ev_back = [torch.cuda.Event() for _ in range(2)]   # y_dev[b] read back
+        for b in range(2):  # recorded once so that the first waits are no-ops
+            ev_done[b].record(stream)
+            ev_back[b].record(stream)
 
-        def e2e_step():
-            x_dev.copy_(x_host, non_blocking=True)
-            moe.moe_layer(shape, x_dev, t["w_r"], bias, t["w_gate_up"], t["w_down"], ws, y=y)
-            y_host.copy_(y, non_blocking=True)
+        def e2e_step(i):
+            b = i % 2
+            h2d.wait_event(ev_done[b])  # the layer of step i-2 has read x_dev[b]
+            with torch.cuda.stream(h2d):
+                x_dev[b].copy_(x_host, non_blocking=True)
+            ev_up[b].record(h2d)
+            stream.wait_event(ev_up[b])
+            stream.wait_event(ev_back[b])  # y_dev[b] of step i-2 is back on the host
+            moe.moe_layer(shape, x_dev[b], t["w_r"], bias, t["w_gate_up"], t["w_down"], ws,
+                          y=y_dev[b], stream=stream)
+            ev_done[b].record(stream)
+            d2h.wait_event(ev_done[b])
+            with torch.cuda.stream(d2h):
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+            ev_back[b].record(d2h)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        for i in range(max(2, args.warmup)):
+            e2e_step(i)
         torch.cuda.synchronize()
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        h2d.wait_event(e0)
+        d2h.wait_event(e0)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        for b in range(2):  # the region ends when the last read-backs are done
+            stream.wait_event(ev_back[b])
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
