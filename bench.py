@@ -162,7 +162,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -191,9 +191,10 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         t0 = getattr(self, "t_start", 0.0)
         t1 = getattr(self, "t_end", float("inf"))
-        inside = [ln for ts, ln in self.lines if t0 <= ts <= t1 + 0.25]
-        if not inside:  # region shorter than the sampling period
-            inside = [ln for _, ln in self.lines[-3:]]
+        inside = [ln for ts, ln in self.lines if t0 <= ts <= t1]
+        if not inside:  # region shorter than the sampling period: the nearest sample
+            near = min(self.lines, key=lambda tl: abs(tl[0] - 0.5 * (t0 + t1)), default=None)
+            inside = [near[1]] if near else []
         for ln in inside:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
@@ -650,7 +651,7 @@ def run_masked(args):
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", choices=sorted(CONFIGS), default=DEFAULT_CONFIG)
