@@ -156,6 +156,7 @@ def _screened_vs_fixed(shape, x, w_r, bias):
     (64, 7168, 256, 8, 4, 8, SCORE_SIGMOID_BIAS),
     (500, 512, 128, 1, 1, 4, SCORE_SOFTMAX),
     (33, 128, 1024, 32, 8, 32, SCORE_SIGMOID_BIAS),   # 32 experts per lane, k = 32
+    (700, 1024, 256, 8, 3, 6, SCORE_SOFTMAX),          # softmax with groups (margin on logits)
     (1, 64, 64, 2, 1, 1, SCORE_SIGMOID_BIAS),
     (4100, 2048, 192, 3, 2, 8, SCORE_SIGMOID_BIAS),   # 33 m-tiles, ragged last tile
 ])
@@ -232,3 +233,15 @@ def test_screened_route_full_size(name):
     # the fixed-order path itself is pinned to the oracle in
     # test_route_bit_exact_full_size; the screen sends a small share back
     assert 0 <= n_flag < cfg.T // 5
+
+
+def test_screened_count_is_minus_one_when_not_screened():
+    ensure_lib()
+    import moe_inputs
+    # E = 16 (not a multiple of 64): the fixed-order path
+    tns = moe_inputs.make_tensors_for_shape(64, 256, 16, 64, device="cuda", seed=2)
+    shape = dict(T=64, d=256, E=16, G=4, topk_group=2, k=2, inter=64,
+                 score=SCORE_SIGMOID_BIAS, bias_scale=0.15)
+    ws = moe.Workspace(moe.moe_workspace_size(shape))
+    moe.moe_route(shape, tns["x"], tns["w_r"], tns["bias"], ws)
+    assert moe.moe_route_screened_count(shape, ws) == -1
