@@ -669,10 +669,61 @@ def parse_args(argv=None):
                     help="time the masked expert FFN of a per-rank slice instead")
     ap.add_argument("--ref-step-s", type=float, default=4.0,
                     help="seconds of oracle work per step of --impl reference")
+    ap.add_argument("--route-only", action="store_true",
+                    help="time the router alone (screened and fixed-order; own line)")
     ap.add_argument("--ffn-rows", default=None, metavar="E,R",
                     help="time the expert FFN alone on E experts x R rows at the workload's "
                          "d and inter (bf16, or FP8 with --fp8; own line)")
     return ap.parse_args(argv)
+
+
+def run_route_only(args):
+    """The router alone on the workload's x and W_r (no expert weights on the
+    device): moe_route without logits (screened where the shape allows) and
+    with logits (the fixed-order path), each timed over the steps."""
+    import torch
+    import dispatch_combine_gb300 as moe
+    torch.cuda.set_device(0)
+    c = CONFIGS[args.config]
+    g = torch.Generator(device="cuda").manual_seed(0)
+    w_r = (torch.randn(c.d, c.E, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    bias = torch.randn(c.E, device="cuda", generator=g, dtype=torch.float32)
+    x = torch.randn(c.T, c.d, device="cuda", generator=g).to(torch.bfloat16)
+    shape = c.shape()
+    b = bias if c.score == SCORE_SIGMOID_BIAS else None
+    ws = moe.Workspace(moe.moe_workspace_size(shape))
+    ids = torch.empty(c.T, c.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(c.T, c.k, dtype=torch.float32, device="cuda")
+    lg = torch.empty(c.T, c.E, dtype=torch.float32, device="cuda")
+    out = {}
+    for label, logits in (("screened", None), ("fixed_order", lg)):
+        def step():
+            moe.moe_route(shape, x, w_r, b, ws, topk_ids=ids, topk_w=w, logits=logits)
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        out[label] = e0.elapsed_time(e1) * 1000.0 / args.steps
+        if logits is None:
+            out["flagged_tokens"] = moe.moe_route_screened_count(shape, ws)
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status error")
+    line = {
+        "metric": "router alone: us per call", "impl": "gb300", "value": out["screened"],
+        "unit": "us", "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(c)},
+        "fixed_order_us": out["fixed_order"], "flagged_tokens": out["flagged_tokens"],
+        "tokens_per_s": c.T / (out["screened"] * 1e-6),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def run_ffn_only(args):
@@ -899,6 +950,8 @@ def main(argv=None):
     c = CONFIGS[args.config]
     if args.ffn_rows:
         return run_ffn_only(args)
+    if args.route_only:
+        return run_route_only(args)
     if args.fp8:
         return run_fp8(args)
     if args.eplb:
