@@ -69,6 +69,7 @@ struct KArgs {
   int ksplit;   // 1-CTA down form: K pieces per tile, summed into a zeroed out (1: none)
   int m_block;  // m-tiles per rasterization block (A rows of a block stay in L2)
   int out_v8;   // output base 32-byte aligned: 32-byte stores
+  int out_tma;  // pair down form: fp32 output through the tmY tensor map (TMA stores)
   int64_t rows_total;
   const int32_t *seg;
   const int32_t *mtile_base;
@@ -384,7 +385,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // the B tile; the even CTA issues the pair MMAs (M=256, N=BN), which read A
 // and B from both CTAs' shared memory and leave rows 0-127 of the
 // accumulator in its TMEM and rows 128-255 in the peer's.  Per SM this halves
-// the B bytes per FLOP and, with 32 KB stages, gives a 6-stage ring.
+// the B bytes per FLOP and, with 32 KB stages, gives a 6-stage ring.  The
+// down form stores its fp32 output with TMA: an epilogue warp whose 32 rows
+// are all valid stages each 32-column chunk in a swizzled shared-memory box
+// and issues one tensor store, so the output leaves as whole 128-byte lines
+// instead of per-row sector writes (other warps store directly).
 //   full[s]       in the even CTA, completed by both CTAs' TMA bytes;
 //   empty[s]      in both CTAs, the pair MMA commit arrives on both;
 //   tmem_full[b]  in both CTAs, the pair MMA commit arrives on both;
@@ -399,13 +404,20 @@ struct Cfg2 {
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BN_OUT = SWIGLU ? BN / 2 : BN;
   static constexpr int HALF = BN / 2;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  // down: one 32-row x 32-column fp32 staging box per epilogue warp for the
+  // TMA stores of the output (128-byte swizzle, 1024-byte aligned)
+  static constexpr int OUT_OFF = STAGES * STAGE_BYTES;
+  static constexpr int OUT_BOX_BYTES = 32 * 32 * 4;
+  static constexpr int OUT_BYTES = SWIGLU ? 0 : 4 * OUT_BOX_BYTES;
+  static constexpr int BAR_OFF = OUT_OFF + OUT_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int MT_OFF = MISC_OFF + 16;
   static constexpr int SMEM_BYTES = MT_OFF + (kMaxE + 1) * 4 + 1024;
   static_assert(BN == 256 || BN == 128, "pair tile width");
   static_assert(STAGES >= 4, "pipeline depth");
+  static_assert(OUT_OFF % 1024 == 0, "swizzled staging alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 // An expert's last 256-row tile that holds at most 128 rows runs swapped
@@ -427,7 +439,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmX,
-                             const __grid_constant__ CUtensorMap tmW, const KArgs args) {
+                             const __grid_constant__ CUtensorMap tmW,
+                             const __grid_constant__ CUtensorMap tmY, const KArgs args) {
   pdl_begin();
   using C = Cfg2<BN, SWIGLU>;
   extern __shared__ uint8_t smem_raw[];
@@ -677,6 +690,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
+      } else if (!SWIGLU && args.out_tma && quad * 32 + static_cast<int>(rank) * 128 + 32 <=
+                                                     t.rows_valid &&
+                 grow - lane >= 0 && grow - lane + 32 <= args.rows_total) {
+        // every row of this warp's 32-row slab is valid: each 32-column
+        // chunk goes through the warp's staging box (row = lane, 16-byte
+        // pieces placed by the 128-byte swizzle) and leaves as one TMA store
+        const uint32_t box = smem_u32(smem + C::OUT_OFF + quad * C::OUT_BOX_BYTES);
+        const uint32_t rbase = box + static_cast<uint32_t>(lane) * 128u;
+        const int row_g = static_cast<int>(grow - lane);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + c * 32, v);
+          tmem_ld_wait();
+          tmem_regs_fence(v);
+          if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the box
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(rbase + static_cast<uint32_t>(((j ^ lane) & 7) * 16), v[4 * j],
+                         v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmY, smem + C::OUT_OFF + quad * C::OUT_BOX_BYTES, t.n * BN + c * 32,
+                         row_g);
+            bulk_commit();
+          }
+        }
       } else {
         float *dst = static_cast<float *>(args.out) + grow * args.ldo +
                      static_cast<int64_t>(t.n) * BN;
@@ -716,6 +758,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (!SWIGLU && lane == 0) bulk_wait_all();  // output stores written before exit
   }
 
   tc_fence_before();
@@ -1125,6 +1168,22 @@ bool make_tmap(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D fp32 tensor [rows, inner] row-major for TMA stores; box = 32 rows x 32
+// elements (128 bytes), 128-byte swizzle.  False if the base is not 16-byte
+// aligned or a row is not a multiple of 16 bytes.
+bool make_tmap_f32_out(CUtensorMap *map, void *base, uint64_t inner, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || (reinterpret_cast<uintptr_t>(base) & 15u) != 0 || inner % 4 != 0 || rows == 0)
+    return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2D e4m3 (byte) tensor [rows, inner]; box = box_rows x 128 bytes, 128-byte
 // swizzle, out-of-bounds rows read as zero.
 bool make_tmap_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
@@ -1157,7 +1216,7 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  F8Args fa;
+  F8Args fa = {};
   KArgs &a = fa.k;
   a.E = p.E;
   a.K = p.K;
@@ -1199,7 +1258,7 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  KArgs a;
+  KArgs a = {};
   a.E = p.E;
   a.K = p.K;
   a.n_tiles = p.n_out / C::BN_OUT;
@@ -1226,7 +1285,7 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
 template <int BN, bool SWIGLU>
 cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   using C = Cfg2<BN, SWIGLU>;
-  CUtensorMap tmA, tmB, tmX, tmW;
+  CUtensorMap tmA, tmB, tmX, tmW, tmY;
   const uint64_t w_rows = static_cast<uint64_t>(p.E) * static_cast<uint64_t>(p.b_rows);
   if (!make_tmap(&tmA, p.a, static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.rows_total),
                  128))
@@ -1243,11 +1302,15 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   } else {
     tmW = tmB;
   }
+  // down: fp32 output stored by TMA where its layout allows (else plain stores)
+  const bool out_tma = !SWIGLU && make_tmap_f32_out(&tmY, p.out, static_cast<uint64_t>(p.n_out),
+                                                    static_cast<uint64_t>(p.rows_total));
+  if (!out_tma) tmY = tmA;
   cudaError_t err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<BN, SWIGLU>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  KArgs a;
+  KArgs a = {};
   a.E = p.E;
   a.K = p.K;
   a.n_tiles = p.n_out / C::BN_OUT;
@@ -1260,6 +1323,7 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.out = p.out;
   a.ldo = p.n_out;
   a.rows_total = p.rows_total;
+  a.out_tma = out_tma ? 1 : 0;
   a.out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
   a.m_block = static_cast<int>((24ll << 20) / (512ll * p.K));
   if (a.m_block < 1) a.m_block = 1;
@@ -1286,7 +1350,7 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   }
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   MOE_LAUNCH_PDL(grouped_gemm_pair_kernel<BN, SWIGLU>, 2 * clusters, kGemmThreads, C::SMEM_BYTES, s, 
-      tmA, tmB, tmX, tmW, a);
+      tmA, tmB, tmX, tmW, tmY, a);
   return cudaGetLastError();
 }
 
