@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libmoe: argument validation, workspace layout and
 // the launch sequence of each entry point.  Nothing here allocates device
 // memory; every buffer is the caller's.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 
@@ -18,12 +19,12 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Workspace regions, in this order (each 256-byte aligned):
-//   status word | mtile_base [E+1] | dispatch chunk counts [chunks*E] |
+//   status word | split flags [kPairSplitFlagWords] | mtile_base [E+1] | dispatch chunk counts [chunks*E] |
 //   logits [T*E] f32 | padded router weight | h [h_rows*inter] bf16 |
 //   (layer only) ids [T*k] | w [T*k] | counts [E] | offsets [E+1] |
 //   dest [T*k] | src [T*k] | x_perm [T*k*d] bf16 | y_perm [T*k*d] f32
 struct Layout {
-  size_t status, mtile, doff, kept, ovf, chunk, logits, wr32, h, ids, w, counts, offsets, dest,
+  size_t status, flags, mtile, doff, kept, ovf, chunk, logits, wr32, h, ids, w, counts, offsets, dest,
       src, x_perm, y_perm;
   size_t end_route, end_dispatch, end_ffn, end_layer;
 };
@@ -37,6 +38,8 @@ Layout make_layout(const moe_shape_t &s, int64_t h_rows, int64_t perm_rows = -1)
   size_t off = 0;
   L.status = off;
   off = align_up(off + 4);
+  L.flags = off;
+  off = align_up(off + 4 * static_cast<size_t>(moe::kPairSplitFlagWords));
   L.mtile = off;
   off = align_up(off + 4 * static_cast<size_t>(s.E + 1));
   L.doff = off;  // expert offsets of the capacity dispatch
@@ -171,7 +174,7 @@ moe_status_t run_gate_up(const moe_shape_t *s, int32_t layout, const void *x_in,
 
 moe_status_t run_down(const moe_shape_t *s, int32_t layout, const void *h, const int32_t *seg,
                       int32_t M_max, int64_t rows, const int32_t *mtile, const void *w_down,
-                      float *y, uint32_t *status, cudaStream_t st) {
+                      float *y, uint32_t *status, uint32_t *split_flags, cudaStream_t st) {
   GemmProblem p;
   std::memset(&p, 0, sizeof p);
   p.E = s->E;
@@ -187,6 +190,7 @@ moe_status_t run_down(const moe_shape_t *s, int32_t layout, const void *h, const
   p.b_rows = s->d;
   p.out = y;
   p.status = status;
+  p.split_flags = split_flags;
   p.pair = use_pair(s, layout, M_max);
   return cuda_status(moe::launch_gemm_down(p, st));
 }
@@ -229,7 +233,9 @@ moe_status_t moe_expert_ffn_workspace_size(const moe_shape_t *shape, int32_t lay
 
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_ws(ws, ws_bytes, 4));
-  return cuda_status(cudaMemsetAsync(ws, 0, 4, stream));
+  // the status word and the split flags of the down GEMM (all zero at rest)
+  const size_t n = std::min(ws_bytes, kAlign + 4 * static_cast<size_t>(moe::kPairSplitFlagWords));
+  return cuda_status(cudaMemsetAsync(ws, 0, n, stream));
 }
 
 moe_status_t moe_get_device_status(void *ws, size_t ws_bytes, moe_stream_t stream,
@@ -346,7 +352,8 @@ moe_status_t moe_expert_ffn(const moe_shape_t *shape, int32_t layout, const void
                                             stream)));
   MOE_TRY(run_gate_up(shape, layout, x_in, seg, M_max, rows, mtile, w_gate_up, h, status,
                       stream));
-  return run_down(shape, layout, h, seg, M_max, rows, mtile, w_down, y_out, status, stream);
+  return run_down(shape, layout, h, seg, M_max, rows, mtile, w_down, y_out, status,
+                  at<uint32_t>(ws, L.flags), stream);
 }
 
 moe_status_t moe_expert_gate_up(const moe_shape_t *shape, int32_t layout, const void *x_in,
@@ -383,7 +390,8 @@ moe_status_t moe_expert_down(const moe_shape_t *shape, int32_t layout, const voi
   MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max,
                                             tile_rows_for(shape, layout, M_max), mtile, status,
                                             stream)));
-  return run_down(shape, layout, h_in, seg, M_max, rows, mtile, w_down, y_out, status, stream);
+  return run_down(shape, layout, h_in, seg, M_max, rows, mtile, w_down, y_out, status,
+                  at<uint32_t>(ws, L.flags), stream);
 }
 
 moe_status_t moe_combine(const moe_shape_t *shape, const float *y_perm, const int32_t *dest,
@@ -444,7 +452,7 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
                       status, stream));
   MOE_TRY(mark(3));
   MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, offsets, 0, n, mtile, w_down, y_perm, status,
-                   stream));
+                   at<uint32_t>(ws, L.flags), stream));
   MOE_TRY(mark(4));
   MOE_TRY(cuda_status(moe::launch_combine(y_perm, n, dest, w, s.T, s.k, s.d, y, stream)));
   return mark(5);
@@ -754,7 +762,7 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
     MOE_TRY(run_gate_up(shape, MOE_LAYOUT_MASKED, x_rows, kp, capacity, pad, mtile, w_gate_up,
                         h, status, stream));
     MOE_TRY(run_down(shape, MOE_LAYOUT_MASKED, h, kp, capacity, pad, mtile, w_down, y_rows,
-                     status, stream));
+                     status, at<uint32_t>(ws, L.flags), stream));
   }
   // second round: the overflow rows, contiguous with offsets ovf_offsets
   if (overflow == MOE_OVERFLOW_SECOND_ROUND) {
@@ -764,7 +772,7 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
     MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_rows + pad * s.d * 2, ovf, 0, n, mtile,
                         w_gate_up, h, status, stream));
     MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, ovf, 0, n, mtile, w_down,
-                     y_rows + pad * s.d, status, stream));
+                     y_rows + pad * s.d, status, at<uint32_t>(ws, L.flags), stream));
   }
   return cuda_status(moe::launch_combine(y_rows, pad + n, dest, w, s.T, s.k, s.d, y, stream));
 }

@@ -100,6 +100,9 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
                "f"(b), "f"(c), "f"(d)
                : "memory");
 }
+__device__ __forceinline__ void red_add_f32(float *p, float a) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
+}
 // 32-byte global stores (one whole sector per lane); p must be 32-byte aligned
 __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8]) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
@@ -170,6 +173,37 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         set_status(status, kStatusTimeout);
         return false;
       }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// flags in global memory between CTAs of one grid
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Bounded wait until *flag != 0 (acquire).  Gives up when *abort is set or
+// limit_ns elapse; in the latter case it sets *abort and records
+// MOE_ERR_TIMEOUT.  Returns true when the flag was seen set.
+__device__ __forceinline__ bool flag_wait_bounded(const uint32_t *flag, volatile int *abort,
+                                                  uint32_t *status, uint64_t limit_ns) {
+  if (ld_acquire_gpu(flag) != 0) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(flag) != 0) return true;
+    if (*abort) return false;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      set_status(status, kStatusTimeout);
+      return false;
     }
   }
 }

@@ -70,6 +70,7 @@ struct KArgs {
   int m_block;  // m-tiles per rasterization block (A rows of a block stay in L2)
   int out_v8;   // output base 32-byte aligned: 32-byte stores
   int out_tma;  // pair down form: fp32 output through the tmY tensor map (TMA stores)
+  uint32_t *split_flags;  // pair down form: flags of the split last wave (nullptr: no split)
   int64_t rows_total;
   const int32_t *seg;
   const int32_t *mtile_base;
@@ -434,6 +435,35 @@ __device__ __forceinline__ int pair_swap_n(const Tile &t) {
   return (t.rows_valid <= 2 * kSwapBoxRows) ? ((t.rows_valid + 15) & ~15) : 0;
 }
 
+// One work item of a CTA pair: a whole tile, or (split last wave of the down
+// form) one K half of a tile.  Items n_full + j, j < 2 * rem, are half
+// j / rem of tile n_full + j % rem; pair c takes items c, c + ncl, ..., so
+// the two halves of a tile run at the same time on pairs j and j + rem.
+struct PairWork {
+  int u;         // tile index
+  int kb0, kb1;  // k-blocks [kb0, kb1)
+  int piece;     // -1 whole tile, 0 first half (adds), 1 second half (stores)
+  int slot;      // split tile j % rem (flag index / 8)
+};
+__device__ __forceinline__ PairWork pair_work(int w, int n_full, int rem, int kblocks) {
+  PairWork pw;
+  if (w < n_full) {
+    pw.u = w;
+    pw.kb0 = 0;
+    pw.kb1 = kblocks;
+    pw.piece = -1;
+    pw.slot = 0;
+  } else {
+    const int j = w - n_full;
+    pw.slot = j % rem;
+    pw.piece = j / rem;
+    pw.u = n_full + pw.slot;
+    pw.kb0 = pw.piece ? kblocks / 2 : 0;
+    pw.kb1 = pw.piece ? kblocks : kblocks / 2;
+  }
+  return pw;
+}
+
 template <int BN, bool SWIGLU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -481,14 +511,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   }
   cluster_sync_all();  // both CTAs' barriers exist before any remote use
   const int total = mt[args.E] * args.n_tiles;
-  if (cid >= total) return;  // uniform across the pair
+  const int kblocks = args.K / kBK;
+  // split of a short last wave (down form): the last rem tiles as K halves
+  int n_full = total, rem = 0;
+  if (!SWIGLU && args.split_flags != nullptr && kblocks >= 2) {
+    const int r = total % ncl;
+    if (r > 0 && 2 * r <= ncl && r <= kPairSplitSlots && total / ncl <= kPairSplitMaxWaves) {
+      n_full = total - r;
+      rem = r;
+    }
+  }
+  const int items = n_full + 2 * rem;
+  if (cid >= items) return;  // uniform across the pair
 
   if (warp == 1) tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int kblocks = args.K / kBK;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -503,8 +543,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; s < C::STAGES; ++s) issued[s] = false;
       tma_prefetch_desc(&tmX);
       if (SWIGLU) tma_prefetch_desc(&tmW);
-      for (int u = cid; u < total && !*abort_flag; u += ncl) {
-        const Tile t = decode_tile<256>(args, mt, u);
+      for (int w = cid; w < items && !*abort_flag; w += ncl) {
+        const PairWork pw = pair_work(w, n_full, rem, kblocks);
+        const Tile t = decode_tile<256>(args, mt, pw.u);
         const int sn = (BN == 256) ? pair_swap_n(t) : 0;
         const int a_row = t.row0 + 128 * static_cast<int>(rank);
         int b_row;
@@ -517,7 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         const int x_row = t.row0 + static_cast<int>(rank) * (sn >> 1);
         const int w_grp = (t.e * args.b_rows + t.n * C::BN_OUT + static_cast<int>(rank) * 64) >> 4;
         const uint32_t tx = sn ? 2u * (C::A_BYTES + kSwapXBytes) : 2u * C::STAGE_BYTES;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = pw.kb0; kb < pw.kb1; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
                                  args.wait_limit_ns))
             break;
@@ -561,8 +602,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool any_mma = false;
-      for (int u = cid; u < total && !*abort_flag; u += ncl) {
-        const int sn = (BN == 256) ? pair_swap_n(decode_tile<256>(args, mt, u)) : 0;
+      for (int w = cid; w < items && !*abort_flag; w += ncl) {
+        const PairWork pw = pair_work(w, n_full, rem, kblocks);
+        const int sn = (BN == 256) ? pair_swap_n(decode_tile<256>(args, mt, pw.u)) : 0;
         // swapped: the A slots hold weight rows (M) and the B slots token rows (N)
         const uint32_t idesc = sn ? mma_idesc_bf16_f32(256, sn) : kIdesc;
         if (!mbar_wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, args.status,
@@ -571,7 +613,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = pw.kb0; kb < pw.kb1; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.status,
                                  args.wait_limit_ns)) {
             ok = false;
@@ -583,7 +625,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             mma_bf16_ss_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
-                             (kb | kk) != 0 ? 1u : 0u);
+                             (kb != pw.kb0 || kk != 0) ? 1u : 0u);
           any_mma = true;
           mma_commit_pair(&empty[stage], 0x3);
           if (++stage == C::STAGES) {
@@ -610,12 +652,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const uint32_t empty_even = mapa_shared(&tmem_empty[0], 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = cid; u < total; u += ncl) {
-      const Tile t = decode_tile<256>(args, mt, u);
+    for (int w = cid; w < items; w += ncl) {
+      const PairWork pw = pair_work(w, n_full, rem, kblocks);
+      const Tile t = decode_tile<256>(args, mt, pw.u);
       const bool waited = mbar_wait_bounded(&tmem_full[acc], acc_phase, abort_flag,
                                             args.status, args.wait_limit_ns);
       if (!__all_sync(0xffffffffu, waited)) break;
       tc_fence_after();
+      // split tile: this warp's 32-row slab has one flag; the first K half
+      // adds onto the second half's stored sums once the flag is up
+      const bool add = !SWIGLU && pw.piece == 0;
+      uint32_t *flag = (!SWIGLU && pw.piece >= 0)
+                           ? args.split_flags + pw.slot * 8 + static_cast<int>(rank) * 4 + quad
+                           : nullptr;
+      if (add) {
+        bool up = true;
+        if (lane == 0) up = flag_wait_bounded(flag, abort_flag, args.status, args.wait_limit_ns);
+        if (!__shfl_sync(0xffffffffu, up ? 1 : 0, 0)) break;
+        (void)ld_acquire_gpu(flag);  // every lane acquires the stored sums
+        __syncwarp();
+        if (lane == 0) *flag = 0;  // cleared for the next launch
+      }
       const uint32_t tb =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
       const int64_t grow = static_cast<int64_t>(t.row0) + prow;
@@ -647,7 +704,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
               }
             } else if (rok) {
               const int col = t.n * BN + static_cast<int>(rank) * 128 + quad * 32 + lane;
-              static_cast<float *>(args.out)[gr * args.ldo + col] = __uint_as_float(v[i]);
+              float *o = static_cast<float *>(args.out) + gr * args.ldo + col;
+              if (add)
+                red_add_f32(o, __uint_as_float(v[i]));
+              else
+                *o = __uint_as_float(v[i]);
             }
           }
         }
@@ -690,7 +751,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
-      } else if (!SWIGLU && args.out_tma && quad * 32 + static_cast<int>(rank) * 128 + 32 <=
+      } else if (!SWIGLU && pw.piece < 0 && args.out_tma &&
+                 quad * 32 + static_cast<int>(rank) * 128 + 32 <=
                                                      t.rows_valid &&
                  grow - lane >= 0 && grow - lane + 32 <= args.rows_total) {
         // every row of this warp's 32-row slab is valid: each 32-column
@@ -729,7 +791,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           tmem_ld_wait();
           tmem_regs_fence(v);
           if (ok) {
-            if (args.out_v8) {
+            if (add) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                red_add_v4(dst + c * 32 + 4 * i, __uint_as_float(v[4 * i]),
+                           __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                           __uint_as_float(v[4 * i + 3]));
+            } else if (args.out_v8) {
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 uint32_t w8[8];
@@ -746,6 +814,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
+      }
+      if (flag != nullptr && !add) {
+        // second K half: its sums are stored; raise the slab's flag
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(flag, 1u);
       }
       tc_fence_before();
       __syncwarp();
@@ -1324,6 +1398,7 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.ldo = p.n_out;
   a.rows_total = p.rows_total;
   a.out_tma = out_tma ? 1 : 0;
+  a.split_flags = SWIGLU ? nullptr : p.split_flags;
   a.out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
   a.m_block = static_cast<int>((24ll << 20) / (512ll * p.K));
   if (a.m_block < 1) a.m_block = 1;

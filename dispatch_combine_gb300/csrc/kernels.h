@@ -87,6 +87,16 @@ cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, i
 constexpr int64_t kPairRowsPerExpert = 256;
 // rows of a 1-CTA GEMM tile (the unit mtile_base counts when pair is false)
 constexpr int kGemmTileRows = 128;
+// The CTA-pair down GEMM splits the tiles of its last, partial wave into two
+// K halves on two pairs when the whole launch is at most kPairSplitMaxWaves
+// waves and the halves fit in one wave: the pair with the second half
+// stores its partial sums and raises one flag per 32-row slab, the pair
+// with the first half waits for the flag (bounded) and adds its sums with
+// fp32 reductions (one add per element, so the result does not depend on
+// timing), then clears the flag.  Flags: kPairSplitSlots tiles x 8 slabs.
+constexpr int kPairSplitMaxWaves = 16;
+constexpr int kPairSplitSlots = 512;
+constexpr int kPairSplitFlagWords = kPairSplitSlots * 8;
 
 // quant.cu: e4m3 codes with fp32 scales, per (row, 128 columns) of [rows,
 // cols] bf16, or per 128 x 128 block of [mats, rows, cols] bf16
@@ -119,6 +129,9 @@ struct GemmProblem {
   bool pair;  // 256-row tiles on CTA pairs (mtile_base counts 256-row tiles)
   int bn;     // 1-CTA down form: output tile width 64, 128 or 256 (0: widest dividing n_out)
   int ksplit; // 1-CTA down form: K pieces per tile added into out, which must hold zeros (0, 1: none)
+  // pair down form: kPairSplitFlagWords zeroed words; with them a short
+  // last wave runs its tiles as two K halves (nullptr: never split)
+  uint32_t *split_flags;
 };
 cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s);
 cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s);

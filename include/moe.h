@@ -101,7 +101,10 @@ moe_status_t moe_workspace_size(const moe_shape_t *shape, size_t *bytes);
 moe_status_t moe_expert_ffn_workspace_size(const moe_shape_t *shape, int32_t layout,
                                            int32_t M_max, size_t *bytes);
 
-/* Clears the device status word at the start of a fresh workspace (async). */
+/* Prepares a fresh workspace (async): clears the device status word and the
+ * flags the expert FFN's down GEMM uses between CTAs (zero at rest, and left
+ * zero by every call that completes).  Call once before the workspace's first
+ * use. */
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronises `stream`, returns the OR of device-side errors recorded in the

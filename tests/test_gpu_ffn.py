@@ -79,9 +79,9 @@ def test_ffn_contiguous(counts, d, inter):
     ([1, 16, 600, 900], 256, 384),  # experts made of one swapped tile
     ([700, 300], 4096, 1024),       # long K
     # down: 15 m-tiles x 16 n-tiles = 240 tiles on 76 pairs, the last 12
-    # (swapped tails among them) split in 4 pieces of 64 columns
+    # (swapped tails among them) run as two K halves on two pairs
     ([520, 520, 520, 520, 530], 4096, 256),
-    # 192 tiles: a last wave of 40 tiles, not split
+    # 192 tiles: a last wave of 40 tiles, not split (80 halves > 76 pairs)
     ([2000, 1000], 4096, 256),
 ])
 def test_ffn_pair_tiles(counts, d, inter):
@@ -186,3 +186,31 @@ def test_ffn_all_experts_empty_writes_nothing():
                        w_down.cuda(), ws, y_out=y)
     assert moe.moe_get_device_status(ws) == 0
     assert torch.all(y == 7.0)
+
+
+@pytest.mark.parametrize("counts,d,inter", [
+    ([300], 512, 256),             # 4 down tiles, all split (2 of them swapped tails)
+    ([600, 260, 1], 1024, 512),    # 6 m-tiles x 4 n-tiles, all split (3 swapped tails)
+    ([520, 520, 520, 520, 530], 4096, 256),  # 240 tiles, the last 12 split
+])
+def test_ffn_pair_split_last_wave(counts, d, inter):
+    """A short down GEMM runs its last wave as two K halves on two CTA pairs
+    (one stores, the other adds after a flag): the result matches the
+    oracle, is bit-identical from call to call, and the flags are left
+    clear for the next call."""
+    ensure_lib()
+    E = len(counts)
+    w_gu, w_down = _weights(E, d, inter, seed=d + 5 * inter)
+    x, offsets, row_e = _contiguous_case(counts, d, inter, seed=d + 11)
+    shape = _shape(E, d, inter, T=x.shape[0], k=1)
+    ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    args = (shape, moe.MOE_LAYOUT_CONTIGUOUS, x.cuda(), offsets.cuda(), 0, w_gu.cuda(),
+            w_down.cuda(), ws)
+    y1 = moe.moe_expert_ffn(*args)
+    y2 = moe.moe_expert_ffn(*args)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32)), "split sums not reproducible"
+    flags = ws.buf[ws.offset + 256: ws.offset + 256 + 4 * 4096]
+    assert int(flags.count_nonzero()) == 0, "split flags left set"
+    check_ffn(y1.cpu().numpy(), bits(x), row_e, bits(w_gu), bits(w_down), "y (split)")
