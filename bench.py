@@ -294,7 +294,10 @@ def run_reference(args, c):
     from moe_inputs import make_layer_tensors
     t = make_layer_tensors(c, device="cpu", seed=0)
     host = host_inputs(t)
-    n = oracle_sample_size(c, host, args.ref_step_s)
+    # each step a bounded token sample; the whole run stays within
+    # --ref-total-s however many steps are asked for (at least one token a step)
+    per_step_s = min(args.ref_step_s, args.ref_total_s / max(args.steps, 1))
+    n = oracle_sample_size(c, host, per_step_s)
     for w in range(args.warmup):  # untimed warm-up steps (one token each)
         time_oracle(c, host, 1, seed=1000 + w)
     total_s, total_tok = 0.0, 0
@@ -668,7 +671,10 @@ def parse_args(argv=None):
     ap.add_argument("--masked", choices=["ep", "tp"], default=None,
                     help="time the masked expert FFN of a per-rank slice instead")
     ap.add_argument("--ref-step-s", type=float, default=4.0,
-                    help="seconds of oracle work per step of --impl reference")
+                    help="seconds of oracle work per step of --impl reference at most")
+    ap.add_argument("--ref-total-s", type=float, default=120.0,
+                    help="seconds of oracle work over all steps of --impl reference (about; "
+                         "each step runs at least one token)")
     ap.add_argument("--route-only", action="store_true",
                     help="time the router alone (screened and fixed-order; own line)")
     ap.add_argument("--ffn-rows", default=None, metavar="E,R",

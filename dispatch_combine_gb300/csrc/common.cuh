@@ -189,16 +189,17 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
 __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// Bounded wait until *flag != 0 (acquire).  Gives up when *abort is set or
-// limit_ns elapse; in the latter case it sets *abort and records
-// MOE_ERR_TIMEOUT.  Returns true when the flag was seen set.
-__device__ __forceinline__ bool flag_wait_bounded(const uint32_t *flag, volatile int *abort,
-                                                  uint32_t *status, uint64_t limit_ns) {
-  if (ld_acquire_gpu(flag) != 0) return true;
+// Bounded wait until *flag == value (acquire).  Gives up when *abort is set
+// or limit_ns elapse; in the latter case it sets *abort and records
+// MOE_ERR_TIMEOUT.  Returns true when the flag was seen at value.
+__device__ __forceinline__ bool flag_wait_bounded(const uint32_t *flag, uint32_t value,
+                                                  volatile int *abort, uint32_t *status,
+                                                  uint64_t limit_ns) {
+  if (ld_acquire_gpu(flag) == value) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     __nanosleep(64);
-    if (ld_acquire_gpu(flag) != 0) return true;
+    if (ld_acquire_gpu(flag) == value) return true;
     if (*abort) return false;
     if ((it & 15u) == 15u && globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;

@@ -23,6 +23,7 @@
 //
 // Every wait is bounded (MOE_ERR_TIMEOUT in the status word, then the CTA
 // drains its in-flight copies and MMAs, frees TMEM and returns).
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -71,6 +72,7 @@ struct KArgs {
   int out_v8;   // output base 32-byte aligned: 32-byte stores
   int out_tma;  // pair down form: fp32 output through the tmY tensor map (TMA stores)
   uint32_t *split_flags;  // pair down form: flags of the split last wave (nullptr: no split)
+  uint32_t split_epoch;   // nonzero value this launch raises the flags to
   int64_t rows_total;
   const int32_t *seg;
   const int32_t *mtile_base;
@@ -667,7 +669,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                            : nullptr;
       if (add) {
         bool up = true;
-        if (lane == 0) up = flag_wait_bounded(flag, abort_flag, args.status, args.wait_limit_ns);
+        if (lane == 0)
+          up = flag_wait_bounded(flag, args.split_epoch, abort_flag, args.status,
+                                 args.wait_limit_ns);
         if (!__shfl_sync(0xffffffffu, up ? 1 : 0, 0)) break;
         (void)ld_acquire_gpu(flag);  // every lane acquires the stored sums
         __syncwarp();
@@ -819,7 +823,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         // second K half: its sums are stored; raise the slab's flag
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_gpu(flag, 1u);
+        if (lane == 0) st_release_gpu(flag, args.split_epoch);
       }
       tc_fence_before();
       __syncwarp();
@@ -1399,6 +1403,14 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.rows_total = p.rows_total;
   a.out_tma = out_tma ? 1 : 0;
   a.split_flags = SWIGLU ? nullptr : p.split_flags;
+  {
+    // a different value per launch, so that a flag left raised by an aborted
+    // launch, or never cleared, is not taken for this launch's
+    static std::atomic<uint32_t> epoch{0};
+    uint32_t e = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    if (e == 0) e = epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    a.split_epoch = e;
+  }
   a.out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
   a.m_block = static_cast<int>((24ll << 20) / (512ll * p.K));
   if (a.m_block < 1) a.m_block = 1;

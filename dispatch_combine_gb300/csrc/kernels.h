@@ -90,10 +90,12 @@ constexpr int kGemmTileRows = 128;
 // The CTA-pair down GEMM splits the tiles of its last, partial wave into two
 // K halves on two pairs when the whole launch is at most kPairSplitMaxWaves
 // waves and the halves fit in one wave: the pair with the second half
-// stores its partial sums and raises one flag per 32-row slab, the pair
-// with the first half waits for the flag (bounded) and adds its sums with
-// fp32 reductions (one add per element, so the result does not depend on
-// timing), then clears the flag.  Flags: kPairSplitSlots tiles x 8 slabs.
+// stores its partial sums and raises one flag per 32-row slab to a value
+// that differs from launch to launch, the pair with the first half waits for
+// that value (bounded) and adds its sums with fp32 reductions (one add per
+// element, so the result does not depend on timing), then clears the flag.
+// The halves run at the same time on a grid whose pairs are all resident.
+// Flags: kPairSplitSlots tiles x 8 slabs.
 constexpr int kPairSplitMaxWaves = 16;
 constexpr int kPairSplitSlots = 512;
 constexpr int kPairSplitFlagWords = kPairSplitSlots * 8;
