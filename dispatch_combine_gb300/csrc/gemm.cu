@@ -432,9 +432,17 @@ struct Cfg2 {
 // [16 gate rows, the 16 matching up rows] (a 4-D tensor map), so a warp's
 // 32 TMEM lanes hold both factors of 16 intermediate columns.
 constexpr int kSwapBoxRows = 64;
-constexpr int kSwapXBytes = kSwapBoxRows * kBK * 2;
 __device__ __forceinline__ int pair_swap_n(const Tile &t) {
   return (t.rows_valid <= 2 * kSwapBoxRows) ? ((t.rows_valid + 15) & ~15) : 0;
+}
+// A swapped tail is paced by its loads, so each CTA loads only the token
+// rows it needs: boxes of 8, 16, 32 or 64 rows (the smallest >= N / 2).
+struct SwapXMaps {
+  CUtensorMap m[4];  // box rows 8, 16, 32, 64
+};
+__device__ __forceinline__ int swap_box_index(int sn) {
+  const int half = sn >> 1;
+  return half <= 8 ? 0 : half <= 16 ? 1 : half <= 32 ? 2 : 3;
 }
 
 // One work item of a CTA pair: a whole tile, or (split last wave of the down
@@ -470,7 +478,7 @@ template <int BN, bool SWIGLU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmX,
+                             const __grid_constant__ SwapXMaps tmX,
                              const __grid_constant__ CUtensorMap tmW,
                              const __grid_constant__ CUtensorMap tmY, const KArgs args) {
   pdl_begin();
@@ -543,7 +551,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       bool issued[C::STAGES];
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) issued[s] = false;
-      tma_prefetch_desc(&tmX);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tma_prefetch_desc(&tmX.m[i]);
       if (SWIGLU) tma_prefetch_desc(&tmW);
       for (int w = cid; w < items && !*abort_flag; w += ncl) {
         const PairWork pw = pair_work(w, n_full, rem, kblocks);
@@ -559,7 +568,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         // index in the 4-D weight map
         const int x_row = t.row0 + static_cast<int>(rank) * (sn >> 1);
         const int w_grp = (t.e * args.b_rows + t.n * C::BN_OUT + static_cast<int>(rank) * 64) >> 4;
-        const uint32_t tx = sn ? 2u * (C::A_BYTES + kSwapXBytes) : 2u * C::STAGE_BYTES;
+        const int xbox = sn ? swap_box_index(sn) : 0;
+        const uint32_t tx =
+            sn ? 2u * (C::A_BYTES + (8u << xbox) * kBK * 2u) : 2u * C::STAGE_BYTES;
         for (int kb = pw.kb0; kb < pw.kb1; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
                                  args.wait_limit_ns))
@@ -574,7 +585,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
               tma_load_4d_pair(smA + stage * C::A_BYTES, &tmW, fbar, kb * kBK, 0, 0, w_grp);
             else
               tma_load_2d_pair(smA + stage * C::A_BYTES, &tmB, fbar, kb * kBK, b_row);
-            tma_load_2d_pair(smB + stage * C::B_BYTES, &tmX, fbar, kb * kBK, x_row);
+            tma_load_2d_pair(smB + stage * C::B_BYTES, &tmX.m[xbox], fbar, kb * kBK, x_row);
           }
           issued[stage] = true;
           issued_phase[stage] = phase;
@@ -1363,16 +1374,18 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
 template <int BN, bool SWIGLU>
 cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   using C = Cfg2<BN, SWIGLU>;
-  CUtensorMap tmA, tmB, tmX, tmW, tmY;
+  CUtensorMap tmA, tmB, tmW, tmY;
+  SwapXMaps tmX;
   const uint64_t w_rows = static_cast<uint64_t>(p.E) * static_cast<uint64_t>(p.b_rows);
   if (!make_tmap(&tmA, p.a, static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.rows_total),
                  128))
     return cudaErrorInvalidValue;
   if (!make_tmap(&tmB, p.b, static_cast<uint64_t>(p.K), w_rows, C::HALF))
     return cudaErrorInvalidValue;
-  if (!make_tmap(&tmX, p.a, static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.rows_total),
-                 kSwapBoxRows))
-    return cudaErrorInvalidValue;
+  for (int i = 0; i < 4; ++i)
+    if (!make_tmap(&tmX.m[i], p.a, static_cast<uint64_t>(p.K),
+                   static_cast<uint64_t>(p.rows_total), 8u << i))
+      return cudaErrorInvalidValue;
   if (SWIGLU) {
     if (!make_tmap_gate_up_groups(&tmW, p.b, static_cast<uint64_t>(p.K), w_rows,
                                   static_cast<uint64_t>(up_off)))
