@@ -467,7 +467,8 @@ def run_gpu(args, c):
     # s-1's read-back overlap step s's layer; all copies lie inside the
     # timed region
     e2e = None
-    if args.e2e_steps > 0:
+    e2e_steps = args.steps if args.e2e_steps is None else args.e2e_steps
+    if e2e_steps > 0:
         x_host = t["x"].cpu().pin_memory()
         y_host = [torch.empty(c.T, c.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
         x_dev = [torch.empty_like(t["x"]) for _ in range(2)]
@@ -506,7 +507,7 @@ def run_gpu(args, c):
         e0.record(stream)
         h2d.wait_event(e0)
         d2h.wait_event(e0)
-        for i in range(args.e2e_steps):
+        for i in range(e2e_steps):
             e2e_step(i)
         for b in range(2):  # the region ends when the last read-backs are done
             stream.wait_event(ev_back[b])
@@ -514,9 +515,9 @@ def run_gpu(args, c):
         torch.cuda.synchronize()
         barrier(world)
         ms = max_over_ranks(e0.elapsed_time(e1), world, device)
-        e2e = {"value": job_value(c.T, world, ms / 1000.0, args.e2e_steps), "unit": UNIT,
+        e2e = {"value": job_value(c.T, world, ms / 1000.0, e2e_steps), "unit": UNIT,
                "h2d_bytes_per_step": c.T * c.d * 2, "d2h_bytes_per_step": c.T * c.d * 2,
-               "steps": args.e2e_steps}
+               "steps": e2e_steps}
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_sample_s > 0:
@@ -658,7 +659,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", choices=sorted(CONFIGS), default=DEFAULT_CONFIG)
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="timed steps of the end-to-end measurement (default: --steps, so both "
+                         "reach the same clocks; 0 = skip)")
     ap.add_argument("--cpu-sample-s", type=float, default=15.0,
                     help="seconds of CPU oracle work for cpu_baseline (0 = skip)")
     ap.add_argument("--fp8", action="store_true",
