@@ -672,8 +672,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                             args.status, args.wait_limit_ns);
       if (!__all_sync(0xffffffffu, waited)) break;
       tc_fence_after();
-      // split tile: this warp's 32-row slab has one flag; the first K half
-      // adds onto the second half's stored sums once the flag is up
+      // split tile: this warp's part of the tile (its 32 TMEM lanes) has one
+      // flag; the first K half adds onto the second half's stored sums once
+      // the flag is up (always the last item of both pairs)
       const bool add = !SWIGLU && pw.piece == 0;
       uint32_t *flag = (!SWIGLU && pw.piece >= 0)
                            ? args.split_flags + pw.slot * 8 + static_cast<int>(rank) * 4 + quad
