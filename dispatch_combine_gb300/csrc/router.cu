@@ -812,35 +812,34 @@ __device__ __forceinline__ float butterfly_sum(float v) {
 }
 
 // Fixed-order dot product of a bf16 row pair of nch 8-element chunks (x in
-// shared memory): lane l sums chunks l, l+32, ... in increasing order (loads
-// four chunks ahead), then the xor butterfly.
+// shared memory): lane l sums chunks l, l+32, ... in increasing order, then
+// the xor butterfly.  The weight chunks are loaded eight (then four) ahead;
+// the x chunks come from shared memory when they are used.
+template <int U>
+__device__ __forceinline__ void canon_block(const uint4 *xr, const uint4 *__restrict__ wr, int c,
+                                            float &acc) {
+  uint4 wv[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) wv[u] = __ldg(wr + c + 32 * u);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    float xf[8], wf[8];
+    bf16x8_to_f32(xr[c + 32 * u], xf);
+    bf16x8_to_f32(wv[u], wf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = __fmaf_rn(xf[i], wf[i], acc);
+  }
+}
 __device__ __forceinline__ float canon_dot(const uint4 *xr, const uint4 *__restrict__ wr,
                                            int nch, int lane) {
   float acc = 0.0f;
   int c = lane;
-  for (; c + 96 < nch; c += 128) {
-    uint4 xv[4], wv[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      xv[u] = xr[c + 32 * u];
-      wv[u] = __ldg(wr + c + 32 * u);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float xf[8], wf[8];
-      bf16x8_to_f32(xv[u], xf);
-      bf16x8_to_f32(wv[u], wf);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc = __fmaf_rn(xf[i], wf[i], acc);
-    }
+  for (; c + 32 * 7 < nch; c += 32 * 8) canon_block<8>(xr, wr, c, acc);
+  if (c + 32 * 3 < nch) {
+    canon_block<4>(xr, wr, c, acc);
+    c += 32 * 4;
   }
-  for (; c < nch; c += 32) {
-    float xf[8], wf[8];
-    bf16x8_to_f32(xr[c], xf);
-    bf16x8_to_f32(__ldg(wr + c), wf);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc = __fmaf_rn(xf[i], wf[i], acc);
-  }
+  for (; c < nch; c += 32) canon_block<1>(xr, wr, c, acc);
   return butterfly_sum(acc);
 }
 
