@@ -678,6 +678,8 @@ def parse_args(argv=None):
     ap.add_argument("--ref-total-s", type=float, default=120.0,
                     help="seconds of oracle work over all steps of --impl reference (about; "
                          "each step runs at least one token)")
+    ap.add_argument("--stage-only", choices=["dispatch", "combine"], default=None,
+                    help="time one bandwidth stage alone on seeded ids (own line)")
     ap.add_argument("--route-only", action="store_true",
                     help="time the router alone (screened and fixed-order; own line)")
     ap.add_argument("--ffn-rows", default=None, metavar="E,R",
@@ -730,6 +732,66 @@ def run_route_only(args):
         "config": {"workload": workload_desc(c)},
         "fixed_order_us": out["fixed_order"], "flagged_tokens": out["flagged_tokens"],
         "tokens_per_s": c.T / (out["screened"] * 1e-6),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_stage_only(args):
+    """One bandwidth stage alone at the workload's T, k, d, E, with its inputs
+    larger than L2: "dispatch" (moe_dispatch with the row gather, on seeded
+    random expert ids with a mild hot-expert skew) or "combine" (moe_combine
+    of a seeded fp32 y_perm).  Reports us per call and the algorithmic bytes
+    over that time against the measured copy bandwidth (own line)."""
+    import torch
+    import dispatch_combine_gb300 as moe
+    from moe_inputs import random_ids
+    torch.cuda.set_device(0)
+    c = CONFIGS[args.config]
+    shape = c.shape()
+    n = c.T * c.k
+    g = torch.Generator(device="cuda").manual_seed(0)
+    ids = random_ids(c.T, c.k, c.E, seed=0, skew=1.0).cuda()
+    # the dispatch's part of a workspace (status, chunk histograms) is small;
+    # the layer's x_perm / y_perm regions are not needed here
+    ws = moe.Workspace(16 << 20)
+    if args.stage_only == "dispatch":
+        x = torch.randn(c.T, c.d, device="cuda", generator=g).to(torch.bfloat16)
+        xp = torch.empty(n, c.d, dtype=torch.bfloat16, device="cuda")
+
+        def step():
+            moe.moe_dispatch(shape, ids, x, ws, x_perm_out=xp)
+    else:
+        _, _, _, dest, _ = moe.moe_dispatch(shape, ids, None, ws)
+        y_perm = torch.randn(n, c.d, device="cuda", generator=g, dtype=torch.float32)
+        w = torch.rand(c.T, c.k, device="cuda", generator=g, dtype=torch.float32)
+        y = torch.empty(c.T, c.d, dtype=torch.bfloat16, device="cuda")
+
+        def step():
+            moe.moe_combine(shape, y_perm, dest, w, y=y)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status error")
+    us = e0.elapsed_time(e1) * 1000.0 / args.steps
+    nbytes = stage_bytes(c)[args.stage_only]
+    peaks, peak_src = load_peaks()
+    line = {
+        "metric": f"{args.stage_only} alone: us per call", "impl": "gb300", "value": us,
+        "unit": "us", "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
+        "dtype": "bf16" if args.stage_only == "dispatch" else "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(c), "ids": "seeded random, skew 1.0"},
+        "bytes": nbytes, "achieved_gbs": nbytes / (us * 1e-6) / 1e9,
+        "hbm_fraction": nbytes / (us * 1e-6) / (peaks["hbm_gbs"] * 1e9),
+        "peak_source": peak_src,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -961,6 +1023,8 @@ def main(argv=None):
         return run_ffn_only(args)
     if args.route_only:
         return run_route_only(args)
+    if args.stage_only:
+        return run_stage_only(args)
     if args.fp8:
         return run_fp8(args)
     if args.eplb:

@@ -271,8 +271,9 @@ def moe_group_topk(shape, scores, topk_ids=None, stream=None):
     return topk_ids
 
 
-def moe_dispatch(shape, topk_ids, x, ws: Workspace, stream=None):
-    """Returns (counts [E], offsets [E+1], src_token [T*k], dest [T*k], x_perm)."""
+def moe_dispatch(shape, topk_ids, x, ws: Workspace, stream=None, x_perm_out=None):
+    """Returns (counts [E], offsets [E+1], src_token [T*k], dest [T*k], x_perm);
+    x_perm is written into x_perm_out when it is given."""
     s = as_shape(shape)
     dev = topk_ids.device
     n = s.T * s.k
@@ -284,7 +285,11 @@ def moe_dispatch(shape, topk_ids, x, ws: Workspace, stream=None):
     x_perm = None
     if x is not None:
         _expect(x, torch.bfloat16, (s.T, s.d), "x")
-        x_perm = torch.empty((n, s.d), dtype=torch.bfloat16, device=dev)
+        if x_perm_out is not None:
+            _expect(x_perm_out, torch.bfloat16, (n, s.d), "x_perm_out")
+            x_perm = x_perm_out
+        else:
+            x_perm = torch.empty((n, s.d), dtype=torch.bfloat16, device=dev)
     _check("moe_dispatch", lib().moe_dispatch(ctypes.byref(s), _ptr(topk_ids), _ptr(x),
                                               _ptr(counts), _ptr(offsets), _ptr(src),
                                               _ptr(dest), _ptr(x_perm), ws.c_ptr, ws.nbytes,
