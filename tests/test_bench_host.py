@@ -101,6 +101,21 @@ def test_reference_arm_json_line(monkeypatch):
                         "d2h_bytes_per_step": 0}
 
 
+def test_reference_arm_total_time_is_bounded(monkeypatch):
+    # however many steps are asked for, the token sample per step shrinks so
+    # that all steps together take about --ref-total-s
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.delenv("RANK", raising=False)
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--config", "tiny", "--steps", "50",
+                         "--warmup", "1", "--ref-total-s", "0.5"])
+    assert rc == 0
+    d = json.loads([ln for ln in buf.getvalue().splitlines() if ln.strip()][0])
+    assert d["steps"] == 50
+    assert d["ms_per_step"] * d["steps"] / 1000.0 < 2.0
+
+
 def test_reference_arm_other_ranks_exit_quietly(monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     monkeypatch.setenv("RANK", "1")
