@@ -446,9 +446,12 @@ __device__ __forceinline__ int swap_box_index(int sn) {
 }
 
 // One work item of a CTA pair: a whole tile, or (split last wave of the down
-// form) one K half of a tile.  Items n_full + j, j < 2 * rem, are half
-// j / rem of tile n_full + j % rem; pair c takes items c, c + ncl, ..., so
-// the two halves of a tile run at the same time on pairs j and j + rem.
+// form) one K half of a tile.  Items n_full + j, j < 2 * rem, are a half of
+// tile n_full + j % rem; pair c takes items c, c + ncl, ..., so the two
+// halves of a tile run at the same time on pairs j % rem and j % rem + rem.
+// The storing half (the later k-blocks) goes to the lower pair, whose CTAs
+// are normally dispatched first, so the adding half waits on a pair that is
+// already running.
 struct PairWork {
   int u;         // tile index
   int kb0, kb1;  // k-blocks [kb0, kb1)
@@ -466,7 +469,7 @@ __device__ __forceinline__ PairWork pair_work(int w, int n_full, int rem, int kb
   } else {
     const int j = w - n_full;
     pw.slot = j % rem;
-    pw.piece = j / rem;
+    pw.piece = (j < rem) ? 1 : 0;
     pw.u = n_full + pw.slot;
     pw.kb0 = pw.piece ? kblocks / 2 : 0;
     pw.kb1 = pw.piece ? kblocks : kblocks / 2;
