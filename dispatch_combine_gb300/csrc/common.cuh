@@ -297,9 +297,10 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// the issuing thread's committed bulk stores have finished reading shared memory
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// all but the most recent of the issuing thread's committed bulk groups have
+// finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // the issuing thread's committed bulk stores are complete (written to global)
 __device__ __forceinline__ void bulk_wait_all() {

@@ -775,29 +775,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                                      t.rows_valid &&
                  grow - lane >= 0 && grow - lane + 32 <= args.rows_total) {
         // every row of this warp's 32-row slab is valid: each 32-column
-        // chunk goes through the warp's staging box (row = lane, 16-byte
-        // pieces placed by the 128-byte swizzle) and leaves as one TMA store
-        const uint32_t box = smem_u32(smem + C::OUT_OFF + quad * C::OUT_BOX_BYTES);
-        const uint32_t rbase = box + static_cast<uint32_t>(lane) * 128u;
+        // chunk leaves as two TMA stores of 16 columns, each staged in one
+        // half of the warp's box (row = lane, 16-byte pieces placed by the
+        // 64-byte swizzle), so one half is filled while the other is stored
+        uint8_t *box = smem + C::OUT_OFF + quad * C::OUT_BOX_BYTES;
         const int row_g = static_cast<int>(grow - lane);
+        const uint32_t swz = static_cast<uint32_t>((lane >> 1) & 3);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tb + c * 32, v);
           tmem_ld_wait();
           tmem_regs_fence(v);
-          if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the box
-          __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_v4(rbase + static_cast<uint32_t>(((j ^ lane) & 7) * 16), v[4 * j],
-                         v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmY, smem + C::OUT_OFF + quad * C::OUT_BOX_BYTES, t.n * BN + c * 32,
-                         row_g);
-            bulk_commit();
+          for (int h = 0; h < 2; ++h) {
+            uint8_t *hb = box + h * (C::OUT_BOX_BYTES / 2);
+            const uint32_t rbase = smem_u32(hb) + static_cast<uint32_t>(lane) * 64u;
+            if (lane == 0) bulk_wait_read_1();  // this half's previous store has read it
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(rbase + ((static_cast<uint32_t>(q) ^ swz) * 16u), v[16 * h + 4 * q],
+                           v[16 * h + 4 * q + 1], v[16 * h + 4 * q + 2], v[16 * h + 4 * q + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmY, hb, t.n * BN + c * 32 + 16 * h, row_g);
+              bulk_commit();
+            }
           }
         }
       } else {
@@ -1261,8 +1266,8 @@ bool make_tmap(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2D fp32 tensor [rows, inner] row-major for TMA stores; box = 32 rows x 32
-// elements (128 bytes), 128-byte swizzle.  False if the base is not 16-byte
+// 2D fp32 tensor [rows, inner] row-major for TMA stores; box = 32 rows x 16
+// elements (64 bytes), 64-byte swizzle.  False if the base is not 16-byte
 // aligned or a row is not a multiple of 16 bytes.
 bool make_tmap_f32_out(CUtensorMap *map, void *base, uint64_t inner, uint64_t rows) {
   EncodeTiledFn fn = encode_fn();
@@ -1270,10 +1275,10 @@ bool make_tmap_f32_out(CUtensorMap *map, void *base, uint64_t inner, uint64_t ro
     return false;
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner * 4};
-  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t box[2] = {16, 32};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
