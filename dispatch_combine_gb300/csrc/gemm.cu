@@ -390,9 +390,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // accumulator in its TMEM and rows 128-255 in the peer's.  Per SM this halves
 // the B bytes per FLOP and, with 32 KB stages, gives a 6-stage ring.  The
 // down form stores its fp32 output with TMA: an epilogue warp whose 32 rows
-// are all valid stages each 32-column chunk in a swizzled shared-memory box
-// and issues one tensor store, so the output leaves as whole 128-byte lines
-// instead of per-row sector writes (other warps store directly).
+// are all valid stages each 32-column chunk in the two 16-column halves of a
+// swizzled shared-memory box and issues one tensor store per half, so the
+// output leaves as whole 64-byte row pieces instead of per-row sector writes
+// (other warps store directly).
 //   full[s]       in the even CTA, completed by both CTAs' TMA bytes;
 //   empty[s]      in both CTAs, the pair MMA commit arrives on both;
 //   tmem_full[b]  in both CTAs, the pair MMA commit arrives on both;
