@@ -38,7 +38,9 @@ from moe_inputs import CONFIGS, SCORE_SIGMOID_BIAS  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (1 GB300); % of HBM / bf16 tensor roofline per stage"
 UNIT = "tokens/s"
-DEFAULT_CONFIG = "few_large"
+DEFAULT_CONFIG = "prefill"
+# timed in the same run when the default workload is: same weights, decode batch
+DEFAULT_ALSO = {"prefill": "decode"}
 L2_BYTES = 126 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # fp32 FMA peak from the unit counts: 152 SMs x 128 fp32 lanes x 2 FLOP per
@@ -292,8 +294,11 @@ def run_reference(args, c):
     import torch
     import oracle
     from moe_inputs import make_layer_tensors
-    t = make_layer_tensors(c, device="cpu", seed=0)
+    # inputs drawn on the GPU when there is one (faster for the large
+    # workloads; drawing is not timed), then copied to the host
+    t = make_layer_tensors(c, device="cuda" if torch.cuda.is_available() else "cpu", seed=0)
     host = host_inputs(t)
+    del t
     # each step a bounded token sample; the whole run stays within
     # --ref-total-s however many steps are asked for (at least one token a step)
     per_step_s = min(args.ref_step_s, args.ref_total_s / max(args.steps, 1))
@@ -328,38 +333,53 @@ def run_reference(args, c):
 # GPU arm
 # --------------------------------------------------------------------------
 
-def run_gpu(args, c):
+# a timed region shorter than this is taken against the burst tensor peak
+# (the GPU has not reached its power cap yet), a longer one against the
+# sustained peak
+BURST_REGION_S = 1.0
+
+
+def tensor_peak(peaks: dict, peak_src: str, region_s: float) -> tuple[float, str]:
+    """The bf16 tensor peak that applies to a timed region of region_s seconds."""
+    if region_s < BURST_REGION_S:
+        return peaks["bf16_tflops"], (f"{peak_src} bf16 burst (timed region {region_s:.2f} s "
+                                      f"< {BURST_REGION_S:.0f} s)")
+    return peaks["bf16_tflops_sustained"], (f"{peak_src} bf16 sustained (timed region "
+                                            f"{region_s:.2f} s)")
+
+
+def layer_bytes(c, n_touched: int) -> int:
+    """Algorithmic HBM bytes of one layer call: the bandwidth stages plus the
+    touched experts' weights streamed once."""
+    sb = stage_bytes(c)
+    return sb["router"] + sb["dispatch"] + sb["combine"] + n_touched * expert_weight_bytes(c)
+
+
+def measure_layer(args, c, t, ws, device, world: int, steps: int, warmup: int) -> dict:
+    """Time `steps` moe_layer calls of workload c after `warmup` untimed ones
+    (CUDA events on the launching stream, clocks sampled inside the timed
+    region, max over ranks) and derive the per-stage roofline record."""
     import torch
     import dispatch_combine_gb300 as moe
-    from moe_inputs import make_layer_tensors
 
-    world, rank, local = dist_env()
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device (the MoE path has no CPU fallback)")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    init_dist(world, "nccl")
-    moe.lib()  # raises if libmoe.so is missing
-
-    t = make_layer_tensors(c, device=device, seed=0)
+    x = t["x"]
     bias = t["bias"] if c.score == SCORE_SIGMOID_BIAS else None
     shape = c.shape()
-    ws = moe.Workspace(moe.moe_workspace_size(shape), device=device)
     y = torch.empty(c.T, c.d, dtype=torch.bfloat16, device=device)
     counts = torch.empty(c.E, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
 
     def step(events=None):
-        moe.moe_layer(shape, t["x"], t["w_r"], bias, t["w_gate_up"], t["w_down"], ws, y=y,
+        moe.moe_layer(shape, x, t["w_r"], bias, t["w_gate_up"], t["w_down"], ws, y=y,
                       counts=counts, stage_events=events)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     if moe.moe_get_device_status(ws) != 0:
-        raise SystemExit("device status error during warm-up")
+        raise SystemExit(f"device status error during warm-up ({c.name})")
 
-    K = args.steps
+    K = steps
     # stage events on every STAGE_EVERY-th timed step (an event between two
     # kernels stops the next one from launching early, so the other steps
     # run without them); the stage times are the averages over those steps
@@ -370,7 +390,7 @@ def run_gpu(args, c):
             e.record(stream)
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(device.index or 0)
     sampler.start()
     time.sleep(0.3)
     barrier(world)
@@ -388,7 +408,7 @@ def run_gpu(args, c):
     clocks = sampler.stop()
     ms_total = start.elapsed_time(end)
     if moe.moe_get_device_status(ws) != 0:
-        raise SystemExit("device status error in the timed region")
+        raise SystemExit(f"device status error in the timed region ({c.name})")
     ms_total_max = max_over_ranks(ms_total, world, device)
     value = job_value(c.T, world, ms_total_max / 1000.0, K)
 
@@ -410,7 +430,9 @@ def run_gpu(args, c):
 
     peaks, peak_src = load_peaks()
     hbm = peaks["hbm_gbs"] * 1e9
-    tensor = peaks["bf16_tflops_sustained"] * 1e12
+    region_s = ms_total / 1000.0
+    tpeak, tpeak_src = tensor_peak(peaks, peak_src, region_s)
+    tensor = tpeak * 1e12
     sb = stage_bytes(c)
     fw = ffn_work(c, n_touched)
     stages = {}
@@ -444,22 +466,69 @@ def run_gpu(args, c):
                      "achieved_gbs": fw[n]["bytes"] / sec / 1e9,
                      "frac": max(t_hbm, t_tc) / sec}
     ffn_sec = (stage_ms["gate_up"] + stage_ms["down"]) / 1000.0
-    ffn_bound = max((fw["gate_up"]["bytes"] + fw["down"]["bytes"]) / hbm,
-                    (fw["gate_up"]["flops"] + fw["down"]["flops"]) / tensor)
+    ffn_flops = fw["gate_up"]["flops"] + fw["down"]["flops"]
+    ffn_wbytes = fw["gate_up"]["bytes"] + fw["down"]["bytes"]
+    ffn_bound = "tensor" if ffn_flops / tensor >= ffn_wbytes / hbm else "hbm"
+    ffn = {"us": ffn_sec * 1e6, "bound": ffn_bound,
+           "frac": max(ffn_wbytes / hbm, ffn_flops / tensor) / ffn_sec,
+           "tensor_frac": ffn_flops / tensor / ffn_sec, "hbm_frac": ffn_wbytes / hbm / ffn_sec,
+           "n_touched_experts": n_touched, "r_imbalance": r_imb,
+           "m_tiles_128": m_tiles, "tile_fill": tile_fill}
+    # the whole layer against its own floor: max(all algorithmic HBM bytes,
+    # FFN FLOPs at the tensor peak) over the measured time per layer
+    lb = layer_bytes(c, n_touched)
+    layer_s = ms_total_max / 1000.0 / K
+    layer = {"us": layer_s * 1e6, "bytes": lb, "flops": ffn_flops,
+             "hbm_frac": lb / hbm / layer_s, "tensor_frac": ffn_flops / tensor / layer_s,
+             "bound": "tensor" if ffn_flops / tensor >= lb / hbm else "hbm"}
+    layer["frac"] = max(layer["hbm_frac"], layer["tensor_frac"])
+
     dominant = max(names, key=lambda n: stage_ms[n])
     dom = stages[dominant]
     if dom["bound"] == "tensor":
-        roof = {"bound": "tensor", "achieved": dom["achieved_tflops"],
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": dom["achieved_tflops"] / peaks["bf16_tflops_sustained"],
-                "traffic": None}
+        roof = {"bound": "tensor", "achieved": dom["achieved_tflops"], "peak": tpeak,
+                "unit": "TFLOP/s", "frac": dom["achieved_tflops"] / tpeak}
+        roof["peak_source"] = tpeak_src
     else:
         ach = dom.get("weight_bytes", dom.get("bytes")) / (stage_ms[dominant] / 1000.0) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / peaks["hbm_gbs"], "traffic": None}
-    roof["kernel"] = dominant
+                "frac": ach / peaks["hbm_gbs"]}
+        roof["peak_source"] = f"{peak_src} HBM copy"
     roof["traffic"] = measured_traffic(c.name, dominant)
-    roof["peak_source"] = (f"{peak_src} ({'bf16 sustained' if roof['bound'] == 'tensor' else 'HBM copy'})")
+    roof["kernel"] = dominant
+    return {"value": value, "ms_total": ms_total_max, "ms_per_step": ms_total_max / K,
+            "steps": K, "warmup": warmup, "roofline": roof, "stages": stages, "ffn": ffn,
+            "layer": layer, "clocks": clocks, "y": y, "launches": moe.moe_layer_launch_count(shape) * K}
+
+
+def run_gpu(args, c):
+    import torch
+    import dispatch_combine_gb300 as moe
+    from moe_inputs import make_layer_tensors
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the MoE path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    moe.lib()  # raises if libmoe.so is missing
+
+    # workloads that share this one's weights and are timed in the same run
+    also = [a for a in (args.also.split(",") if args.also else []) if a and a != c.name]
+    for a in also:
+        o = CONFIGS[a]
+        if (o.d, o.E, o.G, o.inter, o.score) != (c.d, c.E, c.G, c.inter, c.score):
+            raise SystemExit(f"--also {a}: its weights differ from {c.name}'s")
+    t = make_layer_tensors(c, device=device, seed=0, extra_x={a: CONFIGS[a].T for a in also})
+    bias = t["bias"] if c.score == SCORE_SIGMOID_BIAS else None
+    shape = c.shape()
+    ws_bytes = max(moe.moe_workspace_size(CONFIGS[n].shape()) for n in [c.name] + also)
+    ws = moe.Workspace(ws_bytes, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    main = measure_layer(args, c, t, ws, device, world, args.steps, args.warmup)
+    y = main["y"]
 
     # end to end through the C ABI with host buffers: every step copies its
     # x from pinned host memory and reads its y back, on two copy streams
@@ -518,6 +587,21 @@ def run_gpu(args, c):
         e2e = {"value": job_value(c.T, world, ms / 1000.0, e2e_steps), "unit": UNIT,
                "h2d_bytes_per_step": c.T * c.d * 2, "d2h_bytes_per_step": c.T * c.d * 2,
                "steps": e2e_steps}
+        del x_host, y_host, x_dev, y_dev
+
+    # the other workloads of the same weights (the decode batch beside the
+    # prefill one): full stage records of their own, nested in this line
+    also_rec = {}
+    for a in also:
+        ca = CONFIGS[a]
+        ta = dict(t)
+        ta["x"] = t["x_" + a]
+        r = measure_layer(args, ca, ta, ws, device, world, args.also_steps or args.steps,
+                          args.warmup)
+        r.pop("y")
+        also_rec[a] = {"workload": workload_desc(ca), "metric": METRIC, "unit": UNIT, **r}
+        main["launches"] += r.pop("launches")
+        also_rec[a].pop("launches", None)
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_sample_s > 0:
@@ -534,23 +618,25 @@ def run_gpu(args, c):
                if c.E * expert_weight_bytes(c) > L2_BYTES else
                "all inputs fit in L2 (hot-L2 timing)")
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_total_max / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
         "config": {"workload": workload_desc(c), "T": c.T, "d": c.d, "E": c.E, "G": c.G,
                    "topk_group": c.topk_group, "k": c.k, "inter": c.inter,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": l2_note},
-        "roofline": roof,
-        "stages": stages,
-        "ffn": {"us": ffn_sec * 1e6, "frac": ffn_bound / ffn_sec,
-                "n_touched_experts": n_touched, "r_imbalance": r_imb,
-                "m_tiles_128": m_tiles, "tile_fill": tile_fill},
-        "clocks": clocks,
+        "roofline": main["roofline"],
+        "stages": main["stages"],
+        "ffn": main["ffn"],
+        "layer": main["layer"],
+        "clocks": main["clocks"],
         "e2e": e2e,
-        "gpu_launches": moe.moe_layer_launch_count(shape) * K,
+        "gpu_launches": main["launches"],
         "cpu_baseline": cpu,
     }
+    if also_rec:
+        line["also"] = also_rec
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -655,10 +741,16 @@ def run_masked(args):
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--config", choices=sorted(CONFIGS), default=DEFAULT_CONFIG)
+    ap.add_argument("--also", default=None,
+                    help="comma-separated workloads with the same weights, timed in the same "
+                         "run and nested in the line under 'also' (default: decode beside "
+                         "prefill; '' for none)")
+    ap.add_argument("--also-steps", type=int, default=None,
+                    help="timed steps of the --also workloads (default: --steps)")
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="timed steps of the end-to-end measurement (default: --steps, so both "
                          "reach the same clocks; 0 = skip)")
@@ -685,7 +777,10 @@ def parse_args(argv=None):
     ap.add_argument("--ffn-rows", default=None, metavar="E,R",
                     help="time the expert FFN alone on E experts x R rows at the workload's "
                          "d and inter (bf16, or FP8 with --fp8; own line)")
-    return ap.parse_args(argv)
+    a = ap.parse_args(argv)
+    if a.also is None:
+        a.also = DEFAULT_ALSO.get(a.config, "")
+    return a
 
 
 def run_route_only(args):

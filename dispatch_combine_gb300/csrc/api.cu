@@ -247,6 +247,15 @@ moe_status_t moe_get_device_status(void *ws, size_t ws_bytes, moe_stream_t strea
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  // A launch that stopped early (a wait ran out) may have left split flags
+  // of the down GEMM raised, and a replay of a captured graph raises the
+  // same value again: clear them with the error, so that the next launch
+  // cannot take a stale flag for its own.
+  const size_t flags_off = align_up(4);
+  const size_t flags_bytes = 4 * static_cast<size_t>(moe::kPairSplitFlagWords);
+  if (word != 0 && ws_bytes >= flags_off + flags_bytes &&
+      cudaMemsetAsync(static_cast<char *>(ws) + flags_off, 0, flags_bytes, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
   moe_status_t out = MOE_OK;
   for (int b = 31; b >= 1; --b)
     if (word & (1u << b)) {

@@ -27,24 +27,71 @@ constexpr int64_t kNoAllocScratchInts = 262144;
 static __device__ __align__(256) int32_t g_dispatch_scratch[kNoAllocScratchInts];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-int32_t *g_scratch_addr[kMaxDevices] = {};
 
-// Device address of the array on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up
-// once per device, with that device current, and cached.
+// cuCtxGetCurrent / cuCtxGetId of the driver, looked up through the runtime
+// (the library does not link libcuda).  A context's id is never reused, so
+// a cached address is known to belong to the context that is current now.
+struct CtxApi {
+  int (*get_current)(void **ctx) = nullptr;
+  int (*get_id)(void *ctx, unsigned long long *id) = nullptr;
+};
+
+const CtxApi &ctx_api() {
+  static const CtxApi api = [] {
+    CtxApi a;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      a.get_current = reinterpret_cast<int (*)(void **)>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      a.get_id = reinterpret_cast<int (*)(void *, unsigned long long *)>(p);
+    return a;
+  }();
+  return api;
+}
+
+bool current_ctx_id(unsigned long long *id) {
+  const CtxApi &api = ctx_api();
+  void *ctx = nullptr;
+  return api.get_current && api.get_id && api.get_current(&ctx) == 0 && ctx != nullptr &&
+         api.get_id(ctx, id) == 0;
+}
+
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;
+  int32_t *addr = nullptr;
+};
+std::mutex g_scratch_mu;
+ScratchAddr g_scratch_addr[kMaxDevices];
+
+// Device address of the array in the current device's context.  In host
+// code the array's name is only a host-side stand-in, so the address is
+// looked up with the device current -- on the first call on a device, and
+// again whenever that device's context has changed (after a
+// cudaDeviceReset the module is loaded anew, possibly elsewhere) -- and
+// cached with the id of the context it belongs to.
 moe_status_t scratch_address(int32_t **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  unsigned long long id = 0;
+  ScratchAddr &c = g_scratch_addr[dev];
+  if (!current_ctx_id(&id) || c.addr == nullptr || c.ctx_id != id) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr)
       return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<int32_t *>(p);
+    // the lookup has made the device's primary context current if it was not
+    if (!current_ctx_id(&id)) return MOE_ERR_CUDA;
+    c.ctx_id = id;
+    c.addr = static_cast<int32_t *>(p);
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return MOE_OK;
 }
 

@@ -109,7 +109,10 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronises `stream`, returns the OR of device-side errors recorded in the
  * workspace since the last call (as the highest-numbered status found), and
- * clears the word.  The only entry point that blocks the host. */
+ * clears the word.  When the word was not zero it also clears the down
+ * GEMM's flags (a launch that stopped at a timed-out wait can leave them
+ * raised), so the workspace is ready for the next call, a replayed graph
+ * included.  The only entry point that blocks the host. */
 moe_status_t moe_get_device_status(void *ws, size_t ws_bytes, moe_stream_t stream,
                                    moe_status_t *status);
 
@@ -255,7 +258,10 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
  *   chunk (128 up to T*k = 32768, 512 beyond; so T*k <= 524288 at E = 256);
  *   larger shapes return MOE_ERR_UNSUPPORTED.  Nothing is allocated.
  *   The first call on a device looks up the array's device address (no
- *   allocation); make that first call before any stream capture.
+ *   allocation) and caches it with the id of the device's current context;
+ *   a call that finds another context current (after cudaDeviceReset, say)
+ *   looks it up again.  Make the first call on a device, and the first
+ *   after such a reset, before any stream capture.
  *   All calls share the array: calls that overlap on the GPU race; calls
  *   ordered on one stream are safe, and nothing needs clearing between them.
  *   Out-of-range ids are skipped (their counts are missing from `counts`)

@@ -96,7 +96,8 @@ def _normal_bf16(shape, std: float, g: torch.Generator, device) -> torch.Tensor:
 
 
 def make_layer_tensors(cfg: LayerConfig, device="cpu", seed: int = 0,
-                       n_tokens: int | None = None, with_x: bool = True) -> dict:
+                       n_tokens: int | None = None, with_x: bool = True,
+                       extra_x: dict | None = None) -> dict:
     """Draw W_r, bias, W_gate_up, W_down and x for ``cfg`` (see module doc).
 
     Returns a dict of torch tensors on ``device``:
@@ -104,6 +105,10 @@ def make_layer_tensors(cfg: LayerConfig, device="cpu", seed: int = 0,
       w_gate_up [E, 2*inter, d] bf16 (rows 0..inter-1 gate, inter.. up),
       w_down [E, d, inter] bf16.
     ``n_tokens`` overrides T for x only (weights are unchanged).
+    ``extra_x`` maps names to token counts: each gets its own x drawn from
+    the generator state that follows the weights, i.e. the x that
+    ``make_layer_tensors`` gives a workload with the same weights and that
+    many tokens (returned as ``out["x_" + name]``).
     """
     device = torch.device(device)
     g = _gen(device, seed)
@@ -118,8 +123,12 @@ def make_layer_tensors(cfg: LayerConfig, device="cpu", seed: int = 0,
     for e in range(E):
         w_down[e] = _normal_bf16((d, inter), 0.02, g, device)
     out = {"w_r": w_r, "bias": bias, "w_gate_up": w_gu, "w_down": w_down}
+    state = g.get_state()
     if with_x:
         out["x"] = _normal_bf16((T, d), 1.0, g, device)
+    for name, n in (extra_x or {}).items():
+        g.set_state(state)
+        out["x_" + name] = _normal_bf16((n, d), 1.0, g, device)
     return out
 
 

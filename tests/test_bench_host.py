@@ -123,3 +123,25 @@ def test_reference_arm_other_ranks_exit_quietly(monkeypatch):
     with contextlib.redirect_stdout(buf):
         rc = bench.main(["--impl", "reference", "--config", "tiny", "--steps", "1"])
     assert rc == 0 and buf.getvalue() == ""
+
+
+def test_tensor_peak_follows_timed_region_length():
+    peaks = {"hbm_gbs": 6784.5, "bf16_tflops": 1854.8, "bf16_tflops_sustained": 1699.2}
+    p, src = bench.tensor_peak(peaks, "measured", 0.17)
+    assert p == 1854.8 and "burst" in src
+    p, src = bench.tensor_peak(peaks, "measured", 5.2)
+    assert p == 1699.2 and "sustained" in src
+
+
+def test_layer_bytes_prefill():
+    c = bench.CONFIGS["prefill"]
+    sb = bench.stage_bytes(c)
+    # weights of 100 touched experts (88.08 MB each) plus the bandwidth stages
+    assert bench.layer_bytes(c, 100) == sum(sb.values()) + 100 * 3 * 7168 * 2048 * 2
+
+
+def test_default_line_is_prefill_with_decode_nested():
+    a = bench.parse_args([])
+    assert a.config == "prefill" and a.also == "decode"
+    a = bench.parse_args(["--config", "few_large"])
+    assert a.also == ""

@@ -16,7 +16,40 @@ from tests.gpu_common import bits, check_close, ensure_lib, host_bits, layer_inp
 
 pytestmark = pytest.mark.gpu
 
-SAMPLES = {"tiny": None, "few_large": 16, "decode": 16, "prefill": 8}
+# tokens whose outputs are compared: every token of the small workloads;
+# at few_large and prefill a set that covers the first and the last row of
+# every 128-row m-tile of every touched expert
+ALL_TOKENS = {"tiny", "decode"}
+TILE = 128
+
+
+def tile_cover_tokens(ids: np.ndarray, E: int):
+    """Tokens whose assignments include the first and the last row of every
+    128-row m-tile of every expert, from the oracle's dispatch of the oracle
+    routing.  Returns (tokens, number of m-tiles)."""
+    counts, offsets, dest, src = oracle.dispatch(ids, E)
+    rows = []
+    n_tiles = 0
+    for e in range(E):
+        n = int(counts[e])
+        for j in range(0, n, TILE):
+            n_tiles += 1
+            rows += [int(offsets[e]) + j, int(offsets[e]) + min(j + TILE, n) - 1]
+    return np.unique(src[np.array(rows, dtype=np.int64)]).astype(np.int32), n_tiles
+
+
+def tiles_covered(ids: np.ndarray, E: int, toks: np.ndarray) -> int:
+    """m-tiles whose first and last rows both belong to assignments of `toks`."""
+    counts, offsets, dest, src = oracle.dispatch(ids, E)
+    k = ids.shape[1]
+    have = np.zeros(ids.size, dtype=bool)
+    have[dest[(toks[:, None].astype(np.int64) * k + np.arange(k)).ravel()]] = True
+    covered = 0
+    for e in range(E):
+        n = int(counts[e])
+        for j in range(0, n, TILE):
+            covered += int(have[offsets[e] + j] and have[offsets[e] + min(j + TILE, n) - 1])
+    return covered
 
 
 @functools.lru_cache(maxsize=None)
@@ -48,15 +81,15 @@ def test_layer_matches_oracle(name):
     gw = w.cpu().numpy()
     assert np.all(np.abs(gw - ref_w) <= 1e-6 * np.abs(ref_w))
     assert np.array_equal(counts.cpu().numpy(), np.bincount(ref_ids.ravel(), minlength=cfg.E))
-    # outputs of sampled tokens (all tokens for the tiny workload)
-    n = SAMPLES[name]
-    if n is None:
+    if name in ALL_TOKENS:
         toks = np.arange(cfg.T, dtype=np.int32)
+        _, n_tiles = tile_cover_tokens(ref_ids, cfg.E)
     else:
-        rng = np.random.default_rng(0)
-        toks = np.sort(rng.choice(cfg.T, n, replace=False)).astype(np.int32)
-        toks[0] = 0
-        toks[-1] = cfg.T - 1
+        toks, n_tiles = tile_cover_tokens(ref_ids, cfg.E)
+    covered = tiles_covered(ref_ids, cfg.E, toks)
+    print(f"{name}: {len(toks)} of {cfg.T} tokens compared, m-tiles covered "
+          f"{covered} of {n_tiles}")
+    assert covered == n_tiles
     y_ref, ids_t, _ = oracle.layer_tokens(host_bits(name, "x"), host_bits(name, "w_r"),
                                           t["bias"].cpu().numpy(), host_bits(name, "w_gate_up"),
                                           host_bits(name, "w_down"), cfg.shape(), toks)
@@ -147,16 +180,24 @@ def test_masked_expert_slices(variant):
     y = moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_MASKED, buf, mm, M_max, w_gu, w_down, ws)
     torch.cuda.synchronize()
     assert moe.moe_get_device_status(ws) == 0
-    # sampled rows: first/last row of the busiest experts and of a few others
-    order = np.argsort(-mm_host, kind="stable")
-    pick_e = [int(e) for e in order[:4]] + [int(e) for e in order[4:] if mm_host[e] > 0][:4]
+    # the first and the last row of every 128-row m-tile of every slab
     rows, row_e = [], []
-    for i in pick_e:
+    n_tiles = 0
+    for i in range(len(experts)):
         m = int(mm_host[i])
-        for r in sorted({0, m // 2, m - 1}):
-            rows.append((i, r))
-            row_e.append(i)
-    xr = np.stack([bits(buf[i, r]) for i, r in rows])
+        for j in range(0, m, TILE):
+            n_tiles += 1
+            for r in sorted({j, min(j + TILE, m) - 1}):
+                rows.append((i, r))
+                row_e.append(i)
+    have = set(rows)
+    covered = sum(1 for i in range(len(experts)) for j in range(0, int(mm_host[i]), TILE)
+                  if (i, j) in have and (i, min(j + TILE, int(mm_host[i])) - 1) in have)
+    print(f"masked {variant}: {len(rows)} rows compared, m-tiles covered {covered} of {n_tiles}")
+    assert covered == n_tiles
+    idx_i = torch.tensor([i for i, _ in rows], device="cuda")
+    idx_r = torch.tensor([r for _, r in rows], device="cuda")
+    xr = bits(buf[idx_i, idx_r])
     ref = oracle.expert_ffn_rows(xr, np.array(row_e, np.int32), bits(w_gu), bits(w_down))
-    got = np.stack([y[i, r].cpu().numpy() for i, r in rows])
+    got = y[idx_i, idx_r].cpu().numpy()
     check_close(got, ref, bf16_output=False, what=f"masked {variant}")

@@ -46,3 +46,26 @@ def test_host_side_errors_raise():
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_route(cfg.shape(), x_odd, t["w_r"], t["bias"], ws)  # misaligned
     assert ei.value.status == 1
+
+
+def test_reading_an_error_clears_raised_split_flags():
+    # A launch that stopped at a timed-out wait can leave split flags of the
+    # down GEMM raised.  Plant that state on the host (a status word with
+    # the timeout bit, raised flags) and check that reading the status
+    # leaves the flags zero for the next launch.
+    ensure_lib()
+    cfg = CONFIGS["tiny"]
+    ws = moe.Workspace(moe.moe_workspace_size(cfg.shape()))
+    region = ws.buf[ws.offset:ws.offset + ws.nbytes]
+    flags = region[256:256 + 4 * 4096].view(torch.int32)
+    flags[::3] = 7
+    region[:4].view(torch.int32)[0] = 1 << 5
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 5
+    torch.cuda.synchronize()
+    assert int(flags.abs().sum()) == 0
+    # and a clean word leaves the workspace as it is
+    flags[0] = 9
+    assert moe.moe_get_device_status(ws) == 0
+    assert int(flags[0]) == 9
+    flags[0] = 0

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import dispatch_combine_gb300 as moe
+import oracle
 from moe_inputs import random_ids
 from tests.gpu_common import bits, ensure_lib
 
@@ -29,11 +30,27 @@ def _case(T, k, E, d, seed, skew):
     return ids, x.cuda()
 
 
-def test_noalloc_dispatch_equals_workspace_dispatch_twice():
+def _check_against_oracle(ids, x, E, got):
+    """counts, offsets, dest and src_token equal the oracle's stable counting
+    sort; every gathered row is its source token's row, bit for bit."""
+    counts, offsets, dest, src = oracle.dispatch(ids.cpu().numpy(), E)
+    for name, ref, g in zip(["counts", "offsets", "src_token", "dest"],
+                            [counts, offsets, src, dest], got[:4]):
+        assert np.array_equal(g.cpu().numpy(), ref), name
+    if x is not None:
+        assert np.array_equal(bits(got[4]), bits(x)[src])
+
+
+@pytest.mark.parametrize("cases", [
+    # 128 assignments per chunk (T*k <= 32768)
+    [(1000, 8, 256, 136, 11, 2.0), (513, 4, 5, 24, 12, 0.0)],
+    # 512 assignments per chunk (T*k > 32768), then a small call after it
+    [(8192, 8, 256, 64, 13, 1.5), (100, 2, 16, 32, 14, 0.0)],
+])
+def test_noalloc_dispatch_equals_workspace_dispatch_twice(cases):
     ensure_lib()
     # two calls in a row with different routings: the second call reuses the
     # array the first one filled and must not see its leftovers
-    cases = [(1000, 8, 256, 136, 11, 2.0), (513, 4, 5, 24, 12, 0.0)]
     for T, k, E, d, seed, skew in cases:
         shape = _shape(T, d, E, k)
         ids, x = _case(T, k, E, d, seed, skew)
@@ -44,6 +61,18 @@ def test_noalloc_dispatch_equals_workspace_dispatch_twice():
         for name, r, g in zip(["counts", "offsets", "src_token", "dest"], ref[:4], got[:4]):
             assert torch.equal(r, g), name
         assert np.array_equal(bits(ref[4]), bits(got[4]))
+        _check_against_oracle(ids, x, E, got)
+
+
+def test_noalloc_dispatch_at_its_largest_shape():
+    ensure_lib()
+    # ceil(T*k/512) * E = 1024 * 256 = 262144 entries: the whole array
+    T, k, E, d = 65536, 8, 256, 16
+    shape = _shape(T, d, E, k)
+    ids, x = _case(T, k, E, d, 15, 1.0)
+    got = moe.moe_dispatch_noalloc(shape, ids, x)
+    torch.cuda.synchronize()
+    _check_against_oracle(ids, x, E, got)
 
 
 def test_noalloc_dispatch_rejects_shapes_beyond_its_array():
