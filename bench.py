@@ -420,7 +420,7 @@ def measure_layer(args, c, t, ws, device, world: int, steps: int, warmup: int) -
             stage_ms[n] += row[i].elapsed_time(row[i + 1])
     stage_ms = {n: v / len(evs) for n, v in stage_ms.items()}
 
-    n_flagged = moe.moe_route_screened_count(shape, ws)
+    n_refined = moe.moe_route_refined_count(shape, ws)
     cnt = counts.cpu()
     n_touched = int((cnt > 0).sum())
     mean = float(cnt.float().mean())
@@ -441,13 +441,13 @@ def measure_layer(args, c, t, ws, device, world: int, steps: int, warmup: int) -
         stages[n] = {"us": stage_ms[n] * 1000.0, "bound": "hbm", "bytes": sb[n],
                      "achieved_gbs": sb[n] / sec / 1e9, "frac": sb[n] / hbm / sec}
     # screened router: tensor-core logits, then the fixed-order logits of the
-    # k selected experts per token (their weight rows come from L2) and all
-    # E for the flagged tokens; its HBM bytes stay those of the stage
+    # experts each token's intervals leave open (at least its k selected;
+    # their weight rows come from L2); its HBM bytes stay those of the stage
     r_flops = 2.0 * c.T * c.d * c.E
-    if n_flagged >= 0:
-        stages["router"].update({"screened": True, "flagged_tokens": n_flagged,
-                                 "tc_flops": r_flops,
-                                 "refine_l2_bytes": c.T * c.k * c.d * 2 + n_flagged * c.E * c.d * 2})
+    if n_refined >= 0:
+        stages["router"].update({"screened": True, "refined_pairs": n_refined,
+                                 "refined_per_token": n_refined / c.T, "tc_flops": r_flops,
+                                 "refine_l2_bytes": n_refined * c.d * 2})
     # otherwise the logits are fp32 multiply-adds on CUDA cores (fixed order):
     # at large T they bound the stage, not its bytes
     elif r_flops / (FP32_TFLOPS * 1e12) > sb["router"] / hbm:
@@ -526,6 +526,14 @@ def run_gpu(args, c):
     ws_bytes = max(moe.moe_workspace_size(CONFIGS[n].shape()) for n in [c.name] + also)
     ws = moe.Workspace(ws_bytes, device=device)
     stream = torch.cuda.current_stream(device)
+    # the router weight's prepared copy (transposed, with column norms) is
+    # made once, like any one-time weight layout step, and used by every call
+    router_prep = None
+    try:
+        router_prep = moe.moe_router_prepare(shape, t["w_r"])
+    except moe.MoEError as e:
+        if e.status != 2:  # MOE_ERR_UNSUPPORTED: this shape is not screened
+            raise
 
     main = measure_layer(args, c, t, ws, device, world, args.steps, args.warmup)
     y = main["y"]
@@ -613,6 +621,8 @@ def run_gpu(args, c):
                "sample": f"{r['tokens']} of {c.T} tokens (seeded), full layer per token, "
                          f"{r['seconds']:.1f} s"}
 
+    if router_prep is not None:
+        router_prep.release()
     l2_note = ("inputs larger than L2 (expert weights "
                f"{c.E * expert_weight_bytes(c) / 1e9:.2f} GB)"
                if c.E * expert_weight_bytes(c) > L2_BYTES else
@@ -625,7 +635,9 @@ def run_gpu(args, c):
         "config": {"workload": workload_desc(c), "T": c.T, "d": c.d, "E": c.E, "G": c.G,
                    "topk_group": c.topk_group, "k": c.k, "inter": c.inter,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": l2_note},
+                   "l2": l2_note,
+                   "router_weight": ("prepared once (transposed copy + column norms)"
+                                     if router_prep is not None else "used as given")},
         "roofline": main["roofline"],
         "stages": main["stages"],
         "ffn": main["ffn"],
@@ -802,6 +814,12 @@ def run_route_only(args):
     w = torch.empty(c.T, c.k, dtype=torch.float32, device="cuda")
     lg = torch.empty(c.T, c.E, dtype=torch.float32, device="cuda")
     out = {}
+    router_prep = None
+    try:
+        router_prep = moe.moe_router_prepare(shape, w_r)
+    except moe.MoEError as e:
+        if e.status != 2:  # not screened
+            raise
     for label, logits in (("screened", None), ("fixed_order", lg)):
         def step():
             moe.moe_route(shape, x, w_r, b, ws, topk_ids=ids, topk_w=w, logits=logits)
@@ -817,15 +835,17 @@ def run_route_only(args):
         torch.cuda.synchronize()
         out[label] = e0.elapsed_time(e1) * 1000.0 / args.steps
         if logits is None:
-            out["flagged_tokens"] = moe.moe_route_screened_count(shape, ws)
+            out["refined_pairs"] = moe.moe_route_refined_count(shape, ws)
     if moe.moe_get_device_status(ws) != 0:
         raise SystemExit("device status error")
+    if router_prep is not None:
+        router_prep.release()
     line = {
         "metric": "router alone: us per call", "impl": "gb300", "value": out["screened"],
         "unit": "us", "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(c)},
-        "fixed_order_us": out["fixed_order"], "flagged_tokens": out["flagged_tokens"],
+        "fixed_order_us": out["fixed_order"], "refined_pairs": out["refined_pairs"],
         "tokens_per_s": c.T / (out["screened"] * 1e-6),
     }
     print(json.dumps(line), flush=True)

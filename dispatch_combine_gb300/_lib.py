@@ -80,7 +80,10 @@ SIGNATURES = {
     "moe_combine": (_I32, [_PS, _P, _P, _P, _P, _P]),
     "moe_layer": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_layer_launch_count": (_I32, [_PS]),
-    "moe_route_screened_count": (_I32, [_PS, _P, _SZ, _P, _P]),
+    "moe_route_refined_count": (_I32, [_PS, _P, _SZ, _P, _P]),
+    "moe_router_prep_size": (_I32, [_PS, ctypes.POINTER(_SZ)]),
+    "moe_router_prepare": (_I32, [_PS, _P, _P, _SZ, _P]),
+    "moe_router_release": (_I32, [_P]),
     "moe_selftest_wait_timeout": (_I32, [_P, _SZ, _U64, _P]),
 }
 
@@ -215,14 +218,52 @@ def moe_layer_launch_count(shape) -> int:
     return int(lib().moe_layer_launch_count(ctypes.byref(as_shape(shape))))
 
 
-def moe_route_screened_count(shape, ws: Workspace, stream=None) -> int:
-    """Tokens the last screened routing in ws sent to the full fixed-order
-    path (-1: the shape is not screened).  Synchronises the stream."""
+def moe_route_refined_count(shape, ws: Workspace, stream=None) -> int:
+    """(token, expert) pairs whose fixed-order logit the last screened
+    routing in ws computed (-1: the shape is not screened).  Synchronises the
+    stream."""
     out = torch.empty(1, dtype=torch.int32, device="cuda")
-    _check("moe_route_screened_count",
-           lib().moe_route_screened_count(ctypes.byref(as_shape(shape)), ws.c_ptr, ws.nbytes,
-                                          _ptr(out), _stream(stream)))
+    _check("moe_route_refined_count",
+           lib().moe_route_refined_count(ctypes.byref(as_shape(shape)), ws.c_ptr, ws.nbytes,
+                                         _ptr(out), _stream(stream)))
     return int(out.item())
+
+
+def moe_router_prep_size(shape) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_router_prep_size",
+           lib().moe_router_prep_size(ctypes.byref(as_shape(shape)), ctypes.byref(out)))
+    return out.value
+
+
+class RouterPrep:
+    """A prepared copy of a router weight (see moe_router_prepare in moe.h).
+    Holds its buffer and the weight while recorded; release() (or leaving a
+    ``with`` block) drops the record."""
+
+    def __init__(self, shape, w_r, stream=None):
+        n = moe_router_prep_size(shape)
+        self.buf = torch.empty(n + 256, dtype=torch.uint8, device=w_r.device)
+        self.ptr = self.buf.data_ptr() + (-self.buf.data_ptr()) % 256
+        self.w_r = w_r
+        _check("moe_router_prepare",
+               lib().moe_router_prepare(ctypes.byref(as_shape(shape)), _ptr(w_r),
+                                        ctypes.c_void_p(self.ptr), n, _stream(stream)))
+
+    def release(self):
+        if self.w_r is not None:
+            _check("moe_router_release", lib().moe_router_release(_ptr(self.w_r)))
+            self.w_r = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.release()
+
+
+def moe_router_prepare(shape, w_r, stream=None) -> RouterPrep:
+    return RouterPrep(shape, w_r, stream)
 
 
 # --------------------------------------------------------------------------

@@ -22,7 +22,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["router.cu", "dispatch.cu", "combine.cu", "gemm.cu", "api.cu", "noalloc.cu",
+SOURCES = ["router.cu", "route_screen.cu", "dispatch.cu", "combine.cu", "gemm.cu", "api.cu", "noalloc.cu",
            "quant.cu", "eplb.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -793,18 +793,47 @@ int32_t moe_layer_launch_count(const moe_shape_t *shape) {
   return moe::router_launches(shape->T, shape->d, shape->E, shape->G, shape->k) + 7;
 }
 
-moe_status_t moe_route_screened_count(const moe_shape_t *shape, const void *ws, size_t ws_bytes,
-                                      int32_t *count, moe_stream_t stream) {
+moe_status_t moe_route_refined_count(const moe_shape_t *shape, const void *ws, size_t ws_bytes,
+                                     int32_t *count, moe_stream_t stream) {
   MOE_TRY(check_shape(shape));
   if (!count) return MOE_ERR_INVALID_ARG;
   const Layout L = make_layout(*shape, 0);
   MOE_TRY(check_ws(const_cast<void *>(ws), ws_bytes, L.end_route));
-  const int32_t *src = moe::router_flagged_count(at<void>(const_cast<void *>(ws), L.wr32),
+  const int32_t *src = moe::router_refined_count(at<void>(const_cast<void *>(ws), L.wr32),
                                                  shape->T, shape->d, shape->E, shape->G,
                                                  shape->k);
   if (!src) return cuda_status(cudaMemsetAsync(count, 0xff, sizeof(int32_t), stream));
   return cuda_status(cudaMemcpyAsync(count, src, sizeof(int32_t), cudaMemcpyDeviceToDevice,
                                      stream));
+}
+
+moe_status_t moe_router_prep_size(const moe_shape_t *shape, size_t *bytes) {
+  MOE_TRY(check_shape(shape));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const moe_shape_t &s = *shape;
+  if (!moe::router_screened(s.T > 0 ? s.T : 1, s.d, s.E, s.G, s.k)) return MOE_ERR_UNSUPPORTED;
+  *bytes = moe::router_prep_bytes(s.d, s.E);
+  return MOE_OK;
+}
+
+moe_status_t moe_router_prepare(const moe_shape_t *shape, const void *w_r, void *prep,
+                                size_t prep_bytes, moe_stream_t stream) {
+  size_t need = 0;
+  MOE_TRY(moe_router_prep_size(shape, &need));
+  if (!w_r || !aligned16(w_r) || !prep || (reinterpret_cast<uintptr_t>(prep) & 255u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (prep_bytes < need) return MOE_ERR_WORKSPACE;
+  // drop the old record first: until the new one is in, calls make their own copy
+  moe::router_release_prepared(w_r);
+  MOE_TRY(cuda_status(moe::launch_router_prepare(w_r, shape->d, shape->E, prep, stream)));
+  if (!moe::router_register_prepared(w_r, shape->d, shape->E, prep)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t moe_router_release(const void *w_r) {
+  if (!w_r) return MOE_ERR_INVALID_ARG;
+  moe::router_release_prepared(w_r);
+  return MOE_OK;
 }
 
 moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, uint64_t limit_ns,

@@ -23,21 +23,35 @@ cudaError_t launch_router_logits(const void *x, const void *w_r, int T, int d, i
 cudaError_t launch_router_select(const float *logits, const float *bias, int T, int E, int G,
                                  int topk_group, int k, int score, float bias_scale, int mode,
                                  int32_t *ids, float *weights, cudaStream_t s);
+// experts per lane of the warp-per-token selection (0: the general kernel)
+int router_select_per(int E, int G);
+
+// route_screen.cu
 // Routing without a logits output: ids [T,k] and weights [T,k], the same
 // values as launch_router_logits + launch_router_select.  Where the shape
-// allows (router_screened) the logits come from the tensor cores and only
-// the selected ones, or every logit of a token whose selection margin is
-// below kScreenDelta, are recomputed in the canonical order; logits [T,E]
-// is scratch.  status receives the GEMM's wait errors.
+// allows (router_screened) the logits come from the tensor cores, every
+// score gets an interval that provably holds its fixed-order value, and only
+// the experts those intervals leave undecided get their fixed-order logit;
+// logits [T,E] is then unused.  status receives the GEMM's wait errors.
 bool router_screened(int T, int d, int E, int G, int k);
 int router_launches(int T, int d, int E, int G, int k);
+size_t screened_scratch_bytes(int T, int d, int E);
 cudaError_t launch_router(const void *x, const void *w_r, const float *bias, int T, int d, int E,
                           int G, int topk_group, int k, int score, float bias_scale,
                           float *logits, int32_t *ids, float *weights, void *w_scratch,
                           uint32_t *status, cudaStream_t s);
-// tokens of the last launch_router call that took the canonical path
-// (device int in the router scratch; nullptr when the call was not screened)
-const int32_t *router_flagged_count(const void *w_scratch, int T, int d, int E, int G, int k);
+// The screened path's copy of the router weight: transposed to [E, d], then
+// the norms of the columns, router_prep_bytes(d, E) bytes.  A copy made by
+// launch_router_prepare into a caller buffer and registered for w_r is used
+// by every launch_router call with that w_r (and d, E) instead of one made
+// in the scratch on each call.
+size_t router_prep_bytes(int d, int E);
+cudaError_t launch_router_prepare(const void *w_r, int d, int E, void *prep, cudaStream_t s);
+bool router_register_prepared(const void *w_r, int d, int E, void *prep);
+bool router_release_prepared(const void *w_r);
+// (token, expert) pairs the last screened launch_router call on this scratch
+// refined (device int; nullptr when the shape is not screened)
+const int32_t *router_refined_count(const void *w_scratch, int T, int d, int E, int G, int k);
 
 // dispatch.cu
 // Assignments per dispatch chunk: 128 up to 32768 assignments (enough chunks

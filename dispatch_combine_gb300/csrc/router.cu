@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "route_common.cuh"
 
 namespace moe {
 namespace {
@@ -455,50 +456,6 @@ cudaError_t run_logits(const void *x, const uint16_t *wpad, int T, int d, int E,
   return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------------------
-// exp / sigmoid with a fixed evaluation (Cody & Waite 1980 argument
-// reduction; Taylor polynomial of degree 7).
-// ---------------------------------------------------------------------------
-// ln 2 split: head = fl(ln 2) with its 8 low stored bits cleared (16
-// significant bits), tail = fl(ln 2 - head).
-__device__ __forceinline__ float canon_exp(float y) {
-  const float kLn2Head = 0x1.62e4p-1f;
-  const float kLn2Tail = 0x1.7f7d1cp-20f;
-  const float kLog2e = 0x1.715476p+0f;
-  y = fminf(fmaxf(y, -80.0f), 80.0f);
-  const float n = rintf(__fmul_rn(y, kLog2e));
-  float r = __fmaf_rn(-n, kLn2Head, y);
-  r = __fmaf_rn(-n, kLn2Tail, r);
-  // 1/j! rounded to fp32
-  float p = 0x1.a01a02p-13f;
-  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
-  p = __fmaf_rn(p, r, 0x1.111112p-7f);
-  p = __fmaf_rn(p, r, 0x1.555556p-5f);
-  p = __fmaf_rn(p, r, 0x1.555556p-3f);
-  p = __fmaf_rn(p, r, 0x1p-1f);
-  p = __fmaf_rn(p, r, 0x1p+0f);
-  p = __fmaf_rn(p, r, 0x1p+0f);
-  const int ni = static_cast<int>(n);
-  return __fmul_rn(p, __int_as_float((ni + 127) << 23));  // exact: result is normal
-}
-
-__device__ __forceinline__ float canon_sigmoid(float l) {
-  return __fdiv_rn(1.0f, __fadd_rn(1.0f, canon_exp(-l)));
-}
-
-// (value desc, index asc) arg-max over the warp
-__device__ __forceinline__ void warp_argmax(float &v, int &idx) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, off);
-    if (ov > v || (ov == v && oi < idx)) {
-      v = ov;
-      idx = oi;
-    }
-  }
-}
-
 constexpr int kSelWarps = 8;
 
 // One warp per token.  Lane l holds experts l, l+32, ... (E <= 1024).
@@ -731,371 +688,10 @@ __global__ void __launch_bounds__(kSelWarps * 32)
   if (lane < k) weights[(size_t)t * k + lane] = __fdiv_rn(v, sum);
 }
 
-// ---------------------------------------------------------------------------
-// Screened routing.  The logits l[t,e] = sum_i x[t,i] W_r[i,e] come from the
-// tensor cores (bf16 operands, fp32 accumulation in the hardware's order),
-// which differ from the canonical fp32 order by a rounding-level amount.  A
-// token's selection is settled by them when its two decision margins -- the
-// last kept group's score minus the best dropped group's, and the k-th
-// selected score minus the best unselected eligible one -- are both at least
-// kScreenDelta.  A sigmoid score moves by at most a quarter of its logit's
-// error (a softmax score is the logit), a group score by at most twice
-// that, and a margin by at most twice its terms' moves, so any logit error
-// below kScreenDelta / 4 leaves the kept groups and the selected set as
-// they are.  Those tokens get the canonical logits of
-// their k experts only (the order of the tiled kernel) and take their output
-// order and weights from them: ids and weights are the canonical ones.
-// Every other token, or one with a non-finite tensor-core logit, goes to a
-// list that gets all E canonical logits and the plain selection.
-// ---------------------------------------------------------------------------
-constexpr float kScreenDelta = 1e-3f;
-
-// transposed weight wt [E, d] for the tensor-core pass, the one-group tile
-// table of that GEMM (rows [0, T), 128-row tiles) and the list counter
-__global__ void __launch_bounds__(256)
-    router_tc_prep_kernel(const uint16_t *__restrict__ w_r, int d, int E, int T,
-                          uint16_t *__restrict__ wt, int32_t *__restrict__ seg,
-                          int32_t *__restrict__ mtile, int32_t *__restrict__ count,
-                          float *__restrict__ zero, int64_t n_zero) {
-  pdl_begin();
-  // 64 x 64 tile (d and E are multiples of 64), 16-byte loads and stores
-  __shared__ __align__(16) uint16_t tile[64][72];
-  const int e0 = blockIdx.x * 64, i0 = blockIdx.y * 64;
-  const int tid = threadIdx.x;
-  // the logits, when the GEMM adds K pieces into them
-  const int64_t nthr = static_cast<int64_t>(gridDim.x) * gridDim.y * 256;
-  for (int64_t q = (static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x) * 256 + tid;
-       q < n_zero; q += nthr)
-    zero[q] = 0.0f;
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int q = tid + 256 * r;
-    const int il = q >> 3, ch = q & 7;  // input row of the tile, 8-expert chunk
-    *reinterpret_cast<uint4 *>(&tile[il][ch * 8]) =
-        __ldg(reinterpret_cast<const uint4 *>(w_r + (size_t)(i0 + il) * E + e0 + ch * 8));
-  }
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int q = tid + 256 * r;
-    const int el = q & 63, ch = q >> 6;  // expert row of wt, 8-input chunk
-    uint32_t h[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      h[j] = static_cast<uint32_t>(tile[ch * 8 + 2 * j][el]) |
-             (static_cast<uint32_t>(tile[ch * 8 + 2 * j + 1][el]) << 16);
-    *reinterpret_cast<uint4 *>(wt + (size_t)(e0 + el) * d + i0 + ch * 8) =
-        make_uint4(h[0], h[1], h[2], h[3]);
-  }
-  if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) {
-    seg[0] = 0;
-    seg[1] = T;
-    mtile[0] = 0;
-    mtile[1] = (T + kGemmTileRows - 1) / kGemmTileRows;
-    *count = 0;
-  }
-}
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float f[8]) {
-  f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
-  f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-  f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
-  f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
-}
-
-// xor butterfly over the warp (offsets 16 .. 1): every lane ends with the
-// canonical combination of the 32 lane sums
-__device__ __forceinline__ float butterfly_sum(float v) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
-  return v;
-}
-
-// Fixed-order dot product of a bf16 row pair of nch 8-element chunks (x in
-// shared memory): lane l sums chunks l, l+32, ... in increasing order, then
-// the xor butterfly.  The weight chunks are loaded eight (then four) ahead;
-// the x chunks come from shared memory when they are used.
-template <int U>
-__device__ __forceinline__ void canon_block(const uint4 *xr, const uint4 *__restrict__ wr, int c,
-                                            float &acc) {
-  uint4 wv[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) wv[u] = __ldg(wr + c + 32 * u);
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    float xf[8], wf[8];
-    bf16x8_to_f32(xr[c + 32 * u], xf);
-    bf16x8_to_f32(wv[u], wf);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc = __fmaf_rn(xf[i], wf[i], acc);
-  }
-}
-__device__ __forceinline__ float canon_dot(const uint4 *xr, const uint4 *__restrict__ wr,
-                                           int nch, int lane) {
-  float acc = 0.0f;
-  int c = lane;
-  for (; c + 32 * 7 < nch; c += 32 * 8) canon_block<8>(xr, wr, c, acc);
-  if (c + 32 * 3 < nch) {
-    canon_block<4>(xr, wr, c, acc);
-    c += 32 * 4;
-  }
-  for (; c < nch; c += 32) canon_block<1>(xr, wr, c, acc);
-  return butterfly_sum(acc);
-}
-
-// One CTA (8 warps) per token.  Warp 0 selects on the tensor-core logits
-// and takes the two margins; a token that passes gets the fixed-order
-// logits of its k experts (warp w: selected experts w, w+8, ...), then warp
-// 0 orders them and writes ids and weights.  A token that fails is appended
-// to list.
-constexpr int kScreenWarps = 8;
-template <int PER>
-__global__ void __launch_bounds__(kScreenWarps * 32)
-    router_screen_kernel(const float *__restrict__ logits, const float *__restrict__ bias,
-                         const uint16_t *__restrict__ x, const uint16_t *__restrict__ wt, int T,
-                         int d, int E, int G, int topk_group, int k, int score,
-                         float bias_scale, int32_t *__restrict__ ids,
-                         float *__restrict__ weights, int32_t *__restrict__ list,
-                         int32_t *__restrict__ count) {
-  pdl_begin();
-  __shared__ int32_t sh_id[32];
-  __shared__ float sh_l[32];
-  __shared__ int sh_ok;
-  extern __shared__ uint4 sh_x[];  // the token's row, d / 8 chunks
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int t = blockIdx.x;
-  const float kInf = __int_as_float(0x7f800000);
-  const bool sig = score != MOE_SCORE_SOFTMAX;
-  const int nch = d / 8;
-
-  if (warp != 0) {
-    // warps 1..7 bring the token's row into shared memory meanwhile
-    const uint4 *xg = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
-    for (int c = threadIdx.x - 32; c < nch; c += (kScreenWarps - 1) * 32) sh_x[c] = __ldg(xg + c);
-  } else {
-    const float *lt = logits + (size_t)t * E;
-    const int e0 = lane * PER;
-    float s[PER];
-    bool finite = true;
-#pragma unroll
-    for (int m = 0; m < PER; ++m) {
-      const int e = e0 + m;
-      s[m] = -kInf;
-      if (e < E) {
-        const float l = lt[e];
-        finite = finite && isfinite(l);
-        s[m] = sig ? __fadd_rn(canon_sigmoid(l), __fmul_rn(bias_scale, bias[e])) : l;
-      }
-    }
-    uint32_t eligible = 0;
-#pragma unroll
-    for (int m = 0; m < PER; ++m)
-      if (e0 + m < E) eligible |= 1u << m;
-
-    float gmargin = kInf;
-    if (G > 1) {
-      const int gs = E / G;
-      const int lpg = gs / PER;
-      float m1 = -kInf, m2 = -kInf;
-#pragma unroll
-      for (int m = 0; m < PER; ++m) {
-        const float v = s[m];
-        if (v > m1) {
-          m2 = m1;
-          m1 = v;
-        } else if (v > m2) {
-          m2 = v;
-        }
-      }
-      for (int off = 1; off < lpg; off <<= 1) {
-        const float o1 = __shfl_xor_sync(0xffffffffu, m1, off);
-        const float o2 = __shfl_xor_sync(0xffffffffu, m2, off);
-        if (m1 >= o1) {
-          m2 = fmaxf(m2, o1);
-        } else {
-          m2 = fmaxf(m1, o2);
-          m1 = o1;
-        }
-      }
-      const float mine = (gs >= 2) ? __fadd_rn(m1, m2) : m1;
-      const int my_group = (e0 < E) ? e0 / gs : G;
-      int rank = 0;
-      for (int g = 0; g < G; ++g) {
-        const float o = __shfl_sync(0xffffffffu, mine, g * lpg);
-        rank += (o > mine || (o == mine && g < my_group)) ? 1 : 0;
-      }
-      float kept_min = kInf, rest_max = -kInf;
-      for (int g = 0; g < G; ++g) {
-        const float o = __shfl_sync(0xffffffffu, mine, g * lpg);
-        const int rk = __shfl_sync(0xffffffffu, rank, g * lpg);
-        if (rk < topk_group)
-          kept_min = fminf(kept_min, o);
-        else
-          rest_max = fmaxf(rest_max, o);
-      }
-      gmargin = __fsub_rn(kept_min, rest_max);
-      if (my_group >= G || rank >= topk_group) eligible = 0;
-    }
-
-    int my_id = 0;
-    float sk = kInf, sk1 = -kInf;
-    for (int j = 0; j <= k; ++j) {
-      float bv = -kInf;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int m = 0; m < PER; ++m) {
-        if ((eligible >> m) & 1u) {
-          if (s[m] > bv || bi == 0x7fffffff) {
-            bv = s[m];
-            bi = e0 + m;
-          }
-        }
-      }
-      warp_argmax(bv, bi);
-      if (j == k) {
-        if (bi != 0x7fffffff) sk1 = bv;
-        break;
-      }
-      if (bi != 0x7fffffff && bi / PER == lane) eligible &= ~(1u << (bi - e0));
-      if (lane == j) my_id = bi;
-      if (j == k - 1) sk = bv;
-    }
-    const float emargin = __fsub_rn(sk, sk1);
-    const bool ok = __all_sync(0xffffffffu, finite) && gmargin >= kScreenDelta &&
-                    emargin >= kScreenDelta;
-    if (lane < k) sh_id[lane] = my_id;
-    if (lane == 0) {
-      sh_ok = ok ? 1 : 0;
-      if (!ok) list[atomicAdd(count, 1)] = t;
-    }
-  }
-  __syncthreads();
-  if (!sh_ok) return;
-
-  for (int j = warp; j < k; j += kScreenWarps) {
-    const int e = min(max(sh_id[j], 0), E - 1);  // always in range; guards the load
-    const uint4 *wr = reinterpret_cast<const uint4 *>(wt + (size_t)e * d);
-    const float v = canon_dot(sh_x, wr, nch, lane);
-    if (lane == 0) sh_l[j] = v;
-  }
-  __syncthreads();
-  if (warp != 0) return;
-
-  // fixed-order scores: output order (score desc, index asc) and weights
-  const bool act = lane < k;
-  const int my_id = act ? sh_id[lane] : 0;
-  const float lsel = act ? sh_l[lane] : 0.0f;
-  const float sc = act ? (sig ? __fadd_rn(canon_sigmoid(lsel), __fmul_rn(bias_scale, bias[my_id]))
-                              : lsel)
-                       : -kInf;
-  int r = 0;
-  for (int i = 0; i < k; ++i) {
-    const float si = __shfl_sync(0xffffffffu, sc, i);
-    const int ei = __shfl_sync(0xffffffffu, my_id, i);
-    if (si > sc || (si == sc && ei < my_id)) ++r;
-  }
-  const int top = __ffs(__ballot_sync(0xffffffffu, act && r == 0)) - 1;
-  const float l0 = __shfl_sync(0xffffffffu, lsel, top & 31);
-  const float v = act ? (sig ? canon_sigmoid(lsel) : canon_exp(__fsub_rn(lsel, l0))) : 0.0f;
-  float sum = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const int src = __ffs(__ballot_sync(0xffffffffu, act && r == j)) - 1;
-    const float vj = __shfl_sync(0xffffffffu, v, src & 31);
-    sum = (j == 0) ? vj : __fadd_rn(sum, vj);
-  }
-  if (act) {
-    ids[(size_t)t * k + r] = my_id;
-    weights[(size_t)t * k + r] = __fdiv_rn(v, sum);
-  }
-}
-
-// All E canonical logits of the listed tokens, into their rows of logits.
-// Items are (4 listed tokens, 8 * EPW experts): the CTA stages the 4 token
-// rows in shared memory, and warp w takes experts EPW*w .. EPW*w+EPW-1 for
-// the 4 tokens at once (4 * EPW independent sums, each in the fixed order),
-// loading the weight chunks two steps ahead.  EPW = 8 for many listed
-// tokens, 2 for few (more CTAs per token).
-constexpr int kListTok = 4;
-template <int EPW>
-__global__ void __launch_bounds__(256, 2)
-    router_list_logits_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wt,
-                              int d, int E, const int32_t *__restrict__ list,
-                              const int32_t *__restrict__ count, float *__restrict__ logits) {
-  pdl_begin();
-  constexpr int kListSlice = 8 * EPW;
-  extern __shared__ uint4 sh_xl[];  // [kListTok][d / 8]
-  const int n = *count;
-  const int slices = E / kListSlice;
-  const int items = (n + kListTok - 1) / kListTok * slices;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nch = d / 8;
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    const int grp = it / slices, sl = it % slices;
-    int tk[kListTok];
-#pragma unroll
-    for (int q = 0; q < kListTok; ++q) {
-      const int f = grp * kListTok + q;
-      tk[q] = f < n ? list[f] : -1;
-    }
-    __syncthreads();  // the previous item's reads of sh_xl are done
-#pragma unroll
-    for (int q = 0; q < kListTok; ++q) {
-      const uint4 *xg = reinterpret_cast<const uint4 *>(
-          x + (size_t)(tk[q] >= 0 ? tk[q] : list[grp * kListTok]) * d);
-      for (int c = threadIdx.x; c < nch; c += 256) sh_xl[q * nch + c] = __ldg(xg + c);
-    }
-    __syncthreads();
-    const int eb = sl * kListSlice + warp * EPW;
-    const uint4 *wr = reinterpret_cast<const uint4 *>(wt + (size_t)eb * d);
-    float acc[EPW][kListTok];
-#pragma unroll
-    for (int ee = 0; ee < EPW; ++ee)
-#pragma unroll
-      for (int q = 0; q < kListTok; ++q) acc[ee][q] = 0.0f;
-    auto step = [&](int c, const uint4 (&wv)[EPW]) {
-#pragma unroll
-      for (int q = 0; q < kListTok; ++q) {
-        float xf[8];
-        bf16x8_to_f32(sh_xl[q * nch + c], xf);
-#pragma unroll
-        for (int ee = 0; ee < EPW; ++ee) {
-          float wf[8];
-          bf16x8_to_f32(wv[ee], wf);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[ee][q] = __fmaf_rn(xf[i], wf[i], acc[ee][q]);
-        }
-      }
-    };
-    int c = lane;
-    for (; c + 32 < nch; c += 64) {
-      uint4 wa[EPW], wb[EPW];
-#pragma unroll
-      for (int ee = 0; ee < EPW; ++ee) {
-        wa[ee] = __ldg(wr + (size_t)ee * nch + c);
-        wb[ee] = __ldg(wr + (size_t)ee * nch + c + 32);
-      }
-      step(c, wa);
-      step(c + 32, wb);
-    }
-    if (c < nch) {
-      uint4 wa[EPW];
-#pragma unroll
-      for (int ee = 0; ee < EPW; ++ee) wa[ee] = __ldg(wr + (size_t)ee * nch + c);
-      step(c, wa);
-    }
-#pragma unroll
-    for (int ee = 0; ee < EPW; ++ee)
-#pragma unroll
-      for (int q = 0; q < kListTok; ++q) {
-        const float v = butterfly_sum(acc[ee][q]);
-        if (lane == 0 && tk[q] >= 0) logits[(size_t)tk[q] * E + eb + ee] = v;
-      }
-  }
-}
+}  // namespace
 
 // experts per lane of the fast selection (0: the general kernel is needed)
-int select_per(int E, int G) {
+int router_select_per(int E, int G) {
   int per = 1;
   while (per * 32 < E) per *= 2;
   if (per > 32) return 0;
@@ -1107,20 +703,9 @@ int select_per(int E, int G) {
   return per;
 }
 
-// router scratch of the screened path: wt [E, d] bf16, list [T], then
-// count, seg[2], mtile[2]
-size_t screened_list_off(int d, int E) {
-  return (static_cast<size_t>(E) * d * sizeof(uint16_t) + 255) / 256 * 256;
-}
-size_t screened_misc_off(int T, int d, int E) {
-  return screened_list_off(d, E) + (static_cast<size_t>(T) * 4 + 255) / 256 * 256;
-}
-
-}  // namespace
-
 size_t router_scratch_bytes(int T, int d, int E) {
   const size_t pad = static_cast<size_t>(router_d_pad(d)) * router_e_pad(E) * sizeof(uint16_t);
-  const size_t scr = screened_misc_off(T, d, E) + 64;
+  const size_t scr = screened_scratch_bytes(T, d, E);
   return pad > scr ? pad : scr;
 }
 
@@ -1163,7 +748,7 @@ cudaError_t select_impl(const float *logits, const float *bias, int T, int E, in
                         cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int grid = (T + kSelWarps - 1) / kSelWarps;
-  const int per = select_per(E, G);
+  const int per = router_select_per(E, G);
   if (per != 0) {
 #define MOE_SELECT_FAST(P)                                                                  \
   case P:                                                                                   \
@@ -1197,137 +782,5 @@ cudaError_t launch_router_select(const float *logits, const float *bias, int T, 
                      nullptr, nullptr, s);
 }
 
-bool router_screened(int T, int d, int E, int G, int k) {
-  // the listed-token kernel keeps 4 token rows in shared memory: d <= 16K
-  return T > 0 && d % 64 == 0 && d <= 16384 && E % 64 == 0 && E <= 1024 && k <= 32 &&
-         select_per(E, G) != 0;
-}
-
-int router_launches(int T, int d, int E, int G, int k) {
-  // prep, GEMM, screen, listed logits, listed selection
-  if (router_screened(T, d, E, G, k)) return 5;
-  return router_logits_launches(d, E) + 1;
-}
-
-const int32_t *router_flagged_count(const void *w_scratch, int T, int d, int E, int G, int k) {
-  if (!router_screened(T, d, E, G, k)) return nullptr;
-  return reinterpret_cast<const int32_t *>(static_cast<const uint8_t *>(w_scratch) +
-                                           screened_misc_off(T, d, E));
-}
-
-cudaError_t launch_router(const void *x, const void *w_r, const float *bias, int T, int d, int E,
-                          int G, int topk_group, int k, int score, float bias_scale,
-                          float *logits, int32_t *ids, float *weights, void *w_scratch,
-                          uint32_t *status, cudaStream_t s) {
-  if (T == 0) return cudaSuccess;
-  if (!router_screened(T, d, E, G, k)) {
-    cudaError_t err = launch_router_logits(x, w_r, T, d, E, logits, w_scratch, s);
-    if (err != cudaSuccess) return err;
-    return launch_router_select(logits, bias, T, E, G, topk_group, k, score, bias_scale, 0, ids,
-                                weights, s);
-  }
-  uint8_t *base = static_cast<uint8_t *>(w_scratch);
-  uint16_t *wt = reinterpret_cast<uint16_t *>(base);
-  int32_t *list = reinterpret_cast<int32_t *>(base + screened_list_off(d, E));
-  int32_t *misc = reinterpret_cast<int32_t *>(base + screened_misc_off(T, d, E));
-  int32_t *count = misc, *seg = misc + 2, *mtile = misc + 4;
-  // tensor-core logits: one group of T rows, n = E outputs; the widest tile
-  // that still gives half the SMs a tile, and with fewer tiles than SMs the
-  // K range split in pieces of at least 8 k-blocks (64 inputs each)
-  const int64_t mt = (T + kGemmTileRows - 1) / kGemmTileRows;
-  int bn = 64;
-  for (int b = 256; b > 64; b >>= 1)
-    if (E % b == 0 && mt * (E / b) * 2 >= num_sms()) {
-      bn = b;
-      break;
-    }
-  const int64_t tiles = mt * (E / bn);
-  int ksplit = 1;
-  if (tiles < num_sms()) {
-    const int64_t by_sms = num_sms() / tiles;
-    const int64_t by_k = d / 64 / 8;
-    ksplit = static_cast<int>(by_sms < by_k ? by_sms : by_k);
-    if (ksplit < 1) ksplit = 1;
-  }
-  MOE_LAUNCH_PDL(router_tc_prep_kernel, dim3(E / 64, d / 64), 256, 0, s, 
-      static_cast<const uint16_t *>(w_r), d, E, T, wt, seg, mtile, count, logits,
-      ksplit > 1 ? static_cast<int64_t>(T) * E : 0);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-
-  GemmProblem p;
-  std::memset(&p, 0, sizeof p);
-  p.E = 1;
-  p.K = d;
-  p.n_out = E;
-  p.layout = MOE_LAYOUT_CONTIGUOUS;
-  p.seg = seg;
-  p.rows_total = T;
-  p.mtile_base = mtile;
-  p.a = x;
-  p.b = wt;
-  p.b_rows = E;
-  p.out = logits;
-  p.status = status;
-  p.bn = bn;
-  p.ksplit = ksplit;
-  err = launch_gemm_down(p, s);
-  if (err != cudaSuccess) return err;
-
-  const uint16_t *xs = static_cast<const uint16_t *>(x);
-  const size_t xbytes = static_cast<size_t>(d) * sizeof(uint16_t);
-  if (xbytes > 48 * 1024) {
-    // rows above 48 KB (d > 24576) need the opt-in shared-memory size
-    const int need = static_cast<int>(xbytes);
-#define MOE_SCREEN_ATTR(P)                                                              \
-  err = cudaFuncSetAttribute(router_screen_kernel<P>,                                   \
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, need);        \
-  if (err != cudaSuccess) return err;
-    MOE_SCREEN_ATTR(2)
-    MOE_SCREEN_ATTR(4)
-    MOE_SCREEN_ATTR(8)
-    MOE_SCREEN_ATTR(16)
-    MOE_SCREEN_ATTR(32)
-#undef MOE_SCREEN_ATTR
-  }
-  switch (select_per(E, G)) {
-#define MOE_SCREEN(P)                                                                      \
-  case P:                                                                                  \
-    MOE_LAUNCH_PDL(router_screen_kernel<P>, T, kScreenWarps * 32, xbytes, s, logits, bias, xs, wt, T, d, E, G, \
-                                                            topk_group, k, score,          \
-                                                            bias_scale, ids, weights, list, \
-                                                            count);                        \
-    break;
-    MOE_SCREEN(2)
-    MOE_SCREEN(4)
-    MOE_SCREEN(8)
-    MOE_SCREEN(16)
-    MOE_SCREEN(32)
-#undef MOE_SCREEN
-    default:
-      return cudaErrorInvalidValue;
-  }
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-
-  // listed tokens are ~7 % of T: few at small T, where more CTAs per token
-  // (2 experts per warp) shorten the kernel
-  const bool few = T <= 4096;
-  auto list_kernel = few ? router_list_logits_kernel<2> : router_list_logits_kernel<8>;
-  const int64_t items = (static_cast<int64_t>(T) + kListTok - 1) / kListTok * (E / (few ? 16 : 64));
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 4;
-  const size_t lbytes = kListTok * xbytes;
-  if (lbytes > 48 * 1024) {
-    err = cudaFuncSetAttribute(list_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(lbytes));
-    if (err != cudaSuccess) return err;
-  }
-  MOE_LAUNCH_PDL(list_kernel, static_cast<unsigned>(items < cap ? items : cap), 256, lbytes, s, 
-      xs, wt, d, E, list, count, logits);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  return select_impl(logits, bias, T, E, G, topk_group, k, score, bias_scale, 0, ids, weights,
-                     list, count, s);
-}
 
 }  // namespace moe

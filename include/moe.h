@@ -103,8 +103,8 @@ moe_status_t moe_expert_ffn_workspace_size(const moe_shape_t *shape, int32_t lay
 
 /* Prepares a fresh workspace (async): clears the device status word and the
  * flags the expert FFN's down GEMM uses between CTAs (zero at rest, and left
- * zero by every call that completes).  Call once before the workspace's first
- * use. */
+ * zero by every call that completes).  Call once before the workspace's
+ * first use. */
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronises `stream`, returns the OR of device-side errors recorded in the
@@ -131,14 +131,19 @@ moe_status_t moe_get_device_status(void *ws, size_t ws_bytes, moe_stream_t strea
  * 32 lane sums are combined by an xor butterfly), and sigmoid/exp use a
  * fixed Cody-Waite + Taylor evaluation, so ids are reproducible bit-exactly.
  * With logits == NULL, d % 64 == 0, d <= 16384 and E % 64 == 0 the call is
- * screened: the logits are first taken on the tensor cores; a token whose
- * margins (last kept group score minus best dropped one, k-th selected score
- * minus the best unselected eligible one; scores are the logits for softmax)
- * are both >= 1e-3 keeps that selection, with its order and weights from the
- * fixed-order logits of its k experts; every other token gets all E
- * fixed-order logits.  The outputs are those of the fixed order whenever
- * every tensor-core logit is within 2.5e-4 of it (moe_route_screened_count
- * reports the fallbacks).
+ * screened, with the same outputs: the logits are first taken on the tensor
+ * cores, where every accumulation chain is 8 MMAs long; each score gets an
+ * interval that holds its fixed-order value, from the bound
+ *   |l_tc - l_fixed| <= alpha(d) * ||x_t||_2 * ||w_e||_2
+ * (alpha is about 8e-5 at d = 7168; it covers the fixed order's own
+ * rounding and tensor-core accumulation whose every MMA errs by up to 2^-17
+ * of the magnitudes it adds, 64 units in the last place); every expert whose
+ * selection (or whose group's keep decision) the intervals leave open gets
+ * its fixed-order logit, and the selection is made on those.  Every selected
+ * expert is among them, so its weight and order come from fixed-order
+ * logits.  The outputs equal the fixed-order ones for any finite input, with
+ * no margin or data-dependent condition; moe_route_refined_count reports how
+ * many fixed-order logits a call computed.
  */
 moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *w_r,
                        const float *bias, int32_t *topk_ids, float *topk_w,
@@ -406,13 +411,41 @@ moe_status_t moe_eplb_plan(const double *load, int32_t num_experts, int32_t num_
 int32_t moe_layer_launch_count(const moe_shape_t *shape);
 
 /*
- * Tokens that the last screened routing in `ws` (moe_route without logits,
- * moe_layer, moe_layer_capacity, moe_layer_fp8 of this shape) sent to the
- * full fixed-order path: copies one int32 to device memory `count` on
+ * (token, expert) pairs whose fixed-order logit the last screened routing in
+ * `ws` (moe_route without logits, moe_layer, moe_layer_capacity,
+ * moe_layer_fp8 of this shape) computed -- at least T*k, since every
+ * selected expert is refined: copies one int32 to device memory `count` on
  * `stream` (asynchronous); -1 when the shape is not screened.
  */
-moe_status_t moe_route_screened_count(const moe_shape_t *shape, const void *ws, size_t ws_bytes,
-                                      int32_t *count, moe_stream_t stream);
+moe_status_t moe_route_refined_count(const moe_shape_t *shape, const void *ws, size_t ws_bytes,
+                                     int32_t *count, moe_stream_t stream);
+
+/*
+ * A prepared copy of a router weight for the screened path, so that screened
+ * calls skip making it (about 3.7 MB read and written, two launches, at
+ * d = 7168, E = 256).
+ *   moe_router_prep_size: bytes of the copy for this shape (E*d*2 rounded up
+ *     to 256, plus E*4 rounded up to 256; depends on d and E only);
+ *     MOE_ERR_UNSUPPORTED when the shape is not screened.
+ *   moe_router_prepare: writes the copy of w_r [d,E] (transposed to [E,d],
+ *     then the norm of every expert's weight column) into `prep`, device
+ *     memory the caller owns (256-byte aligned, prep_bytes >= the size),
+ *     asynchronously on `stream`, and records `prep` for the pointer w_r.
+ *     Every later screened call (moe_route without logits, moe_layer,
+ *     moe_layer_capacity, moe_layer_fp8) whose w_r is this pointer and whose
+ *     d and E match reads the copy instead of making one.  Up to 64 weights
+ *     can be recorded (MOE_ERR_UNSUPPORTED beyond).  Preparing the same w_r
+ *     again replaces its record.
+ *   moe_router_release: drops the record of w_r (no-op if none).
+ * The record follows the pointer, not the contents: call moe_router_prepare
+ * again after changing the weight in place, and moe_router_release before
+ * freeing the weight or `prep` (an allocator may hand the same address to
+ * another tensor).  `prep` must stay valid while recorded.
+ */
+moe_status_t moe_router_prep_size(const moe_shape_t *shape, size_t *bytes);
+moe_status_t moe_router_prepare(const moe_shape_t *shape, const void *w_r, void *prep,
+                                size_t prep_bytes, moe_stream_t stream);
+moe_status_t moe_router_release(const void *w_r);
 
 /*
  * Self-test of the bounded wait used by every device-side spin: launches one
