@@ -786,6 +786,9 @@ def parse_args(argv=None):
                     help="time one bandwidth stage alone on seeded ids (own line)")
     ap.add_argument("--route-only", action="store_true",
                     help="time the router alone (screened and fixed-order; own line)")
+    ap.add_argument("--ffn-counts", default=None, metavar="WORKLOAD:N",
+                    help="time the expert FFN alone on N of the workload's touched experts with "
+                         "their real row counts (own line)")
     ap.add_argument("--ffn-rows", default=None, metavar="E,R",
                     help="time the expert FFN alone on E experts x R rows at the workload's "
                          "d and inter (bf16, or FP8 with --fp8; own line)")
@@ -978,6 +981,84 @@ def run_ffn_only(args):
     return 0
 
 
+def run_ffn_counts(args):
+    """Expert FFN alone on a subset of a workload's experts with their real
+    row counts (own line): the workload's tokens are routed on the GPU, the
+    touched experts ranked by count, and every (touched / n)-th of them kept,
+    so the subset's count mix follows the full launch's; the rows are the
+    tokens those experts received, in dispatch order.  Small enough on the
+    device for an ncu capture (weights of n experts only)."""
+    import torch
+    import dispatch_combine_gb300 as moe
+    from moe_inputs import make_layer_tensors
+    torch.cuda.set_device(0)
+    name, n_sub = args.ffn_counts.split(":")
+    c = CONFIGS[name]
+    n_sub = int(n_sub)
+    t = make_layer_tensors(c, device="cuda", seed=0, keep_experts=[])
+    shape = c.shape()
+    ws = moe.Workspace(moe.moe_workspace_size(shape))
+    bias = t["bias"] if c.score == SCORE_SIGMOID_BIAS else None
+    ids, _, _ = moe.moe_route(shape, t["x"], t["w_r"], bias, ws)
+    counts, offsets, src, _, _ = moe.moe_dispatch(shape, ids, None, ws)
+    cnt = counts.cpu()
+    touched = [int(e) for e in torch.argsort(cnt, descending=True, stable=True) if cnt[e] > 0]
+    step = max(1, len(touched) // n_sub)
+    sub = sorted(touched[::step][:n_sub])
+    del ws
+    tw = make_layer_tensors(c, device="cuda", seed=0, with_x=False, keep_experts=sub)
+    off_h = offsets.cpu()
+    rows = torch.cat([src[int(off_h[e]):int(off_h[e + 1])] for e in sub]).long()
+    x = t["x"][rows].contiguous()
+    sub_counts = torch.tensor([int(cnt[e]) for e in sub], dtype=torch.int32)
+    offs = torch.zeros(len(sub) + 1, dtype=torch.int32)
+    offs[1:] = torch.cumsum(sub_counts, 0)
+    offs = offs.cuda()
+    fshape = dict(T=int(rows.numel()), d=c.d, E=len(sub), G=1, topk_group=1, k=1,
+                  inter=c.inter, score=1, bias_scale=0.15)
+    fws = moe.Workspace(moe.moe_expert_ffn_workspace_size(fshape, moe.MOE_LAYOUT_CONTIGUOUS))
+    y = torch.empty(rows.numel(), c.d, dtype=torch.float32, device="cuda")
+    del t
+
+    def step_fn():
+        moe.moe_expert_ffn(fshape, moe.MOE_LAYOUT_CONTIGUOUS, x, offs, 0, tw["w_gate_up"],
+                           tw["w_down"], fws, y_out=y)
+
+    for _ in range(args.warmup):
+        step_fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step_fn()
+    e1.record()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(fws) != 0:
+        raise SystemExit("device status error")
+    us = e0.elapsed_time(e1) * 1000.0 / max(args.steps, 1)
+    R = int(rows.numel())
+    gu_w = len(sub) * 2 * c.inter * c.d * 2
+    dn_w = len(sub) * c.d * c.inter * 2
+    line = {
+        "metric": "expert FFN on a real-count expert subset: us per call", "impl": "gb300",
+        "value": us, "unit": "us", "higher_is_better": False, "steps": args.steps,
+        "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{len(sub)} of the {len(touched)} experts touched by "
+                               f"{workload_desc(c)}, every {step}-th by count",
+                   "experts": sub, "counts": sub_counts.tolist(), "rows": R},
+        # algorithmic bytes of each GEMM launch on the subset: weights once,
+        # rows in, result out (h bf16; y fp32)
+        "algorithmic_bytes": {"gate_up": gu_w + R * c.d * 2 + R * c.inter * 2,
+                              "down": dn_w + R * c.inter * 2 + R * c.d * 4},
+        "full_launch_algorithmic_bytes": {
+            "gate_up": len(touched) * 2 * c.inter * c.d * 2 + c.T * c.k * (c.d + c.inter) * 2,
+            "down": len(touched) * c.d * c.inter * 2 + c.T * c.k * (c.inter * 2 + c.d * 4)},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_capacity(args):
     """Time the capacity variant of the layer (its own JSON line): capacity
     C = ceil(c*T*k/E) per expert, overflow dropped or run in a second round."""
@@ -1136,6 +1217,8 @@ def main(argv=None):
     c = CONFIGS[args.config]
     if args.ffn_rows:
         return run_ffn_only(args)
+    if args.ffn_counts:
+        return run_ffn_counts(args)
     if args.route_only:
         return run_route_only(args)
     if args.stage_only:

@@ -97,7 +97,7 @@ def _normal_bf16(shape, std: float, g: torch.Generator, device) -> torch.Tensor:
 
 def make_layer_tensors(cfg: LayerConfig, device="cpu", seed: int = 0,
                        n_tokens: int | None = None, with_x: bool = True,
-                       extra_x: dict | None = None) -> dict:
+                       extra_x: dict | None = None, keep_experts=None) -> dict:
     """Draw W_r, bias, W_gate_up, W_down and x for ``cfg`` (see module doc).
 
     Returns a dict of torch tensors on ``device``:
@@ -109,6 +109,9 @@ def make_layer_tensors(cfg: LayerConfig, device="cpu", seed: int = 0,
     the generator state that follows the weights, i.e. the x that
     ``make_layer_tensors`` gives a workload with the same weights and that
     many tokens (returned as ``out["x_" + name]``).
+    ``keep_experts`` (a list of expert indices) keeps only those experts'
+    weights, in that order: every expert is still drawn, so x and the kept
+    weights are the ones the full draw gives.
     """
     device = torch.device(device)
     g = _gen(device, seed)
@@ -116,12 +119,18 @@ def make_layer_tensors(cfg: LayerConfig, device="cpu", seed: int = 0,
     T = cfg.T if n_tokens is None else n_tokens
     w_r = _normal_bf16((d, E), 0.02, g, device)
     bias = torch.randn(E, generator=g, device=device, dtype=torch.float32)
-    w_gu = torch.empty((E, 2 * inter, d), dtype=torch.bfloat16, device=device)
+    keep = list(range(E)) if keep_experts is None else [int(e) for e in keep_experts]
+    slot = {e: i for i, e in enumerate(keep)}
+    w_gu = torch.empty((len(keep), 2 * inter, d), dtype=torch.bfloat16, device=device)
     for e in range(E):
-        w_gu[e] = _normal_bf16((2 * inter, d), 0.02, g, device)
-    w_down = torch.empty((E, d, inter), dtype=torch.bfloat16, device=device)
+        w = _normal_bf16((2 * inter, d), 0.02, g, device)
+        if e in slot:
+            w_gu[slot[e]] = w
+    w_down = torch.empty((len(keep), d, inter), dtype=torch.bfloat16, device=device)
     for e in range(E):
-        w_down[e] = _normal_bf16((d, inter), 0.02, g, device)
+        w = _normal_bf16((d, inter), 0.02, g, device)
+        if e in slot:
+            w_down[slot[e]] = w
     out = {"w_r": w_r, "bias": bias, "w_gate_up": w_gu, "w_down": w_down}
     state = g.get_state()
     if with_x:
