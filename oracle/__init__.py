@@ -78,6 +78,7 @@ def _load():
             "oracle_route_from_logits": (None, [P, P, I, I, I, I, I, I, F, P, P, P]),
             "oracle_route": (None, [P, P, P, I, I, I, I, I, I, I, F, P, P, P]),
             "oracle_dispatch": (I, [P, I, I, I, P, P, P, P]),
+            "oracle_dispatch_replicated": (I, [P, I, I, I, I, P, P, P, P, P]),
             "oracle_expert_ffn_rows": (None, [P, P, I, I, I, P, P, I, P, P]),
             "oracle_combine": (None, [P, P, P, I, I, I, P]),
             "oracle_layer_tokens": (None, [P, P, P, P, P, I, I, I, I, I, I, I, I, F,
@@ -219,6 +220,25 @@ def dispatch(ids: np.ndarray, E: int):
                                  _p(src))
     if rc != 0:
         raise ValueError("expert id out of range")
+    return counts, offsets, dest, src
+
+
+def dispatch_replicated(ids: np.ndarray, E: int, phys_expert: np.ndarray):
+    """Dispatch onto physical expert copies (reading R15): phys_expert [P] is
+    the logical expert of each physical slot.  Returns counts_phys [P],
+    offsets_phys [P+1], dest [T*k], src [T*k]."""
+    ids = _c(ids, np.int32)
+    pe = _c(phys_expert, np.int32)
+    T, k = ids.shape
+    P = pe.size
+    counts = np.empty(P, dtype=np.int32)
+    offsets = np.empty(P + 1, dtype=np.int32)
+    dest = np.empty(T * k, dtype=np.int32)
+    src = np.empty(T * k, dtype=np.int32)
+    rc = _load().oracle_dispatch_replicated(_p(ids), T, k, E, P, _p(pe), _p(counts),
+                                            _p(offsets), _p(dest), _p(src))
+    if rc != 0:
+        raise ValueError("expert id out of range or expert without a copy")
     return counts, offsets, dest, src
 
 

@@ -51,6 +51,11 @@
  *       a = t*k + j keep their place; later ones overflow.  Dropped ones add
  *       nothing (weights are not renormalised); second-round ones are
  *       computed like any other.
+ *   R15 replicas: the r-th assignment (in increasing a) of logical expert e,
+ *       which has n_rep copies, goes to copy r mod n_rep in the order the
+ *       placement lists them (the least loaded copy, ties to the first,
+ *       when copies fill in that order); rows are contiguous per physical
+ *       copy in placement order, stable in a.
  *
  * Compile with -O2 -ffp-contract=off, no fast-math, so that every floating
  * point operation is exactly the one written.
@@ -340,6 +345,71 @@ int oracle_dispatch(const int32_t *ids, int T, int k, int E, int32_t *counts,
   }
   free(cursor);
   return 0;
+}
+
+/*
+ * Dispatch onto physical expert copies ([ep] "EPLB 与路由约束": hot experts get
+ * copies; [ch15] section 4.3: the gating picks logical experts and the
+ * system routes each assignment to one of the expert's equivalent copies,
+ * the less loaded one).  Copies: phys_expert[p] is the logical expert of
+ * physical slot p (the placement's slot order); copy i of e is the i-th
+ * slot, in increasing p, holding e.  Reading R15: the r-th assignment of e
+ * (increasing a) goes to copy r mod n_rep(e).  Outputs: counts_phys [P],
+ * offsets_phys [P+1], dest [T*k] (row of assignment a), src_token [T*k].
+ * Returns -1 for an out-of-range id or an expert without a copy.
+ */
+int oracle_dispatch_replicated(const int32_t *ids, int T, int k, int E, int P,
+                               const int32_t *phys_expert, int32_t *counts_phys,
+                               int32_t *offsets_phys, int32_t *dest, int32_t *src_token) {
+  int64_t n = (int64_t)T * k;
+  int32_t *n_rep = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+  int32_t *seen = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+  int32_t *slot = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+  int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
+  int rc = 0;
+  for (int p = 0; p < P; ++p) {
+    if (phys_expert[p] < 0 || phys_expert[p] >= E) rc = -1;
+    else n_rep[phys_expert[p]] += 1;
+  }
+  /* 1. the copy of every assignment: count e's assignments in increasing a */
+  for (int64_t a = 0; a < n && rc == 0; ++a) {
+    int e = ids[a];
+    if (e < 0 || e >= E || n_rep[e] == 0) {
+      rc = -1;
+      break;
+    }
+    int r = seen[e]++;
+    int want = r % n_rep[e];
+    /* the want-th slot holding e, in increasing p */
+    int found = -1, c = 0;
+    for (int p = 0; p < P; ++p)
+      if (phys_expert[p] == e) {
+        if (c == want) {
+          found = p;
+          break;
+        }
+        ++c;
+      }
+    slot[a] = found;
+  }
+  if (rc == 0) {
+    /* 2. a stable counting sort of the assignments by slot */
+    for (int p = 0; p < P; ++p) counts_phys[p] = 0;
+    for (int64_t a = 0; a < n; ++a) counts_phys[slot[a]] += 1;
+    offsets_phys[0] = 0;
+    for (int p = 0; p < P; ++p) offsets_phys[p + 1] = offsets_phys[p] + counts_phys[p];
+    for (int p = 0; p < P; ++p) cursor[p] = offsets_phys[p];
+    for (int64_t a = 0; a < n; ++a) {
+      int32_t row = cursor[slot[a]]++;
+      dest[a] = row;
+      src_token[row] = (int32_t)(a / k);
+    }
+  }
+  free(n_rep);
+  free(seen);
+  free(slot);
+  free(cursor);
+  return rc;
 }
 
 /* ------------------------------------------------------------------------ */
