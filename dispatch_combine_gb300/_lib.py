@@ -60,6 +60,8 @@ SIGNATURES = {
     "moe_group_topk": (_I32, [_PS, _P, _P, _P]),
     "moe_dispatch": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_noalloc": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_dispatch_replicated_workspace_size": (_I32, [_PS, _I32, ctypes.POINTER(_SZ)]),
+    "moe_dispatch_replicated": (_I32, [_PS, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_capacity": (_I32, [_I32, _I32, _I32, ctypes.c_double]),
     "moe_eplb_plan": (_I32, [_P, _I32, _I32, _I32, _I32, _I32, _P, _P]),
     "moe_quantize_fp8_rows": (_I32, [_P, ctypes.c_int64, _I32, _P, _P, _P]),
@@ -362,6 +364,41 @@ def moe_dispatch_noalloc(shape, topk_ids, x, stream=None):
            lib().moe_dispatch_noalloc(ctypes.byref(s), _ptr(topk_ids), _ptr(x), _ptr(counts),
                                       _ptr(offsets), _ptr(src), _ptr(dest), _ptr(x_perm),
                                       _stream(stream)))
+    return counts, offsets, src, dest, x_perm
+
+
+def moe_dispatch_replicated_workspace_size(shape, num_physical: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_dispatch_replicated_workspace_size",
+           lib().moe_dispatch_replicated_workspace_size(ctypes.byref(as_shape(shape)),
+                                                        int(num_physical), ctypes.byref(out)))
+    return out.value
+
+
+def moe_dispatch_replicated(shape, phys_expert, topk_ids, x, ws: Workspace, stream=None):
+    """Dispatch onto physical expert copies (phys_expert [P] int32: the
+    logical expert of each physical slot).  Returns (counts_phys [P],
+    offsets_phys [P+1], src_token [T*k], dest [T*k], x_perm or None)."""
+    s = as_shape(shape)
+    dev = topk_ids.device
+    n = s.T * s.k
+    P = int(phys_expert.numel())
+    _expect(topk_ids, torch.int32, (s.T, s.k), "topk_ids")
+    if phys_expert.dtype != torch.int32:
+        raise TypeError("phys_expert: expected torch.int32")
+    counts = torch.empty(P, dtype=torch.int32, device=dev)
+    offsets = torch.empty(P + 1, dtype=torch.int32, device=dev)
+    src = torch.empty(n, dtype=torch.int32, device=dev)
+    dest = torch.empty(n, dtype=torch.int32, device=dev)
+    x_perm = None
+    if x is not None:
+        _expect(x, torch.bfloat16, (s.T, s.d), "x")
+        x_perm = torch.empty((n, s.d), dtype=torch.bfloat16, device=dev)
+    _check("moe_dispatch_replicated",
+           lib().moe_dispatch_replicated(ctypes.byref(s), P, _ptr(phys_expert), _ptr(topk_ids),
+                                         _ptr(x), _ptr(counts), _ptr(offsets), _ptr(src),
+                                         _ptr(dest), _ptr(x_perm), ws.c_ptr, ws.nbytes,
+                                         _stream(stream)))
     return counts, offsets, src, dest, x_perm
 
 

@@ -16,6 +16,9 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
+// physical expert slots of the replicated dispatch at most
+constexpr int32_t kMaxPhysical = 65536;
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Workspace regions, in this order (each 256-byte aligned):
@@ -327,6 +330,75 @@ moe_status_t moe_dispatch(const moe_shape_t *shape, const int32_t *topk_ids, con
   return cuda_status(moe::launch_dispatch(topk_ids, s.T, s.k, s.E, x, s.d, counts, offsets,
                                           src_token, dest, x_perm, at<int32_t>(ws, L.chunk),
                                           nullptr, 128, at<uint32_t>(ws, L.status), stream));
+}
+
+// scratch of moe_dispatch_replicated, in this order (each 256-byte aligned):
+// status word | chunk histograms | counts_log [E] | offsets_log [E+1] |
+// mtile [E+1] | dest_log [T*k] | src_log [T*k] | n_rep [E] | rep_first [E+1] |
+// rep_slots [P] | slot_rank [P]
+struct ReplicaLayout {
+  size_t chunk, counts, offsets, mtile, dest, src, n_rep, rep_first, rep_slots, slot_rank, end;
+};
+ReplicaLayout make_replica_layout(const moe_shape_t &s, int32_t P) {
+  ReplicaLayout L;
+  const int64_t n = static_cast<int64_t>(s.T) * s.k;
+  size_t off = align_up(4);
+  auto take = [&](size_t bytes) {
+    const size_t at_ = off;
+    off = align_up(off + bytes);
+    return at_;
+  };
+  L.chunk = take(4 * static_cast<size_t>(moe::dispatch_num_chunks(n)) * s.E);
+  L.counts = take(4 * static_cast<size_t>(s.E));
+  L.offsets = take(4 * static_cast<size_t>(s.E + 1));
+  L.mtile = take(4 * static_cast<size_t>(s.E + 1));
+  L.dest = take(4 * static_cast<size_t>(n));
+  L.src = take(4 * static_cast<size_t>(n));
+  L.n_rep = take(4 * static_cast<size_t>(s.E));
+  L.rep_first = take(4 * static_cast<size_t>(s.E + 1));
+  L.rep_slots = take(4 * static_cast<size_t>(P));
+  L.slot_rank = take(4 * static_cast<size_t>(P));
+  L.end = off;
+  return L;
+}
+
+moe_status_t moe_dispatch_replicated_workspace_size(const moe_shape_t *shape,
+                                                    int32_t num_physical, size_t *bytes) {
+  MOE_TRY(check_shape(shape));
+  if (!bytes || num_physical < 1 || num_physical > kMaxPhysical) return MOE_ERR_INVALID_ARG;
+  *bytes = make_replica_layout(*shape, num_physical).end;
+  return MOE_OK;
+}
+
+moe_status_t moe_dispatch_replicated(const moe_shape_t *shape, int32_t num_physical,
+                                     const int32_t *phys_expert, const int32_t *topk_ids,
+                                     const void *x, int32_t *counts_phys, int32_t *offsets_phys,
+                                     int32_t *src_token, int32_t *dest, void *x_perm, void *ws,
+                                     size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_shape(shape));
+  if (num_physical < 1 || num_physical > kMaxPhysical) return MOE_ERR_INVALID_ARG;
+  if (shape->T == 0) return MOE_OK;
+  const moe_shape_t &s = *shape;
+  if (!phys_expert || !topk_ids || !counts_phys || !offsets_phys || !src_token || !dest)
+    return MOE_ERR_INVALID_ARG;
+  if (x && !x_perm) return MOE_ERR_INVALID_ARG;
+  if (x && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+  const ReplicaLayout L = make_replica_layout(s, num_physical);
+  MOE_TRY(check_ws(ws, ws_bytes, L.end));
+  moe::ReplicaScratch w;
+  w.chunk = at<int32_t>(ws, L.chunk);
+  w.counts_log = at<int32_t>(ws, L.counts);
+  w.offsets_log = at<int32_t>(ws, L.offsets);
+  w.mtile = at<int32_t>(ws, L.mtile);
+  w.dest_log = at<int32_t>(ws, L.dest);
+  w.src_log = at<int32_t>(ws, L.src);
+  w.n_rep = at<int32_t>(ws, L.n_rep);
+  w.rep_first = at<int32_t>(ws, L.rep_first);
+  w.rep_slots = at<int32_t>(ws, L.rep_slots);
+  w.slot_rank = at<int32_t>(ws, L.slot_rank);
+  return cuda_status(moe::launch_dispatch_replicated(
+      topk_ids, s.T, s.k, s.E, x, s.d, num_physical, phys_expert, counts_phys, offsets_phys,
+      src_token, dest, x_perm, w, at<uint32_t>(ws, 0), stream));
 }
 
 static moe_status_t ffn_common(const moe_shape_t *shape, int32_t layout, const void *x_in,

@@ -296,7 +296,158 @@ __global__ void __launch_bounds__(1024)
   if (e == 0) mtile_base[E] = total;
 }
 
+// ---------------------------------------------------------------------------
+// Dispatch onto physical expert copies ("ep-deploy" page, section "EPLB 与路由
+// 约束": hot experts get copies; "第十五章" section 4.3: each assignment goes
+// to one of its expert's equivalent copies, the less loaded one).  The
+// logical dispatch runs first (its dest gives every assignment its stable
+// rank r among its expert's assignments); the r-th assignment of expert e
+// goes to copy r mod n_rep(e), the copies taken in slot order -- the least
+// loaded copy at every step, ties to the first.  Rows are contiguous per
+// physical slot, in slot order, stable in a = t*k + j inside a slot.
+// ---------------------------------------------------------------------------
+
+// One CTA of 1024 threads.  Warp 0 ranks the slots of each expert in
+// increasing slot order (32 slots at a time, like the scatter): slot_rank[p]
+// = the copy index of slot p, n_rep[e] = copies of e.  Then rep_first =
+// exclusive scan of n_rep, rep_slots[rep_first[e] + i] = the i-th slot of e,
+// counts_phys[p] = the assignments r < n_e with r mod n_rep == i, and
+// offsets_phys = their exclusive scan in slot order.
+__global__ void __launch_bounds__(1024)
+    replica_plan_kernel(const int32_t *__restrict__ phys_expert, int P, int E,
+                        const int32_t *__restrict__ counts_log, int32_t *__restrict__ n_rep,
+                        int32_t *__restrict__ rep_first, int32_t *__restrict__ rep_slots,
+                        int32_t *__restrict__ slot_rank, int32_t *__restrict__ counts_phys,
+                        int32_t *__restrict__ offsets_phys, uint32_t *status) {
+  pdl_begin();
+  extern __shared__ int cursor[];  // [E]
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int e = tid; e < E; e += 1024) cursor[e] = 0;
+  __syncthreads();
+  if (tid < 32) {
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int p0 = 0; p0 < P; p0 += 32) {
+      const int p = p0 + lane;
+      int e = (p < P) ? phys_expert[p] : -1;
+      if (p < P && (e < 0 || e >= E)) {
+        set_status(status, kStatusBadId);
+        e = -1;
+      }
+      const unsigned grp = __match_any_sync(0xffffffffu, e);
+      const int leader = __ffs(grp) - 1;
+      int base = 0;
+      if (e >= 0 && lane == leader) {
+        base = cursor[e];
+        cursor[e] = base + __popc(grp);
+      }
+      base = __shfl_sync(0xffffffffu, base, leader);
+      __syncwarp();
+      if (p < P) slot_rank[p] = (e >= 0) ? base + __popc(grp & lt_mask) : -1;
+    }
+  }
+  __syncthreads();
+  // copies per expert and where each expert's copies start in rep_slots
+  const int nr = (tid < E) ? cursor[tid] : 0;
+  if (tid < E) {
+    n_rep[tid] = nr;
+    if (nr == 0 && counts_log[tid] > 0) set_status(status, kStatusBadId);  // routed, no copy
+  }
+  int total = 0;
+  const int first = block_exclusive_scan(nr, &total);
+  if (tid < E) rep_first[tid] = first;
+  if (tid == 0) rep_first[E] = total;
+  __syncthreads();  // rep_first visible (global, same block)
+  // slot lists and per-slot counts, then their scan in slot order
+  int carry = 0;
+  for (int p0 = 0; p0 < P; p0 += 1024) {
+    const int p = p0 + tid;
+    int c = 0;
+    if (p < P) {
+      const int e = phys_expert[p];
+      const int i = slot_rank[p];
+      if (e >= 0 && e < E && i >= 0) {
+        rep_slots[rep_first[e] + i] = p;
+        const int ne = counts_log[e], m = n_rep[e];
+        c = (ne > i) ? (ne - i + m - 1) / m : 0;
+      }
+      counts_phys[p] = c;
+    }
+    int chunk_total = 0;
+    const int excl = block_exclusive_scan(c, &chunk_total);
+    if (p < P) offsets_phys[p] = carry + excl;
+    carry += chunk_total;
+    __syncthreads();  // the scan's shared totals are reused by the next chunk
+  }
+  if (tid == 0) offsets_phys[P] = carry;
+}
+
+// dest / src_token of the physical rows: the r-th assignment of e goes to
+// copy r mod n_rep(e), row offsets_phys[slot] + r / n_rep(e)
+__global__ void __launch_bounds__(256)
+    replica_scatter_kernel(const int32_t *__restrict__ ids, int64_t n, int k, int E,
+                           const int32_t *__restrict__ offsets_log,
+                           const int32_t *__restrict__ dest_log,
+                           const int32_t *__restrict__ n_rep, const int32_t *__restrict__ rep_first,
+                           const int32_t *__restrict__ rep_slots,
+                           const int32_t *__restrict__ offsets_phys, int32_t *__restrict__ dest,
+                           int32_t *__restrict__ src_token) {
+  pdl_begin();
+  for (int64_t a = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; a < n;
+       a += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int e = ids[a];
+    int row = -1;
+    if (e >= 0 && e < E && n_rep[e] > 0) {
+      const int m = n_rep[e];
+      const int r = dest_log[a] - offsets_log[e];
+      const int p = rep_slots[rep_first[e] + r % m];
+      row = offsets_phys[p] + r / m;
+      src_token[row] = static_cast<int32_t>(a / k);
+    }
+    dest[a] = row;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_dispatch_replicated(const int32_t *ids, int T, int k, int E, const void *x,
+                                       int d, int P, const int32_t *phys_expert,
+                                       int32_t *counts_phys, int32_t *offsets_phys,
+                                       int32_t *src_token, int32_t *dest, void *x_perm,
+                                       const ReplicaScratch &w, uint32_t *status,
+                                       cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(T) * k;
+  if (n == 0) return cudaSuccess;
+  // the logical dispatch: counts, offsets and each assignment's stable rank
+  cudaError_t err = launch_dispatch(ids, T, k, E, nullptr, d, w.counts_log, w.offsets_log,
+                                    w.src_log, w.dest_log, nullptr, w.chunk, w.mtile, 128,
+                                    status, s);
+  if (err != cudaSuccess) return err;
+  MOE_LAUNCH_PDL(replica_plan_kernel, 1, 1024, E * sizeof(int), s, phys_expert, P, E,
+                 static_cast<const int32_t *>(w.counts_log), w.n_rep, w.rep_first, w.rep_slots,
+                 w.slot_rank, counts_phys, offsets_phys, status);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  const int64_t want = (n + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  MOE_LAUNCH_PDL(replica_scatter_kernel, static_cast<unsigned>(want < cap ? want : cap), 256, 0,
+                 s, ids, n, k, E, static_cast<const int32_t *>(w.offsets_log),
+                 static_cast<const int32_t *>(w.dest_log), static_cast<const int32_t *>(w.n_rep),
+                 static_cast<const int32_t *>(w.rep_first),
+                 static_cast<const int32_t *>(w.rep_slots),
+                 static_cast<const int32_t *>(offsets_phys), dest, src_token);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (x != nullptr && x_perm != nullptr) {
+    const int vec = d / 8;
+    const int64_t items = static_cast<int64_t>(T) * ((vec + 255) / 256);
+    const int64_t gwant = (items + kGatherWarps - 1) / kGatherWarps;
+    const unsigned gblocks = static_cast<unsigned>(gwant < cap ? gwant : cap);
+    MOE_LAUNCH_PDL(dispatch_gather_kernel, gblocks, kGatherWarps * 32, 0, s,
+                   static_cast<const uint4 *>(x), ids, static_cast<const int32_t *>(dest), T, k,
+                   E, static_cast<const int32_t *>(offsets_phys + P), n, vec,
+                   static_cast<uint4 *>(x_perm), CapacityArgs{0, 0, 0, nullptr, nullptr});
+    err = cudaGetLastError();
+  }
+  return err;
+}
 
 cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void *x, int d,
                             int32_t *counts, int32_t *offsets, int32_t *src_token,

@@ -87,6 +87,29 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
                             int32_t *dest, void *x_perm, int32_t *chunk_scratch,
                             int32_t *mtile_base, int tile_rows, uint32_t *status,
                             cudaStream_t s, CapacityArgs cap = CapacityArgs{0, 0, 0, nullptr, nullptr});
+// Dispatch onto physical expert copies: phys_expert [P] is the logical
+// expert of each physical slot; the r-th assignment (increasing a) of expert
+// e goes to its copy r mod n_rep(e), copies in slot order.  Outputs
+// counts_phys [P], offsets_phys [P+1], dest [T*k], src_token [T*k] and the
+// gathered rows.  Scratch (device, caller-owned) as listed.
+struct ReplicaScratch {
+  int32_t *chunk;        // dispatch chunk histograms [chunks * E]
+  int32_t *counts_log;   // [E]
+  int32_t *offsets_log;  // [E+1]
+  int32_t *mtile;        // [E+1]
+  int32_t *dest_log;     // [T*k]
+  int32_t *src_log;      // [T*k]
+  int32_t *n_rep;        // [E]
+  int32_t *rep_first;    // [E+1]
+  int32_t *rep_slots;    // [P]
+  int32_t *slot_rank;    // [P]
+};
+cudaError_t launch_dispatch_replicated(const int32_t *ids, int T, int k, int E, const void *x,
+                                       int d, int P, const int32_t *phys_expert,
+                                       int32_t *counts_phys, int32_t *offsets_phys,
+                                       int32_t *src_token, int32_t *dest, void *x_perm,
+                                       const ReplicaScratch &w, uint32_t *status,
+                                       cudaStream_t s);
 // mtile_base[e] = sum_{e'<e} ceil(M_e'/tile_rows) for the contiguous (seg =
 // offsets) or masked (seg = masked_m, clamped to M_max) layout.
 cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,

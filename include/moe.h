@@ -278,6 +278,38 @@ moe_status_t moe_dispatch_noalloc(const moe_shape_t *shape, const int32_t *topk_
                                   moe_stream_t stream);
 
 /*
+ * Dispatch onto physical expert copies ("ep-deploy" handbook page, section
+ * "EPLB 与路由约束": hot experts are copied and placed; "第十五章" section 4.3:
+ * the gating picks logical experts and the system sends each assignment to
+ * one of the expert's equivalent copies, the less loaded one).
+ *   phys_expert [P] int32 (device): the logical expert held by each physical
+ *     slot, in placement order (moe_eplb_plan's gpu_slots: GPU g holds slots
+ *     g*P/G .. (g+1)*P/G - 1).  1 <= P <= 65536.
+ *   The r-th assignment (in increasing a = t*k + j) of logical expert e,
+ *   which has n_rep copies, goes to its copy r mod n_rep, copies counted in
+ *   slot order -- at every step the copy with the fewest rows so far, ties
+ *   to the first; an expert's copies thus differ by at most one row.
+ * Outputs (device, caller-owned): counts_phys [P], offsets_phys [P+1]
+ *   (exclusive scan in slot order, so the rows of a GPU's slots are one
+ *   contiguous range: the send buffer of an expert-parallel dispatch),
+ *   dest [T*k] (row of each assignment; -1 for an id outside [0,E) or an
+ *   expert with no copy), src_token [T*k] (token of each row), x_perm
+ *   [T*k, d] bf16 rows (NULL x to skip the gather).  Rows are contiguous per
+ *   slot and stable in a inside a slot.  With one copy per expert in expert
+ *   order the outputs are moe_dispatch's.
+ * Workspace: moe_dispatch_replicated_workspace_size bytes.  A routed expert
+ *   with no copy, or a slot holding an id outside [0,E), is reported as
+ *   MOE_ERR_INVALID_ARG in the status word.
+ */
+moe_status_t moe_dispatch_replicated_workspace_size(const moe_shape_t *shape,
+                                                    int32_t num_physical, size_t *bytes);
+moe_status_t moe_dispatch_replicated(const moe_shape_t *shape, int32_t num_physical,
+                                     const int32_t *phys_expert, const int32_t *topk_ids,
+                                     const void *x, int32_t *counts_phys, int32_t *offsets_phys,
+                                     int32_t *src_token, int32_t *dest, void *x_perm, void *ws,
+                                     size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Capacity variant ("第十五章：多节点大模型推理" section 4.3, "Capacity Factor"):
  * each expert takes at most C assignments per batch.
  *
