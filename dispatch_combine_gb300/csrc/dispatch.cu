@@ -95,8 +95,14 @@ __global__ void __launch_bounds__(1024)
   const int c0 = q * per, c1 = min(nchunks, c0 + per);
   int local = 0;
   if (eq < E) {
-#pragma unroll 8
-    for (int c = c0; c < c1; ++c) local += chunk_counts[(size_t)c * E + eq];
+    // sixteen loads in flight at a time (a range is up to a few hundred chunks)
+    for (int c = c0; c < c1; c += 16) {
+      int v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) v[u] = (c + u < c1) ? chunk_counts[(size_t)(c + u) * E + eq] : 0;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) local += v[u];
+    }
   }
   part[threadIdx.x] = local;
   __syncthreads();
@@ -108,10 +114,16 @@ __global__ void __launch_bounds__(1024)
   }
   if (eq < E) {
     int r = base;
-    for (int c = c0; c < c1; ++c) {
-      const int v = chunk_counts[(size_t)c * E + eq];
-      chunk_counts[(size_t)c * E + eq] = r;
-      r += v;
+    for (int c = c0; c < c1; c += 16) {
+      int v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) v[u] = (c + u < c1) ? chunk_counts[(size_t)(c + u) * E + eq] : 0;
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (c + u < c1) {
+          chunk_counts[(size_t)(c + u) * E + eq] = r;
+          r += v[u];
+        }
     }
   }
   // thread e < E (range q == 0 of expert e) carries expert e's total
