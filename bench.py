@@ -1081,6 +1081,12 @@ def run_capacity(args):
         moe.moe_layer_capacity(shape, C, policy, t["x"], t["w_r"], bias, t["w_gate_up"],
                                t["w_down"], ws, y=y, counts=counts, kept=kept)
 
+    router_prep = None
+    try:
+        router_prep = moe.moe_router_prepare(shape, t["w_r"])  # once, like the main line
+    except moe.MoEError as e:
+        if e.status != 2:  # MOE_ERR_UNSUPPORTED: this shape is not screened
+            raise
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -1132,6 +1138,12 @@ def run_fp8(args):
     def step():
         moe.moe_layer_fp8(shape, t["x"], t["w_r"], bias, gq, gs, dq, ds, ws, y=y, counts=counts)
 
+    router_prep = None
+    try:
+        router_prep = moe.moe_router_prepare(shape, t["w_r"])  # once, like the main line
+    except moe.MoEError as e:
+        if e.status != 2:  # MOE_ERR_UNSUPPORTED: this shape is not screened
+            raise
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
