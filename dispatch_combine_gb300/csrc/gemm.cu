@@ -449,15 +449,15 @@ __device__ __forceinline__ int swap_box_index(int sn) {
 // One work item of a CTA pair: a whole tile, or (split last wave of the down
 // form) one K half of a tile.  Items n_full + j, j < 2 * rem, are a half of
 // tile n_full + j % rem; pair c takes items c, c + ncl, ..., so the two
-// halves of a tile run at the same time on pairs j % rem and j % rem + rem.
-// The storing half (the later k-blocks) goes to the lower pair, whose CTAs
-// are normally dispatched first, so the adding half waits on a pair that is
-// already running.
+// halves of a tile normally run at the same time on pairs j % rem and
+// j % rem + rem.  Which half stores and which adds is decided at run time
+// (the first to reach its epilogue stores), so neither depends on the other
+// pair being scheduled.
 struct PairWork {
   int u;         // tile index
   int kb0, kb1;  // k-blocks [kb0, kb1)
-  int piece;     // -1 whole tile, 0 first half (adds), 1 second half (stores)
-  int slot;      // split tile j % rem (flag index / 8)
+  int piece;     // -1 whole tile, 0 first K half, 1 second K half
+  int slot;      // split tile j % rem (16 flag words each)
 };
 __device__ __forceinline__ PairWork pair_work(int w, int n_full, int rem, int kblocks) {
   PairWork pw;
@@ -676,22 +676,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                             args.status, args.wait_limit_ns);
       if (!__all_sync(0xffffffffu, waited)) break;
       tc_fence_after();
-      // split tile: this warp's part of the tile (its 32 TMEM lanes) has one
-      // flag; the first K half adds onto the second half's stored sums once
-      // the flag is up (always the last item of both pairs)
-      const bool add = !SWIGLU && pw.piece == 0;
-      uint32_t *flag = (!SWIGLU && pw.piece >= 0)
-                           ? args.split_flags + pw.slot * 8 + static_cast<int>(rank) * 4 + quad
-                           : nullptr;
-      if (add) {
-        bool up = true;
-        if (lane == 0)
-          up = flag_wait_bounded(flag, args.split_epoch, abort_flag, args.status,
-                                 args.wait_limit_ns);
-        if (!__shfl_sync(0xffffffffu, up ? 1 : 0, 0)) break;
-        (void)ld_acquire_gpu(flag);  // every lane acquires the stored sums
-        __syncwarp();
-        if (lane == 0) *flag = 0;  // cleared for the next launch
+      // split tile: this warp's part of the tile (its 32 TMEM lanes) has a
+      // ticket word and a ready word, shared with the same part of the other
+      // K half.  The half whose warp takes the ticket first stores its sums
+      // and raises ready; the other waits for ready and adds its sums with
+      // one fp32 reduction per element.  Either order gives fl(s0 + s1), and
+      // the waiting half waits only for a warp already past its ticket, whose
+      // stores wait on nothing, so no pair has to be resident at any time.
+      uint32_t *ticket = (!SWIGLU && pw.piece >= 0)
+                             ? args.split_flags + pw.slot * 16 +
+                                   (static_cast<int>(rank) * 4 + quad) * 2
+                             : nullptr;
+      bool add = false;
+      if (ticket != nullptr) {
+        uint32_t prev = 0;
+        if (lane == 0) prev = atomicExch(ticket, args.split_epoch);
+        add = __shfl_sync(0xffffffffu, prev, 0) == args.split_epoch;
+        if (add) {
+          bool up = true;
+          if (lane == 0)
+            up = flag_wait_bounded(ticket + 1, args.split_epoch, abort_flag, args.status,
+                                   args.wait_limit_ns);
+          if (!__shfl_sync(0xffffffffu, up ? 1 : 0, 0)) break;
+          (void)ld_acquire_gpu(ticket + 1);  // every lane acquires the stored sums
+          __syncwarp();
+          if (lane == 0) {  // both words cleared for the next launch (or replay)
+            ticket[0] = 0;
+            ticket[1] = 0;
+          }
+        }
       }
       const uint32_t tb =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
@@ -840,11 +853,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      if (flag != nullptr && !add) {
-        // second K half: its sums are stored; raise the slab's flag
+      if (ticket != nullptr && !add) {
+        // the first K half to arrive: its sums are stored; raise ready
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_gpu(flag, args.split_epoch);
+        if (lane == 0) st_release_gpu(ticket + 1, args.split_epoch);
       }
       tc_fence_before();
       __syncwarp();

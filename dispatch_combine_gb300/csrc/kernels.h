@@ -126,16 +126,16 @@ constexpr int64_t kPairRowsPerExpert = 256;
 constexpr int kGemmTileRows = 128;
 // The CTA-pair down GEMM splits the tiles of its last, partial wave into two
 // K halves on two pairs when the whole launch is at most kPairSplitMaxWaves
-// waves and the halves fit in one wave: the pair with the second half
-// stores its partial sums and raises one flag per 32-row slab to a value
-// that differs from launch to launch, the pair with the first half waits for
-// that value (bounded) and adds its sums with fp32 reductions (one add per
-// element, so the result does not depend on timing), then clears the flag.
-// The halves run at the same time on a grid whose pairs are all resident.
-// Flags: kPairSplitSlots tiles x 8 slabs.
+// waves and the halves fit in one wave.  Per 32-row slab the two halves
+// share a ticket word and a ready word: the half that takes the ticket first
+// (an exchange with a value that differs from launch to launch) stores its
+// partial sums and raises ready; the other waits for ready (bounded, on a
+// warp that is already storing) and adds its sums with fp32 reductions (one
+// add per element, so the result does not depend on which came first), then
+// clears both words.  Flags: kPairSplitSlots tiles x 8 slabs x 2 words.
 constexpr int kPairSplitMaxWaves = 16;
-constexpr int kPairSplitSlots = 512;
-constexpr int kPairSplitFlagWords = kPairSplitSlots * 8;
+constexpr int kPairSplitSlots = 256;
+constexpr int kPairSplitFlagWords = kPairSplitSlots * 16;
 
 // quant.cu: e4m3 codes with fp32 scales, per (row, 128 columns) of [rows,
 // cols] bf16, or per 128 x 128 block of [mats, rows, cols] bf16

@@ -198,12 +198,14 @@ moe_status_t moe_dispatch(const moe_shape_t *shape, const int32_t *topk_ids,
  *   w_down    [E, d, inter] bf16
  *   y_out     fp32
  * Experts with no rows cost nothing (their weights are not read).
- * The down GEMM is a persistent grid sized to be resident all at once; when
- * its last wave is short, two CTA pairs share each of its tiles and signal
- * each other through flags in the workspace, with every wait bounded (a
- * timeout sets MOE_ERR_TIMEOUT).  Kernels on other streams that hold SMs for
- * longer than that bound can therefore turn into a reported timeout.
- * Results do not depend on timing.
+ * The down GEMM is a persistent grid; when its last wave is short, two CTA
+ * pairs share each of its tiles (K halves) through flags in the workspace.
+ * The half that reaches its epilogue first stores, the other adds; the only
+ * wait is the adder's, on a half that is already storing, so the launch does
+ * not need its pairs to be resident together (kernels on other streams may
+ * hold SMs).  The wait is bounded all the same (a timeout sets
+ * MOE_ERR_TIMEOUT).  Results do not depend on timing: either order gives the
+ * same fp32 sum.
  */
 moe_status_t moe_expert_ffn(const moe_shape_t *shape, int32_t layout, const void *x_in,
                             const int32_t *seg, int32_t M_max, const void *w_gate_up,

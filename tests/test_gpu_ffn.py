@@ -214,3 +214,30 @@ def test_ffn_pair_split_last_wave(counts, d, inter):
     flags = ws.buf[ws.offset + 256: ws.offset + 256 + 4 * 4096]
     assert int(flags.count_nonzero()) == 0, "split flags left set"
     check_ffn(y1.cpu().numpy(), bits(x), row_e, bits(w_gu), bits(w_down), "y (split)")
+
+
+def test_ffn_pair_split_beside_a_busy_stream():
+    """The split last wave needs no co-residency: with a side stream keeping
+    the SMs busy (plain GEMMs that wait on nothing), the split down GEMM
+    gives bit-for-bit the result of a run on an idle GPU."""
+    ensure_lib()
+    counts, d, inter = [520, 520, 520, 520, 530], 4096, 256
+    E = len(counts)
+    w_gu, w_down = _weights(E, d, inter, seed=d + 5 * inter)
+    x, offsets, row_e = _contiguous_case(counts, d, inter, seed=d + 11)
+    shape = _shape(E, d, inter, T=x.shape[0], k=1)
+    ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    args = (shape, moe.MOE_LAYOUT_CONTIGUOUS, x.cuda(), offsets.cuda(), 0, w_gu.cuda(),
+            w_down.cuda(), ws)
+    y_idle = moe.moe_expert_ffn(*args)
+    torch.cuda.synchronize()
+    a = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16)
+    side = torch.cuda.Stream()
+    for _ in range(3):
+        with torch.cuda.stream(side):
+            for _ in range(6):
+                a = (a @ a) * (1.0 / 64)
+        y_busy = moe.moe_expert_ffn(*args)
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_status(ws) == 0
+        assert torch.equal(y_busy.view(torch.int32), y_idle.view(torch.int32))
