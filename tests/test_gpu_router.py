@@ -181,6 +181,44 @@ def test_screened_route_matches_oracle(T, d, E, G, tg, k, score):
     assert np.all(np.abs(w - ref_w) <= 1e-6 * np.abs(ref_w))
 
 
+@pytest.mark.parametrize("T,d,E,G,tg,k,score", [
+    (8193, 1088, 64, 4, 2, 6, SCORE_SIGMOID_BIAS),   # ragged last tile, d % 128 == 64
+    (9000, 2048, 256, 8, 4, 8, SCORE_SIGMOID_BIAS),
+    (8200, 512, 128, 1, 1, 4, SCORE_SOFTMAX),
+])
+def test_screened_route_large_T(T, d, E, G, tg, k, score):
+    # large token counts (the refinement's one-expert-per-warp form), ragged
+    # T and d % 128 == 64: the same ids and weight bits as the fixed-order
+    # path, and sampled tokens equal to the oracle's
+    ensure_lib()
+    import moe_inputs
+    from tests.gpu_common import bits
+    tns = moe_inputs.make_tensors_for_shape(T, d, E, 64, device="cuda", seed=T + 7 * d + E)
+    shape = dict(T=T, d=d, E=E, G=G, topk_group=tg, k=k, inter=64, score=score,
+                 bias_scale=0.15)
+    ids, w, _, n_ref = _screened_vs_fixed(shape, tns["x"], tns["w_r"], tns["bias"])
+    rows = np.unique(np.concatenate([np.arange(0, T, max(1, T // 40)), [T - 1]]))
+    xs = bits(tns["x"])[rows]
+    ref_ids, ref_w, _ = oracle.route(xs, bits(tns["w_r"]), tns["bias"].cpu().numpy(), G, tg, k,
+                                     score)
+    assert np.array_equal(ids[rows], ref_ids)
+    assert np.all(np.abs(w[rows] - ref_w) <= 1e-6 * np.abs(ref_w))
+
+
+def test_screened_route_large_T_all_ties():
+    # nearly every expert of every token refined, at a large token count
+    ensure_lib()
+    T, d, E, G, tg, k = 8192, 256, 128, 8, 3, 6
+    shape = dict(T=T, d=d, E=E, G=G, topk_group=tg, k=k, inter=64, score=SCORE_SIGMOID_BIAS,
+                 bias_scale=0.15)
+    x = torch.randn(T, d, generator=torch.Generator().manual_seed(6)).to(torch.bfloat16).cuda()
+    w_r = torch.zeros(d, E, dtype=torch.bfloat16, device="cuda")
+    w_r[3, 5] = 1.0  # expert 5 wins where x[:, 3] > 0, else an all-tie
+    bias = torch.zeros(E, dtype=torch.float32, device="cuda")
+    ids, w, _, n_ref = _screened_vs_fixed(shape, x, w_r, bias)
+    assert n_ref > T * 100
+
+
 def test_screened_route_all_ties_refine_everything():
     # zero router weight and bias: every score ties, so every interval
     # overlaps every other and all E experts of every token are refined
