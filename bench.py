@@ -66,18 +66,21 @@ def ffn_flops_per_row(c) -> int:
     return 6 * c.d * c.inter
 
 
-def stage_bytes(c) -> dict:
+def stage_bytes(c, yperm_row_bytes=None) -> dict:
     """Algorithmic bytes of the bandwidth stages for one layer call.
 
     router:   read x and W_r, write ids + weights
     dispatch: read ids and x, write x_perm (bf16) and dest + src_token
-    combine:  read y_perm (fp32) and dest + weights, write y (bf16)
+    combine:  read y_perm and dest + weights, write y (bf16); y_perm rows of
+              yperm_row_bytes (moe_layer_yperm_row_bytes: 4*d fp32, or
+              2*d + d/32 in the compact form; default fp32)
     """
     T, d, E, k = c.T, c.d, c.E, c.k
+    yb = 4 * d if yperm_row_bytes is None else int(yperm_row_bytes)
     return {
         "router": T * d * 2 + d * E * 2 + T * k * 8,
         "dispatch": T * k * 4 + T * d * 2 + T * k * d * 2 + T * k * 8,
-        "combine": T * k * d * 4 + T * k * 8 + T * d * 2,
+        "combine": T * k * yb + T * k * 8 + T * d * 2,
     }
 
 
@@ -348,10 +351,10 @@ def tensor_peak(peaks: dict, peak_src: str, region_s: float) -> tuple[float, str
                                             f"{region_s:.2f} s)")
 
 
-def layer_bytes(c, n_touched: int) -> int:
+def layer_bytes(c, n_touched: int, yperm_row_bytes=None) -> int:
     """Algorithmic HBM bytes of one layer call: the bandwidth stages plus the
     touched experts' weights streamed once."""
-    sb = stage_bytes(c)
+    sb = stage_bytes(c, yperm_row_bytes)
     return sb["router"] + sb["dispatch"] + sb["combine"] + n_touched * expert_weight_bytes(c)
 
 
@@ -433,13 +436,15 @@ def measure_layer(args, c, t, ws, device, world: int, steps: int, warmup: int) -
     region_s = ms_total / 1000.0
     tpeak, tpeak_src = tensor_peak(peaks, peak_src, region_s)
     tensor = tpeak * 1e12
-    sb = stage_bytes(c)
+    yrb = moe.moe_layer_yperm_row_bytes(shape)
+    sb = stage_bytes(c, yrb)
     fw = ffn_work(c, n_touched)
     stages = {}
     for n in ("router", "dispatch", "combine"):
         sec = stage_ms[n] / 1000.0
         stages[n] = {"us": stage_ms[n] * 1000.0, "bound": "hbm", "bytes": sb[n],
                      "achieved_gbs": sb[n] / sec / 1e9, "frac": sb[n] / hbm / sec}
+    stages["combine"]["yperm_row_bytes"] = yrb
     # screened router: tensor-core logits, then the fixed-order logits of the
     # experts each token's intervals leave open (at least its k selected;
     # their weight rows come from L2); its HBM bytes stay those of the stage
@@ -476,7 +481,7 @@ def measure_layer(args, c, t, ws, device, world: int, steps: int, warmup: int) -
            "m_tiles_128": m_tiles, "tile_fill": tile_fill}
     # the whole layer against its own floor: max(all algorithmic HBM bytes,
     # FFN FLOPs at the tensor peak) over the measured time per layer
-    lb = layer_bytes(c, n_touched)
+    lb = layer_bytes(c, n_touched, yrb)
     layer_s = ms_total_max / 1000.0 / K
     layer = {"us": layer_s * 1e6, "bytes": lb, "flops": ffn_flops,
              "hbm_frac": lb / hbm / layer_s, "tensor_frac": ffn_flops / tensor / layer_s,

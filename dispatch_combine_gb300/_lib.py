@@ -82,6 +82,7 @@ SIGNATURES = {
     "moe_combine": (_I32, [_PS, _P, _P, _P, _P, _P]),
     "moe_layer": (_I32, [_PS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_layer_launch_count": (_I32, [_PS]),
+    "moe_layer_yperm_row_bytes": (ctypes.c_int64, [_PS]),
     "moe_route_refined_count": (_I32, [_PS, _P, _SZ, _P, _P]),
     "moe_router_prep_size": (_I32, [_PS, ctypes.POINTER(_SZ)]),
     "moe_router_prepare": (_I32, [_PS, _P, _P, _SZ, _P]),
@@ -218,6 +219,12 @@ def moe_status_string(status: int) -> str:
 
 def moe_layer_launch_count(shape) -> int:
     return int(lib().moe_layer_launch_count(ctypes.byref(as_shape(shape))))
+
+
+def moe_layer_yperm_row_bytes(shape) -> int:
+    """Bytes per routed row of the layer's down-GEMM output as the combine
+    reads it (4*d fp32, or 2*d + d/32 in the compact form)."""
+    return int(lib().moe_layer_yperm_row_bytes(ctypes.byref(as_shape(shape))))
 
 
 def moe_route_refined_count(shape, ws: Workspace, stream=None) -> int:

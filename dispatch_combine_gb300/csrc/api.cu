@@ -175,11 +175,18 @@ moe_status_t run_gate_up(const moe_shape_t *s, int32_t layout, const void *x_in,
   return cuda_status(moe::launch_gemm_gate_up_swiglu(p, st));
 }
 
+// y16_codes: compact output (pair form only): y receives the fp16 values and
+// y16_codes the code bytes; split_part / split_slots the split-tile scratch
 moe_status_t run_down(const moe_shape_t *s, int32_t layout, const void *h, const int32_t *seg,
                       int32_t M_max, int64_t rows, const int32_t *mtile, const void *w_down,
-                      float *y, uint32_t *status, uint32_t *split_flags, cudaStream_t st) {
+                      void *y, uint32_t *status, uint32_t *split_flags, cudaStream_t st,
+                      uint8_t *y16_codes = nullptr, float *split_part = nullptr,
+                      int split_slots = 0) {
   GemmProblem p;
   std::memset(&p, 0, sizeof p);
+  p.out_codes = y16_codes;
+  p.split_part = split_part;
+  p.split_part_slots = split_slots;
   p.E = s->E;
   p.K = s->inter;
   p.n_out = s->d;
@@ -532,6 +539,29 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
   MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_perm, offsets, 0, n, mtile, w_gate_up, h,
                       status, stream));
   MOE_TRY(mark(3));
+  if (use_pair(shape, MOE_LAYOUT_CONTIGUOUS, 0)) {
+    // the CTA-pair down GEMM writes the compact rows (fp16 values and a code
+    // byte per 32 columns, 2 + 1/32 bytes per value instead of 4) into the
+    // y_perm region, then the split tiles' scratch; the combine reads them
+    const size_t vals = align_up(2 * static_cast<size_t>(n) * s.d);
+    const size_t cods = align_up(static_cast<size_t>(n) * (s.d / 32));
+    const size_t region = 4 * static_cast<size_t>(n) * s.d;
+    const size_t slot_bytes = 256 * 256 * 4;
+    const int slots = region > vals + cods
+                          ? static_cast<int>(std::min<size_t>((region - vals - cods) / slot_bytes,
+                                                              moe::kPairSplitSlots))
+                          : 0;
+    uint8_t *base = at<uint8_t>(ws, L.y_perm);
+    uint8_t *codes = base + vals;
+    float *part = reinterpret_cast<float *>(base + vals + cods);
+    MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, offsets, 0, n, mtile, w_down, base, status,
+                     at<uint32_t>(ws, L.flags), stream, codes, slots > 0 ? part : nullptr,
+                     slots));
+    MOE_TRY(mark(4));
+    MOE_TRY(cuda_status(
+        moe::launch_combine16(base, codes, n, dest, w, s.T, s.k, s.d, y, stream)));
+    return mark(5);
+  }
   MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, offsets, 0, n, mtile, w_down, y_perm, status,
                    at<uint32_t>(ws, L.flags), stream));
   MOE_TRY(mark(4));
@@ -856,6 +886,12 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
                      y_rows + pad * s.d, status, at<uint32_t>(ws, L.flags), stream));
   }
   return cuda_status(moe::launch_combine(y_rows, pad + n, dest, w, s.T, s.k, s.d, y, stream));
+}
+
+int64_t moe_layer_yperm_row_bytes(const moe_shape_t *shape) {
+  if (check_shape(shape) != MOE_OK) return 0;
+  if (use_pair(shape, MOE_LAYOUT_CONTIGUOUS, 0)) return 2 * int64_t{shape->d} + shape->d / 32;
+  return 4 * int64_t{shape->d};
 }
 
 int32_t moe_layer_launch_count(const moe_shape_t *shape) {

@@ -7,6 +7,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -92,6 +93,58 @@ __device__ __forceinline__ float bf16hi(uint32_t packed) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// The layer's compact form of the down GEMM's output rows (y16): each group
+// of 32 consecutive columns of a row is stored as 32 fp16 values
+// q_i = rn(y_i * 2^(14 - E)) and one code byte c = E + 127, E the binary
+// exponent of the group's largest |y_i|; y_i = q_i * 2^(c - 141).  The
+// scaling is exact, |q_i| < 2^15, and the rounding error is at most 2^-11
+// of the group's largest magnitude.  A group whose largest |y_i| is below
+// 2^-111 (c < 16) is stored as zero (c = 0).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t y16_code(float group_max_abs) {
+  const uint32_t c = (__float_as_uint(group_max_abs) >> 23) & 0xffu;
+  return c < 16u ? 0u : c;
+}
+// 2^(141 - c): the scale applied before rounding to fp16
+__device__ __forceinline__ float y16_enc_mul(uint32_t c) {
+  return c ? __uint_as_float((268u - c) << 23) : 0.0f;
+}
+// 2^(c - 141): the scale back
+__device__ __forceinline__ float y16_dec_mul(uint32_t c) {
+  return c ? __uint_as_float((c - 14u) << 23) : 0.0f;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+// One group of 32 fp32 values (bit patterns v) to its code (returned) and
+// its 16 packed fp16 pairs h (value 2q in the low half of h[q]): the largest
+// magnitude by three-input max, the scaling by packed multiplies (exact:
+// a power of two).
+__device__ __forceinline__ uint32_t y16_encode32(const uint32_t (&v)[32], uint32_t (&h)[16]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const float a = fabsf(__uint_as_float(v[2 * q])), b = fabsf(__uint_as_float(v[2 * q + 1]));
+    asm("max.f32 %0, %0, %1, %2;" : "+f"(m) : "f"(a), "f"(b));
+  }
+  const uint32_t cc = y16_code(m);
+  const float mul = y16_enc_mul(cc);
+  uint64_t mm;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(mul));
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    uint64_t pr;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(pr) : "r"(v[2 * q]), "r"(v[2 * q + 1]));
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(pr) : "l"(mm));
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(pr));
+    h[q] = pack_f16x2(lo, hi);
+  }
+  return cc;
 }
 
 // four fp32 adds to global memory (no return value)

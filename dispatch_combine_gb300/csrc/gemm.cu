@@ -73,6 +73,13 @@ struct KArgs {
   int out_tma;  // pair down form: fp32 output through the tmY tensor map (TMA stores)
   uint32_t *split_flags;  // pair down form: flags of the split last wave (nullptr: no split)
   uint32_t split_epoch;   // nonzero value this launch raises the flags to
+  // pair down form, compact output (y16): out holds the fp16 values
+  // [rows, ldo] and out_codes the code bytes [rows, ldo / 32]; a split tile's
+  // first K half leaves its fp32 sums in split_part (256 x 256 floats per
+  // split slot, split_part_slots slots).  nullptr: fp32 output.
+  uint8_t *out_codes;
+  float *split_part;
+  int split_part_slots;
   int64_t rows_total;
   const int32_t *seg;
   const int32_t *mtile_base;
@@ -530,7 +537,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   int n_full = total, rem = 0;
   if (!SWIGLU && args.split_flags != nullptr && kblocks >= 2) {
     const int r = total % ncl;
-    if (r > 0 && 2 * r <= ncl && r <= kPairSplitSlots && total / ncl <= kPairSplitMaxWaves) {
+    if (r > 0 && 2 * r <= ncl && r <= kPairSplitSlots && total / ncl <= kPairSplitMaxWaves &&
+        (args.out_codes == nullptr || r <= args.split_part_slots)) {
       n_full = total - r;
       rem = r;
     }
@@ -711,6 +719,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const int64_t grow = static_cast<int64_t>(t.row0) + prow;
       const bool ok = prow < t.rows_valid && grow >= 0 && grow < args.rows_total;
       const int sn = (BN == 256) ? pair_swap_n(t) : 0;
+      // compact output: a split tile's halves meet in split_part (the first
+      // stores its fp32 sums there, the second adds them to its own and
+      // writes the tile), so every value is rounded to fp16 once
+      const bool f16 = !SWIGLU && args.out_codes != nullptr;
+      float *part = (f16 && ticket != nullptr)
+                        ? args.split_part + static_cast<size_t>(pw.slot) * 256 * 256
+                        : nullptr;
+      const bool part_store = part != nullptr && !add;  // first half: partial sums only
       if (sn > 0) {
         // swapped tile: TMEM lane = weight row of this CTA's half, column =
         // token row of the tile
@@ -735,13 +751,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 static_cast<__nv_bfloat16 *>(args.out)[gr * args.ldo + j] =
                     __float2bfloat16_rn(h);
               }
-            } else if (rok) {
-              const int col = t.n * BN + static_cast<int>(rank) * 128 + quad * 32 + lane;
-              float *o = static_cast<float *>(args.out) + gr * args.ldo + col;
-              if (add)
-                red_add_f32(o, __uint_as_float(v[i]));
-              else
-                *o = __uint_as_float(v[i]);
+            } else if (rok) {  // rok is the same for the whole warp
+              const int cl = static_cast<int>(rank) * 128 + quad * 32 + lane;
+              const int col = t.n * BN + cl;
+              float val = __uint_as_float(v[i]);
+              if (f16) {
+                if (part != nullptr) {
+                  float *pp = part + static_cast<size_t>(r) * 256 + cl;
+                  if (part_store)
+                    *pp = val;
+                  else
+                    val = __fadd_rn(val, *pp);
+                }
+                if (!part_store) {
+                  // the group is the warp's 32 consecutive columns of row r;
+                  // non-negative floats order like their bit patterns
+                  const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(val)));
+                  const uint32_t cc = y16_code(__uint_as_float(mb));
+                  static_cast<__half *>(args.out)[gr * args.ldo + col] =
+                      __float2half_rn(val * y16_enc_mul(cc));
+                  if (lane == 0) args.out_codes[gr * (args.ldo / 32) + col / 32] =
+                      static_cast<uint8_t>(cc);
+                }
+              } else {
+                float *o = static_cast<float *>(args.out) + gr * args.ldo + col;
+                if (add)
+                  red_add_f32(o, val);
+                else
+                  *o = val;
+              }
             }
           }
         }
@@ -784,7 +822,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
-      } else if (!SWIGLU && pw.piece < 0 && args.out_tma &&
+      } else if (!SWIGLU && !f16 && pw.piece < 0 && args.out_tma &&
                  quad * 32 + static_cast<int>(rank) * 128 + 32 <=
                                                      t.rows_valid &&
                  grow - lane >= 0 && grow - lane + 32 <= args.rows_total) {
@@ -818,6 +856,93 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
               bulk_commit();
             }
           }
+        }
+      } else if (f16 && pw.piece < 0 && args.out_tma &&
+                 quad * 32 + static_cast<int>(rank) * 128 + 32 <= t.rows_valid &&
+                 grow - lane >= 0 && grow - lane + 32 <= args.rows_total) {
+        // compact output, every row of this warp's 32-row slab valid: each
+        // 32-column chunk becomes 32 fp16 values per row, staged as a 32 x 32
+        // box (64-byte rows, 64-byte swizzle) in one half of the warp's
+        // staging area and written by one TMA store, the halves alternating;
+        // the lane writes its row's 8 code bytes of the tile at the end
+        uint8_t *box = smem + C::OUT_OFF + quad * C::OUT_BOX_BYTES;
+        const int row_g = static_cast<int>(grow - lane);
+        const uint32_t swz = static_cast<uint32_t>((lane >> 1) & 3);
+        uint64_t codes = 0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + c * 32, v);
+          tmem_ld_wait();
+          tmem_regs_fence(v);
+          uint32_t hw[16];
+          const uint32_t cc = y16_encode32(v, hw);
+          codes |= static_cast<uint64_t>(cc) << (8 * c);
+          uint8_t *hb = box + (c & 1) * (C::OUT_BOX_BYTES / 2);
+          const uint32_t rbase = smem_u32(hb) + static_cast<uint32_t>(lane) * 64u;
+          if (lane == 0) bulk_wait_read_1();  // this half's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st_shared_v4(rbase + ((static_cast<uint32_t>(q) ^ swz) * 16u), hw[4 * q],
+                         hw[4 * q + 1], hw[4 * q + 2], hw[4 * q + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmY, hb, t.n * BN + c * 32, row_g);
+            bulk_commit();
+          }
+        }
+        *reinterpret_cast<uint64_t *>(args.out_codes + grow * (args.ldo / 32) +
+                                      static_cast<int64_t>(t.n) * (BN / 32)) = codes;
+      } else if (f16) {
+        // compact output: 32 fp16 values (64 bytes) and one code per chunk
+        __half *dst = static_cast<__half *>(args.out) + grow * args.ldo +
+                      static_cast<int64_t>(t.n) * BN;
+        uint64_t codes = 0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + c * 32, v);
+          tmem_ld_wait();
+          tmem_regs_fence(v);
+          float4 *pp = part != nullptr ? reinterpret_cast<float4 *>(
+                                             part + static_cast<size_t>(prow) * 256 + c * 32)
+                                       : nullptr;
+          if (ok && part_store) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              pp[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                  __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          } else if (ok) {
+            if (pp != nullptr) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 o = pp[q];
+                v[4 * q] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * q]), o.x));
+                v[4 * q + 1] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * q + 1]), o.y));
+                v[4 * q + 2] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * q + 2]), o.z));
+                v[4 * q + 3] = __float_as_uint(__fadd_rn(__uint_as_float(v[4 * q + 3]), o.w));
+              }
+            }
+            uint32_t hw[16];
+            const uint32_t cc = y16_encode32(v, hw);
+            uint32_t w8[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) w8[q] = hw[q];
+            st_global_v8(dst + c * 32, w8);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) w8[q] = hw[8 + q];
+            st_global_v8(dst + c * 32 + 16, w8);
+            codes |= static_cast<uint64_t>(cc) << (8 * c);
+          }
+        }
+        if (ok && !part_store) {
+          uint8_t *cd = args.out_codes + grow * (args.ldo / 32) + static_cast<int64_t>(t.n) * (BN / 32);
+          if (BN / 32 == 8)
+            *reinterpret_cast<uint64_t *>(cd) = codes;
+          else
+            for (int c = 0; c < BN / 32; ++c) cd[c] = static_cast<uint8_t>(codes >> (8 * c));
         }
       } else {
         float *dst = static_cast<float *>(args.out) + grow * args.ldo +
@@ -1296,6 +1421,22 @@ bool make_tmap_f32_out(CUtensorMap *map, void *base, uint64_t inner, uint64_t ro
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D fp16 tensor [rows, inner] row-major for TMA stores of the compact
+// output; box = 32 rows x 32 elements (64 bytes), 64-byte swizzle.  False if
+// the base is not 16-byte aligned or a row is not a multiple of 16 bytes.
+bool make_tmap_f16_out(CUtensorMap *map, void *base, uint64_t inner, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || (reinterpret_cast<uintptr_t>(base) & 15u) != 0 || inner % 8 != 0 || rows == 0)
+    return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2D e4m3 (byte) tensor [rows, inner]; box = box_rows x 128 bytes, 128-byte
 // swizzle, out-of-bounds rows read as zero.
 bool make_tmap_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
@@ -1416,9 +1557,17 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   } else {
     tmW = tmB;
   }
-  // down: fp32 output stored by TMA where its layout allows (else plain stores)
-  const bool out_tma = !SWIGLU && make_tmap_f32_out(&tmY, p.out, static_cast<uint64_t>(p.n_out),
-                                                    static_cast<uint64_t>(p.rows_total));
+  // down: output (fp32, or the compact fp16 values) stored by TMA where its
+  // layout allows (else plain stores)
+  const bool out_f16 = !SWIGLU && p.out_codes != nullptr;
+  if (out_f16 && (p.n_out % 256 != 0 || (reinterpret_cast<uintptr_t>(p.out) & 31u) != 0 ||
+                  (reinterpret_cast<uintptr_t>(p.out_codes) & 7u) != 0))
+    return cudaErrorInvalidValue;
+  const bool out_tma =
+      !SWIGLU && (out_f16 ? make_tmap_f16_out(&tmY, p.out, static_cast<uint64_t>(p.n_out),
+                                              static_cast<uint64_t>(p.rows_total))
+                          : make_tmap_f32_out(&tmY, p.out, static_cast<uint64_t>(p.n_out),
+                                              static_cast<uint64_t>(p.rows_total)));
   if (!out_tma) tmY = tmA;
   cudaError_t err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<BN, SWIGLU>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1438,6 +1587,9 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.ldo = p.n_out;
   a.rows_total = p.rows_total;
   a.out_tma = out_tma ? 1 : 0;
+  a.out_codes = out_f16 ? p.out_codes : nullptr;
+  a.split_part = out_f16 ? p.split_part : nullptr;
+  a.split_part_slots = (out_f16 && p.split_part != nullptr) ? p.split_part_slots : 0;
   a.split_flags = SWIGLU ? nullptr : p.split_flags;
   {
     // a different value per launch, so that a flag left raised by an aborted
@@ -1503,6 +1655,7 @@ cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s) {
 
 cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s) {
   // p.n_out = d, p.b_rows = d, K = inter
+  if (p.out_codes != nullptr && !p.pair) return cudaErrorInvalidValue;  // compact: pair form only
   if (p.pair) {
     if (p.n_out % 256 == 0) return run_gemm_pair<256, false>(p, 0, s);
     return cudaErrorInvalidValue;

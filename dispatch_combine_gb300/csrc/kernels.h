@@ -148,6 +148,11 @@ cudaError_t launch_quantize_blocks_fp8(const void *w, int mats, int rows, int co
 // y[t] = sum_j w[t,j] * y_perm[dest[t*k+j]]; rows outside [0, y_rows) add nothing
 cudaError_t launch_combine(const float *y_perm, int64_t y_rows, const int32_t *dest,
                            const float *w, int T, int k, int d, void *y, cudaStream_t s);
+// the same from the compact rows (fp16 values y16 [y_rows, d], code bytes
+// [y_rows, d / 32]; d a multiple of 32)
+cudaError_t launch_combine16(const void *y16, const uint8_t *codes, int64_t y_rows,
+                             const int32_t *dest, const float *w, int T, int k, int d, void *y,
+                             cudaStream_t s);
 
 // gemm.cu
 struct GemmProblem {
@@ -171,6 +176,14 @@ struct GemmProblem {
   // pair down form: kPairSplitFlagWords zeroed words; with them a short
   // last wave runs its tiles as two K halves (nullptr: never split)
   uint32_t *split_flags;
+  // pair down form, compact output (the layer's y16 form, common.cuh): out
+  // receives fp16 values [rows_total, n_out], out_codes the code bytes
+  // [rows_total, n_out / 32]; split_part holds split_part_slots x 256 x 256
+  // floats for the halves of split tiles (fewer slots: fewer tiles split).
+  // nullptr: fp32 output.
+  uint8_t *out_codes;
+  float *split_part;
+  int split_part_slots;
 };
 cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s);
 cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s);

@@ -237,6 +237,13 @@ moe_status_t moe_combine(const moe_shape_t *shape, const float *y_perm,
 /*
  * The whole layer: route -> dispatch -> gate_up+SwiGLU -> down -> combine,
  * all on `stream`, no host synchronisation, intermediates in the workspace.
+ * Where the expert GEMMs run on CTA pairs (moe_layer_yperm_row_bytes below
+ * 2*d + d/32), the down GEMM keeps its rows in a compact form: each group of
+ * 32 columns as fp16 values scaled by a power of two (the group's largest
+ * magnitude just under 2^15) and one byte for that exponent, a rounding of
+ * at most 2^-11 of the group's largest value; the combine restores each
+ * value exactly from that form before its fp32 sum.  Elsewhere the rows stay
+ * fp32, as moe_expert_ffn writes them.
  *   x [T,d] bf16, w_r [d,E] bf16, bias [E] fp32 (NULL for softmax),
  *   w_gate_up [E,2*inter,d] bf16, w_down [E,d,inter] bf16, y [T,d] bf16 out,
  *   topk_ids [T,k] int32 / topk_w [T,k] fp32 / counts [E] int32: optional
@@ -443,6 +450,13 @@ moe_status_t moe_eplb_plan(const double *load, int32_t num_experts, int32_t num_
  * accounting).
  */
 int32_t moe_layer_launch_count(const moe_shape_t *shape);
+
+/*
+ * Bytes of one routed row of moe_layer's down-GEMM output as the combine
+ * reads it: 4*d (fp32 rows) or 2*d + d/32 (the compact rows); 0 for an
+ * invalid shape.  For byte accounting.
+ */
+int64_t moe_layer_yperm_row_bytes(const moe_shape_t *shape);
 
 /*
  * (token, expert) pairs whose fixed-order logit the last screened routing in

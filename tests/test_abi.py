@@ -18,7 +18,7 @@ def declared_functions():
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
     names = re.findall(
-        r"(?:moe_status_t|int32_t|size_t|void|const\s+char\s*\*)\s*\*?\s*(moe_\w+)\s*\(", text)
+        r"(?:moe_status_t|int32_t|int64_t|size_t|void|const\s+char\s*\*)\s*\*?\s*(moe_\w+)\s*\(", text)
     return sorted(set(names))
 
 
@@ -155,3 +155,20 @@ def test_masked_layout_arguments(lib):
     assert lib.moe_expert_ffn_workspace_size(ctypes.byref(s), 3, 0, ctypes.byref(out)) == 1
     assert lib.moe_expert_ffn_workspace_size(ctypes.byref(s), 1, 256, ctypes.byref(out)) == 0
     assert out.value >= 16 * 256 * 128 * 2
+
+
+def test_layer_yperm_row_bytes(lib):
+    # the layer keeps its down-GEMM rows compact (fp16 + a code byte per 32
+    # columns) exactly where its expert GEMMs run on CTA pairs: at least 256
+    # rows per expert on average, d a multiple of 256, inter of 128
+    lib.moe_layer_yperm_row_bytes.restype = ctypes.c_int64
+    prefill = _shape(T=16384, d=7168, E=256, G=8, topk_group=4, k=8, inter=2048, score=1)
+    decode = _shape(T=512, d=7168, E=256, G=8, topk_group=4, k=8, inter=2048, score=1)
+    few_large = _shape(T=2048, d=4096, E=8, G=1, topk_group=1, k=2, inter=14336)
+    odd_d = _shape(T=2048, d=4160, E=8, G=1, topk_group=1, k=2, inter=1024)
+    assert lib.moe_layer_yperm_row_bytes(ctypes.byref(prefill)) == 2 * 7168 + 7168 // 32
+    assert lib.moe_layer_yperm_row_bytes(ctypes.byref(few_large)) == 2 * 4096 + 4096 // 32
+    assert lib.moe_layer_yperm_row_bytes(ctypes.byref(decode)) == 4 * 7168
+    assert lib.moe_layer_yperm_row_bytes(ctypes.byref(odd_d)) == 4 * 4160
+    bad = _shape(T=-1)
+    assert lib.moe_layer_yperm_row_bytes(ctypes.byref(bad)) == 0

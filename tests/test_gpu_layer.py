@@ -201,3 +201,43 @@ def test_masked_expert_slices(variant):
     ref = oracle.expert_ffn_rows(xr, np.array(row_e, np.int32), bits(w_gu), bits(w_down))
     got = y[idx_i, idx_r].cpu().numpy()
     check_close(got, ref, bf16_output=False, what=f"masked {variant}")
+
+
+@pytest.mark.parametrize("name", ["few_large", "prefill"])
+def test_layer_compact_rows_within_their_bound(name):
+    """Where the expert GEMMs run on CTA pairs the layer keeps the down
+    GEMM's rows as fp16 values with a power-of-two scale per 32 columns.
+    Against the same layer composed from the public calls (fp32 rows), every
+    output differs by at most that form's rounding -- 2^-11 of each group's
+    largest magnitude, weighted like the combine -- plus one bf16 step."""
+    ensure_lib()
+    cfg = CONFIGS[name]
+    shape = cfg.shape()
+    d = cfg.d
+    assert moe.moe_layer_yperm_row_bytes(shape) == 2 * d + d // 32
+    t = layer_inputs(name)
+    bias = t["bias"] if cfg.score == SCORE_SIGMOID_BIAS else None
+    ws = moe.Workspace(moe.moe_workspace_size(shape))
+    y = moe.moe_layer(shape, t["x"], t["w_r"], bias, t["w_gate_up"], t["w_down"], ws)
+    ids, w, _ = moe.moe_route(shape, t["x"], t["w_r"], bias, ws)
+    _, offsets, _, dest, x_perm = moe.moe_dispatch(shape, ids, t["x"], ws)
+    fws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    y_perm = moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_CONTIGUOUS, x_perm, offsets, 0,
+                                t["w_gate_up"], t["w_down"], fws)
+    y_ref = moe.moe_combine(shape, y_perm, dest, w)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0 and moe.moe_get_device_status(fws) == 0
+    del x_perm, fws
+    T, k = cfg.T, cfg.k
+    gmax = y_perm.abs().view(-1, d // 32, 32).amax(-1)               # [T*k, d/32]
+    rows = dest.view(T, k).long()
+    bound = (w.abs().unsqueeze(-1) * gmax[rows]).sum(1) * 2.0 ** -11  # [T, d/32]
+    bound = bound.repeat_interleave(32, dim=1)
+    yr = y_ref.float()
+    mag = yr.abs() + bound
+    ulp = torch.where(mag > 0, torch.exp2(torch.floor(torch.log2(mag)) - 7),
+                      torch.zeros_like(mag))
+    excess = ((y.float() - yr).abs() - bound - ulp).max().item()
+    assert excess <= 0.0, f"{name}: compact rows exceed their bound by {excess:.3e}"
+    same = (y.view(torch.int16) == y_ref.view(torch.int16)).float().mean().item()
+    print(f"{name}: {same * 100:.2f} % of outputs identical to the fp32-row composition")
