@@ -153,6 +153,34 @@ int tile_rows_for(const moe_shape_t *s, int32_t layout, int32_t M_max) {
   return use_pair(s, layout, M_max) ? 256 : 128;
 }
 
+// The layers keep the down GEMM's rows compact (fp16 values and a code byte
+// per 32 columns, common.cuh) when d is a multiple of 256 (whole 256-column
+// down tiles in both GEMM forms).  The fp32 region of `rows` rows holds the
+// values, then the codes, then the split tiles' partial sums.
+bool compact_rows(const moe_shape_t &s) { return s.d % 256 == 0; }
+struct CompactRows {
+  void *vals;
+  uint8_t *codes;
+  float *part;
+  int slots;
+};
+CompactRows compact_layout(void *region, int64_t rows, int d) {
+  CompactRows c;
+  const size_t vals = align_up(2 * static_cast<size_t>(rows) * d);
+  const size_t cods = align_up(static_cast<size_t>(rows) * (d / 32));
+  const size_t bytes = 4 * static_cast<size_t>(rows) * d;
+  const size_t slot_bytes = 256 * 256 * 4;
+  c.slots = bytes > vals + cods
+                ? static_cast<int>(std::min<size_t>((bytes - vals - cods) / slot_bytes,
+                                                    moe::kPairSplitSlots))
+                : 0;
+  uint8_t *base = static_cast<uint8_t *>(region);
+  c.vals = base;
+  c.codes = base + vals;
+  c.part = c.slots > 0 ? reinterpret_cast<float *>(base + vals + cods) : nullptr;
+  return c;
+}
+
 moe_status_t run_gate_up(const moe_shape_t *s, int32_t layout, const void *x_in,
                          const int32_t *seg, int32_t M_max, int64_t rows, const int32_t *mtile,
                          const void *w_gate_up, void *h, uint32_t *status, cudaStream_t st) {
@@ -539,27 +567,15 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
   MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_perm, offsets, 0, n, mtile, w_gate_up, h,
                       status, stream));
   MOE_TRY(mark(3));
-  if (use_pair(shape, MOE_LAYOUT_CONTIGUOUS, 0)) {
-    // the CTA-pair down GEMM writes the compact rows (fp16 values and a code
-    // byte per 32 columns, 2 + 1/32 bytes per value instead of 4) into the
-    // y_perm region, then the split tiles' scratch; the combine reads them
-    const size_t vals = align_up(2 * static_cast<size_t>(n) * s.d);
-    const size_t cods = align_up(static_cast<size_t>(n) * (s.d / 32));
-    const size_t region = 4 * static_cast<size_t>(n) * s.d;
-    const size_t slot_bytes = 256 * 256 * 4;
-    const int slots = region > vals + cods
-                          ? static_cast<int>(std::min<size_t>((region - vals - cods) / slot_bytes,
-                                                              moe::kPairSplitSlots))
-                          : 0;
-    uint8_t *base = at<uint8_t>(ws, L.y_perm);
-    uint8_t *codes = base + vals;
-    float *part = reinterpret_cast<float *>(base + vals + cods);
-    MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, offsets, 0, n, mtile, w_down, base, status,
-                     at<uint32_t>(ws, L.flags), stream, codes, slots > 0 ? part : nullptr,
-                     slots));
+  if (compact_rows(s)) {
+    // the down GEMM writes the compact rows (2 + 1/32 bytes per value instead
+    // of 4) into the y_perm region; the combine reads them
+    const CompactRows c = compact_layout(y_perm, n, s.d);
+    MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, offsets, 0, n, mtile, w_down, c.vals,
+                     status, at<uint32_t>(ws, L.flags), stream, c.codes, c.part, c.slots));
     MOE_TRY(mark(4));
     MOE_TRY(cuda_status(
-        moe::launch_combine16(base, codes, n, dest, w, s.T, s.k, s.d, y, stream)));
+        moe::launch_combine16(c.vals, c.codes, n, dest, w, s.T, s.k, s.d, y, stream)));
     return mark(5);
   }
   MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, offsets, 0, n, mtile, w_down, y_perm, status,
@@ -854,6 +870,9 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
   int32_t *dest = at<int32_t>(ws, L.dest);
   uint8_t *x_rows = at<uint8_t>(ws, L.x_perm);
   float *y_rows = at<float>(ws, L.y_perm);
+  // compact rows (when d allows): the padded rows, then the overflow rows
+  const CompactRows cr = compact_rows(s) ? compact_layout(y_rows, pad + n, s.d)
+                                         : CompactRows{nullptr, nullptr, nullptr, 0};
   uint8_t *h = at<uint8_t>(ws, L.h);
   float *logits = at<float>(ws, L.logits);
 
@@ -872,8 +891,12 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
                                               mtile, status, stream)));
     MOE_TRY(run_gate_up(shape, MOE_LAYOUT_MASKED, x_rows, kp, capacity, pad, mtile, w_gate_up,
                         h, status, stream));
-    MOE_TRY(run_down(shape, MOE_LAYOUT_MASKED, h, kp, capacity, pad, mtile, w_down, y_rows,
-                     status, at<uint32_t>(ws, L.flags), stream));
+    if (cr.vals)
+      MOE_TRY(run_down(shape, MOE_LAYOUT_MASKED, h, kp, capacity, pad, mtile, w_down, cr.vals,
+                       status, at<uint32_t>(ws, L.flags), stream, cr.codes, cr.part, cr.slots));
+    else
+      MOE_TRY(run_down(shape, MOE_LAYOUT_MASKED, h, kp, capacity, pad, mtile, w_down, y_rows,
+                       status, at<uint32_t>(ws, L.flags), stream));
   }
   // second round: the overflow rows, contiguous with offsets ovf_offsets
   if (overflow == MOE_OVERFLOW_SECOND_ROUND) {
@@ -882,15 +905,24 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
                                               status, stream)));
     MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_rows + pad * s.d * 2, ovf, 0, n, mtile,
                         w_gate_up, h, status, stream));
-    MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, ovf, 0, n, mtile, w_down,
-                     y_rows + pad * s.d, status, at<uint32_t>(ws, L.flags), stream));
+    if (cr.vals)
+      MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, ovf, 0, n, mtile, w_down,
+                       static_cast<uint8_t *>(cr.vals) + pad * s.d * 2, status,
+                       at<uint32_t>(ws, L.flags), stream, cr.codes + pad * (s.d / 32), cr.part,
+                       cr.slots));
+    else
+      MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, ovf, 0, n, mtile, w_down,
+                       y_rows + pad * s.d, status, at<uint32_t>(ws, L.flags), stream));
   }
+  if (cr.vals)
+    return cuda_status(moe::launch_combine16(cr.vals, cr.codes, pad + n, dest, w, s.T, s.k, s.d,
+                                             y, stream));
   return cuda_status(moe::launch_combine(y_rows, pad + n, dest, w, s.T, s.k, s.d, y, stream));
 }
 
 int64_t moe_layer_yperm_row_bytes(const moe_shape_t *shape) {
   if (check_shape(shape) != MOE_OK) return 0;
-  if (use_pair(shape, MOE_LAYOUT_CONTIGUOUS, 0)) return 2 * int64_t{shape->d} + shape->d / 32;
+  if (compact_rows(*shape)) return 2 * int64_t{shape->d} + shape->d / 32;
   return 4 * int64_t{shape->d};
 }
 

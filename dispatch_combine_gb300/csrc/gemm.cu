@@ -341,6 +341,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
+      } else if (args.out_codes != nullptr) {
+        // compact output (BN = 256, no K pieces): 32 fp16 values and one code
+        // per 32-column chunk, the row's 8 codes of the tile in one store
+        __half *dst = static_cast<__half *>(args.out) + grow * args.ldo +
+                      static_cast<int64_t>(t.n) * BN;
+        uint64_t codes = 0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + c * 32, v);
+          tmem_ld_wait();
+          tmem_regs_fence(v);
+          if (ok) {
+            uint32_t hw[16];
+            const uint32_t cc = y16_encode32(v, hw);
+            uint32_t w8[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) w8[q] = hw[q];
+            st_global_v8(dst + c * 32, w8);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) w8[q] = hw[8 + q];
+            st_global_v8(dst + c * 32 + 16, w8);
+            codes |= static_cast<uint64_t>(cc) << (8 * c);
+          }
+        }
+        if (ok)
+          *reinterpret_cast<uint64_t *>(args.out_codes + grow * (args.ldo / 32) +
+                                        static_cast<int64_t>(t.n) * (BN / 32)) = codes;
       } else {
         float *dst = static_cast<float *>(args.out) + grow * args.ldo +
                      static_cast<int64_t>(t.n) * BN;
@@ -1531,6 +1559,14 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.status = p.status;
   a.wait_limit_ns = p.wait_limit_ns ? p.wait_limit_ns : kDefaultWaitLimitNs;
   a.ksplit = (!SWIGLU && p.ksplit > 1) ? p.ksplit : 1;
+  if (!SWIGLU && p.out_codes != nullptr) {
+    // compact output: whole 256-column tiles, no K pieces, 32-byte stores
+    if (BN != 256 || a.ksplit != 1 || p.n_out % 256 != 0 ||
+        (reinterpret_cast<uintptr_t>(p.out) & 31u) != 0 ||
+        (reinterpret_cast<uintptr_t>(p.out_codes) & 7u) != 0)
+      return cudaErrorInvalidValue;
+    a.out_codes = p.out_codes;
+  }
   MOE_LAUNCH_PDL(grouped_gemm_kernel<BN, SWIGLU>, num_sms(), kGemmThreads, C::SMEM_BYTES, s, tmA, tmB, a);
   return cudaGetLastError();
 }
@@ -1655,7 +1691,6 @@ cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s) {
 
 cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s) {
   // p.n_out = d, p.b_rows = d, K = inter
-  if (p.out_codes != nullptr && !p.pair) return cudaErrorInvalidValue;  // compact: pair form only
   if (p.pair) {
     if (p.n_out % 256 == 0) return run_gemm_pair<256, false>(p, 0, s);
     return cudaErrorInvalidValue;

@@ -176,11 +176,11 @@ struct GemmProblem {
   // pair down form: kPairSplitFlagWords zeroed words; with them a short
   // last wave runs its tiles as two K halves (nullptr: never split)
   uint32_t *split_flags;
-  // pair down form, compact output (the layer's y16 form, common.cuh): out
-  // receives fp16 values [rows_total, n_out], out_codes the code bytes
-  // [rows_total, n_out / 32]; split_part holds split_part_slots x 256 x 256
-  // floats for the halves of split tiles (fewer slots: fewer tiles split).
-  // nullptr: fp32 output.
+  // down, compact output (the layer's y16 form, common.cuh): out receives
+  // fp16 values [rows_total, n_out], out_codes the code bytes [rows_total,
+  // n_out / 32] (n_out a multiple of 256; the 1-CTA form without K pieces);
+  // pair form: split_part holds split_part_slots x 256 x 256 floats for the
+  // halves of split tiles (fewer slots: fewer tiles split).  nullptr: fp32.
   uint8_t *out_codes;
   float *split_part;
   int split_part_slots;

@@ -237,8 +237,8 @@ moe_status_t moe_combine(const moe_shape_t *shape, const float *y_perm,
 /*
  * The whole layer: route -> dispatch -> gate_up+SwiGLU -> down -> combine,
  * all on `stream`, no host synchronisation, intermediates in the workspace.
- * Where the expert GEMMs run on CTA pairs (moe_layer_yperm_row_bytes below
- * 2*d + d/32), the down GEMM keeps its rows in a compact form: each group of
+ * With d a multiple of 256 (moe_layer_yperm_row_bytes then 2*d + d/32), the
+ * down GEMM keeps its rows in a compact form: each group of
  * 32 columns as fp16 values scaled by a power of two (the group's largest
  * magnitude just under 2^15) and one byte for that exponent, a rounding of
  * at most 2^-11 of the group's largest value; the combine restores each

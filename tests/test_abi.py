@@ -158,9 +158,8 @@ def test_masked_layout_arguments(lib):
 
 
 def test_layer_yperm_row_bytes(lib):
-    # the layer keeps its down-GEMM rows compact (fp16 + a code byte per 32
-    # columns) exactly where its expert GEMMs run on CTA pairs: at least 256
-    # rows per expert on average, d a multiple of 256, inter of 128
+    # the layers keep their down-GEMM rows compact (fp16 + a code byte per 32
+    # columns) where d is a multiple of 256 (whole 256-column down tiles)
     lib.moe_layer_yperm_row_bytes.restype = ctypes.c_int64
     prefill = _shape(T=16384, d=7168, E=256, G=8, topk_group=4, k=8, inter=2048, score=1)
     decode = _shape(T=512, d=7168, E=256, G=8, topk_group=4, k=8, inter=2048, score=1)
@@ -168,7 +167,8 @@ def test_layer_yperm_row_bytes(lib):
     odd_d = _shape(T=2048, d=4160, E=8, G=1, topk_group=1, k=2, inter=1024)
     assert lib.moe_layer_yperm_row_bytes(ctypes.byref(prefill)) == 2 * 7168 + 7168 // 32
     assert lib.moe_layer_yperm_row_bytes(ctypes.byref(few_large)) == 2 * 4096 + 4096 // 32
-    assert lib.moe_layer_yperm_row_bytes(ctypes.byref(decode)) == 4 * 7168
+    assert lib.moe_layer_yperm_row_bytes(ctypes.byref(decode)) == 2 * 7168 + 7168 // 32
+    assert lib.moe_layer_yperm_row_bytes(ctypes.byref(_shape())) == 2 * 256 + 256 // 32
     assert lib.moe_layer_yperm_row_bytes(ctypes.byref(odd_d)) == 4 * 4160
     bad = _shape(T=-1)
     assert lib.moe_layer_yperm_row_bytes(ctypes.byref(bad)) == 0

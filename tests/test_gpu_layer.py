@@ -203,10 +203,10 @@ def test_masked_expert_slices(variant):
     check_close(got, ref, bf16_output=False, what=f"masked {variant}")
 
 
-@pytest.mark.parametrize("name", ["few_large", "prefill"])
+@pytest.mark.parametrize("name", ["tiny", "few_large", "decode", "prefill"])
 def test_layer_compact_rows_within_their_bound(name):
-    """Where the expert GEMMs run on CTA pairs the layer keeps the down
-    GEMM's rows as fp16 values with a power-of-two scale per 32 columns.
+    """With d a multiple of 256 the layer keeps the down GEMM's rows (1-CTA
+    or CTA-pair form) as fp16 values with a power-of-two scale per 32 columns.
     Against the same layer composed from the public calls (fp32 rows), every
     output differs by at most that form's rounding -- 2^-11 of each group's
     largest magnitude, weighted like the combine -- plus one bf16 step."""
