@@ -146,7 +146,7 @@ bool use_pair(const moe_shape_t *s, int32_t layout, int32_t M_max) {
   if (s->inter % 128 != 0 || s->d % 256 != 0) return false;
   if (static_cast<int64_t>(s->T) * s->k < static_cast<int64_t>(moe::kPairRowsPerExpert) * s->E)
     return false;
-  if (layout == MOE_LAYOUT_CONTIGUOUS) return true;
+  if (layout == MOE_LAYOUT_CONTIGUOUS || layout == moe::kLayoutTwoSeg) return true;
   return layout == MOE_LAYOUT_MASKED && M_max >= moe::kPairRowsPerExpert;
 }
 int tile_rows_for(const moe_shape_t *s, int32_t layout, int32_t M_max) {
@@ -181,11 +181,14 @@ CompactRows compact_layout(void *region, int64_t rows, int d) {
   return c;
 }
 
+// seg2: the overflow offsets of the two-segment layout (moe::kLayoutTwoSeg)
 moe_status_t run_gate_up(const moe_shape_t *s, int32_t layout, const void *x_in,
                          const int32_t *seg, int32_t M_max, int64_t rows, const int32_t *mtile,
-                         const void *w_gate_up, void *h, uint32_t *status, cudaStream_t st) {
+                         const void *w_gate_up, void *h, uint32_t *status, cudaStream_t st,
+                         const int32_t *seg2 = nullptr) {
   GemmProblem p;
   std::memset(&p, 0, sizeof p);
+  p.seg2 = seg2;
   p.E = s->E;
   p.K = s->d;
   p.n_out = s->inter;
@@ -209,9 +212,10 @@ moe_status_t run_down(const moe_shape_t *s, int32_t layout, const void *h, const
                       int32_t M_max, int64_t rows, const int32_t *mtile, const void *w_down,
                       void *y, uint32_t *status, uint32_t *split_flags, cudaStream_t st,
                       uint8_t *y16_codes = nullptr, float *split_part = nullptr,
-                      int split_slots = 0) {
+                      int split_slots = 0, const int32_t *seg2 = nullptr) {
   GemmProblem p;
   std::memset(&p, 0, sizeof p);
+  p.seg2 = seg2;
   p.out_codes = y16_codes;
   p.split_part = split_part;
   p.split_part_slots = split_slots;
@@ -884,35 +888,58 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
                                            at<int32_t>(ws, L.doff), at<int32_t>(ws, L.src),
                                            dest, x_rows, at<int32_t>(ws, L.chunk), nullptr,
                                            128, status, stream, cap)));
-  // first round: the padded rows, masked layout with M_max = C
-  if (capacity > 0) {
-    MOE_TRY(cuda_status(moe::launch_ffn_tiles(kp, MOE_LAYOUT_MASKED, s.E, capacity,
-                                              tile_rows_for(shape, MOE_LAYOUT_MASKED, capacity),
-                                              mtile, status, stream)));
-    MOE_TRY(run_gate_up(shape, MOE_LAYOUT_MASKED, x_rows, kp, capacity, pad, mtile, w_gate_up,
-                        h, status, stream));
+  // Second round: where the expert GEMMs stream weights (the 1-CTA form, few
+  // rows per expert), both rounds run as one launch per GEMM -- each
+  // expert's padded rows, then its overflow rows (the two-segment layout) --
+  // so its weights stream once; where they are compute-bound (CTA pairs) the
+  // overflow rows run after the padded ones, which measured faster there.
+  const bool one_launch = overflow == MOE_OVERFLOW_SECOND_ROUND &&
+                          !use_pair(shape, MOE_LAYOUT_CONTIGUOUS, 0);
+  if (one_launch) {
+    MOE_TRY(cuda_status(moe::launch_ffn_tiles(
+        kp, moe::kLayoutTwoSeg, s.E, capacity,
+        tile_rows_for(shape, moe::kLayoutTwoSeg, capacity), mtile, status, stream, ovf)));
+    MOE_TRY(run_gate_up(shape, moe::kLayoutTwoSeg, x_rows, kp, capacity, pad + n, mtile,
+                        w_gate_up, h, status, stream, ovf));
     if (cr.vals)
-      MOE_TRY(run_down(shape, MOE_LAYOUT_MASKED, h, kp, capacity, pad, mtile, w_down, cr.vals,
-                       status, at<uint32_t>(ws, L.flags), stream, cr.codes, cr.part, cr.slots));
+      MOE_TRY(run_down(shape, moe::kLayoutTwoSeg, h, kp, capacity, pad + n, mtile, w_down,
+                       cr.vals, status, at<uint32_t>(ws, L.flags), stream, cr.codes, cr.part,
+                       cr.slots, ovf));
     else
-      MOE_TRY(run_down(shape, MOE_LAYOUT_MASKED, h, kp, capacity, pad, mtile, w_down, y_rows,
-                       status, at<uint32_t>(ws, L.flags), stream));
-  }
-  // second round: the overflow rows, contiguous with offsets ovf_offsets
-  if (overflow == MOE_OVERFLOW_SECOND_ROUND) {
-    MOE_TRY(cuda_status(moe::launch_ffn_tiles(ovf, MOE_LAYOUT_CONTIGUOUS, s.E, 0,
-                                              tile_rows_for(shape, MOE_LAYOUT_CONTIGUOUS, 0), mtile,
-                                              status, stream)));
-    MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_rows + pad * s.d * 2, ovf, 0, n, mtile,
-                        w_gate_up, h, status, stream));
-    if (cr.vals)
-      MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, ovf, 0, n, mtile, w_down,
-                       static_cast<uint8_t *>(cr.vals) + pad * s.d * 2, status,
-                       at<uint32_t>(ws, L.flags), stream, cr.codes + pad * (s.d / 32), cr.part,
-                       cr.slots));
-    else
-      MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, ovf, 0, n, mtile, w_down,
-                       y_rows + pad * s.d, status, at<uint32_t>(ws, L.flags), stream));
+      MOE_TRY(run_down(shape, moe::kLayoutTwoSeg, h, kp, capacity, pad + n, mtile, w_down,
+                       y_rows, status, at<uint32_t>(ws, L.flags), stream, nullptr, nullptr, 0,
+                       ovf));
+  } else {
+    // first round: the padded rows, masked layout with M_max = C
+    if (capacity > 0) {
+      MOE_TRY(cuda_status(moe::launch_ffn_tiles(kp, MOE_LAYOUT_MASKED, s.E, capacity,
+                                                tile_rows_for(shape, MOE_LAYOUT_MASKED, capacity),
+                                                mtile, status, stream)));
+      MOE_TRY(run_gate_up(shape, MOE_LAYOUT_MASKED, x_rows, kp, capacity, pad, mtile, w_gate_up,
+                          h, status, stream));
+      if (cr.vals)
+        MOE_TRY(run_down(shape, MOE_LAYOUT_MASKED, h, kp, capacity, pad, mtile, w_down, cr.vals,
+                         status, at<uint32_t>(ws, L.flags), stream, cr.codes, cr.part, cr.slots));
+      else
+        MOE_TRY(run_down(shape, MOE_LAYOUT_MASKED, h, kp, capacity, pad, mtile, w_down, y_rows,
+                         status, at<uint32_t>(ws, L.flags), stream));
+    }
+    // second round: the overflow rows, contiguous with offsets ovf_offsets
+    if (overflow == MOE_OVERFLOW_SECOND_ROUND) {
+      MOE_TRY(cuda_status(moe::launch_ffn_tiles(ovf, MOE_LAYOUT_CONTIGUOUS, s.E, 0,
+                                                tile_rows_for(shape, MOE_LAYOUT_CONTIGUOUS, 0),
+                                                mtile, status, stream)));
+      MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_rows + pad * s.d * 2, ovf, 0, n, mtile,
+                          w_gate_up, h, status, stream));
+      if (cr.vals)
+        MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, ovf, 0, n, mtile, w_down,
+                         static_cast<uint8_t *>(cr.vals) + pad * s.d * 2, status,
+                         at<uint32_t>(ws, L.flags), stream, cr.codes + pad * (s.d / 32),
+                         cr.part, cr.slots));
+      else
+        MOE_TRY(run_down(shape, MOE_LAYOUT_CONTIGUOUS, h, ovf, 0, n, mtile, w_down,
+                         y_rows + pad * s.d, status, at<uint32_t>(ws, L.flags), stream));
+    }
   }
   if (cr.vals)
     return cuda_status(moe::launch_combine16(cr.vals, cr.codes, pad + n, dest, w, s.T, s.k, s.d,

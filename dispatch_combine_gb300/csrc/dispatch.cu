@@ -278,13 +278,24 @@ __global__ void __launch_bounds__(256)
 
 // mtile_base from offsets (layout 0) or masked_m clamped to M_max (layout 1)
 __global__ void __launch_bounds__(1024)
-    ffn_tiles_kernel(const int32_t *__restrict__ seg, int layout, int E, int M_max,
-                     int tile_rows, int32_t *__restrict__ mtile_base, uint32_t *status) {
+    ffn_tiles_kernel(const int32_t *__restrict__ seg, const int32_t *__restrict__ seg2,
+                     int layout, int E, int M_max, int tile_rows,
+                     int32_t *__restrict__ mtile_base, uint32_t *status) {
   pdl_begin();
   const int e = threadIdx.x;
-  int rows = 0;
+  int rows = 0, tiles2 = 0;
   if (e < E) {
-    if (layout == MOE_LAYOUT_CONTIGUOUS) {
+    if (layout == kLayoutTwoSeg) {
+      // the slab's rows (clamped to M_max), then the overflow rows
+      rows = min(max(seg[e], 0), M_max);
+      if (seg[e] > M_max || seg[e] < 0) set_status(status, kStatusOverflow);
+      int r2 = seg2[e + 1] - seg2[e];
+      if (r2 < 0) {
+        set_status(status, kStatusBadId);
+        r2 = 0;
+      }
+      tiles2 = (r2 + tile_rows - 1) / tile_rows;
+    } else if (layout == MOE_LAYOUT_CONTIGUOUS) {
       rows = seg[e + 1] - seg[e];
       if (rows < 0) {
         set_status(status, kStatusBadId);
@@ -303,7 +314,7 @@ __global__ void __launch_bounds__(1024)
     }
   }
   int total = 0;
-  const int excl = block_exclusive_scan((rows + tile_rows - 1) / tile_rows, &total);
+  const int excl = block_exclusive_scan((rows + tile_rows - 1) / tile_rows + tiles2, &total);
   if (e < E) mtile_base[e] = excl;
   if (e == 0) mtile_base[E] = total;
 }
@@ -522,8 +533,11 @@ cudaError_t launch_gather_rows(const void *src, int row_bytes, const float *src_
 }
 
 cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,
-                             int32_t *mtile_base, uint32_t *status, cudaStream_t s) {
-  MOE_LAUNCH_PDL(ffn_tiles_kernel, 1, 1024, 0, s, seg, layout, E, M_max, tile_rows, mtile_base, status);
+                             int32_t *mtile_base, uint32_t *status, cudaStream_t s,
+                             const int32_t *seg2) {
+  if (layout == kLayoutTwoSeg && seg2 == nullptr) return cudaErrorInvalidValue;
+  MOE_LAUNCH_PDL(ffn_tiles_kernel, 1, 1024, 0, s, seg, seg2, layout, E, M_max, tile_rows,
+                 mtile_base, status);
   return cudaGetLastError();
 }
 

@@ -82,6 +82,7 @@ struct KArgs {
   int split_part_slots;
   int64_t rows_total;
   const int32_t *seg;
+  const int32_t *seg2;  // kLayoutTwoSeg: overflow offsets [E+1]
   const int32_t *mtile_base;
   void *out;
   int64_t ldo;
@@ -114,16 +115,25 @@ __device__ __forceinline__ Tile decode_tile(const KArgs &a, const int32_t *mt, i
   const int within = local - blk * a.m_block * a.n_tiles;
   t.n = within / mb;
   t.m = blk * a.m_block + (within - t.n * mb);
-  int rows, start;
+  int rows, start, m = t.m;
   if (a.layout == MOE_LAYOUT_CONTIGUOUS) {
     start = a.seg[t.e];
     rows = a.seg[t.e + 1] - start;
   } else {
     start = t.e * a.M_max;
     rows = min(max(a.seg[t.e], 0), a.M_max);
+    if (a.layout == kLayoutTwoSeg) {
+      // the slab's tiles, then the overflow rows' tiles
+      const int tiles1 = (rows + TILE_M - 1) / TILE_M;
+      if (m >= tiles1) {
+        m -= tiles1;
+        start = a.E * a.M_max + a.seg2[t.e];
+        rows = a.seg2[t.e + 1] - a.seg2[t.e];
+      }
+    }
   }
-  t.row0 = start + t.m * TILE_M;
-  t.rows_valid = min(TILE_M, rows - t.m * TILE_M);
+  t.row0 = start + m * TILE_M;
+  t.rows_valid = min(TILE_M, rows - m * TILE_M);
   return t;
 }
 
@@ -1507,6 +1517,7 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   a.b_rows = p.b_rows;
   a.up_off = up_off;
   a.seg = p.seg;
+  a.seg2 = p.seg2;
   a.mtile_base = p.mtile_base;
   a.out = p.out;
   a.ldo = p.n_out;
@@ -1548,6 +1559,7 @@ cudaError_t run_gemm(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.b_rows = p.b_rows;
   a.up_off = up_off;
   a.seg = p.seg;
+  a.seg2 = p.seg2;
   a.mtile_base = p.mtile_base;
   a.out = p.out;
   a.ldo = p.n_out;
@@ -1618,6 +1630,7 @@ cudaError_t run_gemm_pair(const GemmProblem &p, int up_off, cudaStream_t s) {
   a.b_rows = p.b_rows;
   a.up_off = up_off;
   a.seg = p.seg;
+  a.seg2 = p.seg2;
   a.mtile_base = p.mtile_base;
   a.out = p.out;
   a.ldo = p.n_out;

@@ -110,10 +110,18 @@ cudaError_t launch_dispatch_replicated(const int32_t *ids, int T, int k, int E, 
                                        int32_t *src_token, int32_t *dest, void *x_perm,
                                        const ReplicaScratch &w, uint32_t *status,
                                        cudaStream_t s);
+// Internal layout of the capacity layer's two rounds in one launch: expert e
+// has the rows of its padded slab, [e * M_max, e * M_max + seg[e]) (seg =
+// kept counts, clamped to M_max), then its overflow rows, [pad + seg2[e],
+// pad + seg2[e + 1]) (seg2 = overflow offsets [E+1], pad = E * M_max); its
+// m-tiles cover the slab's rows first, then the overflow rows.
+constexpr int kLayoutTwoSeg = 2;
 // mtile_base[e] = sum_{e'<e} ceil(M_e'/tile_rows) for the contiguous (seg =
-// offsets) or masked (seg = masked_m, clamped to M_max) layout.
+// offsets) or masked (seg = masked_m, clamped to M_max) layout; for
+// kLayoutTwoSeg the tiles of both of an expert's segments (seg2 as above).
 cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,
-                             int32_t *mtile_base, uint32_t *status, cudaStream_t s);
+                             int32_t *mtile_base, uint32_t *status, cudaStream_t s,
+                             const int32_t *seg2 = nullptr);
 // Expert GEMMs run on CTA pairs with 256-row tiles when the average number
 // of rows per expert reaches this.  A full pair tile moves half the B bytes
 // per FLOP through each SM's shared memory, which bounds the single-CTA
@@ -159,8 +167,9 @@ struct GemmProblem {
   int E;
   int K;                     // reduction length (d for gate_up, inter for down)
   int n_out;                 // output columns (inter for gate_up, d for down)
-  int layout;                // 0 contiguous, 1 masked
-  const int32_t *seg;        // offsets [E+1] or masked_m [E]
+  int layout;                // 0 contiguous, 1 masked, kLayoutTwoSeg
+  const int32_t *seg;        // offsets [E+1] or masked_m [E] (kept counts for kLayoutTwoSeg)
+  const int32_t *seg2;       // kLayoutTwoSeg: overflow offsets [E+1] (rows after E * M_max)
   int M_max;                 // masked slab rows
   int64_t rows_total;        // rows of A / out (T*k or E*M_max)
   const int32_t *mtile_base; // [E+1]

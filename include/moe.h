@@ -358,8 +358,11 @@ moe_status_t moe_layer_capacity_workspace_size(const moe_shape_t *shape, int32_t
  * the padded rows (masked layout, M_max = C), with MOE_OVERFLOW_SECOND_ROUND
  * a second expert FFN over the overflow rows, then the combine over the
  * assignments that have a row (dropped ones add nothing; weights are not
- * renormalised).  Arguments as moe_layer; kept [E] (optional) receives
- * min(n_e, C).  With the second round the output is the uncapped layer's.
+ * renormalised).  Where the expert GEMMs stream their weights (fewer than
+ * 256 rows per expert on average) the two rounds run as one launch per GEMM,
+ * each expert's padded rows then its overflow rows, so every weight is read
+ * once.  Arguments as moe_layer; kept [E] (optional) receives min(n_e, C).
+ * With the second round the output is the uncapped layer's.
  */
 moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int32_t overflow,
                                 const void *x, const void *w_r, const float *bias,
