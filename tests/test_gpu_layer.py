@@ -241,3 +241,46 @@ def test_layer_compact_rows_within_their_bound(name):
     assert excess <= 0.0, f"{name}: compact rows exceed their bound by {excess:.3e}"
     same = (y.view(torch.int16) == y_ref.view(torch.int16)).float().mean().item()
     print(f"{name}: {same * 100:.2f} % of outputs identical to the fp32-row composition")
+
+
+@pytest.mark.parametrize("scale_exp", [40, -60, -118])
+def test_layer_compact_rows_extreme_magnitudes(scale_exp):
+    """The compact rows keep their bound for outputs of any magnitude: the
+    tiny layer with its down weights scaled by 2^scale_exp (outputs near
+    2^40, 2^-60, and below the form's floor of 2^-111, where a group is
+    stored as zero) against the fp32-row composition of the public calls."""
+    ensure_lib()
+    cfg = CONFIGS["tiny"]
+    shape = cfg.shape()
+    d = cfg.d
+    t = layer_inputs("tiny")
+    w_down = (t["w_down"].float() * 2.0 ** scale_exp).to(torch.bfloat16)
+    bias = t["bias"] if cfg.score == SCORE_SIGMOID_BIAS else None
+    ws = moe.Workspace(moe.moe_workspace_size(shape))
+    y = moe.moe_layer(shape, t["x"], t["w_r"], bias, t["w_gate_up"], w_down, ws)
+    ids, w, _ = moe.moe_route(shape, t["x"], t["w_r"], bias, ws)
+    _, offsets, _, dest, x_perm = moe.moe_dispatch(shape, ids, t["x"], ws)
+    fws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    y_perm = moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_CONTIGUOUS, x_perm, offsets, 0,
+                                t["w_gate_up"], w_down, fws)
+    y_ref = moe.moe_combine(shape, y_perm, dest, w)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    T, k = cfg.T, cfg.k
+    gmax = y_perm.abs().view(-1, d // 32, 32).amax(-1)
+    # rounding 2^-11 of the group's largest value; below 2^-111 the group is zero
+    gerr = torch.where(gmax >= 2.0 ** -111, gmax * 2.0 ** -11, gmax)
+    bound = (w.abs().unsqueeze(-1) * gerr[dest.view(T, k).long()]).sum(1)
+    bound = bound.repeat_interleave(32, dim=1)
+    yr = y_ref.float()
+    mag = yr.abs() + bound
+    ulp = torch.where(mag > 0, torch.exp2(torch.floor(torch.log2(mag)) - 7),
+                      torch.zeros_like(mag))
+    # the bf16 step of the smallest normal where the magnitudes are subnormal
+    ulp = torch.maximum(ulp, torch.full_like(ulp, 2.0 ** -133))
+    assert torch.isfinite(y.float()).all()
+    excess = ((y.float() - yr).abs() - bound - ulp).max().item()
+    assert excess <= 0.0, f"scale 2^{scale_exp}: excess {excess:.3e}"
+    if scale_exp < -111:  # most groups under the floor: stored, and summed, as zero
+        assert float(yr.abs().max()) > 0.0
+        assert float((y.float() == 0).float().mean()) > 0.5
