@@ -469,7 +469,7 @@ moe_status_t moe_expert_ffn(const moe_shape_t *shape, int32_t layout, const void
   void *h = at<void>(ws, L.h);
   MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max,
                                             tile_rows_for(shape, layout, M_max), mtile, status,
-                                            stream)));
+                                            stream, nullptr, at<uint32_t>(ws, L.flags))));
   MOE_TRY(run_gate_up(shape, layout, x_in, seg, M_max, rows, mtile, w_gate_up, h, status,
                       stream));
   return run_down(shape, layout, h, seg, M_max, rows, mtile, w_down, y_out, status,
@@ -509,7 +509,7 @@ moe_status_t moe_expert_down(const moe_shape_t *shape, int32_t layout, const voi
   int32_t *mtile = at<int32_t>(ws, L.mtile);
   MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max,
                                             tile_rows_for(shape, layout, M_max), mtile, status,
-                                            stream)));
+                                            stream, nullptr, at<uint32_t>(ws, L.flags))));
   return run_down(shape, layout, h_in, seg, M_max, rows, mtile, w_down, y_out, status,
                   at<uint32_t>(ws, L.flags), stream);
 }
@@ -566,7 +566,9 @@ moe_status_t moe_layer(const moe_shape_t *shape, const void *x, const void *w_r,
   MOE_TRY(cuda_status(moe::launch_dispatch(ids, s.T, s.k, s.E, x, s.d, cnt, offsets, src, dest,
                                            x_perm, at<int32_t>(ws, L.chunk), mtile,
                                            tile_rows_for(shape, MOE_LAYOUT_CONTIGUOUS, 0),
-                                           status, stream)));
+                                           status, stream,
+                                           moe::CapacityArgs{0, 0, 0, nullptr, nullptr},
+                                           at<uint32_t>(ws, L.flags))));
   MOE_TRY(mark(2));
   MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_perm, offsets, 0, n, mtile, w_gate_up, h,
                       status, stream));
@@ -898,7 +900,8 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
   if (one_launch) {
     MOE_TRY(cuda_status(moe::launch_ffn_tiles(
         kp, moe::kLayoutTwoSeg, s.E, capacity,
-        tile_rows_for(shape, moe::kLayoutTwoSeg, capacity), mtile, status, stream, ovf)));
+        tile_rows_for(shape, moe::kLayoutTwoSeg, capacity), mtile, status, stream, ovf,
+        at<uint32_t>(ws, L.flags))));
     MOE_TRY(run_gate_up(shape, moe::kLayoutTwoSeg, x_rows, kp, capacity, pad + n, mtile,
                         w_gate_up, h, status, stream, ovf));
     if (cr.vals)
@@ -914,7 +917,8 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
     if (capacity > 0) {
       MOE_TRY(cuda_status(moe::launch_ffn_tiles(kp, MOE_LAYOUT_MASKED, s.E, capacity,
                                                 tile_rows_for(shape, MOE_LAYOUT_MASKED, capacity),
-                                                mtile, status, stream)));
+                                                mtile, status, stream, nullptr,
+                                                at<uint32_t>(ws, L.flags))));
       MOE_TRY(run_gate_up(shape, MOE_LAYOUT_MASKED, x_rows, kp, capacity, pad, mtile, w_gate_up,
                           h, status, stream));
       if (cr.vals)
@@ -928,7 +932,8 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
     if (overflow == MOE_OVERFLOW_SECOND_ROUND) {
       MOE_TRY(cuda_status(moe::launch_ffn_tiles(ovf, MOE_LAYOUT_CONTIGUOUS, s.E, 0,
                                                 tile_rows_for(shape, MOE_LAYOUT_CONTIGUOUS, 0),
-                                                mtile, status, stream)));
+                                                mtile, status, stream, nullptr,
+                                                at<uint32_t>(ws, L.flags))));
       MOE_TRY(run_gate_up(shape, MOE_LAYOUT_CONTIGUOUS, x_rows + pad * s.d * 2, ovf, 0, n, mtile,
                           w_gate_up, h, status, stream));
       if (cr.vals)

@@ -83,8 +83,12 @@ __device__ int block_exclusive_scan(int v, int *total) {
 __global__ void __launch_bounds__(1024)
     dispatch_scan_kernel(int32_t *__restrict__ chunk_counts, int nchunks, int E,
                          int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
-                         int32_t *__restrict__ mtile_base, int tile_rows, CapacityArgs cap) {
+                         int32_t *__restrict__ mtile_base, int tile_rows, CapacityArgs cap,
+                         uint32_t *__restrict__ zero_flags) {
   pdl_begin();
+  // the down GEMM's split flags start every launch sequence at zero
+  if (zero_flags)
+    for (int i = threadIdx.x; i < kPairSplitFlagWords; i += blockDim.x) zero_flags[i] = 0;
   __shared__ int part[1024];
   int ep = 1;
   while (ep < E) ep <<= 1;
@@ -280,8 +284,12 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(1024)
     ffn_tiles_kernel(const int32_t *__restrict__ seg, const int32_t *__restrict__ seg2,
                      int layout, int E, int M_max, int tile_rows,
-                     int32_t *__restrict__ mtile_base, uint32_t *status) {
+                     int32_t *__restrict__ mtile_base, uint32_t *status,
+                     uint32_t *__restrict__ zero_flags) {
   pdl_begin();
+  // the down GEMM's split flags start every launch sequence at zero
+  if (zero_flags)
+    for (int i = threadIdx.x; i < kPairSplitFlagWords; i += blockDim.x) zero_flags[i] = 0;
   const int e = threadIdx.x;
   int rows = 0, tiles2 = 0;
   if (e < E) {
@@ -476,7 +484,7 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
                             int32_t *counts, int32_t *offsets, int32_t *src_token,
                             int32_t *dest, void *x_perm, int32_t *chunk_scratch,
                             int32_t *mtile_base, int tile_rows, uint32_t *status,
-                            cudaStream_t s, CapacityArgs cap) {
+                            cudaStream_t s, CapacityArgs cap, uint32_t *zero_flags) {
   cap.E = E;
   const int64_t n = (int64_t)T * k;
   const int64_t nchunks = dispatch_num_chunks(n);
@@ -487,7 +495,7 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   MOE_LAUNCH_PDL(dispatch_scan_kernel, 1, 1024, 0, s, chunk_scratch, (int)nchunks, E, counts, offsets,
-                                          mtile_base, tile_rows, cap);
+                                          mtile_base, tile_rows, cap, zero_flags);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const unsigned sblocks = (unsigned)((nchunks + kScatterWarps - 1) / kScatterWarps);
@@ -534,10 +542,10 @@ cudaError_t launch_gather_rows(const void *src, int row_bytes, const float *src_
 
 cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,
                              int32_t *mtile_base, uint32_t *status, cudaStream_t s,
-                             const int32_t *seg2) {
+                             const int32_t *seg2, uint32_t *zero_flags) {
   if (layout == kLayoutTwoSeg && seg2 == nullptr) return cudaErrorInvalidValue;
   MOE_LAUNCH_PDL(ffn_tiles_kernel, 1, 1024, 0, s, seg, seg2, layout, E, M_max, tile_rows,
-                 mtile_base, status);
+                 mtile_base, status, zero_flags);
   return cudaGetLastError();
 }
 

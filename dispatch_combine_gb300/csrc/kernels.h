@@ -86,7 +86,8 @@ cudaError_t launch_dispatch(const int32_t *ids, int T, int k, int E, const void 
                             int32_t *counts, int32_t *offsets, int32_t *src_token,
                             int32_t *dest, void *x_perm, int32_t *chunk_scratch,
                             int32_t *mtile_base, int tile_rows, uint32_t *status,
-                            cudaStream_t s, CapacityArgs cap = CapacityArgs{0, 0, 0, nullptr, nullptr});
+                            cudaStream_t s, CapacityArgs cap = CapacityArgs{0, 0, 0, nullptr, nullptr},
+                            uint32_t *zero_flags = nullptr);
 // Dispatch onto physical expert copies: phys_expert [P] is the logical
 // expert of each physical slot; the r-th assignment (increasing a) of expert
 // e goes to its copy r mod n_rep(e), copies in slot order.  Outputs
@@ -119,9 +120,12 @@ constexpr int kLayoutTwoSeg = 2;
 // mtile_base[e] = sum_{e'<e} ceil(M_e'/tile_rows) for the contiguous (seg =
 // offsets) or masked (seg = masked_m, clamped to M_max) layout; for
 // kLayoutTwoSeg the tiles of both of an expert's segments (seg2 as above).
+// zero_flags (launch_ffn_tiles and launch_dispatch): kPairSplitFlagWords
+// words set to zero (the down GEMM's split flags, so that every launch
+// sequence, a replayed graph's too, starts with them clear); nullptr: none.
 cudaError_t launch_ffn_tiles(const int32_t *seg, int layout, int E, int M_max, int tile_rows,
                              int32_t *mtile_base, uint32_t *status, cudaStream_t s,
-                             const int32_t *seg2 = nullptr);
+                             const int32_t *seg2 = nullptr, uint32_t *zero_flags = nullptr);
 // Expert GEMMs run on CTA pairs with 256-row tiles when the average number
 // of rows per expert reaches this.  A full pair tile moves half the B bytes
 // per FLOP through each SM's shared memory, which bounds the single-CTA

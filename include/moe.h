@@ -205,7 +205,8 @@ moe_status_t moe_dispatch(const moe_shape_t *shape, const int32_t *topk_ids,
  * not need its pairs to be resident together (kernels on other streams may
  * hold SMs).  The wait is bounded all the same (a timeout sets
  * MOE_ERR_TIMEOUT).  Results do not depend on timing: either order gives the
- * same fp32 sum.
+ * same fp32 sum.  Each call clears the flags before the down GEMM runs, so
+ * calls captured in a CUDA graph may be replayed.
  */
 moe_status_t moe_expert_ffn(const moe_shape_t *shape, int32_t layout, const void *x_in,
                             const int32_t *seg, int32_t M_max, const void *w_gate_up,

@@ -241,3 +241,42 @@ def test_ffn_pair_split_beside_a_busy_stream():
         torch.cuda.synchronize()
         assert moe.moe_get_device_status(ws) == 0
         assert torch.equal(y_busy.view(torch.int32), y_idle.view(torch.int32))
+
+
+def test_ffn_pair_split_flags_cleared_by_each_call_and_graph_replays():
+    """Every call clears the down GEMM's split flags before the GEMM runs, so
+    words left behind (planted here on the host, as an aborted launch could
+    leave them) neither disturb the next call nor survive it; and the split
+    FFN captured in a CUDA graph gives the eager result on every replay."""
+    ensure_lib()
+    counts, d, inter = [600, 260, 1], 1024, 512
+    E = len(counts)
+    w_gu, w_down = _weights(E, d, inter, seed=d + 5 * inter)
+    x, offsets, row_e = _contiguous_case(counts, d, inter, seed=d + 11)
+    shape = _shape(E, d, inter, T=x.shape[0], k=1)
+    ws = moe.Workspace(moe.moe_expert_ffn_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    xd, od, gud, dd = x.cuda(), offsets.cuda(), w_gu.cuda(), w_down.cuda()
+    y_ref = moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_CONTIGUOUS, xd, od, 0, gud, dd, ws)
+    torch.cuda.synchronize()
+    flags = ws.buf[ws.offset + 256: ws.offset + 256 + 4 * 4096].view(torch.int32)
+    flags.fill_(12345)
+    y = moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_CONTIGUOUS, xd, od, 0, gud, dd, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    assert int(flags.count_nonzero()) == 0, "planted flags survived the call"
+    assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32))
+    # the same launches captured once and replayed
+    y_g = torch.empty_like(y_ref)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        moe.moe_expert_ffn(shape, moe.MOE_LAYOUT_CONTIGUOUS, xd, od, 0, gud, dd, ws, y_out=y_g,
+                           stream=stream)
+    for _ in range(3):
+        y_g.zero_()
+        flags.fill_(12345)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_status(ws) == 0
+        assert torch.equal(y_g.view(torch.int32), y_ref.view(torch.int32))
