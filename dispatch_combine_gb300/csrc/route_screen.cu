@@ -722,8 +722,14 @@ __global__ void __launch_bounds__(kNeedWarps * 32)
   __syncthreads();
   const int t = blockIdx.x * kNeedWarps + (threadIdx.x >> 5);
   if (t < T) {
+    // the K-group slices of the squared norm: one load per lane, added in
+    // slice order
     float xsq = 0.0f;
-    for (int g = 0; g < ksplit; ++g) xsq = __fadd_rn(xsq, xn2[(size_t)g * T + t]);
+    for (int g0 = 0; g0 < ksplit; g0 += 32) {
+      const float v = (g0 + lane < ksplit) ? xn2[(size_t)(g0 + lane) * T + t] : 0.0f;
+      const int m = min(32, ksplit - g0);
+      for (int g = 0; g < m; ++g) xsq = __fadd_rn(xsq, __shfl_sync(0xffffffffu, v, g));
+    }
     int32_t *r = rec + (size_t)t * (E + kRsRecHead);
     uint32_t kept = 0, amb = 0;
     const int n = rs_decide<PER>(part, __fsqrt_rn(xsq), wn, bias, t, T, E, G, topk_group, k,
