@@ -667,8 +667,8 @@ moe_status_t check_fp8_shape(const moe_shape_t *s) {
 moe_status_t run_ffn_fp8(const moe_shape_t *s, int32_t layout, const void *xq, const float *xs,
                          const int32_t *seg, int32_t M_max, int64_t rows, int32_t *mtile,
                          const void *wgu_q, const float *wgu_s, const void *wd_q,
-                         const float *wd_s, float *y, void *ws, const LayoutF8 &L,
-                         cudaStream_t st) {
+                         const float *wd_s, void *y, void *ws, const LayoutF8 &L,
+                         cudaStream_t st, uint8_t *y16_codes = nullptr) {
   uint32_t *status = at<uint32_t>(ws, L.status);
   GemmProblem p;
   std::memset(&p, 0, sizeof p);
@@ -695,6 +695,7 @@ moe_status_t run_ffn_fp8(const moe_shape_t *s, int32_t layout, const void *xq, c
   p.b = wd_q;
   p.b_rows = s->d;
   p.out = y;
+  p.out_codes = y16_codes;  // compact rows (nullptr: fp32)
   return cuda_status(moe::launch_gemm_fp8_down(p, at<float>(ws, L.hs), wd_s, st));
 }
 
@@ -780,6 +781,16 @@ moe_status_t moe_layer_fp8(const moe_shape_t *shape, const void *x, const void *
                                               offsets + s.E, n, s.T,
                                               at<void>(ws, L.xq_perm), at<float>(ws, L.xs_perm),
                                               stream)));
+  if (compact_rows(s)) {
+    // the down GEMM writes the compact rows, as in moe_layer
+    const CompactRows c = compact_layout(y_perm, n, s.d);
+    MOE_TRY(run_ffn_fp8(shape, MOE_LAYOUT_CONTIGUOUS, at<void>(ws, L.xq_perm),
+                        at<float>(ws, L.xs_perm), offsets, 0, n, mtile, w_gate_up_q,
+                        w_gate_up_scale, w_down_q, w_down_scale, c.vals, ws, L, stream,
+                        c.codes));
+    return cuda_status(
+        moe::launch_combine16(c.vals, c.codes, n, dest, w, s.T, s.k, s.d, y, stream));
+  }
   MOE_TRY(run_ffn_fp8(shape, MOE_LAYOUT_CONTIGUOUS, at<void>(ws, L.xq_perm),
                       at<float>(ws, L.xs_perm), offsets, 0, n, mtile, w_gate_up_q,
                       w_gate_up_scale, w_down_q, w_down_scale, y_perm, ws, L, stream));

@@ -1343,6 +1343,28 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             d4[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
           }
         }
+      } else if (args.out_codes != nullptr) {
+        // compact output: the thread's 64 columns are two 32-column groups,
+        // 128 bytes of fp16 values and two code bytes
+        const int64_t col = static_cast<int64_t>(t.n) * kF8BN + 64 * half;
+        __half *dst = static_cast<__half *>(args.out) + grow * args.ldo + col;
+        uint32_t codes = 0;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint32_t v[32], hw[16];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(acc[32 * g + i]);
+          codes |= y16_encode32(v, hw) << (8 * g);
+          uint32_t w8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w8[i] = hw[i];
+          st_global_v8(dst + 32 * g, w8);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w8[i] = hw[8 + i];
+          st_global_v8(dst + 32 * g + 16, w8);
+        }
+        *reinterpret_cast<uint16_t *>(args.out_codes + grow * (args.ldo / 32) + col / 32) =
+            static_cast<uint16_t>(codes);
       } else {
         float *dst = static_cast<float *>(args.out) + grow * args.ldo +
                      static_cast<int64_t>(t.n) * kF8BN + 64 * half;
@@ -1523,6 +1545,12 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   a.ldo = p.n_out;
   a.rows_total = p.rows_total;
   a.out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+  if (!SWIGLU && p.out_codes != nullptr) {
+    // compact output: 32-byte stores of fp16 values, 2-byte code stores
+    if (!a.out_v8 || p.n_out % kF8BN != 0 || (reinterpret_cast<uintptr_t>(p.out_codes) & 1u))
+      return cudaErrorInvalidValue;
+    a.out_codes = p.out_codes;
+  }
   // A rows of one block: about 24 MB (a 128-row tile holds 128*K bytes)
   a.m_block = static_cast<int>((24ll << 20) / (128ll * p.K));
   if (a.m_block < 1) a.m_block = 1;

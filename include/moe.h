@@ -414,7 +414,8 @@ moe_status_t moe_expert_ffn_fp8(const moe_shape_t *shape, int32_t layout, const 
  * The layer with FP8 experts: route (from bf16 x, as moe_layer), quantize x
  * per row and 128 columns, dispatch the FP8 rows with their scales (the
  * "ep-deploy" page's FP8 dispatch: d + 4*d/128 bytes per row), the FP8
- * expert FFN, and the combine (fp32, as moe_layer).  Weights as
+ * expert FFN, and the combine (fp32 sums, from the compact rows where d is
+ * a multiple of 256, as moe_layer).  Weights as
  * moe_expert_ffn_fp8; y [T,d] bf16; counts [E] optional.
  */
 moe_status_t moe_layer_fp8_workspace_size(const moe_shape_t *shape, size_t *bytes);
