@@ -91,7 +91,10 @@ struct KArgs {
 };
 
 template <int TILE_M = kBM>
-__device__ __forceinline__ Tile decode_tile(const KArgs &a, const int32_t *mt, int u) {
+__device__ __forceinline__ Tile decode_tile(const KArgs &a, const int32_t *mt, int u,
+                                            const int32_t *sg = nullptr) {
+  // sg: a shared-memory copy of a.seg (the row offsets / counts), or nullptr
+  const int32_t *seg = sg ? sg : a.seg;
   Tile t;
   const int q = u / a.n_tiles;
   int lo = 0, hi = a.E - 1;  // largest e with mt[e] <= q
@@ -117,11 +120,11 @@ __device__ __forceinline__ Tile decode_tile(const KArgs &a, const int32_t *mt, i
   t.m = blk * a.m_block + (within - t.n * mb);
   int rows, start, m = t.m;
   if (a.layout == MOE_LAYOUT_CONTIGUOUS) {
-    start = a.seg[t.e];
-    rows = a.seg[t.e + 1] - start;
+    start = seg[t.e];
+    rows = seg[t.e + 1] - start;
   } else {
     start = t.e * a.M_max;
-    rows = min(max(a.seg[t.e], 0), a.M_max);
+    rows = min(max(seg[t.e], 0), a.M_max);
     if (a.layout == kLayoutTwoSeg) {
       // the slab's tiles, then the overflow rows' tiles
       const int tiles1 = (rows + TILE_M - 1) / TILE_M;
@@ -462,7 +465,9 @@ struct Cfg2 {
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int MT_OFF = MISC_OFF + 16;
-  static constexpr int SMEM_BYTES = MT_OFF + (kMaxE + 1) * 4 + 1024;
+  // a copy of the row offsets / counts, so tile decoding reads no global memory
+  static constexpr int SEG_OFF = MT_OFF + (kMaxE + 1) * 4;
+  static constexpr int SMEM_BYTES = SEG_OFF + (kMaxE + 1) * 4 + 1024;
   static_assert(BN == 256 || BN == 128, "pair tile width");
   static_assert(STAGES >= 4, "pipeline depth");
   static_assert(OUT_OFF % 1024 == 0, "swizzled staging alignment");
@@ -546,6 +551,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
   int32_t *mt = reinterpret_cast<int32_t *>(smem + C::MT_OFF);
+  int32_t *sg = reinterpret_cast<int32_t *>(smem + C::SEG_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -554,7 +560,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int cid = static_cast<int>(blockIdx.x >> 1);
   const int ncl = static_cast<int>(gridDim.x >> 1);
 
-  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) mt[i] = args.mtile_base[i];
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) {
+    mt[i] = args.mtile_base[i];
+    // offsets [E+1] (contiguous) or counts [E] (masked, two-segment)
+    sg[i] = (args.layout == MOE_LAYOUT_CONTIGUOUS || i < args.E) ? args.seg[i] : 0;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -606,7 +616,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (SWIGLU) tma_prefetch_desc(&tmW);
       for (int w = cid; w < items && !*abort_flag; w += ncl) {
         const PairWork pw = pair_work(w, n_full, rem, kblocks);
-        const Tile t = decode_tile<256>(args, mt, pw.u);
+        const Tile t = decode_tile<256>(args, mt, pw.u, sg);
         const int sn = (BN == 256) ? pair_swap_n(t) : 0;
         const int a_row = t.row0 + 128 * static_cast<int>(rank);
         int b_row;
@@ -667,7 +677,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       bool any_mma = false;
       for (int w = cid; w < items && !*abort_flag; w += ncl) {
         const PairWork pw = pair_work(w, n_full, rem, kblocks);
-        const int sn = (BN == 256) ? pair_swap_n(decode_tile<256>(args, mt, pw.u)) : 0;
+        const int sn = (BN == 256) ? pair_swap_n(decode_tile<256>(args, mt, pw.u, sg)) : 0;
         // swapped: the A slots hold weight rows (M) and the B slots token rows (N)
         const uint32_t idesc = sn ? mma_idesc_bf16_f32(256, sn) : kIdesc;
         if (!mbar_wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, abort_flag, args.status,
@@ -717,7 +727,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     for (int w = cid; w < items; w += ncl) {
       const PairWork pw = pair_work(w, n_full, rem, kblocks);
-      const Tile t = decode_tile<256>(args, mt, pw.u);
+      const Tile t = decode_tile<256>(args, mt, pw.u, sg);
       const bool waited = mbar_wait_bounded(&tmem_full[acc], acc_phase, abort_flag,
                                             args.status, args.wait_limit_ns);
       if (!__all_sync(0xffffffffu, waited)) break;
