@@ -126,6 +126,28 @@ def test_layer_single_token_and_ragged_T():
         check_close(y.float().cpu().numpy(), y_ref, bf16_output=True, what=f"T={T}")
 
 
+def test_layer_fp32_rows_where_d_is_not_a_multiple_of_256():
+    """d = 448: the layer keeps the down GEMM's rows in fp32 (the compact form
+    needs whole 256-column tiles) and combines them with the fp32 combine;
+    every token against the oracle."""
+    ensure_lib()
+    import moe_inputs
+    T, d, E, inter = 96, 448, 8, 128
+    cfg = CONFIGS["tiny"].replace(T=T, d=d, E=E, G=2, topk_group=1, k=2, inter=inter,
+                                  name="d448")
+    shape = cfg.shape()
+    assert moe.moe_layer_yperm_row_bytes(shape) == 4 * d
+    t = moe_inputs.make_layer_tensors(cfg, device="cuda", seed=448)
+    ws = moe.Workspace(moe.moe_workspace_size(shape))
+    y = moe.moe_layer(shape, t["x"], t["w_r"], t["bias"], t["w_gate_up"], t["w_down"], ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    y_ref, _, _ = oracle.layer_tokens(bits(t["x"]), bits(t["w_r"]), t["bias"].cpu().numpy(),
+                                      bits(t["w_gate_up"]), bits(t["w_down"]), shape,
+                                      np.arange(T, dtype=np.int32))
+    check_close(y.float().cpu().numpy(), y_ref, bf16_output=True, what="d=448")
+
+
 # ---------------------------------------------------------------------------
 # masked per-rank expert slices
 # ---------------------------------------------------------------------------
