@@ -447,11 +447,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 //   tmem_full[b]  in both CTAs, the pair MMA commit arrives on both;
 //   tmem_empty[b] in the even CTA, all 8 epilogue warps of the pair arrive.
 // ---------------------------------------------------------------------------
+// k-blocks per ring stage of the pair kernel (one barrier round trip each)
+constexpr int kPairKPS = 2;
+
 template <int BN, bool SWIGLU>
 struct Cfg2 {
-  static constexpr int A_BYTES = 128 * kBK * 2;
-  static constexpr int B_BYTES = (BN / 2) * kBK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int A_BYTES = 128 * kBK * 2;        // one k-block of this CTA's A
+  static constexpr int B_BYTES = (BN / 2) * kBK * 2;   // one k-block of its B half
+  static constexpr int KPS = kPairKPS;
+  static constexpr int A_STAGE = KPS * A_BYTES;
+  static constexpr int B_STAGE = KPS * B_BYTES;
+  static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
   static constexpr int STAGES = kStageBudget / STAGE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BN_OUT = SWIGLU ? BN / 2 : BN;
@@ -469,7 +475,7 @@ struct Cfg2 {
   static constexpr int SEG_OFF = MT_OFF + (kMaxE + 1) * 4;
   static constexpr int SMEM_BYTES = SEG_OFF + (kMaxE + 1) * 4 + 1024;
   static_assert(BN == 256 || BN == 128, "pair tile width");
-  static_assert(STAGES >= 4, "pipeline depth");
+  static_assert(STAGES * KPS >= 4, "pipeline depth");
   static_assert(OUT_OFF % 1024 == 0, "swizzled staging alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
@@ -541,7 +547,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *smA = smem;
-  uint8_t *smB = smem + C::STAGES * C::A_BYTES;
+  uint8_t *smB = smem + C::STAGES * C::A_STAGE;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
   uint64_t *full = bars;
   uint64_t *empty = bars + C::STAGES;
@@ -629,23 +635,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         const int x_row = t.row0 + static_cast<int>(rank) * (sn >> 1);
         const int w_grp = (t.e * args.b_rows + t.n * C::BN_OUT + static_cast<int>(rank) * 64) >> 4;
         const int xbox = sn ? swap_box_index(sn) : 0;
+        // TMA bytes of one k-block (both CTAs)
         const uint32_t tx =
-            sn ? 2u * (C::A_BYTES + (8u << xbox) * kBK * 2u) : 2u * C::STAGE_BYTES;
-        for (int kb = pw.kb0; kb < pw.kb1; ++kb) {
+            sn ? 2u * (C::A_BYTES + (8u << xbox) * kBK * 2u) : 2u * (C::A_BYTES + C::B_BYTES);
+        for (int kb = pw.kb0; kb < pw.kb1; kb += C::KPS) {
+          const int nk = min(C::KPS, pw.kb1 - kb);  // k-blocks in this stage
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
                                  args.wait_limit_ns))
             break;
-          if (even) mbar_arrive_expect_tx(&full[stage], tx);
+          if (even) mbar_arrive_expect_tx(&full[stage], tx * static_cast<uint32_t>(nk));
           const uint32_t fbar = mapa_shared(&full[stage], 0);
-          if (sn == 0) {
-            tma_load_2d_pair(smA + stage * C::A_BYTES, &tmA, fbar, kb * kBK, a_row);
-            tma_load_2d_pair(smB + stage * C::B_BYTES, &tmB, fbar, kb * kBK, b_row);
-          } else {
-            if (SWIGLU)
-              tma_load_4d_pair(smA + stage * C::A_BYTES, &tmW, fbar, kb * kBK, 0, 0, w_grp);
-            else
-              tma_load_2d_pair(smA + stage * C::A_BYTES, &tmB, fbar, kb * kBK, b_row);
-            tma_load_2d_pair(smB + stage * C::B_BYTES, &tmX.m[xbox], fbar, kb * kBK, x_row);
+          for (int i = 0; i < nk; ++i) {
+            uint8_t *a_dst = smA + stage * C::A_STAGE + i * C::A_BYTES;
+            uint8_t *b_dst = smB + stage * C::B_STAGE + i * C::B_BYTES;
+            const int kc = (kb + i) * kBK;
+            if (sn == 0) {
+              tma_load_2d_pair(a_dst, &tmA, fbar, kc, a_row);
+              tma_load_2d_pair(b_dst, &tmB, fbar, kc, b_row);
+            } else {
+              if (SWIGLU)
+                tma_load_4d_pair(a_dst, &tmW, fbar, kc, 0, 0, w_grp);
+              else
+                tma_load_2d_pair(a_dst, &tmB, fbar, kc, b_row);
+              tma_load_2d_pair(b_dst, &tmX.m[xbox], fbar, kc, x_row);
+            }
           }
           issued[stage] = true;
           issued_phase[stage] = phase;
@@ -686,19 +699,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         bool ok = true;
-        for (int kb = pw.kb0; kb < pw.kb1; ++kb) {
+        for (int kb = pw.kb0; kb < pw.kb1; kb += C::KPS) {
+          const int nk = min(C::KPS, pw.kb1 - kb);
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.status,
                                  args.wait_limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_kmajor_desc(smem_u32(smA + stage * C::A_BYTES));
-          const uint64_t bd = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
+          for (int i = 0; i < nk; ++i) {
+            const uint64_t ad =
+                sw128_kmajor_desc(smem_u32(smA + stage * C::A_STAGE + i * C::A_BYTES));
+            const uint64_t bd =
+                sw128_kmajor_desc(smem_u32(smB + stage * C::B_STAGE + i * C::B_BYTES));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ss_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
-                             (kb != pw.kb0 || kk != 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_ss_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
+                               (kb + i != pw.kb0 || kk != 0) ? 1u : 0u);
+          }
           any_mma = true;
           mma_commit_pair(&empty[stage], 0x3);
           if (++stage == C::STAGES) {
