@@ -44,9 +44,11 @@
  *   R9  expert FFN: h = silu(x.Wg) * (x.Wu), y = h.Wd, accumulated in fp64.
  *   R10 combine: y[t] = sum_j w[t,j] * y_perm[dest[t*k+j]], j ascending.
  *   R13 FP8: e4m3 codes with fp32 block scales, one per (row, 128 columns)
- *       of an activation and per 128 x 128 block of a weight;
- *       s = amax / 448 (1 for an all-zero block), q = round-to-nearest-even
- *       e4m3 of x / s (IEEE fp32 division), saturating at 448.
+ *       of an activation and per 128 x 128 block of a weight; each scale is
+ *       a power of two, s = 2^e with e the smallest integer >= -127 such
+ *       that amax <= 448 * 2^e (1 for an all-zero block, 2^127 when amax is
+ *       not finite), q = round-to-nearest-even e4m3 of x / s (exact: s is a
+ *       power of two), saturating at 448.
  *   R11 capacity: the first C assignments of an expert in increasing
  *       a = t*k + j keep their place; later ones overflow.  Dropped ones add
  *       nothing (weights are not renormalised); second-round ones are
@@ -463,14 +465,23 @@ uint8_t oracle_float_to_e4m3(float x) {
   return (uint8_t)(code | (signbit(x) ? 0x80 : 0));
 }
 
-/* scale of a block with largest magnitude amax: amax / 448 in fp32, 1 when
-   the block is all zeros (R13) */
-static float fp8_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
+/* scale of a block with largest magnitude amax (R13): the power of two
+   2^e with e the smallest integer >= -127 such that amax <= 448 * 2^e,
+   found by counting e up from -127 (each comparison is exact in double);
+   1 when the block is all zeros, 2^127 when amax is not finite */
+static float fp8_scale(float amax) {
+  if (!(amax > 0.0f)) return 1.0f;
+  if (!isfinite(amax)) return ldexpf(1.0f, 127);
+  int e = -127;
+  while ((double)amax > 448.0 * ldexp(1.0, e)) ++e;
+  return ldexpf(1.0f, e);
+}
 
 /*
- * Activations, per row and 128-column block (R13): s = amax / 448,
- * q = e4m3(x / s) with IEEE fp32 division.  x: [rows, cols] bf16, cols a
- * multiple of 128; q: [rows, cols] codes; scales: [rows, cols/128] fp32.
+ * Activations, per row and 128-column block (R13): s the power-of-two scale
+ * above, q = e4m3(x / s) (the fp32 division by a power of two is exact).
+ * x: [rows, cols] bf16, cols a multiple of 128; q: [rows, cols] codes;
+ * scales: [rows, cols/128] fp32.
  */
 void oracle_quantize_rows_fp8(const uint16_t *x, int64_t rows, int cols, uint8_t *q,
                               float *scales) {

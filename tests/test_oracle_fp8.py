@@ -1,7 +1,8 @@
-"""Oracle pins for the FP8 path (e4m3 with block scales): the e4m3 decoder
-against the format's definition, the encoder against a brute-force nearest
-search with ties to the even code, the block quantizers against a numpy
-restatement, and the FP8 FFN against float64 matmuls of the dequantized
+"""Oracle pins for the FP8 path (e4m3 with power-of-two block scales): the
+e4m3 decoder against the format's definition, the encoder against a
+brute-force nearest search with ties to the even code, the block quantizers
+against a numpy restatement whose scale is found by brute force over every
+exponent, and the FP8 FFN against float64 matmuls of the dequantized
 operands."""
 import numpy as np
 import pytest
@@ -50,18 +51,31 @@ def test_encoder_is_nearest_with_ties_to_even():
         assert oracle.float_to_e4m3(x32) == _nearest_code(x32), x32
 
 
+def _pow2_scale(amax):
+    """The block scale by its definition: the smallest power of two 2^e,
+    e in [-127, 127], with amax <= 448 * 2^e (brute force over every e; the
+    float64 products are exact); 1 for an all-zero block."""
+    amax = float(amax)
+    if amax == 0.0:
+        return np.float32(1.0)
+    for e in range(-127, 128):
+        if amax <= 448.0 * 2.0 ** e:
+            return np.float32(2.0 ** e)
+    raise AssertionError(amax)
+
+
 def _quant_rows_np(xf32):
-    """x: [rows, cols] float32 values of bf16; per-128 block amax/448 scale."""
+    """x: [rows, cols] float32 values of bf16; per-128 block power-of-two scale."""
     rows, cols = xf32.shape
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((rows, cols // 128), np.float32)
     for r in range(rows):
         for b in range(cols // 128):
             blk = xf32[r, b * 128:(b + 1) * 128]
-            amax = np.float32(np.abs(blk).max())
-            sc = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+            sc = _pow2_scale(np.abs(blk).max())
             s[r, b] = sc
-            q[r, b * 128:(b + 1) * 128] = [_nearest_code(np.float32(v / sc)) for v in blk]
+            # x / s is exact (s a power of two): the code is the nearest one
+            q[r, b * 128:(b + 1) * 128] = [_nearest_code(float(v) / float(sc)) for v in blk]
     return q, s
 
 
@@ -80,11 +94,36 @@ def test_row_quantizer_matches_numpy_restatement():
     q2, s2 = _quant_rows_np(xf)
     assert np.array_equal(q, q2) and np.array_equal(s, s2)
     assert s[2, 1] == 1.0 and not q[2, 128:256].any()
-    # the largest magnitude of every nonzero block maps to +-448
+    # every scale is a power of two, and the largest magnitude of a nonzero
+    # block lands in (224, 448]: codes 118 (224) .. 126 (448)
+    m, _ = np.frexp(s)
+    assert np.all(m == 0.5)
     for r in range(5):
         for b in range(3):
-            if s[r, b] != 1.0 or q[r, b * 128:(b + 1) * 128].any():
-                assert (q[r, b * 128:(b + 1) * 128] & 0x7f).max() == 126
+            blk = q[r, b * 128:(b + 1) * 128]
+            if blk.any():
+                assert 118 <= (blk & 0x7f).max() <= 126
+
+
+def test_row_quantizer_scale_boundaries_and_clamp():
+    # one block per row: amax exactly 448 * 2^k keeps e = k (the max maps to
+    # 448); the next bf16 above it moves to e = k + 1; magnitudes below
+    # 448 * 2^-127 (bf16 subnormals among them) clamp to 2^-127
+    amaxes = [448.0, 448.0 * 2.0 ** -20, 450.0, 1.0, 2.0 ** -130, 1e-38, 3.0e38]
+    x = np.zeros((len(amaxes), 128), np.float32)
+    x[:, 5] = amaxes
+    x[:, 9] = -0.75 * np.array(amaxes)
+    bits, xf = _bf16(x)
+    q, s = oracle.quantize_rows_fp8(bits)
+    assert s[0, 0] == 1.0 and q[0, 5] == 126
+    assert s[1, 0] == np.float32(2.0 ** -20) and q[1, 5] == 126
+    assert s[2, 0] == 2.0                      # bf16(450) = 450 > 448
+    assert s[3, 0] == np.float32(2.0 ** -8)   # 1 / 2^-8 = 256 <= 448 < 512
+    assert s[4, 0] == np.float32(2.0 ** -127) and s[5, 0] == np.float32(2.0 ** -127)
+    assert s[6, 0] == np.float32(2.0 ** 120)
+    for r, a in enumerate(xf[:, 5]):
+        assert s[r, 0] == _pow2_scale(a)
+        assert q[r, 9] == _nearest_code(float(xf[r, 9]) / float(s[r, 0]))
 
 
 def test_block_quantizer_is_the_row_quantizer_on_128x128_blocks():
@@ -97,10 +136,10 @@ def test_block_quantizer_is_the_row_quantizer_on_128x128_blocks():
         for i in range(2):
             for j in range(3):
                 blk = wf[m, i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
-                amax = np.float32(np.abs(blk).max())
-                sc = np.float32(amax / np.float32(448.0))
+                sc = _pow2_scale(np.abs(blk).max())
                 assert s[m, i, j] == sc
-                codes = np.array([[_nearest_code(np.float32(v / sc)) for v in row] for row in blk])
+                codes = np.array([[_nearest_code(float(v) / float(sc)) for v in row]
+                                  for row in blk])
                 assert np.array_equal(q[m, i * 128:(i + 1) * 128, j * 128:(j + 1) * 128], codes)
 
 
