@@ -662,6 +662,16 @@ moe_status_t check_fp8_shape(const moe_shape_t *s) {
   return MOE_OK;
 }
 
+// FP8 GEMMs on CTA pairs (256 x 256 tiles: d a multiple of 256) under the
+// bf16 GEMMs' row criterion
+bool use_pair_fp8(const moe_shape_t *s, int32_t layout, int32_t M_max) {
+  if (s->d % 256 != 0) return false;
+  if (static_cast<int64_t>(s->T) * s->k < static_cast<int64_t>(moe::kPairRowsPerExpert) * s->E)
+    return false;
+  if (layout == MOE_LAYOUT_CONTIGUOUS) return true;
+  return layout == MOE_LAYOUT_MASKED && M_max >= moe::kPairRowsPerExpert;
+}
+
 // FP8 gate_up + SwiGLU -> h (bf16) -> FP8 codes of h -> FP8 down, over rows
 // whose m-tile prefix (128-row tiles) is in the workspace
 moe_status_t run_ffn_fp8(const moe_shape_t *s, int32_t layout, const void *xq, const float *xs,
@@ -679,6 +689,7 @@ moe_status_t run_ffn_fp8(const moe_shape_t *s, int32_t layout, const void *xq, c
   p.rows_total = rows;
   p.mtile_base = mtile;
   p.status = status;
+  p.pair = use_pair_fp8(s, layout, M_max);
   p.K = s->d;
   p.n_out = s->inter;
   p.a = xq;
@@ -727,7 +738,8 @@ moe_status_t moe_expert_ffn_fp8(const moe_shape_t *shape, int32_t layout, const 
   const LayoutF8 L = make_fp8_layout(*shape, rows);
   MOE_TRY(check_ws(ws, ws_bytes, L.end_ffn));
   int32_t *mtile = at<int32_t>(ws, L.mtile);
-  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max, 128, mtile,
+  MOE_TRY(cuda_status(moe::launch_ffn_tiles(seg, layout, shape->E, M_max,
+                                            use_pair_fp8(shape, layout, M_max) ? 256 : 128, mtile,
                                             at<uint32_t>(ws, L.status), stream)));
   return run_ffn_fp8(shape, layout, x_q, x_scale, seg, M_max, rows, mtile, w_gate_up_q,
                      w_gate_up_scale, w_down_q, w_down_scale, y_out, ws, L, stream);
@@ -773,9 +785,10 @@ moe_status_t moe_layer_fp8(const moe_shape_t *shape, const void *x, const void *
   // the dispatch moves FP8 rows and their scales
   MOE_TRY(cuda_status(moe::launch_quantize_rows_fp8(x, s.T, s.d, at<void>(ws, L.xq),
                                                     at<float>(ws, L.xs), stream)));
-  MOE_TRY(cuda_status(moe::launch_dispatch(ids, s.T, s.k, s.E, nullptr, s.d, cnt, offsets, src,
-                                           dest, nullptr, at<int32_t>(ws, L.chunk), mtile, 128,
-                                           status, stream)));
+  MOE_TRY(cuda_status(moe::launch_dispatch(
+      ids, s.T, s.k, s.E, nullptr, s.d, cnt, offsets, src, dest, nullptr,
+      at<int32_t>(ws, L.chunk), mtile, use_pair_fp8(shape, MOE_LAYOUT_CONTIGUOUS, 0) ? 256 : 128,
+      status, stream)));
   MOE_TRY(cuda_status(moe::launch_gather_rows(at<void>(ws, L.xq), s.d, at<float>(ws, L.xs),
                                               s.d / 128, ids, dest, s.k, s.E, src,
                                               offsets + s.E, n, s.T,

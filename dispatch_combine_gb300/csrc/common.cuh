@@ -311,6 +311,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
                : "memory");
 }
 
+// The same arrival without release ordering: for an arrival that only
+// reports tensor-memory accesses already completed by tcgen05.wait::st or
+// tcgen05.wait::ld (and fenced with tcgen05.fence::before_thread_sync).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 // 2D tiled TMA load into this CTA's shared memory whose completion is
 // signalled on an mbarrier that may live in the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map,
@@ -452,6 +460,45 @@ __device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, ui
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// kind::mxf8f6f4 block-scaled descriptor: A and B e4m3 (format 0 in bits
+// 7-9 and 10-12), both K-major, N >> 3 at bit 17, scale type UE8M0 (bit 23),
+// M >> 4 at bit 24; scale factor ids 0 (bits 4-5 for B, 29-30 for A): each
+// MMA reads byte 0 of its scale cells.
+__host__ __device__ constexpr uint32_t mma_idesc_mxf8_f32(int M, int N) {
+  return (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= (A[smem] * 2^sa) * (B[smem] * 2^sb)^T with e4m3 operands
+// (K = 32 per instruction) and one 8-bit exponent per row of A and per row
+// of B, read from TMEM at sfa_tmem / sfb_tmem (UE8M0: 2^(byte - 127)); one
+// elected thread.  For M = N = 128: row m's A exponent sits at lane m,
+// column m / 32 from sfa_tmem; B row n's at lane 32q + n % 32 of every lane
+// quadrant q, column n / 32 from sfb_tmem.
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem,
+                                            uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Whole warp: thread i writes v[j] to lane (base lane + i), column col + j.
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one elected thread.

@@ -1071,25 +1071,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// FP8 (e4m3) grouped GEMM with block scales.  A rows carry one fp32 scale per
-// 128 columns, B (weights) one per 128 x 128 block; a k-block is 128
-// columns, i.e. one scale block and one 128-byte swizzle row.  The MMA warp
-// issues kind::f8f6f4 MMAs (M=128, N=128, K=32) for one k-block into one of
-// four TMEM partial accumulators; eight promotion warps (two per TMEM lane
-// quadrant, thread = row, each half of the columns) read the partial in one
-// wait, multiply it by the two scales and add it into fp32 registers (64 per
-// thread), then release the partial.  After the last k-block they apply
-// SwiGLU (gate_up: columns 0-63 gate, 64-127 the matching up; a warp holds
-// 32 gate columns and their up columns) or write fp32 (down) straight from
-// registers.
-//   full/empty[s]    stage ring (producer <-> MMA);
-//   pfull/pempty[b]  partial accumulator b (MMA <-> epilogue warps).
+// FP8 (e4m3) grouped GEMM with power-of-two block scales applied by the
+// tensor cores.  A rows carry one scale per 128 columns, B (weights) one per
+// 128 x 128 block; a k-block is 128 columns: one scale block, one 128-byte
+// swizzle row and four block-scaled MMAs (kind::mxf8f6f4, M=128, N=128,
+// K=32) that take both scales from TMEM as 8-bit exponents and accumulate
+// the whole K loop in one TMEM accumulator (two, alternating between tiles,
+// so a tile's epilogue overlaps the next tile's MMAs).
+// The exponents sit in a ring of 8-column TMEM slots, each serving four
+// consecutive k-blocks of a tile: columns 0-3 hold row m's A exponent at
+// lane m, column m / 32; columns 4-7 hold tile column n's B exponent at lane
+// 32q + n % 32 in every lane quadrant q, column 4 + n / 32 (gate_up: columns
+// 0-63 of the tile are gate rows, 64-127 up rows, each with its own weight
+// block); byte j of a cell is k-block 4g + j's exponent, which the MMAs of
+// that k-block select with scale factor id j.
+// Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 scale writers
+// (one per TMEM lane quadrant), warps 6-13 epilogue (two per quadrant, each
+// half of the tile's columns).
+//   full/empty[s]    stage ring (producer and scale writers <-> MMA);
+//   sfull/sempty[g]  scale slot g written (four scale warps) / read by the
+//                    MMAs of its k-blocks;
+//   afull/aempty[b]  accumulator b (MMA <-> eight epilogue warps).
 // ---------------------------------------------------------------------------
 constexpr int kF8BK = 128;  // e4m3 per k-block = bytes per swizzle row
 constexpr int kF8BN = 128;
 constexpr int kF8Stages = 6;
-constexpr int kF8Parts = 4;  // TMEM partial accumulators: the MMA runs up to 3 k-blocks ahead
-constexpr int kF8Threads = 320;  // producer, MMA issuer, 8 promotion warps
+constexpr int kF8Threads = 448;
+constexpr int kF8ScaleCol = 2 * kF8BN;  // first TMEM column of the scale slots
+constexpr int kF8ScaleSlots = 4;        // 8-column slots, each holding 4 k-blocks' exponents
+constexpr int kF8TmemCols = 512;
 
 template <bool SWIGLU>
 struct CfgF8 {
@@ -1098,13 +1108,14 @@ struct CfgF8 {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = kF8Stages;
   static constexpr int BN_OUT = SWIGLU ? kF8BN / 2 : kF8BN;
-  static constexpr int TMEM_COLS = kF8Parts * kF8BN;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * kF8Parts + 1;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * kF8ScaleSlots + 4 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int MT_OFF = MISC_OFF + 16;
   static constexpr int SMEM_BYTES = MT_OFF + (kMaxE + 1) * 4 + 1024;
   static_assert(SMEM_BYTES <= 232448, "227 KB of shared memory per CTA");
+  static_assert(kF8ScaleCol + 8 * kF8ScaleSlots <= kF8TmemCols,
+                "scale slots fit the TMEM allocation");
 };
 
 struct F8Args {
@@ -1117,6 +1128,82 @@ struct F8Args {
 // the shared-memory rows past them are stale and only feed accumulator rows
 // that are never written.
 constexpr int kF8SubRows = 32;
+
+// The UE8M0 byte (the biased exponent) of a power-of-two scale in
+// [2^-127, 2^127]; false for any other value.
+__device__ __forceinline__ bool ue8m0_of(float s, uint32_t &byte) {
+  const uint32_t b = __float_as_uint(s);
+  byte = (b >> 23) & 0xffu;
+  return ((b & 0x807fffffu) == 0u && byte != 0u && byte != 0xffu) || b == 0x00400000u;
+}
+
+// One epilogue thread's part of an FP8 tile row: acc holds two 32-column
+// runs of the accumulator, written at output column col of row grow.
+// gate_up: 32 gate columns, then their up columns -> 32 values of h (bf16,
+// SwiGLU); down: 64 consecutive columns -> compact rows or fp32.
+template <bool SWIGLU>
+__device__ __forceinline__ void f8_store_tile_row(const KArgs &args, int64_t grow, int64_t col,
+                                                  const float (&acc)[64]) {
+  if (SWIGLU) {
+    // gate acc[0..31], up acc[32..63]
+    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(args.out) + grow * args.ldo + col;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t w8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = c * 16 + 2 * i;
+        const float g0 = acc[j], g1 = acc[j + 1];
+        const float u0 = acc[32 + j], u1 = acc[32 + j + 1];
+        w8[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
+                            __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+      }
+      if (args.out_v8) {
+        st_global_v8(dst + c * 16, w8);
+      } else {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 16);
+        d4[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+        d4[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+      }
+    }
+  } else if (args.out_codes != nullptr) {
+    // compact output: the thread's 64 columns are two 32-column groups,
+    // 128 bytes of fp16 values and two code bytes
+    __half *dst = static_cast<__half *>(args.out) + grow * args.ldo + col;
+    uint32_t codes = 0;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      uint32_t vv[32], hw[16];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) vv[i] = __float_as_uint(acc[32 * g + i]);
+      codes |= y16_encode32(vv, hw) << (8 * g);
+      uint32_t w8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w8[i] = hw[i];
+      st_global_v8(dst + 32 * g, w8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w8[i] = hw[8 + i];
+      st_global_v8(dst + 32 * g + 16, w8);
+    }
+    *reinterpret_cast<uint16_t *>(args.out_codes + grow * (args.ldo / 32) + col / 32) =
+        static_cast<uint16_t>(codes);
+  } else {
+    float *dst = static_cast<float *>(args.out) + grow * args.ldo + col;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t w8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w8[i] = __float_as_uint(acc[c * 8 + i]);
+      if (args.out_v8) {
+        st_global_v8(dst + c * 8, w8);
+      } else {
+        float4 *d4 = reinterpret_cast<float4 *>(dst + c * 8);
+        d4[0] = make_float4(acc[c * 8], acc[c * 8 + 1], acc[c * 8 + 2], acc[c * 8 + 3]);
+        d4[1] = make_float4(acc[c * 8 + 4], acc[c * 8 + 5], acc[c * 8 + 6], acc[c * 8 + 7]);
+      }
+    }
+  }
+}
 
 template <bool SWIGLU>
 __global__ void __launch_bounds__(kF8Threads, 1)
@@ -1134,9 +1221,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
   uint64_t *full = bars;
   uint64_t *empty = bars + C::STAGES;
-  uint64_t *pfull = bars + 2 * C::STAGES;
-  uint64_t *pempty = pfull + kF8Parts;
-  uint64_t *drain = pempty + kF8Parts;
+  uint64_t *sfull = bars + 2 * C::STAGES;
+  uint64_t *sempty = sfull + kF8ScaleSlots;
+  uint64_t *afull = sempty + kF8ScaleSlots;
+  uint64_t *aempty = afull + 2;
+  uint64_t *drain = aempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
   int32_t *mt = reinterpret_cast<int32_t *>(smem + C::MT_OFF);
@@ -1149,9 +1238,13 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       mbar_init(&full[st], 1);
       mbar_init(&empty[st], 1);
     }
-    for (int b = 0; b < kF8Parts; ++b) {
-      mbar_init(&pfull[b], 1);
-      mbar_init(&pempty[b], 8);
+    for (int g = 0; g < kF8ScaleSlots; ++g) {
+      mbar_init(&sfull[g], 4);
+      mbar_init(&sempty[g], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&afull[b], 1);
+      mbar_init(&aempty[b], 8);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -1160,7 +1253,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   __syncthreads();
   const int total = mt[args.E] * args.n_tiles;
   if (blockIdx.x >= total) return;
-  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == 1) tmem_alloc(tmem_slot, kF8TmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1225,37 +1318,58 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t kIdesc = mma_idesc_e4m3_f32(kBM, kF8BN);
+      constexpr uint32_t kIdesc = mma_idesc_mxf8_f32(kBM, kF8BN);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t q = 0;  // k-blocks issued so far: partial q % kF8Parts, its use q / kF8Parts
+      int slot = 0;
+      uint32_t sphase = 0;
+      uint32_t tcount = 0;  // tiles issued: accumulator tcount % 2, its use tcount / 2
       bool any_mma = false;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok && !*abort_flag; u += gridDim.x) {
-        for (int kb = 0; kb < kblocks; ++kb, ++q) {
-          const int p = static_cast<int>(q % kF8Parts);
-          if (!mbar_wait_bounded(&pempty[p], ((q / kF8Parts) & 1u) ^ 1u, abort_flag, args.status,
-                                 args.wait_limit_ns) ||
+      for (int u = blockIdx.x; u < total && ok && !*abort_flag; u += gridDim.x, ++tcount) {
+        const uint32_t b = tcount & 1u;
+        if (!mbar_wait_bounded(&aempty[b], ((tcount >> 1) & 1u) ^ 1u, abort_flag, args.status,
+                               args.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + b * kF8BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const int j = kb & 3;  // byte of the slot's cells with this k-block's exponents
+          if ((j == 0 && !mbar_wait_bounded(&sfull[slot], sphase, abort_flag, args.status,
+                                            args.wait_limit_ns)) ||
               !mbar_wait_bounded(&full[stage], phase, abort_flag, args.status,
                                  args.wait_limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(p * kF8BN);
           const uint64_t ad = sw128_kmajor_desc(smem_u32(smA + stage * C::A_BYTES));
           const uint64_t bd = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
+          const uint32_t sfa = tmem_base + static_cast<uint32_t>(kF8ScaleCol + 8 * slot);
+          const uint32_t idesc =
+              kIdesc | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
 #pragma unroll
           for (int kk = 0; kk < kF8BK / 32; ++kk)  // +32 bytes = 32 e4m3 along K
-            mma_e4m3_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, kIdesc, kk != 0 ? 1u : 0u);
+            mma_mxf8_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, sfa, sfa + 4u,
+                        (kb != 0 || kk != 0) ? 1u : 0u);
           any_mma = true;
           mma_commit(&empty[stage]);
-          mma_commit(&pfull[p]);
+          if (j == 3 || kb == kblocks - 1) {
+            mma_commit(&sempty[slot]);
+            if (++slot == kF8ScaleSlots) {
+              slot = 0;
+              sphase ^= 1u;
+            }
+          }
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
+        if (!ok) break;
+        mma_commit(&afull[b]);
       }
       if (any_mma) {
         mma_commit(drain);
@@ -1263,20 +1377,19 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       }
     }
     __syncwarp();
-  } else {
-    // ---------------- promotion + epilogue (warps 2..9) ----------------
-    // Warp w handles TMEM lane quadrant w % 4 and column half h = (w - 2) / 4:
-    // gate_up: gate columns 32h .. 32h+31 and the matching up columns
-    // 64 + 32h .. (so SwiGLU stays in the thread); down: columns 64h .. 64h+63.
+  } else if (warp < 6) {
+    // ---------------- scale writers (warps 2..5) ----------------
+    // The warp of lane quadrant q writes, per four k-blocks, lanes
+    // 32q..32q+31 of a scale slot: its rows' A exponents (columns 0-3) and
+    // the tile's B exponents (columns 4-7: two gate, two up for gate_up).
+    // Scales are loaded a group of four k-blocks ahead.
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int row = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const int col0 = SWIGLU ? 32 * half : 64 * half;            // first TMEM column
-    const int col1 = SWIGLU ? kF8BN / 2 + 32 * half : col0 + 32;  // second 32-column run
-    uint32_t q = 0;
+    const int row = quad * 32 + lane;
+    int slot = 0;
+    uint32_t sphase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+    for (int u = blockIdx.x; u < total && ok && !*abort_flag; u += gridDim.x) {
       const Tile t = decode_tile(args, mt, u);
       const int64_t grow = static_cast<int64_t>(t.row0) + row;
       const bool rok = row < t.rows_valid && grow >= 0 && grow < args.rows_total;
@@ -1289,134 +1402,545 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       } else {
         bs0 = bs1 = fa.b_scale + (static_cast<int64_t>(t.e) * b_blocks + t.n) * kbs;
       }
-      // acc2[i]: this warp's columns 2i, 2i+1 of its two runs (0..15 the
-      // first run, 16..31 the second); promoted with fma.rn.f32x2 (two IEEE
-      // fused multiply-adds, rounded as scalar ones)
-      uint64_t acc2[32];
+      float ca[4], cg[4], cu[4];
+      auto load4 = [&](int kb0, float(&a)[4], float(&g)[4], float(&uu)[4]) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) acc2[c] = 0ull;
-      float sa = rok ? __ldg(as) : 0.0f;
-      // a warp whose 32 rows are all past the tile's rows only keeps the
-      // partial ring moving
-      const bool warp_rows = quad * 32 < t.rows_valid;
-      for (int kb = 0; kb < kblocks; ++kb, ++q) {
-        const int p = static_cast<int>(q % kF8Parts);
-        const float s0 = sa * __ldg(bs0 + kb), s1 = sa * __ldg(bs1 + kb);
-        sa = (rok && kb + 1 < kblocks) ? __ldg(as + kb + 1) : 0.0f;
-        const bool waited = mbar_wait_bounded(&pfull[p], (q / kF8Parts) & 1u, abort_flag,
+        for (int i = 0; i < 4; ++i) {
+          const int kb = kb0 + i;
+          const bool in = kb < kblocks;
+          a[i] = (in && rok) ? __ldg(as + kb) : 1.0f;
+          g[i] = in ? __ldg(bs0 + kb) : 1.0f;
+          uu[i] = in ? __ldg(bs1 + kb) : 1.0f;
+        }
+      };
+      load4(0, ca, cg, cu);
+      for (int kb0 = 0; kb0 < kblocks && ok; kb0 += 4) {
+        float na[4], ng[4], nu[4];
+        load4(kb0 + 4, na, ng, nu);
+        // byte i of each cell: k-block kb0 + i (past the tile's last k-block: 2^0)
+        uint32_t va = 0, vg = 0, vu = 0;
+        bool valid = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t ba, bg, bu;
+          valid = valid & ue8m0_of(ca[i], ba) & ue8m0_of(cg[i], bg) & ue8m0_of(cu[i], bu);
+          va |= ba << (8 * i);
+          vg |= bg << (8 * i);
+          vu |= bu << (8 * i);
+        }
+        if (!valid) set_status(args.status, kStatusBadId);
+        const bool waited = mbar_wait_bounded(&sempty[slot], sphase ^ 1u, abort_flag,
                                               args.status, args.wait_limit_ns);
         if (!__all_sync(0xffffffffu, waited)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t tp = tmem_base + lane_off + static_cast<uint32_t>(p * kF8BN);
-        // the partial is released as soon as its values are in registers, so
-        // the MMA can refill it while the scales are applied
-        auto release = [&]() {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&pempty[p]);
-        };
-        if (!warp_rows) {
-          release();
-        } else {
-          // both 32-column runs in one wait
-          uint32_t v[32], w[32];
-          tmem_ld_32x32b_x32(tp + col0, v);
-          tmem_ld_32x32b_x32(tp + col1, w);
-          tmem_ld_wait();
-          tmem_regs_fence(v);
-          tmem_regs_fence(w);
-          release();
-          // down: one weight block, s0 == s1; gate_up: gate run s0, up run s1
-          uint64_t sc0, sc1;
-          asm("mov.b64 %0, {%1, %1};" : "=l"(sc0) : "f"(s0));
-          asm("mov.b64 %0, {%1, %1};" : "=l"(sc1) : "f"(s1));
+        const uint32_t v[8] = {va, va, va, va, vg, vg, vu, vu};
+        tmem_st_32x32b_x8(tmem_base + lane_off + static_cast<uint32_t>(kF8ScaleCol + 8 * slot), v);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[slot]);
+        if (++slot == kF8ScaleSlots) {
+          slot = 0;
+          sphase ^= 1u;
+        }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            uint64_t pv, pw;
-            asm("mov.b64 %0, {%1, %2};" : "=l"(pv) : "r"(v[2 * j]), "r"(v[2 * j + 1]));
-            asm("mov.b64 %0, {%1, %2};" : "=l"(pw) : "r"(w[2 * j]), "r"(w[2 * j + 1]));
-            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[j]) : "l"(pv), "l"(sc0));
-            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[16 + j]) : "l"(pw), "l"(sc1));
-          }
+        for (int i = 0; i < 4; ++i) {
+          ca[i] = na[i];
+          cg[i] = ng[i];
+          cu[i] = nu[i];
         }
       }
-      if (!ok || !rok) continue;
+    }
+  } else {
+    // ---------------- epilogue (warps 6..13) ----------------
+    // Warp w handles TMEM lane quadrant w % 4 and column half h = (w - 6) / 4:
+    // gate_up: gate columns 32h .. 32h+31 and the matching up columns
+    // 64 + 32h .. (so SwiGLU stays in the thread); down: columns 64h .. 64h+63.
+    const int quad = warp & 3;
+    const int half = (warp - 6) >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int col0 = SWIGLU ? 32 * half : 64 * half;            // first TMEM column
+    const int col1 = SWIGLU ? kF8BN / 2 + 32 * half : col0 + 32;  // second 32-column run
+    uint32_t tcount = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++tcount) {
+      const Tile t = decode_tile(args, mt, u);
+      const int64_t grow = static_cast<int64_t>(t.row0) + row;
+      const bool rok = row < t.rows_valid && grow >= 0 && grow < args.rows_total;
+      const uint32_t b = tcount & 1u;
+      const bool waited = mbar_wait_bounded(&afull[b], (tcount >> 1) & 1u, abort_flag,
+                                            args.status, args.wait_limit_ns);
+      if (!__all_sync(0xffffffffu, waited)) break;
+      tc_fence_after();
+      // a warp whose 32 rows are all past the tile's rows only releases
+      const bool warp_rows = quad * 32 < t.rows_valid;
+      uint32_t v[32], w[32];
+      if (warp_rows) {
+        const uint32_t tp = tmem_base + lane_off + b * kF8BN;
+        tmem_ld_32x32b_x32(tp + col0, v);
+        tmem_ld_32x32b_x32(tp + col1, w);
+        tmem_ld_wait();
+        tmem_regs_fence(v);
+        tmem_regs_fence(w);
+      }
+      // the accumulator is released as soon as its values are in registers
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aempty[b]);
+      if (!warp_rows || !rok) continue;
       float acc[64];
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[2 * c]), "=f"(acc[2 * c + 1]) : "l"(acc2[c]));
-      if (SWIGLU) {
-        // intermediate columns t.n * 64 + 32h .. +31: gate acc[0..31], up acc[32..63]
-        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(args.out) + grow * args.ldo +
-                             static_cast<int64_t>(t.n) * C::BN_OUT + 32 * half;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t w8[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int j = c * 16 + 2 * i;
-            const float g0 = acc[j], g1 = acc[j + 1];
-            const float u0 = acc[32 + j], u1 = acc[32 + j + 1];
-            w8[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
-                                __fdividef(g1, 1.0f + __expf(-g1)) * u1);
-          }
-          if (args.out_v8) {
-            st_global_v8(dst + c * 16, w8);
-          } else {
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 16);
-            d4[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-            d4[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
-          }
-        }
-      } else if (args.out_codes != nullptr) {
-        // compact output: the thread's 64 columns are two 32-column groups,
-        // 128 bytes of fp16 values and two code bytes
-        const int64_t col = static_cast<int64_t>(t.n) * kF8BN + 64 * half;
-        __half *dst = static_cast<__half *>(args.out) + grow * args.ldo + col;
-        uint32_t codes = 0;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          uint32_t v[32], hw[16];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(acc[32 * g + i]);
-          codes |= y16_encode32(v, hw) << (8 * g);
-          uint32_t w8[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) w8[i] = hw[i];
-          st_global_v8(dst + 32 * g, w8);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) w8[i] = hw[8 + i];
-          st_global_v8(dst + 32 * g + 16, w8);
-        }
-        *reinterpret_cast<uint16_t *>(args.out_codes + grow * (args.ldo / 32) + col / 32) =
-            static_cast<uint16_t>(codes);
-      } else {
-        float *dst = static_cast<float *>(args.out) + grow * args.ldo +
-                     static_cast<int64_t>(t.n) * kF8BN + 64 * half;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w8[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) w8[i] = __float_as_uint(acc[c * 8 + i]);
-          if (args.out_v8) {
-            st_global_v8(dst + c * 8, w8);
-          } else {
-            float4 *d4 = reinterpret_cast<float4 *>(dst + c * 8);
-            d4[0] = make_float4(acc[c * 8], acc[c * 8 + 1], acc[c * 8 + 2], acc[c * 8 + 3]);
-            d4[1] = make_float4(acc[c * 8 + 4], acc[c * 8 + 5], acc[c * 8 + 6], acc[c * 8 + 7]);
-          }
-        }
+      for (int c = 0; c < 32; ++c) {
+        acc[c] = __uint_as_float(v[c]);
+        acc[32 + c] = __uint_as_float(w[c]);
       }
+      f8_store_tile_row<SWIGLU>(
+          args, grow,
+          SWIGLU ? static_cast<int64_t>(t.n) * (kF8BN / 2) + 32 * half
+                 : static_cast<int64_t>(t.n) * kF8BN + 64 * half,
+          acc);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem_base, kF8TmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// The same FP8 GEMM on a cluster of two CTAs (cta_group::2 block-scaled
+// MMAs) with 256 x 256 tiles, each K step two M=256 x N=128 MMAs into two
+// 128-column accumulator halves.  Three half buffers rotate through TMEM
+// (columns 0-383): tile i uses buffers 2i % 3 (half 0) and (2i+1) % 3 (half
+// 1), so its half 1 is tile i-1's half 0, which the epilogue reads and
+// releases first: the next tile's MMAs wait only for that read, not for the
+// epilogue's stores.  Each CTA loads its 128 A rows and 128 B
+// rows per stage (32 KB, 6 stages): smem B rows 0-63 feed half 0 and rows
+// 64-127 half 1, the pair MMA taking N/2 rows from each CTA.  gate_up: the
+// even CTA loads 128 gate rows, the odd CTA the matching 128 up rows, so
+// each half holds 64 gate columns and their 64 up columns; down: the even
+// CTA loads output rows c0 + [0, 64) and c0 + [128, 192), the odd CTA
+// c0 + [64, 128) and c0 + [192, 256), so half 0 holds output columns
+// c0 .. c0 + 127 and half 1 the next 128.  Each CTA's MMA half reads its
+// exponents from its own TMEM in the 1-CTA layout; a scale slot has 16
+// columns: A (0-3), half 0's B (4-7), half 1's B (8-11).  An expert's last
+// tile may leave the odd CTA without A rows: it then loads only its B rows.
+//   full[s]          even CTA: both CTAs' copies of stage s landed;
+//   empty[s]         both CTAs: the pair MMAs that read stage s completed;
+//   sfull[g]         even CTA: both CTAs' exponents of scale slot g are in TMEM;
+//   sempty[g]        both CTAs: the pair MMAs that read slot g completed;
+//   hfull[b]         both CTAs: half buffer b holds a complete tile half;
+//   hempty[b]        even CTA: both CTAs' epilogue warps have read buffer b.
+// ---------------------------------------------------------------------------
+constexpr int kF8PairStages = 6;
+constexpr int kF8PairBN = 256;
+constexpr int kF8PairSlotCols = 16;
+constexpr int kF8PairScaleCol = 3 * 128;  // after the three half buffers
+
+template <bool SWIGLU>
+struct CfgF8P {
+  static constexpr int A_BYTES = kBM * kF8BK;
+  static constexpr int B_BYTES = (kF8PairBN / 2) * kF8BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = kF8PairStages;
+  static constexpr int BN_OUT = SWIGLU ? kF8PairBN / 2 : kF8PairBN;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * kF8ScaleSlots + 2 * 3 + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int MT_OFF = MISC_OFF + 16;
+  static constexpr int SEG_OFF = MT_OFF + (kMaxE + 1) * 4;
+  static constexpr int SMEM_BYTES = SEG_OFF + (kMaxE + 1) * 4 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "227 KB of shared memory per CTA");
+  static_assert(kF8PairScaleCol + kF8PairSlotCols * kF8ScaleSlots <= kF8TmemCols,
+                "scale slots fit the TMEM allocation");
+};
+
+// D (M=256: rows 0-127 in this CTA's TMEM, 128-255 in the peer's) (+)=
+// block-scaled e4m3 A (128 rows per CTA) * B^T (N/2 rows per CTA); each CTA's
+// half reads its exponents from its own TMEM at sfa_tmem / sfb_tmem.
+__device__ __forceinline__ void mma_mxf8_ss_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Whole warp: thread i writes v[j] to lane (base lane + i), column col + j.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
+// TMA bytes of A that one CTA of the pair loads for a tile with rows_valid
+// rows (its 128-row half: none, 32-row boxes, or one 128-row box)
+__device__ __forceinline__ uint32_t f8_pair_a_bytes(int rows_valid, int rank) {
+  const int here = min(max(rows_valid - 128 * rank, 0), 128);
+  const int subs = (here + kF8SubRows - 1) / kF8SubRows;
+  return static_cast<uint32_t>(subs) * kF8SubRows * kF8BK;
+}
+
+template <bool SWIGLU>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
+    grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                                 const __grid_constant__ CUtensorMap tmA32,
+                                 const __grid_constant__ CUtensorMap tmB, const F8Args fa) {
+  pdl_begin();
+  using C = CfgF8P<SWIGLU>;
+  const KArgs &args = fa.k;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *smA = smem;
+  uint8_t *smB = smem + C::STAGES * C::A_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + C::STAGES;
+  uint64_t *sfull = bars + 2 * C::STAGES;
+  uint64_t *sempty = sfull + kF8ScaleSlots;
+  uint64_t *hfull = sempty + kF8ScaleSlots;
+  uint64_t *hempty = hfull + 3;
+  uint64_t *drain = hempty + 3;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+  int32_t *mt = reinterpret_cast<int32_t *>(smem + C::MT_OFF);
+  int32_t *sg = reinterpret_cast<int32_t *>(smem + C::SEG_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool even = rank == 0;
+  const int cid = static_cast<int>(blockIdx.x >> 1);
+  const int ncl = static_cast<int>(gridDim.x >> 1);
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) {
+    mt[i] = args.mtile_base[i];
+    sg[i] = (args.layout == MOE_LAYOUT_CONTIGUOUS || i < args.E) ? args.seg[i] : 0;
+  }
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < C::STAGES; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 1);
+    }
+    for (int g = 0; g < kF8ScaleSlots; ++g) {
+      mbar_init(&sfull[g], 8);
+      mbar_init(&sempty[g], 1);
+    }
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(&hfull[b], 1);
+      mbar_init(&hempty[b], 16);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  cluster_sync_all();  // both CTAs' barriers exist before any remote use
+  const int total = mt[args.E] * args.n_tiles;
+  if (cid >= total) return;  // uniform across the pair
+  if (warp == 1) tmem_alloc_pair(tmem_slot, kF8TmemCols);
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int kblocks = args.K / kF8BK;
+  const int kbs = kblocks;
+  const int b_blocks = args.b_rows / 128;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmA32);
+      tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[C::STAGES];
+      bool issued[C::STAGES];
+#pragma unroll
+      for (int st = 0; st < C::STAGES; ++st) issued[st] = false;
+      for (int u = cid; u < total && !*abort_flag; u += ncl) {
+        const Tile t = decode_tile<256>(args, mt, u, sg);
+        const uint32_t a_here = f8_pair_a_bytes(t.rows_valid, static_cast<int>(rank));
+        // both CTAs' bytes of one k-block, expected on the even CTA's barrier
+        const uint32_t tx = 2u * C::B_BYTES + f8_pair_a_bytes(t.rows_valid, 0) +
+                            f8_pair_a_bytes(t.rows_valid, 1);
+        const int a_row = t.row0 + 128 * static_cast<int>(rank);
+        int b_row0, b_row1;  // this CTA's B rows for smem rows 0-63 and 64-127
+        if (SWIGLU) {
+          b_row0 = t.e * args.b_rows + (even ? 0 : args.up_off) + t.n * C::BN_OUT;
+          b_row1 = b_row0 + 64;
+        } else {
+          b_row0 = t.e * args.b_rows + t.n * kF8PairBN + 64 * static_cast<int>(rank);
+          b_row1 = b_row0 + 128;
+        }
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
+                                 args.wait_limit_ns))
+            break;
+          if (even) mbar_arrive_expect_tx(&full[stage], tx);
+          const uint32_t fbar = mapa_shared(&full[stage], 0);
+          uint8_t *a_dst = smA + stage * C::A_BYTES;
+          uint8_t *b_dst = smB + stage * C::B_BYTES;
+          if (a_here == static_cast<uint32_t>(C::A_BYTES)) {
+            tma_load_2d_pair(a_dst, &tmA, fbar, kb * kF8BK, a_row);
+          } else {
+            for (uint32_t i = 0; i * kF8SubRows * kF8BK < a_here; ++i)
+              tma_load_2d_pair(a_dst + i * kF8SubRows * kF8BK, &tmA32, fbar, kb * kF8BK,
+                               a_row + static_cast<int>(i) * kF8SubRows);
+          }
+          tma_load_2d_pair(b_dst, &tmB, fbar, kb * kF8BK, b_row0);
+          tma_load_2d_pair(b_dst + 64 * kF8BK, &tmB, fbar, kb * kF8BK, b_row1);
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // drain: the even CTA sees its full barriers; the odd CTA knows its
+      // copies landed once the pair MMA that read them released the slot
+      for (int st = 0; st < C::STAGES; ++st)
+        if (issued[st]) {
+          if (even)
+            wait_drain(&full[st], issued_phase[st], args.wait_limit_ns);
+          else
+            wait_drain(&empty[st], issued_phase[st], args.wait_limit_ns);
+        }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && even) {
+      // ---------------- pair MMA issuer (even CTA) ----------------
+      constexpr uint32_t kIdesc = mma_idesc_mxf8_f32(256, 128);
+      int stage = 0;
+      uint32_t phase = 0;
+      int slot = 0;
+      uint32_t sphase = 0;
+      uint32_t tcount = 0;
+      uint32_t hpar = 0;  // bit b: parity of half buffer b's next use
+      bool any_mma = false;
+      bool ok = true;
+      for (int u = cid; u < total && ok && !*abort_flag; u += ncl, ++tcount) {
+        const uint32_t h0 = (2u * tcount) % 3u, h1 = (2u * tcount + 1u) % 3u;
+        if (!mbar_wait_bounded(&hempty[h0], ((hpar >> h0) & 1u) ^ 1u, abort_flag, args.status,
+                               args.wait_limit_ns) ||
+            !mbar_wait_bounded(&hempty[h1], ((hpar >> h1) & 1u) ^ 1u, abort_flag, args.status,
+                               args.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + 128u * h0, d1 = tmem_base + 128u * h1;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const int j = kb & 3;  // byte of the slot's cells with this k-block's exponents
+          if ((j == 0 && !mbar_wait_bounded(&sfull[slot], sphase, abort_flag, args.status,
+                                            args.wait_limit_ns)) ||
+              !mbar_wait_bounded(&full[stage], phase, abort_flag, args.status,
+                                 args.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(smA + stage * C::A_BYTES));
+          const uint64_t bd0 = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
+          const uint64_t bd1 = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES + 64 * kF8BK));
+          const uint32_t sfa =
+              tmem_base + static_cast<uint32_t>(kF8PairScaleCol + kF8PairSlotCols * slot);
+          const uint32_t idesc =
+              kIdesc | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
+#pragma unroll
+          for (int kk = 0; kk < kF8BK / 32; ++kk) {
+            const uint32_t acc = (kb != 0 || kk != 0) ? 1u : 0u;
+            mma_mxf8_ss_pair(d0, ad + 2u * kk, bd0 + 2u * kk, idesc, sfa, sfa + 4u, acc);
+            mma_mxf8_ss_pair(d1, ad + 2u * kk, bd1 + 2u * kk, idesc, sfa, sfa + 8u, acc);
+          }
+          any_mma = true;
+          mma_commit_pair(&empty[stage], 0x3);
+          if (j == 3 || kb == kblocks - 1) {
+            mma_commit_pair(&sempty[slot], 0x3);
+            if (++slot == kF8ScaleSlots) {
+              slot = 0;
+              sphase ^= 1u;
+            }
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&hfull[h0], 0x3);
+        mma_commit_pair(&hfull[h1], 0x3);
+        hpar ^= (1u << h0) | (1u << h1);
+      }
+      if (any_mma) {
+        mma_commit_pair(drain, 0x1);
+        wait_drain(drain, 0, args.wait_limit_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ---------------- scale writers (warps 2..5, both CTAs) ----------------
+    // Per four k-blocks, lanes 32q..32q+31 of a slot: this CTA's rows' A
+    // exponents (columns 0-3) and both halves' B exponents (4-7, 8-11;
+    // gate_up: two gate, two up columns each, down: one block per half).
+    const int quad = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int prow = static_cast<int>(rank) * 128 + quad * 32 + lane;  // row in the 256-row tile
+    int slot = 0;
+    uint32_t sphase = 0;
+    bool ok = true;
+    for (int u = cid; u < total && ok && !*abort_flag; u += ncl) {
+      const Tile t = decode_tile<256>(args, mt, u, sg);
+      const int64_t grow = static_cast<int64_t>(t.row0) + prow;
+      const bool rok = prow < t.rows_valid && grow >= 0 && grow < args.rows_total;
+      const float *as = fa.a_scale + (rok ? grow : 0) * kbs;
+      // gate_up: gate and up blocks (both halves); down: half 0's and half 1's blocks
+      const float *bs0, *bs1;
+      if (SWIGLU) {
+        bs0 = fa.b_scale + (static_cast<int64_t>(t.e) * b_blocks + (t.n * C::BN_OUT) / 128) * kbs;
+        bs1 = fa.b_scale +
+              (static_cast<int64_t>(t.e) * b_blocks + (args.up_off + t.n * C::BN_OUT) / 128) * kbs;
+      } else {
+        bs0 = fa.b_scale + (static_cast<int64_t>(t.e) * b_blocks + 2 * t.n) * kbs;
+        bs1 = bs0 + kbs;
+      }
+      float ca[4], c0[4], c1[4];
+      auto load4 = [&](int kb0, float(&a)[4], float(&b0)[4], float(&b1)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int kb = kb0 + i;
+          const bool in = kb < kblocks;
+          a[i] = (in && rok) ? __ldg(as + kb) : 1.0f;
+          b0[i] = in ? __ldg(bs0 + kb) : 1.0f;
+          b1[i] = in ? __ldg(bs1 + kb) : 1.0f;
+        }
+      };
+      load4(0, ca, c0, c1);
+      for (int kb0 = 0; kb0 < kblocks && ok; kb0 += 4) {
+        float na[4], n0[4], n1[4];
+        load4(kb0 + 4, na, n0, n1);
+        // byte i of each cell: k-block kb0 + i (past the tile's last k-block: 2^0)
+        uint32_t va = 0, v0 = 0, v1 = 0;
+        bool valid = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t ba, b0, b1;
+          valid = valid & ue8m0_of(ca[i], ba) & ue8m0_of(c0[i], b0) & ue8m0_of(c1[i], b1);
+          va |= ba << (8 * i);
+          v0 |= b0 << (8 * i);
+          v1 |= b1 << (8 * i);
+        }
+        if (!valid) set_status(args.status, kStatusBadId);
+        const bool waited = mbar_wait_bounded(&sempty[slot], sphase ^ 1u, abort_flag,
+                                              args.status, args.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, waited)) {
+          ok = false;
+          break;
+        }
+        // gate_up: each half's B columns 0-63 gate (v0), 64-127 up (v1);
+        // down: half 0 all v0, half 1 all v1
+        const uint32_t h0a = v0, h0b = SWIGLU ? v1 : v0;
+        const uint32_t h1a = SWIGLU ? v0 : v1, h1b = v1;
+        const uint32_t v[16] = {va, va, va, va, h0a, h0a, h0b, h0b,
+                                h1a, h1a, h1b, h1b, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu,
+                                0x7f7f7f7fu};
+        tmem_st_32x32b_x16(
+            tmem_base + lane_off + static_cast<uint32_t>(kF8PairScaleCol + kF8PairSlotCols * slot),
+            v);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(mapa_shared(&sfull[slot], 0));
+        if (++slot == kF8ScaleSlots) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ca[i] = na[i];
+          c0[i] = n0[i];
+          c1[i] = n1[i];
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 6..13, both CTAs) ----------------
+    // For each half of a tile in turn (half 0 first, releasing it for the
+    // next tile's MMAs): warp w takes TMEM lane quadrant w % 4 and part
+    // p = (w - 6) / 4 of the half.  gate_up: gate columns 32p..32p+31 of the
+    // half and their up columns 64 + 32p.. -> h columns t.n * 128 + 64 * half
+    // + 32p; down: columns 64p..64p+63 -> output columns t.n * 256 +
+    // 128 * half + 64p.
+    const int quad = warp & 3;
+    const int part = (warp - 6) >> 2;
+    const int prow = static_cast<int>(rank) * 128 + quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int col0 = SWIGLU ? 32 * part : 64 * part;
+    const int col1 = SWIGLU ? 64 + 32 * part : 64 * part + 32;
+    uint32_t tcount = 0;
+    uint32_t hpar = 0;  // bit b: parity of half buffer b's next completion
+    bool ok = true;
+    for (int u = cid; u < total && ok; u += ncl, ++tcount) {
+      const Tile t = decode_tile<256>(args, mt, u, sg);
+      const int64_t grow = static_cast<int64_t>(t.row0) + prow;
+      const bool rok = prow < t.rows_valid && grow >= 0 && grow < args.rows_total;
+      const bool warp_rows = static_cast<int>(rank) * 128 + quad * 32 < t.rows_valid;
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t b = (2u * tcount + static_cast<uint32_t>(half)) % 3u;
+        const bool waited = mbar_wait_bounded(&hfull[b], (hpar >> b) & 1u, abort_flag,
+                                              args.status, args.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, waited)) {
+          ok = false;
+          break;
+        }
+        hpar ^= 1u << b;
+        tc_fence_after();
+        uint32_t v[32], w[32];
+        if (warp_rows) {
+          const uint32_t tp = tmem_base + lane_off + 128u * b;
+          tmem_ld_32x32b_x32(tp + col0, v);
+          tmem_ld_32x32b_x32(tp + col1, w);
+          tmem_ld_wait();
+          tmem_regs_fence(v);
+          tmem_regs_fence(w);
+        }
+        // the half is released as soon as its values are in registers
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(mapa_shared(&hempty[b], 0));
+        if (!warp_rows || !rok) continue;
+        float acc[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          acc[i] = __uint_as_float(v[i]);
+          acc[32 + i] = __uint_as_float(w[i]);
+        }
+        f8_store_tile_row<SWIGLU>(
+            args, grow,
+            SWIGLU ? static_cast<int64_t>(t.n) * C::BN_OUT + 64 * half + 32 * part
+                   : static_cast<int64_t>(t.n) * kF8PairBN + 128 * half + 64 * part,
+            acc);
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // no CTA leaves while its peer may still use its memory
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kF8TmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -1537,7 +2061,7 @@ bool make_tmap_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t r
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool SWIGLU>
@@ -1587,8 +2111,40 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   a.ksplit = 1;
   fa.a_scale = a_scale;
   fa.b_scale = b_scale;
-  MOE_LAUNCH_PDL(grouped_gemm_fp8_kernel<SWIGLU>, num_sms(), kF8Threads, C::SMEM_BYTES, s, tmA, tmA32,
-                                                                                tmB, fa);
+  if (!p.pair) {
+    MOE_LAUNCH_PDL(grouped_gemm_fp8_kernel<SWIGLU>, num_sms(), kF8Threads, C::SMEM_BYTES, s, tmA,
+                   tmA32, tmB, fa);
+    return cudaGetLastError();
+  }
+  // CTA pairs on 256-row tiles (mtile_base counts 256-row tiles)
+  using P = CfgF8P<SWIGLU>;
+  err = cudaFuncSetAttribute(grouped_gemm_fp8_pair_kernel<SWIGLU>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  if (p.n_out % P::BN_OUT != 0) return cudaErrorInvalidValue;
+  a.n_tiles = p.n_out / P::BN_OUT;
+  a.m_block = static_cast<int>((24ll << 20) / (256ll * p.K));
+  if (a.m_block < 1) a.m_block = 1;
+  int clusters = 0;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    cfg.blockDim = dim3(kF8Threads);
+    cfg.dynamicSmemBytes = P::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_fp8_pair_kernel<SWIGLU>, &cfg);
+    if (err != cudaSuccess) return err;
+  }
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  MOE_LAUNCH_PDL(grouped_gemm_fp8_pair_kernel<SWIGLU>, 2 * clusters, kF8Threads, P::SMEM_BYTES, s,
+                 tmA, tmA32, tmB, fa);
   return cudaGetLastError();
 }
 

@@ -4,17 +4,29 @@
 // scales", 7168 + 224 bytes per token) and the FP8 grouped GEMM of
 // "推理INFRA方法论-02-parallelism" ("DeepGEMM masked, FP8") use e4m3 values
 // with fp32 scales: one per (row, 128 columns) of an activation and one per
-// 128 x 128 block of a weight.  Here: s = amax / 448 (1 for an all-zero
-// block), q = e4m3(x / s) rounded to nearest even with saturation at 448,
-// both divisions in IEEE fp32, so the codes are reproducible bit for bit.
+// 128 x 128 block of a weight.  Here each scale is a power of two, so that
+// the tensor cores can apply it themselves (as an 8-bit exponent): s = 2^e
+// with e the smallest integer >= -127 such that amax <= 448 * 2^e (1 for an
+// all-zero block, 2^127 when amax is not finite); q = e4m3(x / s) rounded to
+// nearest even with saturation at 448.  Dividing by a power of two is exact,
+// so the codes are reproducible bit for bit.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 namespace {
 
+// The power-of-two scale from amax's bits: amax = (1 + f) * 2^(E - 127) with
+// E its exponent field, and 448 * 2^(E - 135) = 1.75 * 2^(E - 127), so
+// e = E - 135 when f <= 0.75 (mantissa field <= 0x600000), else E - 134.
 __device__ __forceinline__ float fp8_block_scale(float amax) {
-  return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  if (!(amax > 0.0f)) return 1.0f;
+  const uint32_t b = __float_as_uint(amax);
+  const int ef = static_cast<int>((b >> 23) & 0xffu);
+  if (ef == 0xff) return __uint_as_float(254u << 23);  // 2^127
+  int e = ef - 135 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
+  if (e <= -127) return __uint_as_float(0x00400000u);  // 2^-127 (an fp32 subnormal)
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
 // two fp32 -> two e4m3 codes (lo in bits 0-7), round to nearest even,

@@ -375,9 +375,12 @@ moe_status_t moe_layer_capacity(const moe_shape_t *shape, int32_t capacity, int3
  * FP8 quantization (e4m3 with fp32 block scales; the "ep-deploy" page's
  * cost model dispatches FP8 with scales, 7168 + 224 bytes per token, and
  * "推理INFRA方法论-02-parallelism" measures the FP8 grouped expert GEMM):
- *   s = amax / 448 of the block (1 when the block is all zeros),
- *   q = e4m3(x / s), IEEE fp32 division, round to nearest even, saturating
- *   at 448.
+ *   s = 2^e, e the smallest integer >= -127 with amax <= 448 * 2^e for
+ *   the block's largest magnitude amax (1 when the block is all zeros, 2^127
+ *   when amax is not finite): a power of two, which the FP8 GEMM hands to the
+ *   tensor cores as an 8-bit exponent;
+ *   q = e4m3(x / s) (exact division), round to nearest even, saturating at
+ *   448.
  * moe_quantize_fp8_rows: x [rows, cols] bf16 -> q [rows, cols] e4m3 codes,
  *   scales [rows, cols/128] fp32 (one per row and 128 columns).
  * moe_quantize_fp8_blocks: w [mats, rows, cols] bf16 -> q [mats, rows, cols],
@@ -397,9 +400,13 @@ moe_status_t moe_quantize_fp8_blocks(const void *w, int32_t mats, int32_t rows, 
  *   w_down_q [E, d, inter] e4m3 codes with w_*_scale [E, rows/128, cols/128]
  *   fp32 (per 128 x 128 block, as moe_quantize_fp8_blocks); seg, M_max and
  *   the layouts as moe_expert_ffn; y_out [rows, d] fp32.
- *   Each 128-column k-block is multiplied on the tensor core in fp32 and
- *   added with its two scales; h = silu(g) * u is stored in bf16, quantized
- *   per row and 128 columns, and multiplied by w_down the same way.
+ *   The tensor cores apply both scales of each 128-column k-block
+ *   themselves (block-scaled MMAs, the scales as 8-bit exponents) and
+ *   accumulate in fp32; h = silu(g) * u is stored in bf16, quantized per row
+ *   and 128 columns, and multiplied by w_down the same way.  Every scale
+ *   must be a power of two in [2^-127, 2^127], as the quantizers above make
+ *   them; any other value sets MOE_ERR_INVALID_ARG in the device status
+ *   (and the affected outputs are undefined).
  *   d and inter must be multiples of 128 (MOE_ERR_UNSUPPORTED otherwise).
  */
 moe_status_t moe_expert_ffn_fp8_workspace_size(const moe_shape_t *shape, int32_t layout,

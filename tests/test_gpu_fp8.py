@@ -1,4 +1,4 @@
-"""FP8 path (e4m3 codes with fp32 block scales) against the oracle: the
+"""FP8 path (e4m3 codes with power-of-two fp32 block scales) against the oracle: the
 quantizers bit-exact, the FP8 expert FFN (contiguous and masked layouts,
 ragged tiles) and the FP8 layer within the stated tolerance."""
 import numpy as np
@@ -121,7 +121,35 @@ def test_ffn_fp8_masked(masked_m, M_max, T):
         assert np.isnan(yc[e * M_max + m:(e + 1) * M_max]).all()
 
 
-@pytest.mark.parametrize("name,n_samples", [("tiny", None), ("decode", 4), ("few_large", 3)])
+@pytest.mark.parametrize("pair_rows", [False, True])
+def test_ffn_fp8_flags_a_scale_that_is_not_a_power_of_two(pair_rows):
+    # the tensor cores take each scale as an 8-bit exponent: any other value
+    # is reported in the device status (1-CTA and CTA-pair forms)
+    ensure_lib()
+    counts = [300, 260] if pair_rows else [40, 9]
+    E, d, inter = len(counts), 256, 128
+    rows = sum(counts)
+    x = _rand_bf16((rows, d), 5)
+    (gq, gs, dq, ds), _ = _weights_fp8(E, d, inter, seed=6)
+    xq, xs = moe.moe_quantize_fp8_rows(x.cuda())
+    offsets = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32).cuda()
+    shape = _shape(E, d, inter, rows)
+    ws = moe.Workspace(moe.moe_expert_ffn_fp8_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    moe.moe_expert_ffn_fp8(shape, moe.MOE_LAYOUT_CONTIGUOUS, xq, xs, offsets, 0, gq, gs, dq, ds,
+                           ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    bad = gs.clone()
+    bad.view(-1)[1] *= 1.5
+    moe.moe_expert_ffn_fp8(shape, moe.MOE_LAYOUT_CONTIGUOUS, xq, xs, offsets, 0, gq, bad, dq, ds,
+                           ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 1          # MOE_ERR_INVALID_ARG
+    assert moe.moe_get_device_status(ws) == 0          # read and cleared
+
+
+@pytest.mark.parametrize("name,n_samples", [("tiny", None), ("decode", 4), ("few_large", 3),
+                                            ("prefill", 2)])
 def test_layer_fp8_matches_oracle(name, n_samples):
     ensure_lib()
     cfg = CONFIGS[name]
