@@ -1173,6 +1173,42 @@ def run_fp8(args):
     w_bytes = touched * 3 * c.d * c.inter          # e4m3: one byte per weight
     flops = 6.0 * c.T * c.k * c.d * c.inter
     peaks, peak_src = load_peaks()
+    # the FP8 expert FFN alone (both GEMMs and the h quantization between
+    # them) on the same routing's rows in dispatch order
+    rws = moe.Workspace(moe.moe_workspace_size(shape))
+    ids, _, _ = moe.moe_route(shape, t["x"], t["w_r"], bias, rws)
+    _, offsets, _, _, x_perm = moe.moe_dispatch(shape, ids, t["x"], rws)
+    xq_p, xs_p = moe.moe_quantize_fp8_rows(x_perm)
+    del x_perm, rws
+    fshape = dict(T=c.T * c.k, d=c.d, E=c.E, G=1, topk_group=1, k=1, inter=c.inter, score=1,
+                  bias_scale=0.15)
+    fws = moe.Workspace(moe.moe_expert_ffn_fp8_workspace_size(fshape,
+                                                              moe.MOE_LAYOUT_CONTIGUOUS))
+    y_f = torch.empty(c.T * c.k, c.d, dtype=torch.float32, device="cuda")
+
+    def ffn_step():
+        moe.moe_expert_ffn_fp8(fshape, moe.MOE_LAYOUT_CONTIGUOUS, xq_p, xs_p, offsets, 0, gq, gs,
+                               dq, ds, fws, y_out=y_f)
+
+    for _ in range(args.warmup):
+        ffn_step()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        ffn_step()
+    e1.record()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(fws) != 0:
+        raise SystemExit("device status error")
+    ffn_s = e0.elapsed_time(e1) / 1000.0 / args.steps
+    # algorithmic bytes of the FFN: the touched weights once; gate_up reads
+    # the FP8 rows and their scales and writes h (bf16); the quantization
+    # reads h and writes its codes and scales; down reads those and writes
+    # the fp32 rows
+    n = c.T * c.k
+    ffn_bytes = (w_bytes + n * (c.d + 4 * (c.d // 128)) + n * c.inter * 2
+                 + n * (c.inter * 2 + c.inter + 4 * (c.inter // 128))
+                 + n * (c.inter + 4 * (c.inter // 128)) + n * c.d * 4)
     line = {
         "metric": METRIC + " (FP8 e4m3 experts, block scales)", "impl": "gb300",
         "value": c.T / (ms / 1000.0), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
@@ -1184,6 +1220,15 @@ def run_fp8(args):
         "layer_weight_bytes_fp8": w_bytes,
         "layer_hbm_fraction_of_weights": w_bytes / (ms / 1000.0) / (peaks["hbm_gbs"] * 1e9),
         "layer_tflops": flops / (ms / 1000.0) / 1e12,
+        # expert FFN alone, fp32 output rows (the layer writes compact rows):
+        # the touched experts' FP8 weight bytes over HBM, and its FLOPs
+        "ffn": {"us": ffn_s * 1e6,
+                "hbm_fraction_of_weights": w_bytes / ffn_s / (peaks["hbm_gbs"] * 1e9),
+                "algorithmic_bytes": ffn_bytes,
+                "hbm_fraction": ffn_bytes / ffn_s / (peaks["hbm_gbs"] * 1e9),
+                "tflops": flops / ffn_s / 1e12,
+                "fp8_tensor_fraction": flops / ffn_s / 1e12 / (2.0 * peaks["bf16_tflops"]),
+                "peak_source": peak_src + " (fp8 peak: 2 x the bf16 measured burst, the nominal ratio)"},
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

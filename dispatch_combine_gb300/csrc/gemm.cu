@@ -1944,6 +1944,368 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// The FP8 GEMM's 1-CTA form with 128 x 256 tiles (used where the routed rows
+// are few per expert, so the weights are the bound): per K step two M=128 x
+// N=128 block-scaled MMAs into two accumulator halves that rotate through
+// three TMEM half buffers as in the pair form.  A stage holds 128 A rows and
+// 256 B rows (48 KB, 4 stages): 32 KB of weights per stage and 128 KB in
+// flight.  gate_up: smem B rows 0-63 gate i0.., 64-127 up i0.., 128-191
+// gate i0+64.., 192-255 up i0+64.. (i0 = 128 t.n), so each half holds 64 gate
+// columns and their up columns; down: rows c0 .. c0+255 (c0 = 256 t.n).
+// The exponent slots are the pair form's (16 columns: A, half 0's B, half
+// 1's B).
+// ---------------------------------------------------------------------------
+constexpr int kF8WideStages = 4;
+
+template <bool SWIGLU>
+struct CfgF8W {
+  static constexpr int A_BYTES = kBM * kF8BK;
+  static constexpr int B_BYTES = kF8PairBN * kF8BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = kF8WideStages;
+  static constexpr int BN_OUT = SWIGLU ? kF8PairBN / 2 : kF8PairBN;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * kF8ScaleSlots + 2 * 3 + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int MT_OFF = MISC_OFF + 16;
+  static constexpr int SMEM_BYTES = MT_OFF + (kMaxE + 1) * 4 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "227 KB of shared memory per CTA");
+  static_assert(kF8PairScaleCol + kF8PairSlotCols * kF8ScaleSlots <= kF8TmemCols,
+                "scale slots fit the TMEM allocation");
+};
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(kF8Threads, 1)
+    grouped_gemm_fp8_wide_kernel(const __grid_constant__ CUtensorMap tmA,
+                                 const __grid_constant__ CUtensorMap tmA32,
+                                 const __grid_constant__ CUtensorMap tmB, const F8Args fa) {
+  pdl_begin();
+  using C = CfgF8W<SWIGLU>;
+  const KArgs &args = fa.k;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *smA = smem;
+  uint8_t *smB = smem + C::STAGES * C::A_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + C::STAGES;
+  uint64_t *sfull = bars + 2 * C::STAGES;
+  uint64_t *sempty = sfull + kF8ScaleSlots;
+  uint64_t *hfull = sempty + kF8ScaleSlots;
+  uint64_t *hempty = hfull + 3;
+  uint64_t *drain = hempty + 3;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+  int32_t *mt = reinterpret_cast<int32_t *>(smem + C::MT_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) mt[i] = args.mtile_base[i];
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < C::STAGES; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 1);
+    }
+    for (int g = 0; g < kF8ScaleSlots; ++g) {
+      mbar_init(&sfull[g], 4);
+      mbar_init(&sempty[g], 1);
+    }
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(&hfull[b], 1);
+      mbar_init(&hempty[b], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int total = mt[args.E] * args.n_tiles;
+  if (blockIdx.x >= total) return;
+  if (warp == 1) tmem_alloc(tmem_slot, kF8TmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int kblocks = args.K / kF8BK;
+  const int kbs = kblocks;
+  const int b_blocks = args.b_rows / 128;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmA32);
+      tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[C::STAGES];
+      bool issued[C::STAGES];
+#pragma unroll
+      for (int st = 0; st < C::STAGES; ++st) issued[st] = false;
+      for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x) {
+        const Tile t = decode_tile(args, mt, u);
+        const int subs = (t.rows_valid + kF8SubRows - 1) / kF8SubRows;  // 1..4
+        const uint32_t tx = C::B_BYTES + (subs < kBM / kF8SubRows ? subs * kF8SubRows * kF8BK
+                                                                  : C::A_BYTES);
+        // the four 64-row B boxes of a stage (smem rows 0, 64, 128, 192)
+        int b_row[4];
+        if (SWIGLU) {
+          const int g0 = t.e * args.b_rows + t.n * C::BN_OUT;
+          b_row[0] = g0;
+          b_row[1] = g0 + args.up_off;
+          b_row[2] = g0 + 64;
+          b_row[3] = g0 + args.up_off + 64;
+        } else {
+          const int c0 = t.e * args.b_rows + t.n * kF8PairBN;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) b_row[q] = c0 + 64 * q;
+        }
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
+                                 args.wait_limit_ns))
+            break;
+          uint8_t *a_dst = smA + stage * C::A_BYTES;
+          uint8_t *b_dst = smB + stage * C::B_BYTES;
+          mbar_arrive_expect_tx(&full[stage], tx);
+          if (subs < kBM / kF8SubRows) {
+            for (int i = 0; i < subs; ++i)
+              tma_load_2d(a_dst + i * kF8SubRows * kF8BK, &tmA32, &full[stage], kb * kF8BK,
+                          t.row0 + i * kF8SubRows);
+          } else {
+            tma_load_2d(a_dst, &tmA, &full[stage], kb * kF8BK, t.row0);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            tma_load_2d(b_dst + q * 64 * kF8BK, &tmB, &full[stage], kb * kF8BK, b_row[q]);
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int st = 0; st < C::STAGES; ++st)
+        if (issued[st]) wait_drain(&full[st], issued_phase[st], args.wait_limit_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t kIdesc = mma_idesc_mxf8_f32(kBM, 128);
+      int stage = 0;
+      uint32_t phase = 0;
+      int slot = 0;
+      uint32_t sphase = 0;
+      uint32_t tcount = 0;
+      uint32_t hpar = 0;  // bit b: parity of half buffer b's next use
+      bool any_mma = false;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok && !*abort_flag; u += gridDim.x, ++tcount) {
+        const uint32_t h0 = (2u * tcount) % 3u, h1 = (2u * tcount + 1u) % 3u;
+        if (!mbar_wait_bounded(&hempty[h0], ((hpar >> h0) & 1u) ^ 1u, abort_flag, args.status,
+                               args.wait_limit_ns) ||
+            !mbar_wait_bounded(&hempty[h1], ((hpar >> h1) & 1u) ^ 1u, abort_flag, args.status,
+                               args.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + 128u * h0, d1 = tmem_base + 128u * h1;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const int j = kb & 3;  // byte of the slot's cells with this k-block's exponents
+          if ((j == 0 && !mbar_wait_bounded(&sfull[slot], sphase, abort_flag, args.status,
+                                            args.wait_limit_ns)) ||
+              !mbar_wait_bounded(&full[stage], phase, abort_flag, args.status,
+                                 args.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(smA + stage * C::A_BYTES));
+          const uint64_t bd0 = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
+          const uint64_t bd1 =
+              sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES + 128 * kF8BK));
+          const uint32_t sfa =
+              tmem_base + static_cast<uint32_t>(kF8PairScaleCol + kF8PairSlotCols * slot);
+          const uint32_t idesc =
+              kIdesc | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
+#pragma unroll
+          for (int kk = 0; kk < kF8BK / 32; ++kk) {
+            const uint32_t acc = (kb != 0 || kk != 0) ? 1u : 0u;
+            mma_mxf8_ss(d0, ad + 2u * kk, bd0 + 2u * kk, idesc, sfa, sfa + 4u, acc);
+            mma_mxf8_ss(d1, ad + 2u * kk, bd1 + 2u * kk, idesc, sfa, sfa + 8u, acc);
+          }
+          any_mma = true;
+          mma_commit(&empty[stage]);
+          if (j == 3 || kb == kblocks - 1) {
+            mma_commit(&sempty[slot]);
+            if (++slot == kF8ScaleSlots) {
+              slot = 0;
+              sphase ^= 1u;
+            }
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&hfull[h0]);
+        mma_commit(&hfull[h1]);
+        hpar ^= (1u << h0) | (1u << h1);
+      }
+      if (any_mma) {
+        mma_commit(drain);
+        wait_drain(drain, 0, args.wait_limit_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ---------------- scale writers (warps 2..5) ----------------
+    // Per four k-blocks, lanes 32q..32q+31 of a slot: the rows' A exponents
+    // (columns 0-3) and both halves' B exponents (4-7, 8-11; gate_up: two
+    // gate, two up columns each, down: one block per half).
+    const int quad = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int row = quad * 32 + lane;
+    int slot = 0;
+    uint32_t sphase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok && !*abort_flag; u += gridDim.x) {
+      const Tile t = decode_tile(args, mt, u);
+      const int64_t grow = static_cast<int64_t>(t.row0) + row;
+      const bool rok = row < t.rows_valid && grow >= 0 && grow < args.rows_total;
+      const float *as = fa.a_scale + (rok ? grow : 0) * kbs;
+      const float *bs0, *bs1;
+      if (SWIGLU) {
+        bs0 = fa.b_scale + (static_cast<int64_t>(t.e) * b_blocks + (t.n * C::BN_OUT) / 128) * kbs;
+        bs1 = fa.b_scale +
+              (static_cast<int64_t>(t.e) * b_blocks + (args.up_off + t.n * C::BN_OUT) / 128) * kbs;
+      } else {
+        bs0 = fa.b_scale + (static_cast<int64_t>(t.e) * b_blocks + 2 * t.n) * kbs;
+        bs1 = bs0 + kbs;
+      }
+      float ca[4], c0[4], c1[4];
+      auto load4 = [&](int kb0, float(&a)[4], float(&b0)[4], float(&b1)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int kb = kb0 + i;
+          const bool in = kb < kblocks;
+          a[i] = (in && rok) ? __ldg(as + kb) : 1.0f;
+          b0[i] = in ? __ldg(bs0 + kb) : 1.0f;
+          b1[i] = in ? __ldg(bs1 + kb) : 1.0f;
+        }
+      };
+      load4(0, ca, c0, c1);
+      for (int kb0 = 0; kb0 < kblocks && ok; kb0 += 4) {
+        float na[4], n0[4], n1[4];
+        load4(kb0 + 4, na, n0, n1);
+        uint32_t va = 0, v0 = 0, v1 = 0;
+        bool valid = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t ba, b0, b1;
+          valid = valid & ue8m0_of(ca[i], ba) & ue8m0_of(c0[i], b0) & ue8m0_of(c1[i], b1);
+          va |= ba << (8 * i);
+          v0 |= b0 << (8 * i);
+          v1 |= b1 << (8 * i);
+        }
+        if (!valid) set_status(args.status, kStatusBadId);
+        const bool waited = mbar_wait_bounded(&sempty[slot], sphase ^ 1u, abort_flag,
+                                              args.status, args.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, waited)) {
+          ok = false;
+          break;
+        }
+        const uint32_t h0a = v0, h0b = SWIGLU ? v1 : v0;
+        const uint32_t h1a = SWIGLU ? v0 : v1, h1b = v1;
+        const uint32_t v[16] = {va, va, va, va, h0a, h0a, h0b, h0b,
+                                h1a, h1a, h1b, h1b, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu,
+                                0x7f7f7f7fu};
+        tmem_st_32x32b_x16(
+            tmem_base + lane_off + static_cast<uint32_t>(kF8PairScaleCol + kF8PairSlotCols * slot),
+            v);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull[slot]);
+        if (++slot == kF8ScaleSlots) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ca[i] = na[i];
+          c0[i] = n0[i];
+          c1[i] = n1[i];
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 6..13) ----------------
+    // As in the pair form: each half in turn (half 0 first), warp w taking
+    // lane quadrant w % 4 and part p = (w - 6) / 4 of the half.
+    const int quad = warp & 3;
+    const int part = (warp - 6) >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int col0 = SWIGLU ? 32 * part : 64 * part;
+    const int col1 = SWIGLU ? 64 + 32 * part : 64 * part + 32;
+    uint32_t tcount = 0;
+    uint32_t hpar = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++tcount) {
+      const Tile t = decode_tile(args, mt, u);
+      const int64_t grow = static_cast<int64_t>(t.row0) + row;
+      const bool rok = row < t.rows_valid && grow >= 0 && grow < args.rows_total;
+      const bool warp_rows = quad * 32 < t.rows_valid;
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t b = (2u * tcount + static_cast<uint32_t>(half)) % 3u;
+        const bool waited = mbar_wait_bounded(&hfull[b], (hpar >> b) & 1u, abort_flag,
+                                              args.status, args.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, waited)) {
+          ok = false;
+          break;
+        }
+        hpar ^= 1u << b;
+        tc_fence_after();
+        uint32_t v[32], w[32];
+        if (warp_rows) {
+          const uint32_t tp = tmem_base + lane_off + 128u * b;
+          tmem_ld_32x32b_x32(tp + col0, v);
+          tmem_ld_32x32b_x32(tp + col1, w);
+          tmem_ld_wait();
+          tmem_regs_fence(v);
+          tmem_regs_fence(w);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hempty[b]);
+        if (!warp_rows || !rok) continue;
+        float acc[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          acc[i] = __uint_as_float(v[i]);
+          acc[32 + i] = __uint_as_float(w[i]);
+        }
+        f8_store_tile_row<SWIGLU>(
+            args, grow,
+            SWIGLU ? static_cast<int64_t>(t.n) * C::BN_OUT + 64 * half + 32 * part
+                   : static_cast<int64_t>(t.n) * kF8PairBN + 128 * half + 64 * part,
+            acc);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kF8TmemCols);
+}
+
+// ---------------------------------------------------------------------------
 // bounded-wait self test: one thread waits on a barrier nobody arrives on
 // ---------------------------------------------------------------------------
 __global__ void wait_selftest_kernel(uint32_t *status, uint64_t limit_ns) {
@@ -2111,6 +2473,17 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   a.ksplit = 1;
   fa.a_scale = a_scale;
   fa.b_scale = b_scale;
+  if (!p.pair && p.n_out % CfgF8W<SWIGLU>::BN_OUT == 0) {
+    // 1-CTA form with 256-column tiles (128-row m-tiles, as mtile_base counts)
+    using W = CfgF8W<SWIGLU>;
+    err = cudaFuncSetAttribute(grouped_gemm_fp8_wide_kernel<SWIGLU>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, W::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    a.n_tiles = p.n_out / W::BN_OUT;
+    MOE_LAUNCH_PDL(grouped_gemm_fp8_wide_kernel<SWIGLU>, num_sms(), kF8Threads, W::SMEM_BYTES, s,
+                   tmA, tmA32, tmB, fa);
+    return cudaGetLastError();
+  }
   if (!p.pair) {
     MOE_LAUNCH_PDL(grouped_gemm_fp8_kernel<SWIGLU>, num_sms(), kF8Threads, C::SMEM_BYTES, s, tmA,
                    tmA32, tmB, fa);
