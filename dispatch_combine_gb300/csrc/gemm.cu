@@ -1512,33 +1512,35 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 
 // ---------------------------------------------------------------------------
 // The same FP8 GEMM on a cluster of two CTAs (cta_group::2 block-scaled
-// MMAs) with 256 x 256 tiles, each K step two M=256 x N=128 MMAs into two
-// 128-column accumulator halves.  Three half buffers rotate through TMEM
-// (columns 0-383): tile i uses buffers 2i % 3 (half 0) and (2i+1) % 3 (half
-// 1), so its half 1 is tile i-1's half 0, which the epilogue reads and
-// releases first: the next tile's MMAs wait only for that read, not for the
-// epilogue's stores.  Each CTA loads its 128 A rows and 128 B
-// rows per stage (32 KB, 6 stages): smem B rows 0-63 feed half 0 and rows
-// 64-127 half 1, the pair MMA taking N/2 rows from each CTA.  gate_up: the
-// even CTA loads 128 gate rows, the odd CTA the matching 128 up rows, so
-// each half holds 64 gate columns and their 64 up columns; down: the even
-// CTA loads output rows c0 + [0, 64) and c0 + [128, 192), the odd CTA
-// c0 + [64, 128) and c0 + [192, 256), so half 0 holds output columns
-// c0 .. c0 + 127 and half 1 the next 128.  Each CTA's MMA half reads its
-// exponents from its own TMEM in the 1-CTA layout; a scale slot has 16
-// columns: A (0-3), half 0's B (4-7), half 1's B (8-11).  An expert's last
-// tile may leave the odd CTA without A rows: it then loads only its B rows.
+// MMAs) with 256 x 256 tiles: one M=256 x N=256 MMA per K step, the even
+// CTA's 128 B rows giving accumulator columns 0-127 (half 0) and the odd
+// CTA's columns 128-255 (half 1).  (Two N=128 MMAs per step would read the A
+// tile from shared memory twice; shared-memory bandwidth, not the tensor
+// core, then sets the pace.)  The accumulator windows alternate between
+// TMEM columns [0, 256) (even tiles) and [128, 384) (odd tiles), three
+// 128-column slots in all; the epilogue reads the middle slot first and
+// releases it, so the next tile's MMAs wait only for that read, and a
+// slot's other user is two tiles back.  Each CTA loads 128 A rows and 128 B
+// rows per stage (32 KB, 6 stages).  gate_up: the even CTA loads gate rows
+// i0 .. i0+63 and their up rows, the odd CTA gate rows i0+64 .. i0+127 and
+// theirs (i0 = 128 t.n), so each half holds 64 gate columns and their 64 up
+// columns; down: CTA r loads output rows c0 + 128r .. c0 + 128r + 127.
+// Each CTA's MMA half reads its exponents from its own TMEM in the 1-CTA
+// layout (N = 256: B column n's exponent at lane 32q + n % 32, column
+// n / 32); a scale slot has 16 columns: A (0-3), B (4-11).  An expert's
+// last tile may leave the odd CTA without A rows: it then loads only its B
+// rows.
 //   full[s]          even CTA: both CTAs' copies of stage s landed;
 //   empty[s]         both CTAs: the pair MMAs that read stage s completed;
 //   sfull[g]         even CTA: both CTAs' exponents of scale slot g are in TMEM;
 //   sempty[g]        both CTAs: the pair MMAs that read slot g completed;
-//   hfull[b]         both CTAs: half buffer b holds a complete tile half;
-//   hempty[b]        even CTA: both CTAs' epilogue warps have read buffer b.
+//   hfull[b]         both CTAs: TMEM slot b holds a complete tile half;
+//   hempty[b]        even CTA: both CTAs' epilogue warps have read slot b.
 // ---------------------------------------------------------------------------
 constexpr int kF8PairStages = 6;
 constexpr int kF8PairBN = 256;
 constexpr int kF8PairSlotCols = 16;
-constexpr int kF8PairScaleCol = 3 * 128;  // after the three half buffers
+constexpr int kF8PairScaleCol = 3 * 128;  // after the three accumulator slots
 
 template <bool SWIGLU>
 struct CfgF8P {
@@ -1678,11 +1680,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
         const int a_row = t.row0 + 128 * static_cast<int>(rank);
         int b_row0, b_row1;  // this CTA's B rows for smem rows 0-63 and 64-127
         if (SWIGLU) {
-          b_row0 = t.e * args.b_rows + (even ? 0 : args.up_off) + t.n * C::BN_OUT;
-          b_row1 = b_row0 + 64;
+          b_row0 = t.e * args.b_rows + t.n * C::BN_OUT + 64 * static_cast<int>(rank);
+          b_row1 = b_row0 + args.up_off;
         } else {
-          b_row0 = t.e * args.b_rows + t.n * kF8PairBN + 64 * static_cast<int>(rank);
-          b_row1 = b_row0 + 128;
+          b_row0 = t.e * args.b_rows + t.n * kF8PairBN + 128 * static_cast<int>(rank);
+          b_row1 = b_row0 + 64;
         }
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.status,
@@ -1723,17 +1725,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
   } else if (warp == 1) {
     if (lane == 0 && even) {
       // ---------------- pair MMA issuer (even CTA) ----------------
-      constexpr uint32_t kIdesc = mma_idesc_mxf8_f32(256, 128);
+      constexpr uint32_t kIdesc = mma_idesc_mxf8_f32(256, kF8PairBN);
       int stage = 0;
       uint32_t phase = 0;
       int slot = 0;
       uint32_t sphase = 0;
       uint32_t tcount = 0;
-      uint32_t hpar = 0;  // bit b: parity of half buffer b's next use
+      uint32_t hpar = 0;  // bit b: parity of slot b's next use
       bool any_mma = false;
       bool ok = true;
       for (int u = cid; u < total && ok && !*abort_flag; u += ncl, ++tcount) {
-        const uint32_t h0 = (2u * tcount) % 3u, h1 = (2u * tcount + 1u) % 3u;
+        const uint32_t h0 = tcount & 1u, h1 = h0 + 1u;  // the tile's two slots
         if (!mbar_wait_bounded(&hempty[h0], ((hpar >> h0) & 1u) ^ 1u, abort_flag, args.status,
                                args.wait_limit_ns) ||
             !mbar_wait_bounded(&hempty[h1], ((hpar >> h1) & 1u) ^ 1u, abort_flag, args.status,
@@ -1742,7 +1744,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tmem_base + 128u * h0, d1 = tmem_base + 128u * h1;
+        const uint32_t d_tmem = tmem_base + 128u * h0;
         for (int kb = 0; kb < kblocks; ++kb) {
           const int j = kb & 3;  // byte of the slot's cells with this k-block's exponents
           if ((j == 0 && !mbar_wait_bounded(&sfull[slot], sphase, abort_flag, args.status,
@@ -1754,17 +1756,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
           }
           tc_fence_after();
           const uint64_t ad = sw128_kmajor_desc(smem_u32(smA + stage * C::A_BYTES));
-          const uint64_t bd0 = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
-          const uint64_t bd1 = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES + 64 * kF8BK));
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
           const uint32_t sfa =
               tmem_base + static_cast<uint32_t>(kF8PairScaleCol + kF8PairSlotCols * slot);
           const uint32_t idesc =
               kIdesc | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
 #pragma unroll
           for (int kk = 0; kk < kF8BK / 32; ++kk) {
-            const uint32_t acc = (kb != 0 || kk != 0) ? 1u : 0u;
-            mma_mxf8_ss_pair(d0, ad + 2u * kk, bd0 + 2u * kk, idesc, sfa, sfa + 4u, acc);
-            mma_mxf8_ss_pair(d1, ad + 2u * kk, bd1 + 2u * kk, idesc, sfa, sfa + 8u, acc);
+            mma_mxf8_ss_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, sfa, sfa + 4u,
+                             (kb != 0 || kk != 0) ? 1u : 0u);
           }
           any_mma = true;
           mma_commit_pair(&empty[stage], 0x3);
@@ -1878,9 +1878,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
     }
   } else {
     // ---------------- epilogue (warps 6..13, both CTAs) ----------------
-    // For each half of a tile in turn (half 0 first, releasing it for the
-    // next tile's MMAs): warp w takes TMEM lane quadrant w % 4 and part
-    // p = (w - 6) / 4 of the half.  gate_up: gate columns 32p..32p+31 of the
+    // For each half of a tile in turn (the one in the middle slot first,
+    // releasing it for the next tile's MMAs): warp w takes TMEM lane
+    // quadrant w % 4 and part p = (w - 6) / 4 of the half.  gate_up: gate columns 32p..32p+31 of the
     // half and their up columns 64 + 32p.. -> h columns t.n * 128 + 64 * half
     // + 32p; down: columns 64p..64p+63 -> output columns t.n * 256 +
     // 128 * half + 64p.
@@ -1891,15 +1891,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
     const int col0 = SWIGLU ? 32 * part : 64 * part;
     const int col1 = SWIGLU ? 64 + 32 * part : 64 * part + 32;
     uint32_t tcount = 0;
-    uint32_t hpar = 0;  // bit b: parity of half buffer b's next completion
+    uint32_t hpar = 0;  // bit b: parity of slot b's next completion
     bool ok = true;
     for (int u = cid; u < total && ok; u += ncl, ++tcount) {
       const Tile t = decode_tile<256>(args, mt, u, sg);
       const int64_t grow = static_cast<int64_t>(t.row0) + prow;
       const bool rok = prow < t.rows_valid && grow >= 0 && grow < args.rows_total;
       const bool warp_rows = static_cast<int>(rank) * 128 + quad * 32 < t.rows_valid;
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t b = (2u * tcount + static_cast<uint32_t>(half)) % 3u;
+      for (int it = 0; it < 2; ++it) {
+        // even tiles: slots 0, 1 (half 1 in the middle slot); odd: slots 1, 2
+        const int half = (tcount & 1u) ? it : 1 - it;
+        const uint32_t b = (tcount & 1u) + static_cast<uint32_t>(half);
         const bool waited = mbar_wait_bounded(&hfull[b], (hpar >> b) & 1u, abort_flag,
                                               args.status, args.wait_limit_ns);
         if (!__all_sync(0xffffffffu, waited)) {
