@@ -1947,15 +1947,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
 
 // ---------------------------------------------------------------------------
 // The FP8 GEMM's 1-CTA form with 128 x 256 tiles (used where the routed rows
-// are few per expert, so the weights are the bound): per K step two M=128 x
-// N=128 block-scaled MMAs into two accumulator halves that rotate through
-// three TMEM half buffers as in the pair form.  A stage holds 128 A rows and
+// are few per expert, so the weights are the bound): one M=128 x N=256
+// block-scaled MMA per K step, the accumulator windows alternating over
+// three 128-column TMEM slots as in the pair form.  A stage holds 128 A rows and
 // 256 B rows (48 KB, 4 stages): 32 KB of weights per stage and 128 KB in
 // flight.  gate_up: smem B rows 0-63 gate i0.., 64-127 up i0.., 128-191
 // gate i0+64.., 192-255 up i0+64.. (i0 = 128 t.n), so each half holds 64 gate
 // columns and their up columns; down: rows c0 .. c0+255 (c0 = 256 t.n).
-// The exponent slots are the pair form's (16 columns: A, half 0's B, half
-// 1's B).
+// The exponent slots are the pair form's (16 columns: A in 0-3, B in 4-11,
+// B column n's exponent at lane 32q + n % 32, column 4 + n / 32).
 // ---------------------------------------------------------------------------
 constexpr int kF8WideStages = 4;
 
@@ -2095,17 +2095,17 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t kIdesc = mma_idesc_mxf8_f32(kBM, 128);
+      constexpr uint32_t kIdesc = mma_idesc_mxf8_f32(kBM, kF8PairBN);
       int stage = 0;
       uint32_t phase = 0;
       int slot = 0;
       uint32_t sphase = 0;
       uint32_t tcount = 0;
-      uint32_t hpar = 0;  // bit b: parity of half buffer b's next use
+      uint32_t hpar = 0;  // bit b: parity of slot b's next use
       bool any_mma = false;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok && !*abort_flag; u += gridDim.x, ++tcount) {
-        const uint32_t h0 = (2u * tcount) % 3u, h1 = (2u * tcount + 1u) % 3u;
+        const uint32_t h0 = tcount & 1u, h1 = h0 + 1u;  // the tile's two slots
         if (!mbar_wait_bounded(&hempty[h0], ((hpar >> h0) & 1u) ^ 1u, abort_flag, args.status,
                                args.wait_limit_ns) ||
             !mbar_wait_bounded(&hempty[h1], ((hpar >> h1) & 1u) ^ 1u, abort_flag, args.status,
@@ -2114,7 +2114,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tmem_base + 128u * h0, d1 = tmem_base + 128u * h1;
+        const uint32_t d_tmem = tmem_base + 128u * h0;
         for (int kb = 0; kb < kblocks; ++kb) {
           const int j = kb & 3;  // byte of the slot's cells with this k-block's exponents
           if ((j == 0 && !mbar_wait_bounded(&sfull[slot], sphase, abort_flag, args.status,
@@ -2126,18 +2126,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           }
           tc_fence_after();
           const uint64_t ad = sw128_kmajor_desc(smem_u32(smA + stage * C::A_BYTES));
-          const uint64_t bd0 = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
-          const uint64_t bd1 =
-              sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES + 128 * kF8BK));
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(smB + stage * C::B_BYTES));
           const uint32_t sfa =
               tmem_base + static_cast<uint32_t>(kF8PairScaleCol + kF8PairSlotCols * slot);
           const uint32_t idesc =
               kIdesc | (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
 #pragma unroll
           for (int kk = 0; kk < kF8BK / 32; ++kk) {
-            const uint32_t acc = (kb != 0 || kk != 0) ? 1u : 0u;
-            mma_mxf8_ss(d0, ad + 2u * kk, bd0 + 2u * kk, idesc, sfa, sfa + 4u, acc);
-            mma_mxf8_ss(d1, ad + 2u * kk, bd1 + 2u * kk, idesc, sfa, sfa + 8u, acc);
+            mma_mxf8_ss(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, sfa, sfa + 4u,
+                        (kb != 0 || kk != 0) ? 1u : 0u);
           }
           any_mma = true;
           mma_commit(&empty[stage]);
@@ -2247,8 +2244,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     }
   } else {
     // ---------------- epilogue (warps 6..13) ----------------
-    // As in the pair form: each half in turn (half 0 first), warp w taking
-    // lane quadrant w % 4 and part p = (w - 6) / 4 of the half.
+    // As in the pair form: each half in turn (the one in the middle slot
+    // first), warp w taking lane quadrant w % 4 and part p = (w - 6) / 4 of
+    // the half.
     const int quad = warp & 3;
     const int part = (warp - 6) >> 2;
     const int row = quad * 32 + lane;
@@ -2263,8 +2261,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       const int64_t grow = static_cast<int64_t>(t.row0) + row;
       const bool rok = row < t.rows_valid && grow >= 0 && grow < args.rows_total;
       const bool warp_rows = quad * 32 < t.rows_valid;
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t b = (2u * tcount + static_cast<uint32_t>(half)) % 3u;
+      for (int it = 0; it < 2; ++it) {
+        // even tiles: slots 0, 1 (half 1 in the middle slot); odd: slots 1, 2
+        const int half = (tcount & 1u) ? it : 1 - it;
+        const uint32_t b = (tcount & 1u) + static_cast<uint32_t>(half);
         const bool waited = mbar_wait_bounded(&hfull[b], (hpar >> b) & 1u, abort_flag,
                                               args.status, args.wait_limit_ns);
         if (!__all_sync(0xffffffffu, waited)) {
