@@ -37,28 +37,62 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-// One warp per (row, 128-column block): 4 values per lane.
+// A row's 128-column blocks are consecutive in memory (cols is a multiple
+// of 128), so block b of the whole array starts at element 128 b and its
+// scale is scales[b].  Half a warp per block, 16 bytes (8 values) per lane,
+// kQRowsUnroll block pairs per warp in flight; grid-stride over the blocks.
+// Dividing by the power-of-two scale is the exact product with its
+// reciprocal, so the codes are those of the division.
+constexpr int kQRowsUnroll = 4;
+
 __global__ void __launch_bounds__(256)
-    quantize_rows_kernel(const __nv_bfloat16 *__restrict__ x, int64_t rows, int cols,
+    quantize_rows_kernel(const __nv_bfloat16 *__restrict__ x, int64_t blocks,
                          uint8_t *__restrict__ q, float *__restrict__ scales) {
   pdl_begin();
   const int lane = threadIdx.x & 31;
-  const int nb = cols / 128;
-  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (item >= rows * nb) return;
-  const int64_t r = item / nb;
-  const int b = static_cast<int>(item - r * nb);
-  const size_t o = static_cast<size_t>(r) * cols + static_cast<size_t>(b) * 128 + lane * 4;
-  const uint2 raw = *reinterpret_cast<const uint2 *>(x + o);
-  const float v0 = bf16lo(raw.x), v1 = bf16hi(raw.x), v2 = bf16lo(raw.y), v3 = bf16hi(raw.y);
-  float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+  const int hl = lane & 15;  // lane within the half warp
+  const int half = lane >> 4;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t base = warp * 2 * kQRowsUnroll; base < blocks;
+       base += nwarps * 2 * kQRowsUnroll) {
+    uint4 raw[kQRowsUnroll];
 #pragma unroll
-  for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float s = fp8_block_scale(amax);
-  const uint32_t packed = static_cast<uint32_t>(e4m3x2(__fdiv_rn(v0, s), __fdiv_rn(v1, s))) |
-                          (static_cast<uint32_t>(e4m3x2(__fdiv_rn(v2, s), __fdiv_rn(v3, s))) << 16);
-  *reinterpret_cast<uint32_t *>(q + o) = packed;
-  if (lane == 0) scales[r * nb + b] = s;
+    for (int j = 0; j < kQRowsUnroll; ++j) {
+      const int64_t b = base + 2 * j + half;
+      raw[j] = b < blocks ? *reinterpret_cast<const uint4 *>(x + b * 128 + hl * 8)
+                          : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < kQRowsUnroll; ++j) {
+      const int64_t b = base + 2 * j + half;
+      const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+      float v[8];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        v[2 * t] = bf16lo(w[t]);
+        v[2 * t + 1] = bf16hi(w[t]);
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fabsf(v[t]));
+#pragma unroll
+      for (int off = 8; off; off >>= 1)  // within the half warp
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      if (b >= blocks) continue;
+      const float sc = fp8_block_scale(amax);
+      const float inv = __frcp_rn(sc);  // exact: sc is a power of two
+      uint32_t out[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        out[t] = static_cast<uint32_t>(e4m3x2(__fmul_rn(v[4 * t], inv), __fmul_rn(v[4 * t + 1], inv))) |
+                 (static_cast<uint32_t>(e4m3x2(__fmul_rn(v[4 * t + 2], inv),
+                                               __fmul_rn(v[4 * t + 3], inv)))
+                  << 16);
+      *reinterpret_cast<uint2 *>(q + b * 128 + hl * 8) = make_uint2(out[0], out[1]);
+      if (hl == 0) scales[b] = sc;
+    }
+  }
 }
 
 // One CTA of 256 threads per 128 x 128 block: each thread 64 values.
@@ -115,10 +149,14 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_quantize_rows_fp8(const void *x, int64_t rows, int cols, void *q,
                                      float *scales, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  const int64_t warps = rows * (cols / 128);
-  const int64_t blocks = (warps * 32 + 255) / 256;
-  MOE_LAUNCH_PDL(quantize_rows_kernel, static_cast<unsigned>(blocks), 256, 0, s, 
-      static_cast<const __nv_bfloat16 *>(x), rows, cols, static_cast<uint8_t *>(q), scales);
+  const int64_t nblk = rows * (cols / 128);
+  // 8 warps per CTA, 2 * kQRowsUnroll blocks per warp and pass; at most 8
+  // CTAs per SM, the rest by the grid-stride loop
+  int64_t ctas = (nblk + 8 * 2 * kQRowsUnroll - 1) / (8 * 2 * kQRowsUnroll);
+  const int64_t cap = 8ll * num_sms();
+  if (ctas > cap) ctas = cap;
+  MOE_LAUNCH_PDL(quantize_rows_kernel, static_cast<unsigned>(ctas), 256, 0, s,
+                 static_cast<const __nv_bfloat16 *>(x), nblk, static_cast<uint8_t *>(q), scales);
   return cudaGetLastError();
 }
 
