@@ -1529,7 +1529,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 // layout (N = 256: B column n's exponent at lane 32q + n % 32, column
 // n / 32); a scale slot has 16 columns: A (0-3), B (4-11).  An expert's
 // last tile may leave the odd CTA without A rows: it then loads only its B
-// rows.
+// rows.  The down form's compact rows leave through TMA tensor stores: each
+// epilogue warp whose 32 rows are all valid stages a 32 x 32 fp16 box
+// (64-byte swizzle) in its own 2 KB of shared memory per 32-column group
+// (per-thread 32-byte global stores kept the load/store queue full).
 //   full[s]          even CTA: both CTAs' copies of stage s landed;
 //   empty[s]         both CTAs: the pair MMAs that read stage s completed;
 //   sfull[g]         even CTA: both CTAs' exponents of scale slot g are in TMEM;
@@ -1549,13 +1552,18 @@ struct CfgF8P {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = kF8PairStages;
   static constexpr int BN_OUT = SWIGLU ? kF8PairBN / 2 : kF8PairBN;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  // down: one 32 x 32 fp16 staging box per epilogue warp (compact rows)
+  static constexpr int OUT_OFF = STAGES * STAGE_BYTES;
+  static constexpr int OUT_BOX_BYTES = 32 * 32 * 2;
+  static constexpr int OUT_BYTES = SWIGLU ? 0 : 8 * OUT_BOX_BYTES;
+  static constexpr int BAR_OFF = OUT_OFF + OUT_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * kF8ScaleSlots + 2 * 3 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int MT_OFF = MISC_OFF + 16;
   static constexpr int SEG_OFF = MT_OFF + (kMaxE + 1) * 4;
   static constexpr int SMEM_BYTES = SEG_OFF + (kMaxE + 1) * 4 + 1024;
   static_assert(SMEM_BYTES <= 232448, "227 KB of shared memory per CTA");
+  static_assert(OUT_OFF % 2048 == 0, "swizzled staging alignment");
   static_assert(kF8PairScaleCol + kF8PairSlotCols * kF8ScaleSlots <= kF8TmemCols,
                 "scale slots fit the TMEM allocation");
 };
@@ -1598,7 +1606,8 @@ template <bool SWIGLU>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
     grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                                  const __grid_constant__ CUtensorMap tmA32,
-                                 const __grid_constant__ CUtensorMap tmB, const F8Args fa) {
+                                 const __grid_constant__ CUtensorMap tmB,
+                                 const __grid_constant__ CUtensorMap tmY, const F8Args fa) {
   pdl_begin();
   using C = CfgF8P<SWIGLU>;
   const KArgs &args = fa.k;
@@ -1923,7 +1932,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote_relaxed(mapa_shared(&hempty[b], 0));
-        if (!warp_rows || !rok) continue;
+        if (!warp_rows) continue;
+        if (!SWIGLU && args.out_tma &&
+            static_cast<int>(rank) * 128 + quad * 32 + 32 <= t.rows_valid &&
+            grow - lane >= 0 && grow - lane + 32 <= args.rows_total) {
+          // compact rows by TMA: per 32-column group the warp's 32 rows of
+          // fp16 values as one box, then the lane's two code bytes
+          uint8_t *box = smem + C::OUT_OFF + (warp - 6) * C::OUT_BOX_BYTES;
+          const int row_g = static_cast<int>(grow - lane);
+          const uint32_t swz = static_cast<uint32_t>((lane >> 1) & 3);
+          const uint32_t rbase = smem_u32(box) + static_cast<uint32_t>(lane) * 64u;
+          const int64_t col = static_cast<int64_t>(t.n) * kF8PairBN + 128 * half + 64 * part;
+          uint32_t codes = 0;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            uint32_t hw[16];
+            codes |= y16_encode32(g ? w : v, hw) << (8 * g);
+            if (lane == 0) bulk_wait_read_0();  // the previous store has read the box
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(rbase + ((static_cast<uint32_t>(q) ^ swz) * 16u), hw[4 * q],
+                           hw[4 * q + 1], hw[4 * q + 2], hw[4 * q + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmY, box, static_cast<int32_t>(col + 32 * g), row_g);
+              bulk_commit();
+            }
+          }
+          *reinterpret_cast<uint16_t *>(args.out_codes + grow * (args.ldo / 32) + col / 32) =
+              static_cast<uint16_t>(codes);
+          continue;
+        }
+        if (!rok) continue;
         float acc[64];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -1939,6 +1981,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
     }
   }
 
+  if (!SWIGLU && warp >= 6 && lane == 0) bulk_wait_all();  // output stores written
   tc_fence_before();
   cluster_sync_all();  // no CTA leaves while its peer may still use its memory
   tc_fence_after();
@@ -2493,6 +2536,13 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   }
   // CTA pairs on 256-row tiles (mtile_base counts 256-row tiles)
   using P = CfgF8P<SWIGLU>;
+  // down, compact rows: fp16 values leave through TMA stores
+  CUtensorMap tmY = tmA;
+  a.out_tma = 0;
+  if (!SWIGLU && a.out_codes != nullptr &&
+      make_tmap_f16_out(&tmY, p.out, static_cast<uint64_t>(p.n_out),
+                        static_cast<uint64_t>(p.rows_total)))
+    a.out_tma = 1;
   err = cudaFuncSetAttribute(grouped_gemm_fp8_pair_kernel<SWIGLU>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES);
   if (err != cudaSuccess) return err;
@@ -2519,7 +2569,7 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   }
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   MOE_LAUNCH_PDL(grouped_gemm_fp8_pair_kernel<SWIGLU>, 2 * clusters, kF8Threads, P::SMEM_BYTES, s,
-                 tmA, tmA32, tmB, fa);
+                 tmA, tmA32, tmB, tmY, fa);
   return cudaGetLastError();
 }
 
