@@ -1202,13 +1202,11 @@ def run_fp8(args):
         raise SystemExit("device status error")
     ffn_s = e0.elapsed_time(e1) / 1000.0 / args.steps
     # algorithmic bytes of the FFN: the touched weights once; gate_up reads
-    # the FP8 rows and their scales and writes h (bf16); the quantization
-    # reads h and writes its codes and scales; down reads those and writes
-    # the fp32 rows
+    # the FP8 rows and their scales and writes h's codes and scales (h is
+    # quantized in its epilogue); down reads those and writes the fp32 rows
     n = c.T * c.k
-    ffn_bytes = (w_bytes + n * (c.d + 4 * (c.d // 128)) + n * c.inter * 2
-                 + n * (c.inter * 2 + c.inter + 4 * (c.inter // 128))
-                 + n * (c.inter + 4 * (c.inter // 128)) + n * c.d * 4)
+    h_bytes = n * (c.inter + 4 * (c.inter // 128))
+    ffn_bytes = w_bytes + n * (c.d + 4 * (c.d // 128)) + 2 * h_bytes + n * c.d * 4
     line = {
         "metric": METRIC + " (FP8 e4m3 experts, block scales)", "impl": "gb300",
         "value": c.T / (ms / 1000.0), "unit": UNIT, "n_gpus": 1, "steps": args.steps,

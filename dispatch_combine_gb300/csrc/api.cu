@@ -617,12 +617,12 @@ moe_status_t moe_quantize_fp8_blocks(const void *w, int32_t mats, int32_t rows, 
 // ---------------------------------------------------------------------------
 
 struct LayoutF8 {
-  size_t status, mtile, chunk, logits, wr32, h, hq, hs, ids, w, counts, offsets, dest, src, xq,
+  size_t status, mtile, chunk, logits, wr32, hq, hs, ids, w, counts, offsets, dest, src, xq,
       xs, xq_perm, xs_perm, y_perm;
   size_t end_ffn, end_layer;
 };
 
-// FFN part (h in bf16, then its FP8 codes and scales) for `rows` rows; the
+// FFN part (the FP8 codes and scales of h) for `rows` rows; the
 // layer part adds routing, dispatch and the FP8 activations
 LayoutF8 make_fp8_layout(const moe_shape_t &s, int64_t rows) {
   LayoutF8 L;
@@ -635,7 +635,6 @@ LayoutF8 make_fp8_layout(const moe_shape_t &s, int64_t rows) {
   };
   L.status = take(4);
   L.mtile = take(4 * static_cast<size_t>(s.E + 1));
-  L.h = take(2 * static_cast<size_t>(rows) * s.inter);
   L.hq = take(static_cast<size_t>(rows) * s.inter);
   L.hs = take(4 * static_cast<size_t>(rows) * (s.inter / 128));
   L.end_ffn = off;
@@ -695,11 +694,12 @@ moe_status_t run_ffn_fp8(const moe_shape_t *s, int32_t layout, const void *xq, c
   p.a = xq;
   p.b = wgu_q;
   p.b_rows = 2 * s->inter;
-  p.out = at<void>(ws, L.h);
+  // gate_up quantizes h (its bf16 values, per row and 128 columns) in its
+  // epilogue: h leaves as e4m3 codes and scales
+  p.out = at<void>(ws, L.hq);
+  p.out_h_scales = at<float>(ws, L.hs);
   MOE_TRY(cuda_status(moe::launch_gemm_fp8_gate_up_swiglu(p, xs, wgu_s, st)));
-  MOE_TRY(cuda_status(moe::launch_quantize_rows_fp8(at<void>(ws, L.h), rows, s->inter,
-                                                    at<void>(ws, L.hq), at<float>(ws, L.hs),
-                                                    st)));
+  p.out_h_scales = nullptr;
   p.K = s->inter;
   p.n_out = s->d;
   p.a = at<void>(ws, L.hq);

@@ -467,6 +467,33 @@ __device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// FP8 (e4m3) block quantization, shared by the quantizers and the FP8
+// gate_up epilogue.  A block's scale is the power of two s = 2^e with e the
+// smallest integer >= -127 such that amax <= 448 * 2^e (1 for an all-zero
+// block, 2^127 for a non-finite amax), taken from amax's bits: amax =
+// (1 + f) * 2^(E - 127) with E its exponent field, and 448 * 2^(E - 135) =
+// 1.75 * 2^(E - 127), so e = E - 135 when f <= 0.75 (mantissa field <=
+// 0x600000), else E - 134.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fp8_block_scale(float amax) {
+  if (!(amax > 0.0f)) return 1.0f;
+  const uint32_t b = __float_as_uint(amax);
+  const int ef = static_cast<int>((b >> 23) & 0xffu);
+  if (ef == 0xff) return __uint_as_float(254u << 23);  // 2^127
+  int e = ef - 135 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
+  if (e <= -127) return __uint_as_float(0x00400000u);  // 2^-127 (an fp32 subnormal)
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+// two fp32 -> two e4m3 codes (lo in bits 0-7), round to nearest even,
+// saturating to +-448
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // kind::mxf8f6f4 block-scaled descriptor: A and B e4m3 (format 0 in bits
 // 7-9 and 10-12), both K-major, N >> 3 at bit 17, scale type UE8M0 (bit 23),
 // M >> 4 at bit 24; scale factor ids 0 (bits 4-5 for B, 29-30 for A): each

@@ -80,6 +80,7 @@ struct KArgs {
   uint8_t *out_codes;
   float *split_part;
   int split_part_slots;
+  float *out_h_scales;  // FP8 gate_up: h quantized in the epilogue (nullptr: bf16 h)
   int64_t rows_total;
   const int32_t *seg;
   const int32_t *seg2;  // kLayoutTwoSeg: overflow offsets [E+1]
@@ -1205,6 +1206,75 @@ __device__ __forceinline__ void f8_store_tile_row(const KArgs &args, int64_t gro
   }
 }
 
+// SwiGLU of a thread's 32 gate values v and their up values w, rounded to
+// bf16 (h's storage format), two per register in column order.
+__device__ __forceinline__ void f8_swiglu_bf16(const uint32_t (&v)[32], const uint32_t (&w)[32],
+                                               uint32_t (&hb)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float g0 = __uint_as_float(v[2 * i]), g1 = __uint_as_float(v[2 * i + 1]);
+    const float u0 = __uint_as_float(w[2 * i]), u1 = __uint_as_float(w[2 * i + 1]);
+    hb[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
+                        __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+  }
+}
+
+__device__ __forceinline__ float f8_bf16x2_absmax(const uint32_t (&hb)[16], float m) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fabsf(bf16lo(hb[i])), fabsf(bf16hi(hb[i]))));
+  return m;
+}
+
+// 32 bf16 values of h -> their e4m3 codes at dst (32 bytes, 32-byte aligned),
+// times the exact reciprocal of the power-of-two scale: the codes of the
+// row quantizer.
+__device__ __forceinline__ void f8_store_codes32(uint8_t *dst, const uint32_t (&hb)[16],
+                                                 float inv) {
+  uint32_t q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t a = hb[2 * i], b = hb[2 * i + 1];
+    q[i] = static_cast<uint32_t>(e4m3x2(__fmul_rn(bf16lo(a), inv), __fmul_rn(bf16hi(a), inv))) |
+           (static_cast<uint32_t>(e4m3x2(__fmul_rn(bf16lo(b), inv), __fmul_rn(bf16hi(b), inv)))
+            << 16);
+  }
+  st_global_v8(dst, q);
+}
+
+// The fused h quantization of one tile row (gate_up, 256-column tiles): the
+// row's 128 h columns, one scale block, are held by two threads (parts 0 and
+// 1, warps w and w + 4 of one lane quadrant) as two 32-column runs each
+// (halves 0 and 1).  Each warp posts its rows' partial maxima in xch
+// (double-buffered by use), arrives on the quadrant's barrier, waits for
+// the other warp (bounded) and quantizes its runs with the row's scale.
+// Returns false if the wait ran out.
+__device__ __forceinline__ bool f8_quantize_row(const KArgs &args, const Tile &t, int64_t grow,
+                                                bool rok, int row, int part, uint32_t use,
+                                                const uint32_t (&h0)[16], const uint32_t (&h1)[16],
+                                                float *xch, uint64_t *xbar,
+                                                volatile int *abort_flag) {
+  const int lane = threadIdx.x & 31;
+  float m = rok ? f8_bf16x2_absmax(h1, f8_bf16x2_absmax(h0, 0.0f)) : 0.0f;
+  float *buf = xch + (use & 1u) * 256;
+  buf[part * 128 + row] = m;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(xbar);
+  const bool waited = mbar_wait_bounded(xbar, use & 1u, abort_flag, args.status,
+                                        args.wait_limit_ns);
+  if (!__all_sync(0xffffffffu, waited)) return false;
+  m = fmaxf(m, buf[(1 - part) * 128 + row]);
+  if (rok) {
+    const float sc = fp8_block_scale(m);
+    const float inv = __frcp_rn(sc);  // exact: sc is a power of two
+    uint8_t *dst = static_cast<uint8_t *>(args.out) + grow * args.ldo +
+                   static_cast<int64_t>(t.n) * 128 + 32 * part;
+    f8_store_codes32(dst, h0, inv);
+    f8_store_codes32(dst + 64, h1, inv);
+    if (part == 0) args.out_h_scales[grow * (args.ldo / 128) + t.n] = sc;
+  }
+  return true;
+}
+
 template <bool SWIGLU>
 __global__ void __launch_bounds__(kF8Threads, 1)
     grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -1552,12 +1622,13 @@ struct CfgF8P {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = kF8PairStages;
   static constexpr int BN_OUT = SWIGLU ? kF8PairBN / 2 : kF8PairBN;
-  // down: one 32 x 32 fp16 staging box per epilogue warp (compact rows)
+  // down: one 32 x 32 fp16 staging box per epilogue warp (compact rows);
+  // gate_up: the row maxima exchanged by the fused h quantization
   static constexpr int OUT_OFF = STAGES * STAGE_BYTES;
   static constexpr int OUT_BOX_BYTES = 32 * 32 * 2;
-  static constexpr int OUT_BYTES = SWIGLU ? 0 : 8 * OUT_BOX_BYTES;
+  static constexpr int OUT_BYTES = SWIGLU ? 2 * 2 * 128 * 4 : 8 * OUT_BOX_BYTES;
   static constexpr int BAR_OFF = OUT_OFF + OUT_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * kF8ScaleSlots + 2 * 3 + 1;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * kF8ScaleSlots + 2 * 3 + 1 + 4;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int MT_OFF = MISC_OFF + 16;
   static constexpr int SEG_OFF = MT_OFF + (kMaxE + 1) * 4;
@@ -1624,6 +1695,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
   uint64_t *hfull = sempty + kF8ScaleSlots;
   uint64_t *hempty = hfull + 3;
   uint64_t *drain = hempty + 3;
+  uint64_t *xbar = drain + 1;  // per lane quadrant: the fused h quantization's exchange
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
   int32_t *mt = reinterpret_cast<int32_t *>(smem + C::MT_OFF);
@@ -1653,6 +1725,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
       mbar_init(&hempty[b], 16);
     }
     mbar_init(drain, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&xbar[q], 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1901,12 +1974,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
     const int col1 = SWIGLU ? 64 + 32 * part : 64 * part + 32;
     uint32_t tcount = 0;
     uint32_t hpar = 0;  // bit b: parity of slot b's next completion
+    const bool fuse = SWIGLU && args.out_h_scales != nullptr;
+    float *xch = reinterpret_cast<float *>(smem + C::OUT_OFF);
+    uint32_t xuse = 0;  // uses of this quadrant's exchange barrier
     bool ok = true;
     for (int u = cid; u < total && ok; u += ncl, ++tcount) {
       const Tile t = decode_tile<256>(args, mt, u, sg);
       const int64_t grow = static_cast<int64_t>(t.row0) + prow;
       const bool rok = prow < t.rows_valid && grow >= 0 && grow < args.rows_total;
       const bool warp_rows = static_cast<int>(rank) * 128 + quad * 32 < t.rows_valid;
+      uint32_t hq0[16], hq1[16];  // fused quantization: this thread's h runs of the tile
       for (int it = 0; it < 2; ++it) {
         // even tiles: slots 0, 1 (half 1 in the middle slot); odd: slots 1, 2
         const int half = (tcount & 1u) ? it : 1 - it;
@@ -1933,6 +2010,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_remote_relaxed(mapa_shared(&hempty[b], 0));
         if (!warp_rows) continue;
+        if (fuse) {
+          if (half == 0)
+            f8_swiglu_bf16(v, w, hq0);
+          else
+            f8_swiglu_bf16(v, w, hq1);
+          continue;
+        }
         if (!SWIGLU && args.out_tma &&
             static_cast<int>(rank) * 128 + quad * 32 + 32 <= t.rows_valid &&
             grow - lane >= 0 && grow - lane + 32 <= args.rows_total) {
@@ -1978,6 +2062,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kF8Threads, 1)
                    : static_cast<int64_t>(t.n) * kF8PairBN + 128 * half + 64 * part,
             acc);
       }
+      if (fuse && ok && warp_rows &&
+          !f8_quantize_row(args, t, grow, rok, quad * 32 + lane, part, xuse++, hq0, hq1, xch,
+                           &xbar[quad], abort_flag))
+        ok = false;
     }
   }
 
@@ -2009,8 +2097,11 @@ struct CfgF8W {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = kF8WideStages;
   static constexpr int BN_OUT = SWIGLU ? kF8PairBN / 2 : kF8PairBN;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * kF8ScaleSlots + 2 * 3 + 1;
+  // gate_up: the row maxima exchanged by the fused h quantization
+  static constexpr int XCH_OFF = STAGES * STAGE_BYTES;
+  static constexpr int XCH_BYTES = SWIGLU ? 2 * 2 * 128 * 4 : 0;
+  static constexpr int BAR_OFF = XCH_OFF + XCH_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * kF8ScaleSlots + 2 * 3 + 1 + 4;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int MT_OFF = MISC_OFF + 16;
   static constexpr int SMEM_BYTES = MT_OFF + (kMaxE + 1) * 4 + 1024;
@@ -2040,6 +2131,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   uint64_t *hfull = sempty + kF8ScaleSlots;
   uint64_t *hempty = hfull + 3;
   uint64_t *drain = hempty + 3;
+  uint64_t *xbar = drain + 1;  // per lane quadrant: the fused h quantization's exchange
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
   int32_t *mt = reinterpret_cast<int32_t *>(smem + C::MT_OFF);
@@ -2061,6 +2153,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       mbar_init(&hempty[b], 8);
     }
     mbar_init(drain, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&xbar[q], 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -2298,12 +2391,16 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     const int col1 = SWIGLU ? 64 + 32 * part : 64 * part + 32;
     uint32_t tcount = 0;
     uint32_t hpar = 0;
+    const bool fuse = SWIGLU && args.out_h_scales != nullptr;
+    float *xch = reinterpret_cast<float *>(smem + C::XCH_OFF);
+    uint32_t xuse = 0;  // uses of this quadrant's exchange barrier
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++tcount) {
       const Tile t = decode_tile(args, mt, u);
       const int64_t grow = static_cast<int64_t>(t.row0) + row;
       const bool rok = row < t.rows_valid && grow >= 0 && grow < args.rows_total;
       const bool warp_rows = quad * 32 < t.rows_valid;
+      uint32_t hq0[16], hq1[16];  // fused quantization: this thread's h runs of the tile
       for (int it = 0; it < 2; ++it) {
         // even tiles: slots 0, 1 (half 1 in the middle slot); odd: slots 1, 2
         const int half = (tcount & 1u) ? it : 1 - it;
@@ -2328,6 +2425,13 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&hempty[b]);
+        if (warp_rows && fuse) {
+          if (half == 0)
+            f8_swiglu_bf16(v, w, hq0);
+          else
+            f8_swiglu_bf16(v, w, hq1);
+          continue;
+        }
         if (!warp_rows || !rok) continue;
         float acc[64];
 #pragma unroll
@@ -2341,6 +2445,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                    : static_cast<int64_t>(t.n) * kF8PairBN + 128 * half + 64 * part,
             acc);
       }
+      if (fuse && ok && warp_rows &&
+          !f8_quantize_row(args, t, grow, rok, quad * 32 + lane, part, xuse++, hq0, hq1, xch,
+                           &xbar[quad], abort_flag))
+        ok = false;
     }
   }
 
@@ -2504,6 +2612,11 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
   a.ldo = p.n_out;
   a.rows_total = p.rows_total;
   a.out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+  if (SWIGLU && p.out_h_scales != nullptr) {
+    // h quantized in the epilogue: 32-byte stores of e4m3 codes
+    if (!a.out_v8 || p.n_out % 128 != 0) return cudaErrorInvalidValue;
+    a.out_h_scales = p.out_h_scales;
+  }
   if (!SWIGLU && p.out_codes != nullptr) {
     // compact output: 32-byte stores of fp16 values, 2-byte code stores
     if (!a.out_v8 || p.n_out % kF8BN != 0 || (reinterpret_cast<uintptr_t>(p.out_codes) & 1u))
@@ -2530,6 +2643,7 @@ cudaError_t run_gemm_fp8(const GemmProblem &p, const float *a_scale, const float
     return cudaGetLastError();
   }
   if (!p.pair) {
+    if (a.out_h_scales != nullptr) return cudaErrorInvalidValue;  // 128-column tiles: bf16 h only
     MOE_LAUNCH_PDL(grouped_gemm_fp8_kernel<SWIGLU>, num_sms(), kF8Threads, C::SMEM_BYTES, s, tmA,
                    tmA32, tmB, fa);
     return cudaGetLastError();

@@ -197,6 +197,10 @@ struct GemmProblem {
   uint8_t *out_codes;
   float *split_part;
   int split_part_slots;
+  // FP8 gate_up with 256-column tiles: out receives h's e4m3 codes [rows,
+  // n_out] and out_h_scales its power-of-two scales [rows, n_out / 128], the
+  // quantization of the bf16 h done in the epilogue (nullptr: bf16 h)
+  float *out_h_scales;
 };
 cudaError_t launch_gemm_gate_up_swiglu(const GemmProblem &p, cudaStream_t s);
 cudaError_t launch_gemm_down(const GemmProblem &p, cudaStream_t s);

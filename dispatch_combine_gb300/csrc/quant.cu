@@ -16,27 +16,6 @@
 namespace moe {
 namespace {
 
-// The power-of-two scale from amax's bits: amax = (1 + f) * 2^(E - 127) with
-// E its exponent field, and 448 * 2^(E - 135) = 1.75 * 2^(E - 127), so
-// e = E - 135 when f <= 0.75 (mantissa field <= 0x600000), else E - 134.
-__device__ __forceinline__ float fp8_block_scale(float amax) {
-  if (!(amax > 0.0f)) return 1.0f;
-  const uint32_t b = __float_as_uint(amax);
-  const int ef = static_cast<int>((b >> 23) & 0xffu);
-  if (ef == 0xff) return __uint_as_float(254u << 23);  // 2^127
-  int e = ef - 135 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
-  if (e <= -127) return __uint_as_float(0x00400000u);  // 2^-127 (an fp32 subnormal)
-  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-}
-
-// two fp32 -> two e4m3 codes (lo in bits 0-7), round to nearest even,
-// saturating to +-448
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // A row's 128-column blocks are consecutive in memory (cols is a multiple
 // of 128), so block b of the whole array starts at element 128 b and its
 // scale is scales[b].  Half a warp per block, 16 bytes (8 values) per lane,
