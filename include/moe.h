@@ -402,8 +402,9 @@ moe_status_t moe_quantize_fp8_blocks(const void *w, int32_t mats, int32_t rows, 
  *   the layouts as moe_expert_ffn; y_out [rows, d] fp32.
  *   The tensor cores apply both scales of each 128-column k-block
  *   themselves (block-scaled MMAs, the scales as 8-bit exponents) and
- *   accumulate in fp32; h = silu(g) * u is stored in bf16, quantized per row
- *   and 128 columns, and multiplied by w_down the same way.  Every scale
+ *   accumulate in fp32; h = silu(g) * u is rounded to bf16 and quantized per
+ *   row and 128 columns (in the gate_up epilogue where the tiles allow), and
+ *   multiplied by w_down the same way.  Every scale
  *   must be a power of two in [2^-127, 2^127], as the quantizers above make
  *   them; any other value sets MOE_ERR_INVALID_ARG in the device status
  *   (and the affected outputs are undefined).
