@@ -449,24 +449,6 @@ __host__ __device__ constexpr uint32_t mma_idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// kind::f8f6f4 descriptor: D fp32 (bit 4), A and B e4m3 (format 0 in bits
-// 7-9 and 10-12), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t mma_idesc_e4m3_f32(int M, int N) {
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T with e4m3 operands (K = 32 per
-// instruction), one elected thread.
-__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // FP8 (e4m3) block quantization, shared by the quantizers and the FP8
 // gate_up epilogue.  A block's scale is the power of two s = 2^e with e the
