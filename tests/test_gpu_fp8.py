@@ -34,6 +34,27 @@ def test_quantize_rows_bit_exact():
     assert np.array_equal(s.cpu().numpy(), rs)
 
 
+def test_quantize_rows_scale_boundaries_bit_exact():
+    # the power-of-two scale at its boundaries: amax exactly 448 * 2^k, the
+    # next bf16 above it, values whose amax clamps the exponent at -127 (bf16
+    # subnormals among them), amax near the bf16 maximum, an all-zero block;
+    # each row one 128-column block, the rest of the row random
+    ensure_lib()
+    amaxes = [448.0, 448.0 * 2.0 ** -20, 448.0 * 2.0 ** 30, 450.0, 1.0, 1.75, 1.7578125,
+              2.0 ** -130, 1e-38, 3.0e38, 0.0]
+    x = _rand_bf16((len(amaxes), 256), 3) * 1e-3
+    for r, a in enumerate(amaxes):
+        x[r, :128] = 0.0
+        x[r, 5] = a
+        x[r, 9] = -0.75 * a
+        x[r, 17] = a * 2.0 ** -12
+    q, s = moe.moe_quantize_fp8_rows(x.cuda())
+    rq, rs = oracle.quantize_rows_fp8(bits(x))
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert rs[0, 0] == 1.0 and rs[3, 0] == 2.0 and rs[len(amaxes) - 1, 0] == 1.0
+
+
 def test_quantize_blocks_bit_exact():
     ensure_lib()
     w = _rand_bf16((3, 256, 384), 2) * 0.02
