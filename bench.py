@@ -1212,8 +1212,8 @@ def run_fp8(args):
         "value": c.T / (ms / 1000.0), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "e4m3",
         "data": "synthetic",
-        "config": {"workload": workload_desc(c), "weights": "e4m3, fp32 scale per 128x128 block",
-                   "activations": "e4m3, fp32 scale per row and 128 columns",
+        "config": {"workload": workload_desc(c), "weights": "e4m3, power-of-two fp32 scale per 128x128 block",
+                   "activations": "e4m3, power-of-two fp32 scale per row and 128 columns (h: in the gate_up epilogue)",
                    "touched_experts": touched},
         "layer_weight_bytes_fp8": w_bytes,
         "layer_hbm_fraction_of_weights": w_bytes / (ms / 1000.0) / (peaks["hbm_gbs"] * 1e9),
