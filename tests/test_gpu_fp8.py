@@ -111,6 +111,36 @@ def test_ffn_fp8_contiguous(counts, d, inter):
     check_close(y.cpu().numpy(), ref, bf16_output=False, what="y (fp8)")
 
 
+def test_ffn_fp8_prefill_shape_every_tile():
+    # the CTA-pair FP8 GEMMs (h quantized in the gate_up epilogue) at the
+    # prefill expert shape, d = 7168 and inter = 2048, on a skewed mix of
+    # expert row counts (an odd half with no rows, tails just under and over a
+    # 128-row half, full and partial tiles): the first and the last row of
+    # every 128-row m-tile compared with the oracle
+    ensure_lib()
+    counts = [5, 130, 255, 257, 601, 2413]
+    E, d, inter = len(counts), 7168, 2048
+    rows = sum(counts)
+    x = _rand_bf16((rows, d), 21)
+    (gq, gs, dq, ds), (rgq, rgs, rdq, rds) = _weights_fp8(E, d, inter, seed=22)
+    xq, xs = moe.moe_quantize_fp8_rows(x.cuda())
+    offs = np.concatenate([[0], np.cumsum(counts)])
+    offsets = torch.tensor(offs, dtype=torch.int32).cuda()
+    shape = _shape(E, d, inter, rows)   # rows / expert >= 256: CTA-pair tiles
+    ws = moe.Workspace(moe.moe_expert_ffn_fp8_workspace_size(shape, moe.MOE_LAYOUT_CONTIGUOUS))
+    y = moe.moe_expert_ffn_fp8(shape, moe.MOE_LAYOUT_CONTIGUOUS, xq, xs, offsets, 0, gq, gs, dq,
+                               ds, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    sel = sorted({int(offs[e]) + j for e, c in enumerate(counts) for t0 in range(0, c, 128)
+                  for j in (t0, min(t0 + 128, c) - 1)})
+    sel = np.array(sel, dtype=np.int64)
+    row_e = np.repeat(np.arange(E), counts).astype(np.int32)[sel]
+    rxq, rxs = oracle.quantize_rows_fp8(bits(x)[sel])
+    ref = oracle.expert_ffn_rows_fp8(rxq, rxs, row_e, rgq, rgs, rdq, rds)
+    check_close(y.cpu().numpy()[sel], ref, bf16_output=False, what="y (fp8, prefill shape)")
+
+
 @pytest.mark.parametrize("masked_m,M_max,T", [
     ([0, 5, 256], 256, 1),
     ([0, 5, 300, 512], 512, 1300),   # T*k >= 256 per expert and M_max >= 256: pair tiles
