@@ -9,7 +9,7 @@ import dispatch_combine_gb300 as moe
 import oracle
 from moe_inputs import CONFIGS, SCORE_SIGMOID_BIAS
 from tests.gpu_common import bf16_to_f64, bits, check_close, ensure_lib, host_bits, layer_inputs
-from tests.test_gpu_layer import oracle_routing
+from tests.test_gpu_layer import oracle_routing, tile_cover_tokens, tiles_covered
 
 pytestmark = pytest.mark.gpu
 
@@ -199,7 +199,9 @@ def test_ffn_fp8_flags_a_scale_that_is_not_a_power_of_two(pair_rows):
     assert moe.moe_get_device_status(ws) == 0          # read and cleared
 
 
-@pytest.mark.parametrize("name,n_samples", [("tiny", None), ("decode", 4), ("few_large", 3),
+# n_samples: None every token, "tiles" the tokens covering the first and the
+# last row of every 128-row m-tile of every expert, else that many sampled
+@pytest.mark.parametrize("name,n_samples", [("tiny", None), ("decode", "tiles"), ("few_large", "tiles"),
                                             ("prefill", 2)])
 def test_layer_fp8_matches_oracle(name, n_samples):
     ensure_lib()
@@ -215,6 +217,9 @@ def test_layer_fp8_matches_oracle(name, n_samples):
     ids, w = oracle_routing(name)
     if n_samples is None:
         toks = np.arange(cfg.T)
+    elif n_samples == "tiles":
+        toks, n_tiles = tile_cover_tokens(ids, cfg.E)
+        assert tiles_covered(ids, cfg.E, toks) == n_tiles
     else:
         toks = np.sort(np.random.default_rng(2).choice(cfg.T, n_samples, replace=False))
     experts = np.unique(ids[toks])
